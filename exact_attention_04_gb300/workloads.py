@@ -1,0 +1,101 @@
+"""Seeded synthetic inputs shaped like the pages' attention workloads.
+
+This module is shared by the tests, the benchmark and the smoke check.  It
+draws random numbers and nothing else: it holds none of the attention
+arithmetic, so the CPU oracle and the CUDA library can both be fed from it
+without sharing any of the method.
+
+Recipe (every tensor is drawn in fp32 on the CPU with ``torch.Generator``
+seeded as stated, then rounded to bf16; the same bf16 bytes go to the GPU
+and, widened exactly to float64, to the oracle):
+
+* Q, K, V ~ iid N(0, 1), drawn in that order from one generator seeded with
+  ``seed``; where ``qk_gain`` != 1 the fp32 Q and K are multiplied by it
+  before rounding (the large-head-dimension workload uses 3, which makes the
+  score standard deviation about 9 and stresses the max subtraction).
+* dO ~ iid N(0, 1) from a generator seeded with ``seed + 100``.
+* key-padding lengths ~ uniform integers in [lo, hi] (inclusive) from a
+  generator seeded with ``seed + 200``.
+"""
+from dataclasses import dataclass
+import math
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    seed: int
+    backward: bool
+    qk_gain: float = 1.0
+    kv_len_range: tuple = None     # (lo, hi) inclusive, or None for no padding
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def fwd_flops(self) -> float:
+        """4*B*H*N^2*d, halved under the causal mask (padding not discounted)."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2 if self.causal else f
+
+    def bwd_flops(self) -> float:
+        """2.5 x the forward count."""
+        return 2.5 * self.fwd_flops()
+
+
+def _long_seq(N, causal):
+    return Workload(f"long_seq_b{32768 // N}_h32_n{N}_d128_{'causal' if causal else 'full'}",
+                    B=32768 // N, H=32, N=N, d=128, causal=causal, seed=3, backward=False)
+
+
+WORKLOADS = {w.name: w for w in [
+    Workload("single_head_b1_h1_n256_d64", 1, 1, 256, 64, causal=False, seed=0, backward=False),
+    Workload("bert_large_b16_h16_n512_d64_pad", 16, 16, 512, 64, causal=False, seed=1,
+             backward=True, kv_len_range=(256, 512)),
+    Workload("gpt2_small_b8_h12_n1024_d64_causal", 8, 12, 1024, 64, causal=True, seed=2,
+             backward=True),
+    *[_long_seq(N, c) for N in (4096, 8192, 16384, 32768) for c in (False, True)],
+    Workload("large_head_b2_h16_n8192_d128_causal", 2, 16, 8192, 128, causal=True, seed=4,
+             backward=True, qk_gain=3.0),
+    Workload("large_head_b2_h16_n8192_d256_causal", 2, 16, 8192, 256, causal=True, seed=4,
+             backward=True, qk_gain=3.0),
+]}
+
+
+def make_inputs(w: Workload, with_grad_out: bool = None):
+    """CPU tensors for workload ``w``: dict with q, k, v (bf16 [B,H,N,d]),
+    optionally do (bf16) and kv_len (int32 [B] or None)."""
+    shape = (w.B, w.H, w.N, w.d)
+    g = torch.Generator().manual_seed(w.seed)
+    q = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    if w.qk_gain != 1.0:
+        q.mul_(w.qk_gain)
+        k.mul_(w.qk_gain)
+    out = {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}
+    del q, k, v
+    if with_grad_out is None:
+        with_grad_out = w.backward
+    if with_grad_out:
+        g2 = torch.Generator().manual_seed(w.seed + 100)
+        out["do"] = torch.randn(shape, generator=g2, dtype=torch.float32).to(torch.bfloat16)
+    out["kv_len"] = None
+    if w.kv_len_range is not None:
+        lo, hi = w.kv_len_range
+        g3 = torch.Generator().manual_seed(w.seed + 200)
+        out["kv_len"] = torch.randint(lo, hi + 1, (w.B,), generator=g3, dtype=torch.int32)
+    return out
+
+
+def random_case(B, H, N, d, seed, causal=False, kv_len_range=None, qk_gain=1.0, backward=True):
+    """An ad-hoc workload (edge-case tests) drawn with the same recipe."""
+    return Workload(f"case_b{B}_h{H}_n{N}_d{d}", B, H, N, d, causal=causal, seed=seed,
+                    backward=backward, qk_gain=qk_gain, kv_len_range=kv_len_range)

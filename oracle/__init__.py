@@ -1,0 +1,124 @@
+"""CPU fp64 oracle for exact attention.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+library under ``exact_attention_04_gb300`` never imports it, and this package
+imports nothing from that library: the two share only the seeded input
+generators, which hold none of the method's arithmetic.
+
+Two parts:
+
+* ``attn_oracle.c`` (loaded here through ctypes): the plain definition of
+  attention forward and backward, written out row by row in double precision.
+  See the header of that file for the passages it follows.
+* ``softmax_ref.py``: the pages' softmax recurrences (three-pass safe softmax,
+  the online normaliser, the one-pass softmax-times-V and the associative
+  block merge) in numpy float64, and a tiled forward built from them.
+
+Every input is float64; callers widen bf16 tensors exactly before calling.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int)
+        c_int, c_double = ctypes.c_int, ctypes.c_double
+        lib.fa_oracle_forward.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int,
+                                          c_double, c_int, ip, c_int]
+        lib.fa_oracle_forward.restype = c_int
+        lib.fa_oracle_forward_rows.argtypes = [dp, dp, dp, c_int, c_int, c_double, c_int, c_int,
+                                               ip, c_int, dp, dp, c_int]
+        lib.fa_oracle_forward_rows.restype = c_int
+        lib.fa_oracle_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int,
+                                           c_int, c_double, c_int, ip, c_int]
+        lib.fa_oracle_backward.restype = c_int
+        lib.fa_oracle_num_threads.argtypes = []
+        lib.fa_oracle_num_threads.restype = c_int
+        _lib = lib
+    return _lib
+
+
+def _f64(a):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    return a
+
+
+def _ptr(a, ctype=ctypes.c_double):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def default_threads() -> int:
+    """Threads the oracle uses by default: every host core."""
+    return max(1, os.cpu_count() or 1)
+
+
+def compiled_threads() -> int:
+    """OpenMP's own thread limit inside the library (1 when built without OpenMP)."""
+    return _load().fa_oracle_num_threads()
+
+
+def _kv(kv_len, B):
+    if kv_len is None:
+        return None, None
+    kv = np.ascontiguousarray(np.asarray(kv_len, dtype=np.int32).reshape(B))
+    return kv, _ptr(kv, ctypes.c_int)
+
+
+def attention_fwd(q, k, v, scale, causal=False, kv_len=None, threads=None):
+    """O [B,H,N,d] and LSE [B,H,N] of exact attention (float64 numpy arrays)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, N, d = q.shape
+    assert k.shape == q.shape and v.shape == q.shape
+    o = np.empty_like(q)
+    lse = np.empty((B, H, N), dtype=np.float64)
+    kv, kvp = _kv(kv_len, B)
+    rc = _load().fa_oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                   float(scale), int(bool(causal)), kvp,
+                                   threads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle forward failed ({rc})")
+    return o, lse
+
+
+def attention_fwd_rows(q, k, v, rows, scale, causal=False, kv_len=None, threads=None):
+    """Forward for selected query rows of one head; q, k, v are [N, d]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    N, d = q.shape
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+    o = np.empty((rows.size, d), dtype=np.float64)
+    lse = np.empty(rows.size, dtype=np.float64)
+    length = N if kv_len is None else int(kv_len)
+    rc = _load().fa_oracle_forward_rows(_ptr(q), _ptr(k), _ptr(v), N, d, float(scale),
+                                        int(bool(causal)), length, _ptr(rows, ctypes.c_int),
+                                        int(rows.size), _ptr(o), _ptr(lse),
+                                        threads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle forward_rows failed ({rc})")
+    return o, lse
+
+
+def attention_bwd(q, k, v, do, scale, causal=False, kv_len=None, threads=None):
+    """dQ, dK, dV [B,H,N,d] and D [B,H,N] (D_i = sum_j P_ij dP_ij)."""
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, H, N, d = q.shape
+    dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+    D = np.empty((B, H, N), dtype=np.float64)
+    kv, kvp = _kv(kv_len, B)
+    rc = _load().fa_oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), _ptr(D), B, H, N, d, float(scale),
+                                    int(bool(causal)), kvp, threads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle backward failed ({rc})")
+    return dq, dk, dv, D
