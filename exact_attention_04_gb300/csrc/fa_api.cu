@@ -1,0 +1,229 @@
+// C-ABI front end: argument validation, TMA tensor maps, the per-device
+// status word, and dispatch to the kernels.  No allocation, no
+// synchronisation (except fa_check), no host copies.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+// Written by kernels that gave up waiting; read and cleared by fa_check.
+__device__ int g_fa_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  bool supported = false;
+  int num_sms = 0;
+  int max_smem = 0;        // opt-in dynamic shared memory per block
+  int* status = nullptr;   // device address of g_fa_status on this device
+};
+
+DeviceInfo g_dev[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// Per-device facts, looked up once with that device current.
+DeviceInfo* device_info(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceInfo& di = g_dev[dev];
+  std::call_once(di.once, [&di, dev] {
+    int major = 0, minor = 0;
+    di.err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (di.err == cudaSuccess)
+      di.err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (di.err == cudaSuccess)
+      di.err = cudaDeviceGetAttribute(&di.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (di.err == cudaSuccess)
+      di.err = cudaDeviceGetAttribute(&di.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    di.supported = (major == 10 && minor == 3);
+    if (di.err == cudaSuccess && di.supported)
+      di.err = cudaGetSymbolAddress(reinterpret_cast<void**>(&di.status), g_fa_status);
+  });
+  if (dev_out) *dev_out = dev;
+  return &di;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status_t check_sizes(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  const long long elems = static_cast<long long>(B) * H * N * d;
+  if (elems >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+// bf16 [BH, N, d] as a 3-D tensor (d, N, BH): box of 64 columns x 128 rows,
+// 128-byte swizzle, rows past N read as zero.
+bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(d) * N * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t round_up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char* fa_status_string(fa_status_t s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int H, int N, int d, float scale, int causal, const int* kv_len,
+                   void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_INVALID_ARG;
+  if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+  const fa_status_t sz = check_sizes(B, H, N, d, scale);
+  if (sz != FA_OK) return sz;
+  DeviceInfo* di = device_info(nullptr);
+  if (!di || di->err != cudaSuccess) return FA_ERR_CUDA;
+  if (!di->supported) return FA_ERR_UNSUPPORTED;
+  fa::FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int BH = B * H;
+  if (!make_map(&p.tq, q, d, N, BH) || !make_map(&p.tk, k, d, N, BH) ||
+      !make_map(&p.tv, v, d, N, BH))
+    return FA_ERR_CUDA;
+  p.o = o;
+  p.lse = lse;
+  p.kv_len = kv_len;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.status = di->status;
+  if (fa::launch_fwd(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+// Workspace layout: D [B*H, Npad] fp32, L2 [B*H, Npad] fp32, dQ_acc [B*H, N, d]
+// fp32, each region starting on a 256-byte boundary (Npad = N rounded up to 128).
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (check_sizes(B, H, N, d, 1.f) != FA_OK) return 0;
+  const size_t npad = (static_cast<size_t>(N) + 127) / 128 * 128;
+  const size_t padded_rows = static_cast<size_t>(B) * H * npad;
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return 2 * round_up256(padded_rows * sizeof(float)) + round_up256(rows * d * sizeof(float));
+}
+
+fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   float scale, int causal, const int* kv_len, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_INVALID_ARG;
+  if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+  const fa_status_t sz = check_sizes(B, H, N, d, scale);
+  if (sz != FA_OK) return sz;
+  if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  DeviceInfo* di = device_info(nullptr);
+  if (!di || di->err != cudaSuccess) return FA_ERR_CUDA;
+  if (!di->supported) return FA_ERR_UNSUPPORTED;
+  fa::BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int BH = B * H;
+  if (!make_map(&p.tq, q, d, N, BH) || !make_map(&p.tk, k, d, N, BH) ||
+      !make_map(&p.tv, v, d, N, BH) || !make_map(&p.tdo, dO, d, N, BH))
+    return FA_ERR_CUDA;
+  if (d == 256) return FA_ERR_UNSUPPORTED;
+  const int npad = (N + 127) / 128 * 128;
+  const size_t stat_bytes = round_up256(static_cast<size_t>(BH) * npad * sizeof(float));
+  p.o = o;
+  p.dO = dO;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.delta = static_cast<float*>(workspace);
+  p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + stat_bytes);
+  p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * stat_bytes);
+  p.Npad = npad;
+  p.kv_len = kv_len;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.status = di->status;
+  if (fa::launch_bwd(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+fa_status_t fa_check(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceInfo* di = device_info(nullptr);
+  if (!di || di->err != cudaSuccess || !di->supported) return FA_ERR_CUDA;
+  int status = 0;
+  if (cudaMemcpyFromSymbol(&status, g_fa_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (status != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    return (status & 0xff) == fa::kStatusTimeout ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,545 @@
+// Attention forward for sm_103a.
+//
+// One CTA per SM (persistent), 192 threads in four roles:
+//   warp 0      TMA producer: Q tile once per tile, then K_j and V_j into a
+//               STAGES-deep shared-memory ring (full/empty mbarriers).
+//   warp 1      MMA issuer (one thread): S = Q K_j^T into tensor memory,
+//               then O += P_j V_j with P read from tensor memory.  Also
+//               allocates and frees the tensor memory.
+//   warps 2..5  softmax: thread r owns query row r of the tile (TMEM lane r).
+//               Reads its row of S, masks, updates the running max m and sum
+//               l, writes P = exp2(S*c - m) as bf16 into tensor memory,
+//               rescales its row of O when m moved, and runs the epilogue
+//               O / l, LSE = (m + log2 l) * ln 2.
+//
+// The recurrence is the online softmax of "注意力为什么受限于显存带宽：用算术
+// 强度与分块把 FlashAttention 推导清楚" (section 六) and "4. FlashAttention 深度
+// 剖析" (sections 4.2.3-4.2.4): S is kept in base-2 units (c = scale*log2 e
+// folded into one FMA), O~ and l share the reference maximum, and the final
+// division by l happens once (section 4.3.2; section 4.4.2 for the point of
+// dividing once).  The reference maximum is only raised when the running
+// maximum exceeds it by more than kRescaleSlack (log2 units); until then
+// P <= 2^kRescaleSlack, which bf16 and fp32 hold exactly as well, and the
+// result is the same because O~ and l are always taken against the same
+// reference.
+//
+// Loop order: outer over Q tiles, inner over key blocks (section 4.4.3);
+// key blocks entirely above the causal diagonal are never loaded (section
+// 4.3.2, last note).  Tensor memory columns: S [0,128), O [128, 128+D),
+// P double buffer [128+D, 256+D) as packed bf16 pairs (64 columns each).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;          // query rows per tile = TMEM lanes = MMA M
+constexpr int BN = 128;          // keys per block = MMA N of S
+constexpr int CHUNK = 128 * 128; // bytes of one 128-row x 64-column bf16 chunk (SW128 atom rows)
+constexpr float kRescaleSlack = 8.0f;
+constexpr int kThreads = 192;
+
+template <int D>
+struct Cfg {
+  static constexpr int NCH = D / 64;                 // 128-byte column chunks per row
+  static constexpr int TILE_BYTES = NCH * CHUNK;     // one Q tile or one K/V block
+  static constexpr int STAGES = D == 64 ? 4 : (D == 128 ? 3 : 1);
+  static constexpr uint32_t TM_S = 0;
+  static constexpr uint32_t TM_O = 128;
+  static constexpr uint32_t TM_P = 128 + D;
+  static constexpr uint32_t TM_COLS = 512;
+  static_assert(TM_P + 128 <= TM_COLS, "tensor memory budget");
+};
+
+template <int D>
+struct FwdSmem {
+  alignas(1024) uint8_t q[Cfg<D>::TILE_BYTES];
+  alignas(1024) uint8_t k[Cfg<D>::STAGES][Cfg<D>::TILE_BYTES];
+  alignas(1024) uint8_t v[Cfg<D>::STAGES][Cfg<D>::TILE_BYTES];
+  uint64_t q_full, q_empty;
+  uint64_t k_full[Cfg<D>::STAGES], k_empty[Cfg<D>::STAGES];
+  uint64_t v_full[Cfg<D>::STAGES], v_empty[Cfg<D>::STAGES];
+  uint64_t s_full, s_free;
+  uint64_t p_full[2], p_free[2];
+  uint64_t o_free;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Wait sites reported in the status word.
+enum Site {
+  kSiteProdQ = 1, kSiteProdK, kSiteProdV, kSiteMmaQ, kSiteMmaK, kSiteMmaS, kSiteMmaP, kSiteMmaV,
+  kSiteMmaO, kSiteSmS, kSiteSmP, kSiteSmO, kSiteSmEpi, kSiteDrain
+};
+
+__device__ __forceinline__ void record_failure(int* status, volatile int* abort, int site) {
+  atomicCAS(status, 0, status_code(site));
+  *abort = 1;
+}
+
+// Static persistent schedule.  Non-causal: one unit per (bh, q-tile), bh-major
+// so CTAs running at the same time share K/V in L2.  Causal: a unit pairs
+// q-tile T-1-p (longest: T-p key blocks) with q-tile p (p+1 key blocks), the
+// longest first, so every unit costs T+1 key blocks and the static
+// round-robin assignment is balanced.
+struct Sched {
+  int T, P, units, causal;
+  __device__ Sched(int BH, int N, int causal_) : causal(causal_) {
+    T = (N + BM - 1) / BM;
+    P = (T + 1) / 2;
+    units = causal ? BH * P : BH * T;
+  }
+  __device__ int ntiles(int u) const {
+    if (!causal) return 1;
+    const int p = u % P;
+    return (p == T - 1 - p) ? 1 : 2;
+  }
+  __device__ void tile(int u, int k, int& bh, int& m) const {
+    if (!causal) {
+      bh = u / T;
+      m = u % T;
+    } else {
+      bh = u / P;
+      const int p = u % P;
+      m = (k == 0) ? (T - 1 - p) : p;
+    }
+  }
+};
+
+__device__ __forceinline__ int seq_len(const FwdParams& p, int bh) {
+  int len = p.N;
+  if (p.kv_len) {
+    len = __ldg(p.kv_len + bh / p.H);
+    len = len < 0 ? 0 : (len > p.N ? p.N : len);
+  }
+  return len;
+}
+
+__device__ __forceinline__ int kv_blocks(int m, int len, int causal) {
+  int end = len;
+  if (causal && m * BM + BM < end) end = m * BM + BM;
+  return (end + BN - 1) / BN;
+}
+
+// All 32 lanes wait; the decision is made uniform across the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  bool ok = mbar_wait(bar, parity, abort, kWaitTimeoutNs);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
+  const uintptr_t aligned = (raw + 1023) & ~static_cast<uintptr_t>(1023);
+  if (aligned - raw + sizeof(FwdSmem<D>) > dynamic_smem_size()) {
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, status_code(kSiteSmemLayout));
+    return;
+  }
+  FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(aligned);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  volatile int* abort = &sm.abort;
+
+  if (threadIdx.x == 0) {
+    sm.abort = 0;
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.s_free, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.p_full[b], 4);
+      mbar_init(&sm.p_free[b], 1);
+    }
+    mbar_init(&sm.o_free, 4);
+    mbar_init(&sm.mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+  const int BH = p.B * p.H;
+  const Sched sched(BH, p.N, p.causal);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tq);
+      prefetch_tmap(&p.tk);
+      prefetch_tmap(&p.tv);
+      uint32_t q_it = 0, k_it = 0, v_it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+        for (int kt = 0; ok && kt < sched.ntiles(u); ++kt) {
+          int bh, m;
+          sched.tile(u, kt, bh, m);
+          const int nkv = kv_blocks(m, seq_len(p, bh), p.causal);
+          if (nkv == 0) continue;
+          if (!mbar_wait(&sm.q_empty, (q_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+            record_failure(p.status, abort, kSiteProdQ);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.q_full, C::TILE_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(sm.q + c * CHUNK, &p.tq, &sm.q_full, 64 * c, m * BM, bh);
+          ++q_it;
+          for (int j = 0; j < nkv; ++j) {
+            const int st = k_it % C::STAGES;
+            const uint32_t ph = (k_it / C::STAGES) & 1;
+            if (!mbar_wait(&sm.k_empty[st], ph ^ 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteProdK);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.k_full[st], C::TILE_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c)
+              tma_load_3d(sm.k[st] + c * CHUNK, &p.tk, &sm.k_full[st], 64 * c, j * BN, bh);
+            ++k_it;
+            if (!mbar_wait(&sm.v_empty[st], ph ^ 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteProdV);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.v_full[st], C::TILE_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c)
+              tma_load_3d(sm.v[st] + c * CHUNK, &p.tv, &sm.v_full[st], 64 * c, j * BN, bh);
+            ++v_it;
+          }
+        }
+      }
+      // No copy may still be landing in shared memory when the CTA exits:
+      // wait (bounded, ignoring the abort flag) for the last phase issued on
+      // every full barrier.  In a normal run these phases completed long ago.
+      if (q_it > 0 && !mbar_wait(&sm.q_full, (q_it - 1) & 1, nullptr, kWaitTimeoutNs))
+        record_failure(p.status, abort, kSiteDrain);
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (k_it > static_cast<uint32_t>(s)) {
+          const uint32_t n = (k_it - 1 - s) / C::STAGES;
+          if (!mbar_wait(&sm.k_full[s], n & 1, nullptr, kWaitTimeoutNs))
+            record_failure(p.status, abort, kSiteDrain);
+        }
+        if (v_it > static_cast<uint32_t>(s)) {
+          const uint32_t n = (v_it - 1 - s) / C::STAGES;
+          if (!mbar_wait(&sm.v_full[s], n & 1, nullptr, kWaitTimeoutNs))
+            record_failure(p.status, abort, kSiteDrain);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, 0, 0);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 0, 1);
+      const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q), 16, 1024);
+      uint32_t q_it = 0, kv_it = 0, t_it = 0;
+      bool ok = true;
+      // O += P_i V_i for global block index i; `first` starts a new accumulation.
+      auto issue_pv = [&](uint32_t i, bool first) -> bool {
+        const uint32_t b = i & 1;
+        if (!mbar_wait(&sm.p_full[b], (i >> 1) & 1, abort, kWaitTimeoutNs)) {
+          record_failure(p.status, abort, kSiteMmaP);
+          return false;
+        }
+        const int st = i % C::STAGES;
+        if (!mbar_wait(&sm.v_full[st], (i / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+          record_failure(p.status, abort, kSiteMmaV);
+          return false;
+        }
+        if (first && !mbar_wait(&sm.o_free, (t_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+          record_failure(p.status, abort, kSiteMmaO);
+          return false;
+        }
+        tc_fence_after_sync();
+        // V block: BN rows (keys) x D columns, MN-major B operand: 64-column
+        // chunks BN*128 bytes apart (LBO), 8-key groups 1024 bytes apart (SBO).
+        const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), BN * 128, 1024);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          mma_bf16_ts(tmem + C::TM_O, tmem + C::TM_P + 64 * b + kk * 8,
+                      dv0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescPV,
+                      (first && kk == 0) ? 0u : 1u);
+        }
+        mma_commit(&sm.v_empty[st]);
+        mma_commit(&sm.p_free[b]);
+        return true;
+      };
+      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+        for (int kt = 0; ok && kt < sched.ntiles(u); ++kt) {
+          int bh, m;
+          sched.tile(u, kt, bh, m);
+          const int nkv = kv_blocks(m, seq_len(p, bh), p.causal);
+          if (nkv == 0) continue;
+          if (!mbar_wait(&sm.q_full, q_it & 1, abort, kWaitTimeoutNs)) {
+            record_failure(p.status, abort, kSiteMmaQ);
+            ok = false;
+            break;
+          }
+          ++q_it;
+          for (int j = 0; j < nkv; ++j) {
+            const int st = kv_it % C::STAGES;
+            if (!mbar_wait(&sm.k_full[st], (kv_it / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteMmaK);
+              ok = false;
+              break;
+            }
+            if (!mbar_wait(&sm.s_free, (kv_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteMmaS);
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[st]), 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
+              mma_bf16_ss(tmem + C::TM_S, dq0 + (off >> 4), dk0 + (off >> 4), kIdescS,
+                          kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&sm.k_empty[st]);
+            mma_commit(&sm.s_full);
+            if (j == nkv - 1) mma_commit(&sm.q_empty);
+            if (j > 0 && !issue_pv(kv_it - 1, j == 1)) {
+              ok = false;
+              break;
+            }
+            ++kv_it;
+          }
+          if (!ok) break;
+          if (!issue_pv(kv_it - 1, nkv == 1)) {
+            ok = false;
+            break;
+          }
+          ++t_it;
+        }
+      }
+      // Every tcgen05 op issued above must finish before tensor memory is freed.
+      mma_commit(&sm.mma_done);
+      if (!mbar_wait(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
+        record_failure(p.status, abort, kSiteDrain);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
+    const int row_local = quarter * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float c2 = p.scale_log2;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o);
+    uint32_t kv_it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+      for (int kt = 0; ok && kt < sched.ntiles(u); ++kt) {
+        int bh, m;
+        sched.tile(u, kt, bh, m);
+        const int len = seq_len(p, bh);
+        const int nkv = kv_blocks(m, len, p.causal);
+        const int row = m * BM + row_local;
+        const size_t row_off = static_cast<size_t>(bh) * p.N + row;
+        if (nkv == 0) {
+          if (row < p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(out + row_off * D);
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+            p.lse[row_off] = -INFINITY;
+          }
+          continue;
+        }
+        float m_ref = -INFINITY;    // reference maximum, base-2 units of S*scale
+        float l = 0.f;
+        for (int j = 0; j < nkv; ++j) {
+          if (!warp_wait(&sm.s_full, kv_it & 1, abort)) {
+            if (lane == 0) record_failure(p.status, abort, kSiteSmS);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          uint32_t sr[BN];
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) tmem_ld_x32(t_lane + C::TM_S + 32 * c, sr + 32 * c);
+          tmem_wait_ld();
+          reg_fence<BN>(sr);
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.s_free);
+          float s[BN];
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
+          // masks: keys past the sequence (tail / padding) and above the diagonal
+          const int key0 = j * BN;
+          if (key0 + BN > len || (p.causal && key0 + BN - 1 > m * BM)) {
+            const int lim_pad = len - key0;                     // c >= lim_pad: past the sequence
+            const int lim_causal = p.causal ? row - key0 : BN;  // c > lim_causal: above the diagonal
+#pragma unroll
+            for (int c = 0; c < BN; ++c)
+              if (c >= lim_pad || c > lim_causal) s[c] = -INFINITY;
+          }
+          float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+          for (int c = 4; c < BN; c += 4) {
+            mx0 = fmaxf(mx0, s[c]);
+            mx1 = fmaxf(mx1, s[c + 1]);
+            mx2 = fmaxf(mx2, s[c + 2]);
+            mx3 = fmaxf(mx3, s[c + 3]);
+          }
+          const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
+          float alpha = 1.f;
+          bool rescale = false;
+          if (m_ref == -INFINITY) {
+            if (m_blk != -INFINITY) {
+              alpha = 0.f;
+              m_ref = m_blk;
+            }
+          } else if (m_blk > m_ref + kRescaleSlack) {
+            alpha = ex2_approx(m_ref - m_blk);
+            m_ref = m_blk;
+            rescale = true;
+          }
+          const float base = (m_ref == -INFINITY) ? 0.f : m_ref;
+          float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+          uint32_t pk[BN / 2];
+#pragma unroll
+          for (int c = 0; c < BN / 2; c += 2) {
+            const float p0 = ex2_approx(fmaf(s[2 * c], c2, -base));
+            const float p1 = ex2_approx(fmaf(s[2 * c + 1], c2, -base));
+            const float p2 = ex2_approx(fmaf(s[2 * c + 2], c2, -base));
+            const float p3 = ex2_approx(fmaf(s[2 * c + 3], c2, -base));
+            rs0 += p0;
+            rs1 += p1;
+            rs2 += p2;
+            rs3 += p3;
+            pk[c] = pack_bf16x2(p0, p1);
+            pk[c + 1] = pack_bf16x2(p2, p3);
+          }
+          l = l * alpha + ((rs0 + rs1) + (rs2 + rs3));
+          const uint32_t b = kv_it & 1;
+          if (!warp_wait(&sm.p_free[b], ((kv_it >> 1) & 1) ^ 1, abort)) {
+            if (lane == 0) record_failure(p.status, abort, kSiteSmP);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          tmem_st_x32(t_lane + C::TM_P + 64 * b, pk);
+          tmem_st_x32(t_lane + C::TM_P + 64 * b + 32, pk + 32);
+          if (__any_sync(0xffffffffu, rescale && j > 0)) {
+            // O must hold every earlier P V before it is scaled: wait for the
+            // previous block's P V to complete.
+            const uint32_t prev = kv_it - 1;
+            if (!warp_wait(&sm.p_free[prev & 1], (prev >> 1) & 1, abort)) {
+              if (lane == 0) record_failure(p.status, abort, kSiteSmO);
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t orr[32];
+              tmem_ld_x32(t_lane + C::TM_O + 32 * c, orr);
+              tmem_wait_ld();
+              reg_fence<32>(orr);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+              tmem_st_x32(t_lane + C::TM_O + 32 * c, orr);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.p_full[b]);
+          ++kv_it;
+        }
+        if (!ok) break;
+        // epilogue: wait for the tile's last P V, then O / l and LSE
+        const uint32_t last = kv_it - 1;
+        if (!warp_wait(&sm.p_free[last & 1], (last >> 1) & 1, abort)) {
+          if (lane == 0) record_failure(p.status, abort, kSiteSmEpi);
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld_x32(t_lane + C::TM_O + 32 * c, orr);
+          tmem_wait_ld();
+          reg_fence<32>(orr);
+          if (row < p.N) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              packed[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
+                                      __uint_as_float(orr[2 * i + 1]) * inv_l);
+            uint4* dst = reinterpret_cast<uint4*>(out + row_off * D + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                  packed[4 * i + 3]);
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.o_free);
+        if (row < p.N)
+          p.lse[row_off] = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, Cfg<D>::TM_COLS);
+  }
+}
+
+template <int D>
+cudaError_t launch(const FwdParams& p, int num_sms, int max_smem, cudaStream_t stream) {
+  const size_t smem = smem_request(sizeof(FwdSmem<D>), max_smem);
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int T = (p.N + BM - 1) / BM;
+  const long long units = p.causal ? static_cast<long long>(p.B) * p.H * ((T + 1) / 2)
+                                   : static_cast<long long>(p.B) * p.H * T;
+  const int grid = static_cast<int>(units < num_sms ? units : num_sms);
+  fa_fwd_kernel<D><<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdParams& p, int d, int num_sms, int max_smem, cudaStream_t stream) {
+  switch (d) {
+    case 64: return launch<64>(p, num_sms, max_smem, stream);
+    case 128: return launch<128>(p, num_sms, max_smem, stream);
+    case 256: return launch<256>(p, num_sms, max_smem, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,64 @@
+// Internal interface between the C-ABI front end (fa_api.cu) and the kernel
+// translation units.  Not installed; not part of the public header.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Device status word values written by kernels that gave up waiting:
+// low byte FA_ERR_TIMEOUT (4), the rest identifies the wait site.
+constexpr int kStatusTimeout = 4;
+__host__ __device__ constexpr int status_code(int site) { return kStatusTimeout | (site << 8); }
+
+// Kernels give up on any single wait after this much global time.
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+struct FwdParams {
+  CUtensorMap tq, tk, tv;      // bf16 [BH, N, d] viewed as 3-D (d, N, BH), box (64, 128, 1), SW128
+  void* o;                     // bf16 [B, H, N, d]
+  float* lse;                  // fp32 [B, H, N]
+  const int* kv_len;           // int32 [B] or nullptr
+  int B, H, N;
+  int causal;
+  float scale_log2;            // scale * log2(e)
+  int* status;                 // device status word
+};
+
+struct BwdParams {
+  CUtensorMap tq, tk, tv, tdo; // bf16 [BH, N, d] as above
+  const void* o;               // bf16 [B, H, N, d]
+  const void* dO;              // bf16 [B, H, N, d]
+  const float* lse;            // fp32 [B, H, N]
+  void* dq;                    // bf16 [B, H, N, d]
+  void* dk;                    // bf16
+  void* dv;                    // bf16
+  float* delta;                // fp32 [B*H, Npad] workspace: D = rowsum(dO o O), 0 past N
+  float* lse2;                 // fp32 [B*H, Npad] workspace: LSE * log2(e), +inf past N
+  float* dq_acc;               // fp32 [B, H, N, d] workspace
+  const int* kv_len;
+  int B, H, N;
+  int Npad;                    // N rounded up to a multiple of 128
+  int causal;
+  float scale;
+  float scale_log2;
+  int* status;
+};
+
+// Wait site recorded when the dynamic shared memory cannot hold the kernel's
+// layout at a 1024-byte aligned base.
+constexpr int kSiteSmemLayout = 99;
+
+// Dynamic shared memory to request for a layout of `bytes` that must start on
+// a 1024-byte boundary: up to 1 KB of slack, never above the per-block limit.
+inline size_t smem_request(size_t bytes, int max_optin) {
+  const size_t room = static_cast<size_t>(max_optin) > bytes ? max_optin - bytes : 0;
+  return bytes + (room < 1024 ? room : 1024);
+}
+
+cudaError_t launch_fwd(const FwdParams& p, int d, int num_sms, int max_smem, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdParams& p, int d, int num_sms, int max_smem, cudaStream_t stream);
+
+}  // namespace fa

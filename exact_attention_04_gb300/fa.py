@@ -1,0 +1,169 @@
+"""Python binding of libfa.so: argument marshalling only.
+
+The functions named like the C ABI (``fa_fwd``, ``fa_bwd``, ...) take torch
+tensors that already live on the GPU, check dtype / shape / contiguity, and
+pass raw device pointers and the current CUDA stream to the library.  Every
+step of the computation runs in the library's kernels; there is no fallback.
+If libfa.so is missing or cannot be loaded the call raises.
+
+``forward`` and ``backward`` are conveniences that allocate the outputs (and
+the backward workspace) with torch before calling the C ABI.
+"""
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa.so")
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {fa_status_string(status)}")
+
+
+def load():
+    """Open libfa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m exact_attention_04_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp]
+        lib.fa_fwd.restype = i
+        lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+        lib.fa_bwd_workspace_bytes.restype = sz
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
+        lib.fa_bwd.restype = i
+        lib.fa_check.argtypes = [vp]
+        lib.fa_check.restype = i
+        lib.fa_status_string.argtypes = [i]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = i
+        _lib = lib
+    return _lib
+
+
+EXPORTS = ("fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_check", "fa_status_string",
+           "fa_version")
+
+
+def fa_status_string(status: int) -> str:
+    return load().fa_status_string(int(status)).decode()
+
+
+def fa_version() -> int:
+    return load().fa_version()
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _check_qkv(name, t, shape=None):
+    if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+        raise ValueError(f"{name}: expected a contiguous bf16 CUDA tensor [B,H,N,d]")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+
+
+def _check_kv_len(kv_len, B):
+    if kv_len is None:
+        return None
+    if not kv_len.is_cuda or kv_len.dtype != torch.int32 or kv_len.numel() != B \
+            or not kv_len.is_contiguous():
+        raise ValueError("kv_len: expected a contiguous int32 CUDA tensor of length B")
+    return kv_len
+
+
+def _raise(status, where):
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def fa_fwd(q, k, v, o, lse, scale, causal=False, kv_len=None, stream=None):
+    """Calls fa_fwd; q, k, v, o bf16 [B,H,N,d] and lse fp32 [B,H,N] on the GPU."""
+    _check_qkv("q", q)
+    B, H, N, d = q.shape
+    _check_qkv("k", k, q.shape)
+    _check_qkv("v", v, q.shape)
+    _check_qkv("o", o, q.shape)
+    if lse.dtype != torch.float32 or not lse.is_cuda or tuple(lse.shape) != (B, H, N) \
+            or not lse.is_contiguous():
+        raise ValueError("lse: expected a contiguous fp32 CUDA tensor [B,H,N]")
+    kv_len = _check_kv_len(kv_len, B)
+    st = load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
+                       int(bool(causal)), _ptr(kv_len), _stream_ptr(stream))
+    _raise(st, "fa_fwd")
+
+
+def fa_bwd_workspace_bytes(B, H, N, d) -> int:
+    return int(load().fa_bwd_workspace_bytes(B, H, N, d))
+
+
+def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, kv_len=None, workspace=None,
+           stream=None):
+    """Calls fa_bwd; workspace is a uint8 CUDA tensor of fa_bwd_workspace_bytes()."""
+    _check_qkv("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, q.shape)
+    if lse.dtype != torch.float32 or not lse.is_cuda or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse: expected fp32 CUDA tensor [B,H,N]")
+    kv_len = _check_kv_len(kv_len, B)
+    if workspace is None or not workspace.is_cuda:
+        raise ValueError("workspace: expected a CUDA tensor")
+    nbytes = workspace.numel() * workspace.element_size()
+    st = load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                       _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                       _ptr(kv_len), _ptr(workspace), nbytes, _stream_ptr(stream))
+    _raise(st, "fa_bwd")
+
+
+def fa_check(stream=None):
+    """Waits for the stream; raises FAError if a kernel timed out or failed."""
+    _raise(load().fa_check(_stream_ptr(stream)), "fa_check")
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)
+
+
+def forward(q, k, v, scale=None, causal=False, kv_len=None, stream=None):
+    """(O, LSE) with outputs allocated by torch on q's device."""
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, default_scale(d) if scale is None else scale, causal, kv_len, stream)
+    return o, lse
+
+
+def workspace(B, H, N, d, device):
+    return torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=device)
+
+
+def backward(q, k, v, o, lse, do, scale=None, causal=False, kv_len=None, ws=None, stream=None):
+    """(dQ, dK, dV) with outputs (and, if not given, the workspace) allocated by torch."""
+    B, H, N, d = q.shape
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    if ws is None:
+        ws = workspace(B, H, N, d, q.device)
+    fa_bwd(q, k, v, o, do, lse, dq, dk, dv, default_scale(d) if scale is None else scale,
+           causal, kv_len, ws, stream)
+    return dq, dk, dv

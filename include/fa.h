@@ -1,0 +1,113 @@
+/*
+ * fa.h - exact scaled-dot-product attention for one NVIDIA GB300 (sm_103a).
+ *
+ * O = softmax(scale * Q K^T [+ mask]) V, computed FlashAttention-style: the
+ * N x N score matrix S and probability matrix P never reach device memory.
+ * The forward keeps a running row maximum m, row sum l and unnormalised
+ * output O~ per query row and updates them block by block with the online
+ * softmax recurrence ("注意力为什么受限于显存带宽：用算术强度与分块把
+ * FlashAttention 推导清楚", section 六; "4. FlashAttention 深度剖析",
+ * sections 4.2.2-4.2.4 and 4.3.2); it saves the per-row log-sum-exp
+ * L = m + log l, from which the backward recomputes P (same pages, section
+ * 八 and section 4.3.4).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Tensors are caller-owned DEVICE memory.  Q, K, V, O, dO, dQ, dK, dV are
+ *   bf16 (__nv_bfloat16 bit patterns), contiguous [B, H, N, d] (d fastest),
+ *   each base address 16-byte aligned.  LSE is fp32 [B, H, N].
+ * - Supported head dimensions: d = 64, 128, 256.  B, H, N >= 1 and
+ *   B*H*N*d < 2^31 elements per tensor.
+ * - scale multiplies Q K^T; it must be finite and > 0 (1/sqrt(d) is usual).
+ * - causal != 0 masks key j for query i when j > i (0-based; N queries and
+ *   N keys).
+ * - kv_len is NULL (no padding) or a DEVICE pointer to int32[B]: keys
+ *   j >= kv_len[b] are masked for every query of batch b.  Values are
+ *   clamped to [0, N]; a query row that sees no key at all gets O = 0 and
+ *   LSE = -inf (its gradients are 0).
+ * - stream is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream).  Every call only enqueues work and returns; nothing here
+ *   synchronises except fa_check().  The library never allocates memory.
+ * - Outputs are fully overwritten.
+ * - Errors: FA_ERR_INVALID_ARG (null or misaligned pointer, bad size,
+ *   scale not finite or <= 0, workspace too small), FA_ERR_UNSUPPORTED (head
+ *   dimension, or a GPU that is not sm_103), FA_ERR_CUDA (a CUDA call or
+ *   kernel launch failed; cudaGetLastError() holds the detail).  Argument
+ *   errors are reported before anything is enqueued.
+ * - Kernels never spin forever: every wait inside them gives up after about
+ *   two seconds, records FA_ERR_TIMEOUT in a per-device status word and
+ *   returns; fa_check() reports and clears it.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,
+  FA_ERR_UNSUPPORTED = 2,
+  FA_ERR_CUDA = 3,
+  FA_ERR_TIMEOUT = 4
+} fa_status_t;
+
+/*
+ * Forward.  Writes O = softmax(scale*QK^T + mask) V (bf16 [B,H,N,d]) and
+ * LSE_i = ln sum_j exp(scale*q_i.k_j) over the visible keys (fp32 [B,H,N],
+ * natural log, the statistic L = m + log l of "4. FlashAttention 深度剖析"
+ * section 4.3.2).  Tiling and the online update follow section 4.3.2 of
+ * that page with the loop order "outer over Q tiles" of its section 4.4.3;
+ * key blocks entirely above the causal diagonal are skipped (section 4.3.2,
+ * last note).
+ */
+fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int N, int d, float scale, int causal,
+                   const int* kv_len, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for these sizes: the fp32 row
+ * statistic D = rowsum(dO o O) [B,H,N] and the fp32 dQ accumulator
+ * [B,H,N,d], each rounded up to 256 bytes.  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward by recomputation ("注意力为什么受限于显存带宽…" section 八;
+ * "4. FlashAttention 深度剖析" section 4.3.4): P is rebuilt on chip from
+ * Q, K and the saved LSE (P_ij = exp(scale*q_i.k_j - LSE_i)); then
+ *   D = rowsum(dO o O),  dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),
+ *   dQ = scale * dS K,   dK = scale * dS^T Q.
+ * Inputs q, k, v, o, dO (bf16 [B,H,N,d]) and lse (fp32 [B,H,N], as written
+ * by fa_fwd with the same scale, causal and kv_len).  Outputs dq, dk, dv
+ * (bf16 [B,H,N,d]).  workspace: caller-owned device memory of at least
+ * fa_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte aligned; its contents on
+ * entry do not matter and on return are unspecified.  dQ is accumulated in
+ * fp32 with atomic adds, so its last bits can differ from run to run.
+ */
+fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                   const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                   int B, int H, int N, int d, float scale, int causal, const int* kv_len,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Waits for `stream`, then reads and clears the current device's status
+ * word.  FA_ERR_TIMEOUT if a kernel gave up waiting since the last check,
+ * FA_ERR_CUDA if the stream reports an error, FA_OK otherwise.
+ */
+fa_status_t fa_check(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status_t status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,105 @@
+"""Host-side checks of the C-ABI library (no GPU needed).
+
+The library must load, export every function include/fa.h declares, and
+reject bad arguments with the documented status codes before touching the
+device.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_04_gb300 import build as fabuild
+from exact_attention_04_gb300 import fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fabuild.build()
+    return fa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_check",
+                     "fa_status_string", "fa_version"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(fa.EXPORTS)
+
+
+def test_status_strings_and_version(lib):
+    assert fa.fa_status_string(fa.FA_OK) == "FA_OK"
+    assert fa.fa_status_string(fa.FA_ERR_TIMEOUT) == "FA_ERR_TIMEOUT"
+    assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"
+    assert fa.fa_version() >= 10000
+
+
+def test_workspace_bytes(lib):
+    B, H, N, d = 2, 3, 200, 64
+    npad = 256
+    stat = -(-B * H * npad * 4 // 256) * 256
+    acc = -(-B * H * N * d * 4 // 256) * 256
+    assert fa.fa_bwd_workspace_bytes(B, H, N, d) == 2 * stat + acc
+    assert fa.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
+    assert fa.fa_bwd_workspace_bytes(1, 1, 1, 96) == 0
+
+
+P = ctypes.c_void_p
+
+
+def fwd(lib, q=0x1000, k=0x1000, v=0x1000, o=0x1000, lse=0x1000, B=1, H=1, N=128, d=64,
+        scale=0.125, causal=0, kv=None):
+    return lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, N, d, scale, causal,
+                      P(kv) if kv else None, None)
+
+
+def test_forward_argument_errors(lib):
+    assert fwd(lib, q=0) == fa.FA_ERR_INVALID_ARG             # null pointer
+    assert fwd(lib, o=0x1008) == fa.FA_ERR_INVALID_ARG        # misaligned output
+    assert fwd(lib, lse=0x1002) == fa.FA_ERR_INVALID_ARG      # misaligned lse
+    assert fwd(lib, kv=0x1001) == fa.FA_ERR_INVALID_ARG       # misaligned kv_len
+    assert fwd(lib, N=0) == fa.FA_ERR_INVALID_ARG
+    assert fwd(lib, B=-1) == fa.FA_ERR_INVALID_ARG
+    assert fwd(lib, scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert fwd(lib, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert fwd(lib, scale=float("inf")) == fa.FA_ERR_INVALID_ARG
+    assert fwd(lib, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert fwd(lib, d=32) == fa.FA_ERR_UNSUPPORTED
+    assert fwd(lib, B=1 << 14, H=1 << 10, N=1 << 10, d=64) == fa.FA_ERR_INVALID_ARG  # 2^31 elements
+
+
+def test_backward_argument_errors(lib):
+    ok = 0x1000
+
+    def bwd(ws=ok, ws_bytes=1 << 40, d=64, dq=ok, scale=0.125):
+        return lib.fa_bwd(P(ok), P(ok), P(ok), P(ok), P(ok), P(ok), P(dq), P(ok), P(ok), 1, 1, 128,
+                          d, scale, 0, None, P(ws), ws_bytes, None)
+    assert bwd(dq=0) == fa.FA_ERR_INVALID_ARG
+    assert bwd(ws=0) == fa.FA_ERR_INVALID_ARG
+    assert bwd(ws=0x1010) == fa.FA_ERR_INVALID_ARG            # workspace must be 256-aligned
+    assert bwd(ws_bytes=16) == fa.FA_ERR_INVALID_ARG          # too small
+    assert bwd(d=80) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(scale=-1.0) == fa.FA_ERR_INVALID_ARG
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    lse = torch.zeros(1, 1, 128)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(q, q, q, q, lse, 0.125)

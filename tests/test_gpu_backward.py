@@ -1,0 +1,93 @@
+"""Backward parity on the GPU: dQ, dK, dV of libfa.so against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_04_gb300 import build as fabuild
+from exact_attention_04_gb300 import fa
+from exact_attention_04_gb300.workloads import WORKLOADS, make_inputs, random_case
+
+import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fabuild.build()
+    fa.load()
+
+
+SMALL = [
+    (1, 1, 128, 64, False, None),
+    (2, 2, 383, 64, False, None),
+    (2, 2, 383, 64, True, None),
+    (1, 2, 129, 128, False, None),
+    (2, 1, 300, 128, True, None),
+    (3, 1, 333, 64, False, (1, 333)),
+    (3, 2, 257, 128, True, (100, 257)),
+    (1, 1, 1, 64, True, None),
+    (1, 2, 17, 128, False, None),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,kv", SMALL)
+def test_backward_small_full_oracle(B, H, N, d, causal, kv):
+    w = random_case(B, H, N, d, seed=N * 3 + d, causal=causal, kv_len_range=kv)
+    inp = make_inputs(w)
+    g, o, lse = P.gpu_forward(w, inp)
+    grads = P.gpu_backward(w, g, o, lse)
+    P.compare_backward(w, inp, grads)
+
+
+def test_backward_padded_keys_have_zero_gradient():
+    w = random_case(2, 2, 300, 64, seed=5, causal=False, kv_len_range=(90, 200))
+    inp = make_inputs(w)
+    g, o, lse = P.gpu_forward(w, inp)
+    dq, dk, dv = P.gpu_backward(w, g, o, lse)
+    for b in range(w.B):
+        n = int(inp["kv_len"][b])
+        assert torch.count_nonzero(dk[b, :, n:]) == 0
+        assert torch.count_nonzero(dv[b, :, n:]) == 0
+
+
+def test_backward_key_gradients_sum_to_zero():
+    """Rows of dS sum to zero, so sum_j dK_j = 0 per head (up to bf16 rounding)."""
+    w = random_case(1, 2, 512, 128, seed=9, causal=True)
+    inp = make_inputs(w)
+    g, o, lse = P.gpu_forward(w, inp)
+    dq, dk, dv = P.gpu_backward(w, g, o, lse)
+    s = dk.float().sum(dim=2).abs().max().item()
+    assert s <= 2e-2 * dk.float().abs().max().item() * 8
+
+
+def test_bert_large_config_backward_sampled_heads():
+    w = WORKLOADS["bert_large_b16_h16_n512_d64_pad"]
+    inp = make_inputs(w)
+    g, o, lse = P.gpu_forward(w, inp)
+    grads = P.gpu_backward(w, g, o, lse)
+    errs = P.compare_backward(w, inp, grads, P.sample_heads(w.B, w.H, 6))
+    print(f"{w.name}: rel errs dQ dK dV = {errs}")
+
+
+def test_gpt2_config_backward_sampled_heads():
+    w = WORKLOADS["gpt2_small_b8_h12_n1024_d64_causal"]
+    inp = make_inputs(w)
+    g, o, lse = P.gpu_forward(w, inp)
+    grads = P.gpu_backward(w, g, o, lse)
+    errs = P.compare_backward(w, inp, grads, P.sample_heads(w.B, w.H, 4))
+    print(f"{w.name}: rel errs dQ dK dV = {errs}")
+
+
+def test_large_head_d128_config_backward_sampled_heads():
+    w = WORKLOADS["large_head_b2_h16_n8192_d128_causal"]
+    inp = make_inputs(w)
+    g, o, lse = P.gpu_forward(w, inp)
+    grads = P.gpu_backward(w, g, o, lse)
+    errs = P.compare_backward(w, inp, grads, [(0, 0), (1, 15)])
+    print(f"{w.name}: rel errs dQ dK dV = {errs}")
+
+
+def test_status_clean_after_runs():
+    fa.fa_check()

@@ -1,0 +1,121 @@
+"""Forward parity on the GPU: libfa.so against the fp64 oracle, same inputs."""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_04_gb300 import build as fabuild
+from exact_attention_04_gb300 import fa
+from exact_attention_04_gb300.workloads import WORKLOADS, make_inputs, random_case
+
+import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fabuild.build()
+    fa.load()
+
+
+SMALL = [
+    # B, H, N, d, causal, kv_len range
+    (1, 1, 128, 64, False, None),
+    (2, 3, 383, 64, False, None),         # ragged tail, several tiles
+    (2, 2, 383, 64, True, None),
+    (1, 2, 129, 128, False, None),        # one row past a tile
+    (2, 2, 300, 128, True, None),
+    (3, 1, 333, 128, False, (1, 333)),    # key padding incl. very short rows
+    (3, 2, 257, 64, True, (100, 257)),    # padding and causal together
+    (1, 2, 17, 128, True, None),
+    (1, 1, 1, 64, False, None),           # a single key
+    (2, 1, 640, 256, False, None),
+    (1, 2, 200, 256, True, None),
+    (2, 1, 260, 256, False, (130, 260)),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,kv", SMALL)
+def test_forward_small_full_oracle(B, H, N, d, causal, kv):
+    w = random_case(B, H, N, d, seed=N + d, causal=causal, kv_len_range=kv, backward=False)
+    inp = make_inputs(w)
+    _, o, lse = P.gpu_forward(w, inp)
+    P.compare_forward_full(w, inp, o, lse)
+
+
+def test_single_head_config_exactly():
+    w = WORKLOADS["single_head_b1_h1_n256_d64"]
+    inp = make_inputs(w)
+    _, o, lse = P.gpu_forward(w, inp)
+    eo, el = P.compare_forward_full(w, inp, o, lse)
+    print(f"{w.name}: max|dO|={eo:.3e} max|dLSE|={el:.3e}")
+
+
+def test_forward_is_deterministic():
+    w = random_case(2, 2, 500, 128, seed=7, causal=True, backward=False)
+    g = P.to_gpu(make_inputs(w))
+    o1, l1 = fa.forward(g["q"], g["k"], g["v"], causal=True)
+    o2, l2 = fa.forward(g["q"], g["k"], g["v"], causal=True)
+    fa.fa_check()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_identical_keys_give_mean_of_values(d):
+    """Closed form: with every key equal, P is uniform over the visible keys."""
+    B, H, N = 1, 2, 300
+    w = random_case(B, H, N, d, seed=3, causal=True, backward=False)
+    inp = make_inputs(w)
+    inp["k"] = inp["k"][:, :, :1].expand(B, H, N, d).contiguous()
+    g, o, lse = P.gpu_forward(w, inp)
+    v = P.f64(inp["v"])
+    ref = np.cumsum(v, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+    P.check_o(P.f64(o), ref, "identical keys")
+
+
+def test_large_scores_stress_max_subtraction():
+    """Scores of magnitude ~1e3 would overflow exp without the max subtraction."""
+    w = random_case(1, 2, 256, 128, seed=11, causal=False, qk_gain=12.0, backward=False)
+    inp = make_inputs(w)
+    _, o, lse = P.gpu_forward(w, inp)
+    assert torch.isfinite(o.float()).all()
+    P.compare_forward_full(w, inp, o, lse)
+
+
+def test_bert_large_config_forward_sampled_heads():
+    w = WORKLOADS["bert_large_b16_h16_n512_d64_pad"]
+    inp = make_inputs(w)
+    _, o, lse = P.gpu_forward(w, inp)
+    P.compare_forward_full(w, inp, o, lse, P.sample_heads(w.B, w.H, 8))
+
+
+def test_gpt2_config_forward_sampled_heads():
+    w = WORKLOADS["gpt2_small_b8_h12_n1024_d64_causal"]
+    inp = make_inputs(w)
+    _, o, lse = P.gpu_forward(w, inp)
+    P.compare_forward_full(w, inp, o, lse, P.sample_heads(w.B, w.H, 6))
+
+
+LONG = [n for n in WORKLOADS if n.startswith("long_seq")]
+
+
+@pytest.mark.parametrize("name", LONG)
+def test_long_sequence_configs_sampled_rows(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, with_grad_out=False)
+    _, o, lse = P.gpu_forward(w, inp)
+    P.compare_forward_rows(w, inp, o, lse, P.sample_heads(w.B, w.H, 4), P.sample_rows(w.N, 40))
+
+
+@pytest.mark.parametrize("name", ["large_head_b2_h16_n8192_d128_causal",
+                                  "large_head_b2_h16_n8192_d256_causal"])
+def test_large_head_configs_forward_sampled_rows(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, with_grad_out=False)
+    _, o, lse = P.gpu_forward(w, inp)
+    P.compare_forward_rows(w, inp, o, lse, P.sample_heads(w.B, w.H, 4), P.sample_rows(w.N, 40))
+
+
+def test_status_clean_after_runs():
+    fa.fa_check()
