@@ -1,0 +1,488 @@
+#!/usr/bin/env python3
+"""Attention forward+backward throughput on one GB300, as TFLOP/s and as a
+fraction of the dense-bf16 roofline.
+
+One step = the whole path on one batch already resident in device memory:
+fa_fwd, then the backward as its three launches (fa_bwd_prep, fa_bwd_dkdv,
+fa_bwd_dq).  FLOPs per the usual convention: forward 4*B*H*N^2*d, backward
+2.5x forward, both halved under the causal mask.
+
+Default workload: B=2, H=16, N=8192, d=128, causal, Q/K scaled by 3 (the
+large-head-dimension training step); its inputs (4 x 64 MiB) are larger than
+L2, so no flush is needed between steps.  A vs-N sweep over the other
+workloads (forward, or forward+backward where they have one) follows, each
+with an L2 flush between timed iterations.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs the same per-GPU workload (weak scaling, no
+data-path collective); rank 0 prints one JSON line.
+"""
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from exact_attention_04_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s on 1 GB300 and % of dense-BF16 roofline vs N"
+HEADLINE = "large_head_b2_h16_n8192_d128_causal"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ["fa_fwd.cu", "sm103_ptx.cuh"],
+    "bwd_main_kernel": ["fa_bwd.cu", "sm103_ptx.cuh"],
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        t = torch.tensor([x], dtype=torch.float64,
+                         device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {k: float(pk[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(kernel):
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES.get(kernel, []):
+        with open(os.path.join(ROOT, "exact_attention_04_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it still
+    describes the current source of that kernel on this workload."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            entries = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for e in entries:
+        if e.get("kernel") == kernel and e.get("workload") == workload \
+                and e.get("source_sha") == source_sha(kernel):
+            return e.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.idx)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max((float(r[3]) for r in rows
+                                                         if r[3].replace(".", "").isdigit()),
+                                                        default=None)}
+
+
+def flush_l2(buf):
+    buf.zero_()
+
+
+# ------------------------------------------------------------------ our arm
+
+class Runner:
+    """Holds device buffers for one workload and runs its step."""
+
+    def __init__(self, w, inp, fa):
+        self.w, self.fa = w, fa
+        d = torch.device("cuda")
+        self.q, self.k, self.v = (inp[n].to(d) for n in ("q", "k", "v"))
+        self.kv = None if inp["kv_len"] is None else inp["kv_len"].to(d)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device=d)
+        # d=256 has no backward kernel yet; its forward is still timed
+        self.backward = w.backward and w.d in (64, 128)
+        if self.backward:
+            self.do = inp["do"].to(d)
+            self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+            self.ws = fa.workspace(w.B, w.H, w.N, w.d, d)
+
+    def fwd(self):
+        self.fa.fa_fwd(self.q, self.k, self.v, self.o, self.lse, self.w.scale, self.w.causal,
+                       self.kv)
+
+    def prep(self):
+        self.fa.fa_bwd_prep(self.o, self.do, self.lse, self.ws)
+
+    def main(self):
+        self.fa.fa_bwd_dkdv(self.q, self.k, self.v, self.do, self.dk, self.dv, self.w.scale,
+                            self.w.causal, self.kv, self.ws)
+
+    def post(self):
+        self.fa.fa_bwd_dq(self.dq, self.w.scale, self.ws)
+
+    def phases(self):
+        return [("fa_fwd_kernel", self.fwd)] + ([("bwd_pre_kernel", self.prep),
+                                                 ("bwd_main_kernel", self.main),
+                                                 ("bwd_post_kernel", self.post)]
+                                                if self.backward else [])
+
+    def step(self):
+        for _, f in self.phases():
+            f()
+
+
+def time_steps(runner, steps, flush=None):
+    """Per-phase and per-step device times (ms) over `steps` timed steps."""
+    phases = runner.phases()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
+          for _ in range(steps)]
+    per_phase = {name: 0.0 for name, _ in phases}
+    step_ms = []
+    for s in range(steps):
+        if flush is not None:
+            flush()
+        ev[s][0].record()
+        for i, (_, f) in enumerate(phases):
+            f()
+            ev[s][i + 1].record()
+    torch.cuda.synchronize()
+    for s in range(steps):
+        for i, (name, _) in enumerate(phases):
+            per_phase[name] += ev[s][i].elapsed_time(ev[s][i + 1])
+        step_ms.append(ev[s][0].elapsed_time(ev[s][-1]))
+    return {k: v / steps for k, v in per_phase.items()}, step_ms
+
+
+def bytes_of(*ts):
+    return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+
+def run_ours(args, dist):
+    from exact_attention_04_gb300 import build as fabuild
+    from exact_attention_04_gb300 import fa
+
+    fabuild.build()
+    fa.load()
+    torch.cuda.set_device(dist.local_rank)
+    w = WORKLOADS[args.workload]
+    if dist.rank:
+        w = dataclasses.replace(w, seed=w.seed + 1000 * dist.rank)
+    inp = make_inputs(w)
+    r = Runner(w, inp, fa)
+    flops_fwd = w.fwd_flops()
+    flops_bwd = w.bwd_flops() if r.backward else 0.0
+    flops_step = flops_fwd + flops_bwd
+
+    for _ in range(max(args.warmup, 3)):
+        r.step()
+    torch.cuda.synchronize()
+    fa.fa_check()
+
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    clocks = ClockSampler(visible.split(",")[dist.local_rank] if visible else dist.local_rank)
+    clocks.start()
+    time.sleep(0.3)                      # let the sampler start
+    for _ in range(max(args.warmup, 3)):
+        r.step()                         # keep the GPU loaded while sampling begins
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks.mark_start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    per_phase, step_ms = time_steps(r, args.steps)
+    end.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks.mark_end()
+    clk = clocks.stop()
+    fa.fa_check()
+    total_ms = start.elapsed_time(end)
+    total_ms = dist.max(total_ms)
+    ms_per_step = total_ms / args.steps
+    value = dist.world * flops_step / (ms_per_step * 1e-3) / 1e12
+
+    # dominant kernel and its roofline
+    peaks, peak_src = load_peaks()
+    kernel = max(per_phase, key=per_phase.get)
+    kflops = {"fa_fwd_kernel": flops_fwd, "bwd_main_kernel": flops_bwd}
+    if kernel in kflops:
+        achieved = kflops[kernel] / (per_phase[kernel] * 1e-3) / 1e12
+        roof = {"kernel": kernel, "bound": "tensor", "achieved": round(achieved, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": committed_traffic(kernel, w.name),
+                "peak_source": f"{peak_src} bf16 dense, burst",
+                "avg_launch_ms": round(per_phase[kernel], 4)}
+    else:
+        roof = {"kernel": kernel, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": None, "traffic": None}
+
+    # end to end through the C ABI with pinned host buffers
+    e2e = run_e2e(r, w, fa, min(args.steps, 20), flops_step, dist)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "pass": "fwd+bwd" if w.backward else "fwd",
+                   "parallelism": f"replica x{dist.world} (weak scaling, no collective)",
+                   "l2": "inputs larger than L2, no flush"},
+        "fwd_tflops": round(flops_fwd / (per_phase["fa_fwd_kernel"] * 1e-3) / 1e12, 2),
+        "bwd_tflops": (round(flops_bwd / (sum(per_phase[k] for k in per_phase
+                                               if k != "fa_fwd_kernel") * 1e-3) / 1e12, 2)
+                       if r.backward else None),
+        "kernel_ms": {k: round(v, 4) for k, v in per_phase.items()},
+        "step_ms_median": round(statistics.median(step_ms), 4),
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": args.steps * len(r.phases()),
+        "clocks": clk,
+    }
+    del r
+    torch.cuda.empty_cache()
+    if not args.no_sweep:
+        result["sweep"] = run_sweep(fa, peaks)
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, inp)
+    return result
+
+
+def run_e2e(r, w, fa, steps, flops_step, dist):
+    """Same step with host->device copies of the inputs and device->host copies
+    of every output inside the timed region (pinned host memory)."""
+    hin = {n: getattr(r, n).cpu().pin_memory() for n in (["q", "k", "v"] +
+                                                         (["do"] if r.backward else []))}
+    outs = ["o", "lse"] + (["dq", "dk", "dv"] if r.backward else [])
+    hout = {n: torch.empty_like(getattr(r, n), device="cpu").pin_memory() for n in outs}
+    h2d = bytes_of(*hin.values())
+    d2h = bytes_of(*hout.values())
+
+    def one():
+        for n, t in hin.items():
+            getattr(r, n).copy_(t, non_blocking=True)
+        r.step()
+        for n, t in hout.items():
+            t.copy_(getattr(r, n), non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    dist.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    ms = dist.max(s.elapsed_time(e)) / steps
+    fa.fa_check()
+    return {"value": round(dist.world * flops_step / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4)}
+
+
+def run_sweep(fa, peaks):
+    """Every other workload, timed briefly: TFLOP/s, fraction of peak, GB/s of
+    algorithmic traffic (inputs read + outputs written once)."""
+    out = []
+    flush_buf = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    cache = {}
+    for name, w in WORKLOADS.items():
+        if name == HEADLINE:
+            continue
+        key = (w.B, w.H, w.N, w.d, w.seed, w.qk_gain, w.kv_len_range, w.backward)
+        if key not in cache:
+            cache.clear()
+            cache[key] = make_inputs(w)
+        inp = cache[key]
+        r = Runner(w, inp, fa)
+        for _ in range(3):
+            r.step()
+        torch.cuda.synchronize()
+        steps = 10
+        per_phase, _ = time_steps(r, steps, flush=lambda: flush_l2(flush_buf))
+        fa.fa_check()
+        fwd_ms = per_phase["fa_fwd_kernel"]
+        rowb = w.B * w.H * w.N
+        fwd_bytes = 8 * rowb * w.d + 4 * rowb
+        entry = {"workload": name, "N": w.N, "d": w.d, "causal": w.causal,
+                 "fwd_ms": round(fwd_ms, 4),
+                 "fwd_tflops": round(w.fwd_flops() / (fwd_ms * 1e-3) / 1e12, 2),
+                 "fwd_frac_of_peak": round(w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
+                                           / peaks["bf16_tflops"], 4),
+                 "fwd_gbs": round(fwd_bytes / (fwd_ms * 1e-3) / 1e9, 1)}
+        if r.backward:
+            bwd_ms = sum(v for k, v in per_phase.items() if k != "fa_fwd_kernel")
+            bwd_bytes = 16 * rowb * w.d + 12 * rowb
+            entry.update({"bwd_ms": round(bwd_ms, 4),
+                          "bwd_tflops": round(w.bwd_flops() / (bwd_ms * 1e-3) / 1e12, 2),
+                          "bwd_frac_of_peak": round(w.bwd_flops() / (bwd_ms * 1e-3) / 1e12
+                                                    / peaks["bf16_tflops"], 4),
+                          "bwd_gbs": round(bwd_bytes / (bwd_ms * 1e-3) / 1e9, 1)})
+        if w.backward and not r.backward:
+            entry["bwd"] = "not built for this head dimension"
+        out.append(entry)
+        del r
+        torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------------------ the oracle as baseline
+
+def oracle_sample(w, inp):
+    """One head (b=0, h=0) of the workload, forward and (if the workload has
+    one) backward, in the fp64 oracle on every host core."""
+    import oracle
+    f64 = {n: inp[n][0:1, 0:1].float().double().numpy() for n in ("q", "k", "v")}
+    if w.backward:
+        f64["do"] = inp["do"][0:1, 0:1].float().double().numpy()
+    kv = None if inp["kv_len"] is None else [int(inp["kv_len"][0])]
+    threads = oracle.default_threads()
+    one = dataclasses.replace(w, B=1, H=1)
+    flops = one.fwd_flops() + (one.bwd_flops() if w.backward else 0.0)
+
+    def run():
+        oracle.attention_fwd(f64["q"], f64["k"], f64["v"], w.scale, causal=w.causal, kv_len=kv,
+                             threads=threads)
+        if w.backward:
+            oracle.attention_bwd(f64["q"], f64["k"], f64["v"], f64["do"], w.scale,
+                                 causal=w.causal, kv_len=kv, threads=threads)
+    desc = (f"head (b=0,h=0) of {w.name}: N={w.N}, d={w.d}, "
+            f"{'forward+backward' if w.backward else 'forward'}, fp64")
+    return run, flops, threads, desc
+
+
+def cpu_baseline(w, inp):
+    run, flops, threads, desc = oracle_sample(w, inp)
+    t0 = time.perf_counter()
+    run()
+    sec = time.perf_counter() - t0
+    return {"value": round(flops / sec / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "sample": desc, "seconds": round(sec, 3)}
+
+
+def run_reference(args, dist):
+    if dist.rank != 0:
+        return None
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    run, flops, threads, desc = oracle_sample(w, inp)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    sec = sum(times) / len(times)
+    value = round(flops / sec / 1e12, 6)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "causal": w.causal, "pass": "fwd+bwd" if w.backward else "fwd",
+                       "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    try:
+        res = run_reference(args, dist) if args.impl == "reference" else run_ours(args, dist)
+        if dist.rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -162,54 +162,139 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   return 2 * round_up256(padded_rows * sizeof(float)) + round_up256(rows * d * sizeof(float));
 }
 
-fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
-                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-                   float scale, int causal, const int* kv_len, void* workspace,
-                   size_t workspace_bytes, void* stream) {
-  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !workspace)
-    return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u) || !aligned16(dq) || !aligned16(dk) ||
-      !aligned16(dv))
-    return FA_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// Common checks of the backward entry points and the parameter block they
+// share.  Pointer arguments are checked by each caller.
+fa_status_t bwd_setup(fa::BwdParams* p, DeviceInfo** di, int B, int H, int N, int d, float scale,
+                      int causal, const int* kv_len, void* workspace, size_t workspace_bytes) {
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FA_ERR_INVALID_ARG;
   if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
   const fa_status_t sz = check_sizes(B, H, N, d, scale);
   if (sz != FA_OK) return sz;
   if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
-  DeviceInfo* di = device_info(nullptr);
-  if (!di || di->err != cudaSuccess) return FA_ERR_CUDA;
-  if (!di->supported) return FA_ERR_UNSUPPORTED;
-  fa::BwdParams p;
-  std::memset(&p, 0, sizeof(p));
+  *di = device_info(nullptr);
+  if (!*di || (*di)->err != cudaSuccess) return FA_ERR_CUDA;
+  if (!(*di)->supported) return FA_ERR_UNSUPPORTED;
+  std::memset(p, 0, sizeof(*p));
   const int BH = B * H;
-  if (!make_map(&p.tq, q, d, N, BH) || !make_map(&p.tk, k, d, N, BH) ||
-      !make_map(&p.tv, v, d, N, BH) || !make_map(&p.tdo, dO, d, N, BH))
-    return FA_ERR_CUDA;
-  if (d == 256) return FA_ERR_UNSUPPORTED;
   const int npad = (N + 127) / 128 * 128;
   const size_t stat_bytes = round_up256(static_cast<size_t>(BH) * npad * sizeof(float));
+  p->delta = static_cast<float*>(workspace);
+  p->lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + stat_bytes);
+  p->dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * stat_bytes);
+  p->Npad = npad;
+  p->kv_len = kv_len;
+  p->B = B;
+  p->H = H;
+  p->N = N;
+  p->causal = causal ? 1 : 0;
+  p->scale = scale;
+  p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p->status = (*di)->status;
+  return FA_OK;
+}
+
+fa_status_t bwd_prep_impl(const fa::BwdParams& p, int d, void* stream) {
+  return fa::launch_bwd_prep(p, d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                     : FA_ERR_CUDA;
+}
+
+fa_status_t bwd_main_impl(fa::BwdParams& p, const DeviceInfo* di, const void* q, const void* k,
+                          const void* v, const void* dO, int d, void* stream) {
+  const int BH = p.B * p.H;
+  if (!make_map(&p.tq, q, d, p.N, BH) || !make_map(&p.tk, k, d, p.N, BH) ||
+      !make_map(&p.tv, v, d, p.N, BH) || !make_map(&p.tdo, dO, d, p.N, BH))
+    return FA_ERR_CUDA;
+  return fa::launch_bwd_main(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+fa_status_t bwd_post_impl(const fa::BwdParams& p, int d, void* stream) {
+  return fa::launch_bwd_post(p, d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
+                                                                                     : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_bwd_prep(const void* o, const void* dO, const float* lse, int B, int H, int N,
+                        int d, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!o || !dO || !lse || !aligned16(o) || !aligned16(dO) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FA_ERR_INVALID_ARG;
+  fa::BwdParams p;
+  DeviceInfo* di = nullptr;
+  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, 1.f, 0, nullptr, workspace,
+                                   workspace_bytes);
+  if (st != FA_OK) return st;
+  p.o = o;
+  p.dO = dO;
+  p.lse = lse;
+  return bwd_prep_impl(p, d, stream);
+}
+
+fa_status_t fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                        void* dv, int B, int H, int N, int d, float scale, int causal,
+                        const int* kv_len, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dk) ||
+      !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  fa::BwdParams p;
+  DeviceInfo* di = nullptr;
+  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, causal, kv_len, workspace,
+                                   workspace_bytes);
+  if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;
+  p.dk = dk;
+  p.dv = dv;
+  return bwd_main_impl(p, di, q, k, v, dO, d, stream);
+}
+
+fa_status_t fa_bwd_dq(void* dq, int B, int H, int N, int d, float scale, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!dq || !aligned16(dq)) return FA_ERR_INVALID_ARG;
+  fa::BwdParams p;
+  DeviceInfo* di = nullptr;
+  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, 0, nullptr, workspace,
+                                   workspace_bytes);
+  if (st != FA_OK) return st;
+  p.dq = dq;
+  return bwd_post_impl(p, d, stream);
+}
+
+fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   float scale, int causal, const int* kv_len, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  fa::BwdParams p;
+  DeviceInfo* di = nullptr;
+  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, causal, kv_len, workspace,
+                                   workspace_bytes);
+  if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;
   p.o = o;
   p.dO = dO;
   p.lse = lse;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  p.delta = static_cast<float*>(workspace);
-  p.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + stat_bytes);
-  p.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * stat_bytes);
-  p.Npad = npad;
-  p.kv_len = kv_len;
-  p.B = B;
-  p.H = H;
-  p.N = N;
-  p.causal = causal ? 1 : 0;
-  p.scale = scale;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.status = di->status;
-  if (fa::launch_bwd(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return FA_ERR_CUDA;
-  return FA_OK;
+  fa_status_t r = bwd_prep_impl(p, d, stream);
+  if (r == FA_OK) r = bwd_main_impl(p, di, q, k, v, dO, d, stream);
+  if (r == FA_OK) r = bwd_post_impl(p, d, stream);
+  return r;
 }
 
 fa_status_t fa_check(void* stream) {

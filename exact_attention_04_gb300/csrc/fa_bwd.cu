@@ -610,36 +610,52 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const __grid_constant__ B
 }
 
 template <int D>
-cudaError_t launch(const BwdParams& p, int num_sms, int max_smem, cudaStream_t stream) {
+cudaError_t launch_prep(const BwdParams& p, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.B) * p.H * p.Npad;
   constexpr int ROWS = 256 / (D / 8);
   bwd_pre_kernel<D><<<static_cast<unsigned>((rows + ROWS - 1) / ROWS), 256, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_main(const BwdParams& p, int num_sms, int max_smem, cudaStream_t stream) {
   const size_t smem = smem_request(sizeof(BwdSmem<D>), max_smem);
-  e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
+  cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int T = (p.N + BN - 1) / BN;
   const long long units = p.causal ? static_cast<long long>(p.B) * p.H * ((T + 1) / 2)
                                    : static_cast<long long>(p.B) * p.H * T;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   bwd_main_kernel<D><<<grid, kThreads, smem, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const long long n8 = static_cast<long long>(p.B) * p.H * p.N * D / 8;
-  bwd_post_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(p, n8);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdParams& p, int d, int num_sms, int max_smem, cudaStream_t stream) {
+cudaError_t launch_bwd_prep(const BwdParams& p, int d, cudaStream_t stream) {
   switch (d) {
-    case 64: return launch<64>(p, num_sms, max_smem, stream);
-    case 128: return launch<128>(p, num_sms, max_smem, stream);
+    case 64: return launch_prep<64>(p, stream);
+    case 128: return launch_prep<128>(p, stream);
+    case 256: return launch_prep<256>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_bwd_main(const BwdParams& p, int d, int num_sms, int max_smem,
+                            cudaStream_t stream) {
+  switch (d) {
+    case 64: return launch_main<64>(p, num_sms, max_smem, stream);
+    case 128: return launch_main<128>(p, num_sms, max_smem, stream);
     default: return cudaErrorNotSupported;
   }
+}
+
+cudaError_t launch_bwd_post(const BwdParams& p, int d, cudaStream_t stream) {
+  const long long n8 = static_cast<long long>(p.B) * p.H * p.N * d / 8;
+  bwd_post_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(p, n8);
+  return cudaGetLastError();
 }
 
 }  // namespace fa

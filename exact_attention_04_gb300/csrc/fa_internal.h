@@ -59,6 +59,9 @@ inline size_t smem_request(size_t bytes, int max_optin) {
 }
 
 cudaError_t launch_fwd(const FwdParams& p, int d, int num_sms, int max_smem, cudaStream_t stream);
-cudaError_t launch_bwd(const BwdParams& p, int d, int num_sms, int max_smem, cudaStream_t stream);
+cudaError_t launch_bwd_prep(const BwdParams& p, int d, cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdParams& p, int d, int num_sms, int max_smem,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_post(const BwdParams& p, int d, cudaStream_t stream);
 
 }  // namespace fa

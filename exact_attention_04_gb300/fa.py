@@ -44,6 +44,12 @@ def load():
         lib.fa_bwd_workspace_bytes.restype = sz
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
         lib.fa_bwd.restype = i
+        lib.fa_bwd_prep.argtypes = [vp, vp, vp, i, i, i, i, vp, sz, vp]
+        lib.fa_bwd_prep.restype = i
+        lib.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, vp, sz, vp]
+        lib.fa_bwd_dkdv.restype = i
+        lib.fa_bwd_dq.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
+        lib.fa_bwd_dq.restype = i
         lib.fa_check.argtypes = [vp]
         lib.fa_check.restype = i
         lib.fa_status_string.argtypes = [i]
@@ -54,8 +60,8 @@ def load():
     return _lib
 
 
-EXPORTS = ("fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_check", "fa_status_string",
-           "fa_version")
+EXPORTS = ("fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_prep", "fa_bwd_dkdv",
+           "fa_bwd_dq", "fa_check", "fa_status_string", "fa_version")
 
 
 def fa_status_string(status: int) -> str:
@@ -134,6 +140,47 @@ def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, kv_len=None, wo
                        _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                        _ptr(kv_len), _ptr(workspace), nbytes, _stream_ptr(stream))
     _raise(st, "fa_bwd")
+
+
+def _ws(workspace):
+    if workspace is None or not workspace.is_cuda:
+        raise ValueError("workspace: expected a CUDA tensor")
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
+def fa_bwd_prep(o, do, lse, workspace, stream=None):
+    """First backward phase: D, LSE*log2(e) into the workspace; zero the dQ accumulator."""
+    _check_qkv("o", o)
+    B, H, N, d = o.shape
+    _check_qkv("do", do, o.shape)
+    if lse.dtype != torch.float32 or not lse.is_cuda or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse: expected fp32 CUDA tensor [B,H,N]")
+    wp, wn = _ws(workspace)
+    _raise(load().fa_bwd_prep(_ptr(o), _ptr(do), _ptr(lse), B, H, N, d, wp, wn,
+                              _stream_ptr(stream)), "fa_bwd_prep")
+
+
+def fa_bwd_dkdv(q, k, v, do, dk, dv, scale, causal=False, kv_len=None, workspace=None,
+                stream=None):
+    """Second backward phase: dK, dV and the fp32 dQ accumulation."""
+    _check_qkv("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("do", do), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, q.shape)
+    kv_len = _check_kv_len(kv_len, B)
+    wp, wn = _ws(workspace)
+    _raise(load().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dk), _ptr(dv), B, H, N,
+                              d, float(scale), int(bool(causal)), _ptr(kv_len), wp, wn,
+                              _stream_ptr(stream)), "fa_bwd_dkdv")
+
+
+def fa_bwd_dq(dq, scale, workspace, stream=None):
+    """Third backward phase: dQ = bf16(scale * accumulator)."""
+    _check_qkv("dq", dq)
+    B, H, N, d = dq.shape
+    wp, wn = _ws(workspace)
+    _raise(load().fa_bwd_dq(_ptr(dq), B, H, N, d, float(scale), wp, wn, _stream_ptr(stream)),
+           "fa_bwd_dq")
 
 
 def fa_check(stream=None):

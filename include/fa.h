@@ -70,8 +70,9 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
 
 /*
  * Bytes of device workspace fa_bwd needs for these sizes: the fp32 row
- * statistic D = rowsum(dO o O) [B,H,N] and the fp32 dQ accumulator
- * [B,H,N,d], each rounded up to 256 bytes.  Returns 0 for invalid sizes.
+ * statistics D = rowsum(dO o O) and LSE*log2(e), each [B*H, Npad] with Npad =
+ * N rounded up to 128, and the fp32 dQ accumulator [B,H,N,d]; each region
+ * starts on a 256-byte boundary.  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -92,6 +93,27 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o,
                    const void* dO, const float* lse, void* dq, void* dk, void* dv,
                    int B, int H, int N, int d, float scale, int causal, const int* kv_len,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The three launches fa_bwd makes, callable one by one (same workspace, same
+ * stream order); fa_bwd is exactly fa_bwd_prep, fa_bwd_dkdv, fa_bwd_dq.
+ *
+ * fa_bwd_prep: D_i = rowsum(dO o O)_i and LSE_i * log2(e) into the workspace
+ *   (padded to a multiple of 128 rows), and zeroes the fp32 dQ accumulator.
+ * fa_bwd_dkdv: recomputes P per 128x128 tile from Q, K and the saved LSE,
+ *   writes dK and dV (bf16) and adds dS K into the fp32 dQ accumulator;
+ *   needs fa_bwd_prep to have run on this workspace.
+ * fa_bwd_dq:   dQ = bf16(scale * accumulator); needs fa_bwd_dkdv.
+ * Argument rules and errors are those of fa_bwd for the arguments each takes.
+ */
+fa_status_t fa_bwd_prep(const void* o, const void* dO, const float* lse, int B, int H, int N,
+                        int d, void* workspace, size_t workspace_bytes, void* stream);
+fa_status_t fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                        void* dv, int B, int H, int N, int d, float scale, int causal,
+                        const int* kv_len, void* workspace, size_t workspace_bytes,
+                        void* stream);
+fa_status_t fa_bwd_dq(void* dq, int B, int H, int N, int d, float scale, void* workspace,
+                      size_t workspace_bytes, void* stream);
 
 /*
  * Waits for `stream`, then reads and clears the current device's status
