@@ -50,6 +50,9 @@ def load():
         lib.fa_bwd_dkdv.restype = i
         lib.fa_bwd_dq.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
         lib.fa_bwd_dq.restype = i
+        lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp,
+                                       vp]
+        lib.fa_bwd_noalloc.restype = i
         lib.fa_check.argtypes = [vp]
         lib.fa_check.restype = i
         lib.fa_status_string.argtypes = [i]
@@ -61,7 +64,7 @@ def load():
 
 
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_prep", "fa_bwd_dkdv",
-           "fa_bwd_dq", "fa_check", "fa_status_string", "fa_version")
+           "fa_bwd_dq", "fa_bwd_noalloc", "fa_check", "fa_status_string", "fa_version")
 
 
 def fa_status_string(status: int) -> str:
@@ -181,6 +184,24 @@ def fa_bwd_dq(dq, scale, workspace, stream=None):
     wp, wn = _ws(workspace)
     _raise(load().fa_bwd_dq(_ptr(dq), B, H, N, d, float(scale), wp, wn, _stream_ptr(stream)),
            "fa_bwd_dq")
+
+
+def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, kv_len=None,
+                   stream=None):
+    """fa_bwd without a workspace, for callers that cannot allocate device
+    memory: the library's own fixed scratch array is used instead (see
+    include/fa.h for its size limit and the rule that overlapping calls race)."""
+    _check_qkv("q", q)
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, q.shape)
+    if lse.dtype != torch.float32 or not lse.is_cuda or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse: expected fp32 CUDA tensor [B,H,N]")
+    kv_len = _check_kv_len(kv_len, B)
+    _raise(load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d, float(scale),
+                                 int(bool(causal)), _ptr(kv_len), _stream_ptr(stream)),
+           "fa_bwd_noalloc")
 
 
 def fa_check(stream=None):

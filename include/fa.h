@@ -116,6 +116,34 @@ fa_status_t fa_bwd_dq(void* dq, int B, int H, int N, int d, float scale, void* w
                       size_t workspace_bytes, void* stream);
 
 /*
+ * fa_bwd_noalloc: the backward pass for callers that cannot allocate device
+ * memory.  Same arguments, results and errors as fa_bwd, minus the workspace:
+ * the scratch fa_bwd needs (fa_bwd_workspace_bytes(B,H,N,d) bytes) comes from
+ * a fixed array of FA_BWD_NOALLOC_MAX_SCRATCH_BYTES that the library keeps in
+ * device memory, so this call allocates nothing.  It is meant for code that is
+ * not allowed to allocate: an allocator or memory-pool hook that must not
+ * re-enter itself, a plugin that is handed only its tensors, or a loop that
+ * cannot take cudaMalloc's implicit synchronisation.
+ *
+ * - Sizes whose scratch exceeds the maximum return FA_ERR_INVALID_ARG before
+ *   anything is enqueued (64 MiB covers, e.g., B*H*N*d up to about 16M
+ *   elements).
+ * - Every GPU that loads this part of the library holds the array until the
+ *   process exits.  Its device address is looked up on the first call on each
+ *   device (with that device current); make that first call before any
+ *   stream capture.
+ * - All calls share the array: calls whose kernels overlap on the GPU race
+ *   and give wrong gradients.  Calls ordered on one stream are fine; each call
+ *   re-initialises the scratch it reads, so no state carries over.
+ * The pages describe no such variant; it exists only for such callers.
+ */
+#define FA_BWD_NOALLOC_MAX_SCRATCH_BYTES (64u * 1024u * 1024u)
+fa_status_t fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                           const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                           int B, int H, int N, int d, float scale, int causal,
+                           const int* kv_len, void* stream);
+
+/*
  * Waits for `stream`, then reads and clears the current device's status
  * word.  FA_ERR_TIMEOUT if a kernel gave up waiting since the last check,
  * FA_ERR_CUDA if the stream reports an error, FA_OK otherwise.
