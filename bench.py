@@ -39,7 +39,7 @@ HEADLINE = "large_head_b2_h16_n8192_d128_causal"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd.cu", "sm103_ptx.cuh"],
-    "bwd_main_kernel": ["fa_bwd.cu", "sm103_ptx.cuh"],
+    "bwd_main_kernel": ["fa_bwd.cu", "fa_bwd_dt.cu", "fa_api.cu", "sm103_ptx.cuh"],
 }
 
 
@@ -182,8 +182,7 @@ class Runner:
         self.kv = None if inp["kv_len"] is None else inp["kv_len"].to(d)
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device=d)
-        # d=256 has no backward kernel yet; its forward is still timed
-        self.backward = w.backward and w.d in (64, 128)
+        self.backward = w.backward
         if self.backward:
             self.do = inp["do"].to(d)
             self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))

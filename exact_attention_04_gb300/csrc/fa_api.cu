@@ -83,16 +83,16 @@ fa_status_t check_sizes(int B, int H, int N, int d, float scale) {
   return FA_OK;
 }
 
-// bf16 [BH, N, d] as a 3-D tensor (d, N, BH): box of 64 columns x 128 rows,
-// 128-byte swizzle, rows past N read as zero.
-bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH) {
+// bf16 [BH, N, d] as a 3-D tensor (d, N, BH): box of 64 columns x box_rows
+// rows, 128-byte swizzle, rows past N read as zero.
+bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(d) * N * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -205,13 +205,17 @@ fa_status_t bwd_prep_impl(const fa::BwdParams& p, int d, void* stream) {
 fa_status_t bwd_main_impl(fa::BwdParams& p, const DeviceInfo* di, const void* q, const void* k,
                           const void* v, const void* dO, int d, void* stream) {
   const int BH = p.B * p.H;
-  if (!make_map(&p.tq, q, d, p.N, BH) || !make_map(&p.tk, k, d, p.N, BH) ||
-      !make_map(&p.tv, v, d, p.N, BH) || !make_map(&p.tdo, dO, d, p.N, BH))
+  // d = 64: 128-query steps with dQ in query rows; d = 128, 256: 64-query
+  // steps with dQ^T in head-dimension rows (fa_bwd_dt.cu).
+  const bool dt = d != 64;
+  const int qrows = dt ? 64 : 128;
+  if (!make_map(&p.tq, q, d, p.N, BH, qrows) || !make_map(&p.tk, k, d, p.N, BH) ||
+      !make_map(&p.tv, v, d, p.N, BH) || !make_map(&p.tdo, dO, d, p.N, BH, qrows))
     return FA_ERR_CUDA;
-  return fa::launch_bwd_main(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? FA_OK
-             : FA_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = dt ? fa::launch_bwd_main_dt(p, d, di->num_sms, di->max_smem, s)
+                           : fa::launch_bwd_main(p, d, di->num_sms, di->max_smem, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status_t bwd_post_impl(const fa::BwdParams& p, int d, void* stream) {
@@ -252,7 +256,6 @@ fa_status_t fa_bwd_dkdv(const void* q, const void* k, const void* v, const void*
   const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, causal, kv_len, workspace,
                                    workspace_bytes);
   if (st != FA_OK) return st;
-  if (d == 256) return FA_ERR_UNSUPPORTED;
   p.dk = dk;
   p.dv = dv;
   return bwd_main_impl(p, di, q, k, v, dO, d, stream);
@@ -284,7 +287,6 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
   const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, causal, kv_len, workspace,
                                    workspace_bytes);
   if (st != FA_OK) return st;
-  if (d == 256) return FA_ERR_UNSUPPORTED;
   p.o = o;
   p.dO = dO;
   p.lse = lse;

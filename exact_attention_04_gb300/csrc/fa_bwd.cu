@@ -1,4 +1,6 @@
-// Attention backward for sm_103a: three launches on one stream.
+// Attention backward for sm_103a: three launches on one stream.  The main
+// kernel in this file serves head dimension 64; 128 and 256 use the kernel
+// in fa_bwd_dt.cu (same pre- and post-kernels).
 //
 //  1. bwd_pre   D_i = sum_t dO_it * O_it and L2_i = LSE_i * log2(e) per query
 //               row (padded to a multiple of 128 rows: D = 0, L2 = +inf past
@@ -647,7 +649,6 @@ cudaError_t launch_bwd_main(const BwdParams& p, int d, int num_sms, int max_smem
                             cudaStream_t stream) {
   switch (d) {
     case 64: return launch_main<64>(p, num_sms, max_smem, stream);
-    case 128: return launch_main<128>(p, num_sms, max_smem, stream);
     default: return cudaErrorNotSupported;
   }
 }

@@ -1,0 +1,613 @@
+// Backward main kernel for head dimensions 128 and 256 ("dQ transposed").
+//
+// Work item: (bh, block of 128 keys, half h of the head dimension).  The CTA
+// keeps K and V of its key block in shared memory and streams the query
+// blocks of 64 rows (Q_i, dO_i, and the per-row statistics) through a ring.
+// Per query block, on the tensor core (M = 128 everywhere):
+//   S^T   = K Q_i^T            (128 keys x 64 queries, contraction over all of d)
+//   dP^T  = V dO_i^T
+//   P^T   = exp2(S^T*c - L2_i)  and  dS^T = P^T o (dP^T - D_i)   (row warps)
+//   dV_h += P^T dO_i[:, h]      dK_h += dS^T Q_i[:, h]           (A from tensor memory)
+//   dQ^T_h = K[:, h]^T dS^T     (128 head-dim rows x 64 queries)
+// dQ^T sits in tensor memory with one lane per head-dimension column, so the
+// four drain warps add it to the fp32 accumulator in global memory with
+// atomics that are contiguous across each warp (128 bytes per instruction).
+// With d = 256 the two halves of a key block are separate work items; both
+// recompute S^T and dP^T (the price of fitting dK and dV in tensor memory).
+//
+// Recomputation of P from the saved statistic: "注意力为什么受限于显存带宽：用
+// 算术强度与分块把 FlashAttention 推导清楚" section 八; "4. FlashAttention 深度
+// 剖析" section 4.3.4.  Gradient formulas: chain rule through the row softmax.
+//
+// Warps: 0 TMA producer, 1 MMA issuer (owns tensor memory), 2..5 key-row warps
+// (P^T, dS^T, dK/dV epilogue), 6..9 dQ drain warps.
+// Tensor memory columns: S^T [0,64) with P^T bf16 over [0,32), dP^T [64,128)
+// with dS^T bf16 over [64,96), dV_h [128,256), dK_h [256,384), dQ^T_h [384,448).
+// Successive tcgen05.mma issued by one thread execute in order, so an MMA that
+// overwrites columns an earlier MMA reads as an operand needs no extra wait.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+constexpr int BQ = 64;             // queries per step
+constexpr int BK = 128;            // keys per work item
+constexpr int DH = 128;            // head-dimension columns of dK, dV, dQ per work item
+constexpr int KCH = 128 * 128;     // 128 rows x 128 bytes
+constexpr int QCH = 64 * 128;      // 64 rows x 128 bytes
+constexpr int kThreads = 320;
+
+template <int D>
+struct DtCfg {
+  static constexpr int NCH = D / 64;
+  static constexpr int NSPLIT = D / DH;
+  static constexpr int KV_BYTES = NCH * KCH;
+  static constexpr int Q_BYTES = NCH * QCH;
+  static constexpr int STAGES = D == 128 ? 3 : 1;
+  static constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DV = 128, TM_DK = 256, TM_DQ = 384;
+  static constexpr uint32_t TM_COLS = 512;
+};
+
+template <int D>
+struct DtSmem {
+  alignas(1024) uint8_t k[DtCfg<D>::KV_BYTES];
+  alignas(1024) uint8_t v[DtCfg<D>::KV_BYTES];
+  alignas(1024) uint8_t q[DtCfg<D>::STAGES][DtCfg<D>::Q_BYTES];
+  alignas(1024) uint8_t dO[DtCfg<D>::STAGES][DtCfg<D>::Q_BYTES];
+  alignas(1024) uint8_t ds[2][KCH];              // dS^T bf16, 128 keys x 64 queries, double buffer
+  alignas(16) float lse2[DtCfg<D>::STAGES][BQ];
+  alignas(16) float delta[DtCfg<D>::STAGES][BQ];
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[DtCfg<D>::STAGES], q_empty[DtCfg<D>::STAGES];
+  uint64_t s_full, p_full, dp_full, ds_full, ds_free[2], dq_full, dq_free, acc_full, acc_free;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+enum Site {
+  kSiteProdKV = 64, kSiteProdQ, kSiteMmaKV, kSiteMmaQ, kSiteMmaP, kSiteMmaDs, kSiteMmaDq,
+  kSiteMmaAcc, kSiteRowS, kSiteRowDp, kSiteRowDsFree, kSiteRowAcc, kSiteDrainDq, kSiteDtDrain
+};
+
+__device__ __forceinline__ void record_failure(int* status, volatile int* abort, int site) {
+  atomicCAS(status, 0, status_code(site));
+  *abort = 1;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  bool ok = mbar_wait(bar, parity, abort, kWaitTimeoutNs);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Units are (bh, key-block pair or key block, half).  Causal: key block n
+// meets query blocks from its diagonal on, so blocks p and T-1-p are paired,
+// longest first.  The halves of one key block are adjacent units so they run
+// at the same time and share K, V, Q, dO in L2.
+struct DtSched {
+  int T, P, per_bh, units, causal, nsplit;
+  __device__ DtSched(int BH, int N, int causal_, int nsplit_) : causal(causal_), nsplit(nsplit_) {
+    T = (N + BK - 1) / BK;
+    P = (T + 1) / 2;
+    per_bh = causal ? P : T;
+    units = BH * per_bh * nsplit;
+  }
+  __device__ void decode(int u, int& bh, int& pp, int& h) const {
+    bh = u / (per_bh * nsplit);
+    const int rem = u % (per_bh * nsplit);
+    pp = rem / nsplit;
+    h = rem % nsplit;
+  }
+  __device__ int nitems(int pp) const {
+    if (!causal) return 1;
+    return (pp == T - 1 - pp) ? 1 : 2;
+  }
+  __device__ int block(int pp, int k) const {
+    if (!causal) return pp;
+    return (k == 0) ? pp : (T - 1 - pp);
+  }
+};
+
+__device__ __forceinline__ int dt_len(const BwdParams& p, int bh) {
+  int len = p.N;
+  if (p.kv_len) {
+    len = __ldg(p.kv_len + bh / p.H);
+    len = len < 0 ? 0 : (len > p.N ? p.N : len);
+  }
+  return len;
+}
+
+// Query-step range [i0, i1) (blocks of 64) for key block n; empty when the
+// key block lies past the sequence.
+__device__ __forceinline__ void dt_range(const BwdParams& p, int n, int len, int& i0, int& i1) {
+  if (n * BK >= len) {
+    i0 = i1 = 0;
+    return;
+  }
+  i0 = p.causal ? (n * BK) / BQ : 0;
+  i1 = (p.N + BQ - 1) / BQ;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_constant__ BwdParams p) {
+  using C = DtCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
+  const uintptr_t aligned = (raw + 1023) & ~static_cast<uintptr_t>(1023);
+  if (aligned - raw + sizeof(DtSmem<D>) > dynamic_smem_size()) {
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, status_code(kSiteSmemLayout));
+    return;
+  }
+  DtSmem<D>& sm = *reinterpret_cast<DtSmem<D>*>(aligned);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  volatile int* abort = &sm.abort;
+
+  if (threadIdx.x == 0) {
+    sm.abort = 0;
+    mbar_init(&sm.kv_full, 1);
+    mbar_init(&sm.kv_empty, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.p_full, 4);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.ds_full, 4);
+    mbar_init(&sm.ds_free[0], 1);
+    mbar_init(&sm.ds_free[1], 1);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_free, 4);
+    mbar_init(&sm.acc_full, 1);
+    mbar_init(&sm.acc_free, 4);
+    mbar_init(&sm.mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+  const int BH = p.B * p.H;
+  const DtSched sched(BH, p.N, p.causal, C::NSPLIT);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tq);
+      prefetch_tmap(&p.tk);
+      prefetch_tmap(&p.tv);
+      prefetch_tmap(&p.tdo);
+      uint32_t w_it = 0, g = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+        int bh, pp, h;
+        sched.decode(u, bh, pp, h);
+        for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
+          const int n = sched.block(pp, kt);
+          int i0, i1;
+          dt_range(p, n, dt_len(p, bh), i0, i1);
+          if (i0 >= i1) continue;
+          if (!mbar_wait(&sm.kv_empty, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+            record_failure(p.status, abort, kSiteProdKV);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.kv_full, 2 * C::KV_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c) {
+            tma_load_3d(sm.k + c * KCH, &p.tk, &sm.kv_full, 64 * c, n * BK, bh);
+            tma_load_3d(sm.v + c * KCH, &p.tv, &sm.kv_full, 64 * c, n * BK, bh);
+          }
+          ++w_it;
+          for (int i = i0; i < i1; ++i) {
+            const int st = g % C::STAGES;
+            if (!mbar_wait(&sm.q_empty[st], ((g / C::STAGES) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteProdQ);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.q_full[st], 2 * C::Q_BYTES + 2 * BQ * 4);
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c) {
+              tma_load_3d(sm.q[st] + c * QCH, &p.tq, &sm.q_full[st], 64 * c, i * BQ, bh);
+              tma_load_3d(sm.dO[st] + c * QCH, &p.tdo, &sm.q_full[st], 64 * c, i * BQ, bh);
+            }
+            const size_t roff = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(i) * BQ;
+            bulk_load(sm.lse2[st], p.lse2 + roff, BQ * 4, &sm.q_full[st]);
+            bulk_load(sm.delta[st], p.delta + roff, BQ * 4, &sm.q_full[st]);
+            ++g;
+          }
+        }
+      }
+      // no copy may still be landing in shared memory when the CTA exits
+      if (w_it > 0 && !mbar_wait(&sm.kv_full, (w_it - 1) & 1, nullptr, kWaitTimeoutNs))
+        record_failure(p.status, abort, kSiteDtDrain);
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (g > static_cast<uint32_t>(s)) {
+          const uint32_t nph = (g - 1 - s) / C::STAGES;
+          if (!mbar_wait(&sm.q_full[s], nph & 1, nullptr, kWaitTimeoutNs))
+            record_failure(p.status, abort, kSiteDtDrain);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(BK, BQ, 0, 0);      // S^T, dP^T
+      constexpr uint32_t kIdAcc = idesc_bf16_f32(BK, DH, 0, 1);    // dV, dK (B MN-major)
+      constexpr uint32_t kIdDq = idesc_bf16_f32(DH, BQ, 1, 1);     // dQ^T (A, B MN-major)
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sm.k), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sm.v), 16, 1024);
+      uint32_t w_it = 0, g = 0;
+      bool ok = true;
+      auto fail = [&](int site) {
+        record_failure(p.status, abort, site);
+        ok = false;
+      };
+      auto wait_q = [&](uint32_t gg) -> bool {
+        if (!mbar_wait(&sm.q_full[gg % C::STAGES], (gg / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+          fail(kSiteMmaQ);
+          return false;
+        }
+        tc_fence_after_sync();
+        return true;
+      };
+      auto issue_s = [&](uint32_t gg) {
+        const int st = gg % C::STAGES;
+        const uint64_t dq = sdesc_sw128(smem_u32(sm.q[st]), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + C::TM_S, dK0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
+                      dq + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
+        mma_commit(&sm.s_full);
+      };
+      auto issue_dp = [&](uint32_t gg) {
+        const int st = gg % C::STAGES;
+        const uint64_t ddo = sdesc_sw128(smem_u32(sm.dO[st]), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + C::TM_DP, dV0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
+                      ddo + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
+        mma_commit(&sm.dp_full);
+      };
+      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+        int bh, pp, h;
+        sched.decode(u, bh, pp, h);
+        // K[:, h] as the MN-major A operand of dQ^T: 64-column chunks 2h, 2h+1
+        const uint64_t dKmn = sdesc_sw128(smem_u32(sm.k) + 2 * h * KCH, KCH, 1024);
+        for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
+          const int n = sched.block(pp, kt);
+          int i0, i1;
+          dt_range(p, n, dt_len(p, bh), i0, i1);
+          if (i0 >= i1) continue;
+          const int nsteps = i1 - i0;
+          if (!mbar_wait(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
+            fail(kSiteMmaKV);
+            break;
+          }
+          if (!wait_q(g)) break;
+          issue_s(g);
+          issue_dp(g);
+          for (int s = 0; s < nsteps; ++s, ++g) {
+            const int st = g % C::STAGES;
+            const bool first = (s == 0);
+            // dV_h += P^T dO_i[:, h]
+            if (!mbar_wait(&sm.p_full, g & 1, abort, kWaitTimeoutNs)) {
+              fail(kSiteMmaP);
+              break;
+            }
+            if (first && !mbar_wait(&sm.acc_free, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              fail(kSiteMmaAcc);
+              break;
+            }
+            tc_fence_after_sync();
+            const uint64_t dOmn = sdesc_sw128(smem_u32(sm.dO[st]) + 2 * h * QCH, QCH, 1024);
+            const uint64_t dQmn = sdesc_sw128(smem_u32(sm.q[st]) + 2 * h * QCH, QCH, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BQ / 16; ++kk)
+              mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + kk * 8, dOmn + ((kk * 2048) >> 4),
+                          kIdAcc, (first && kk == 0) ? 0u : 1u);
+            // with a ring of two or more stages the next S^T goes ahead of dK
+            // and dQ^T, so the row warps can start on it while those run
+            const bool ahead = C::STAGES >= 2 && s + 1 < nsteps;
+            if (ahead) {
+              if (!wait_q(g + 1)) break;
+              issue_s(g + 1);
+            }
+            // dK_h += dS^T Q_i[:, h]
+            if (!mbar_wait(&sm.ds_full, g & 1, abort, kWaitTimeoutNs)) {
+              fail(kSiteMmaDs);
+              break;
+            }
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < BQ / 16; ++kk)
+              mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + kk * 8, dQmn + ((kk * 2048) >> 4),
+                          kIdAcc, (first && kk == 0) ? 0u : 1u);
+            mma_commit(&sm.q_empty[st]);
+            // dQ^T_h = K[:, h]^T dS^T, once the drain has emptied the previous one
+            if (g > 0 && !mbar_wait(&sm.dq_free, (g - 1) & 1, abort, kWaitTimeoutNs)) {
+              fail(kSiteMmaDq);
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t b = g & 1;
+            const uint64_t dDS = sdesc_sw128(smem_u32(sm.ds[b]), KCH, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_bf16_ss(tmem + C::TM_DQ, dKmn + ((kk * 2048) >> 4), dDS + ((kk * 2048) >> 4),
+                          kIdDq, kk > 0 ? 1u : 0u);
+            mma_commit(&sm.dq_full);
+            mma_commit(&sm.ds_free[b]);
+            if (s + 1 < nsteps) {
+              if (!ahead) {
+                if (!wait_q(g + 1)) break;
+                issue_s(g + 1);
+              }
+              issue_dp(g + 1);
+            } else {
+              mma_commit(&sm.acc_full);
+              mma_commit(&sm.kv_empty);
+            }
+          }
+          ++w_it;
+        }
+      }
+      // every tcgen05 op issued above must finish before tensor memory is freed
+      mma_commit(&sm.mma_done);
+      if (!mbar_wait(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
+        record_failure(p.status, abort, kSiteDtDrain);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ key-row warps
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;            // key row of the block = tensor-memory lane
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float c2 = p.scale_log2;
+    __nv_bfloat16* dk_out = static_cast<__nv_bfloat16*>(p.dk);
+    __nv_bfloat16* dv_out = static_cast<__nv_bfloat16*>(p.dv);
+    uint32_t w_it = 0, g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+      int bh, pp, h;
+      sched.decode(u, bh, pp, h);
+      for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
+        const int n = sched.block(pp, kt);
+        const int len = dt_len(p, bh);
+        int i0, i1;
+        dt_range(p, n, len, i0, i1);
+        const int key = n * BK + r;
+        const size_t out_off = (static_cast<size_t>(bh) * p.N + key) * D + h * DH;
+        if (i0 >= i1) {
+          // key block entirely past the sequence: zero gradients
+          if (key < p.N) {
+            uint4* a = reinterpret_cast<uint4*>(dk_out + out_off);
+            uint4* bq = reinterpret_cast<uint4*>(dv_out + out_off);
+#pragma unroll
+            for (int t = 0; t < DH / 8; ++t) {
+              a[t] = make_uint4(0, 0, 0, 0);
+              bq[t] = make_uint4(0, 0, 0, 0);
+            }
+          }
+          continue;
+        }
+        for (int i = i0; i < i1; ++i, ++g) {
+          const int st = g % C::STAGES;
+          const int q0 = i * BQ;
+          // ---- P^T = exp2(S^T * c - L2), masked; bf16 copy back to tensor memory
+          if (!warp_wait(&sm.s_full, g & 1, abort)) {
+            if (lane == 0) record_failure(p.status, abort, kSiteRowS);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const bool need_mask = (n * BK + BK > len) || (p.causal && n * BK + BK - 1 > q0);
+          const bool row_dead = key >= len;                       // whole row masked
+          const int lim_causal = p.causal ? key - q0 : -BQ - 1;   // c < lim_causal masked
+          float pr[BQ];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t sr[32];
+            tmem_ld_x32(t_lane + C::TM_S + 32 * half, sr);
+            tmem_wait_ld();
+            reg_fence<32>(sr);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const float4 l4 = reinterpret_cast<const float4*>(sm.lse2[st])[8 * half + t];
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int c = 32 * half + 4 * t + e;
+                float pv = ex2_approx(fmaf(__uint_as_float(sr[4 * t + e]), c2, -lv[e]));
+                if (need_mask && (row_dead || c < lim_causal)) pv = 0.f;
+                pr[c] = pv;
+              }
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+              pk[t] = pack_bf16x2(pr[32 * half + 2 * t], pr[32 * half + 2 * t + 1]);
+            tmem_st_x16(t_lane + C::TM_S + 16 * half, pk);
+          }
+          tmem_wait_st();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.p_full);
+          // ---- dS^T = P^T o (dP^T - D)
+          if (!warp_wait(&sm.dp_full, g & 1, abort)) {
+            if (lane == 0) record_failure(p.status, abort, kSiteRowDp);
+            ok = false;
+            break;
+          }
+          // the shared copy (B operand of dQ^T) goes to buffer g & 1 once the
+          // dQ^T that last read that buffer has finished
+          const uint32_t b = g & 1;
+          if (!warp_wait(&sm.ds_free[b], ((g >> 1) & 1) ^ 1, abort)) {
+            if (lane == 0) record_failure(p.status, abort, kSiteRowDsFree);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          uint8_t* rowp = sm.ds[b] + r * 128;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t sr[32];
+            tmem_ld_x32(t_lane + C::TM_DP + 32 * half, sr);
+            tmem_wait_ld();
+            reg_fence<32>(sr);
+            uint32_t pk[16];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const float4 d4 = reinterpret_cast<const float4*>(sm.delta[st])[8 * half + t];
+              const int c = 32 * half + 4 * t;
+              pk[2 * t] = pack_bf16x2(pr[c] * (__uint_as_float(sr[4 * t]) - d4.x),
+                                      pr[c + 1] * (__uint_as_float(sr[4 * t + 1]) - d4.y));
+              pk[2 * t + 1] = pack_bf16x2(pr[c + 2] * (__uint_as_float(sr[4 * t + 2]) - d4.z),
+                                          pr[c + 3] * (__uint_as_float(sr[4 * t + 3]) - d4.w));
+            }
+            tmem_st_x16(t_lane + C::TM_DP + 16 * half, pk);
+            // row = key r, 64 queries = 8 units of 16 bytes, XOR-swizzled by (r & 7)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int unit = 4 * half + t;
+              *reinterpret_cast<uint4*>(rowp + ((unit ^ (r & 7)) << 4)) =
+                  make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+          tmem_wait_st();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.ds_full);
+        }
+        if (!ok) break;
+        // ---- dK_h, dV_h rows of this key block
+        if (!warp_wait(&sm.acc_full, w_it & 1, abort)) {
+          if (lane == 0) record_failure(p.status, abort, kSiteRowAcc);
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll 1
+        for (int c4 = 0; c4 < DH / 32; ++c4) {
+          uint32_t a[32], bb[32];
+          tmem_ld_x32(t_lane + C::TM_DV + 32 * c4, a);
+          tmem_ld_x32(t_lane + C::TM_DK + 32 * c4, bb);
+          tmem_wait_ld();
+          reg_fence<32>(a);
+          reg_fence<32>(bb);
+          if (key < p.N) {
+            uint32_t pv[16], pkk[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+              pv[t] = pack_bf16x2(__uint_as_float(a[2 * t]), __uint_as_float(a[2 * t + 1]));
+              pkk[t] = pack_bf16x2(__uint_as_float(bb[2 * t]) * p.scale,
+                                   __uint_as_float(bb[2 * t + 1]) * p.scale);
+            }
+            uint4* dvp = reinterpret_cast<uint4*>(dv_out + out_off + 32 * c4);
+            uint4* dkp = reinterpret_cast<uint4*>(dk_out + out_off + 32 * c4);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              dvp[t] = make_uint4(pv[4 * t], pv[4 * t + 1], pv[4 * t + 2], pv[4 * t + 3]);
+              dkp[t] = make_uint4(pkk[4 * t], pkk[4 * t + 1], pkk[4 * t + 2], pkk[4 * t + 3]);
+            }
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_free);
+        ++w_it;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain warps
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;            // head-dimension column within the half
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    uint32_t g = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+      int bh, pp, h;
+      sched.decode(u, bh, pp, h);
+      for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
+        const int n = sched.block(pp, kt);
+        int i0, i1;
+        dt_range(p, n, dt_len(p, bh), i0, i1);
+        for (int i = i0; i < i1; ++i, ++g) {
+          if (!warp_wait(&sm.dq_full, g & 1, abort)) {
+            if (lane == 0) record_failure(p.status, abort, kSiteDrainDq);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const int q0 = i * BQ;
+          float* acc = p.dq_acc + (static_cast<size_t>(bh) * p.N + q0) * D + h * DH + r;
+          const int nq = p.N - q0 < BQ ? p.N - q0 : BQ;
+          uint32_t v0[32], v1[32];
+          tmem_ld_x32(t_lane + C::TM_DQ, v0);
+          tmem_ld_x32(t_lane + C::TM_DQ + 32, v1);
+          tmem_wait_ld();
+          reg_fence<32>(v0);
+          reg_fence<32>(v1);
+          // the whole tile is in registers: tensor memory is free for the next dQ^T
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.dq_free);
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c < nq) atomicAdd(acc + static_cast<size_t>(c) * D, __uint_as_float(v0[c]));
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (32 + c < nq) atomicAdd(acc + static_cast<size_t>(32 + c) * D, __uint_as_float(v1[c]));
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, DtCfg<D>::TM_COLS);
+  }
+}
+
+template <int D>
+cudaError_t launch(const BwdParams& p, int num_sms, int max_smem, cudaStream_t stream) {
+  const size_t smem = smem_request(sizeof(DtSmem<D>), max_smem);
+  cudaError_t e = cudaFuncSetAttribute(bwd_dt_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int T = (p.N + BK - 1) / BK;
+  const long long per_bh = p.causal ? (T + 1) / 2 : T;
+  const long long units = static_cast<long long>(p.B) * p.H * per_bh * DtCfg<D>::NSPLIT;
+  const int grid = static_cast<int>(units < num_sms ? units : num_sms);
+  bwd_dt_kernel<D><<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main_dt(const BwdParams& p, int d, int num_sms, int max_smem,
+                               cudaStream_t stream) {
+  switch (d) {
+    case 128: return launch<128>(p, num_sms, max_smem, stream);
+    case 256: return launch<256>(p, num_sms, max_smem, stream);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+}  // namespace fa

@@ -29,6 +29,11 @@ SMALL = [
     (3, 2, 257, 128, True, (100, 257)),
     (1, 1, 1, 64, True, None),
     (1, 2, 17, 128, False, None),
+    (2, 2, 320, 128, True, (200, 320)),
+    (1, 2, 200, 256, True, None),
+    (2, 1, 260, 256, False, (130, 260)),
+    (1, 1, 64, 256, False, None),
+    (2, 1, 129, 256, True, None),
 ]
 
 
@@ -82,6 +87,15 @@ def test_gpt2_config_backward_sampled_heads():
 
 def test_large_head_d128_config_backward_sampled_heads():
     w = WORKLOADS["large_head_b2_h16_n8192_d128_causal"]
+    inp = make_inputs(w)
+    g, o, lse = P.gpu_forward(w, inp)
+    grads = P.gpu_backward(w, g, o, lse)
+    errs = P.compare_backward(w, inp, grads, [(0, 0), (1, 15)])
+    print(f"{w.name}: rel errs dQ dK dV = {errs}")
+
+
+def test_large_head_d256_config_backward_sampled_heads():
+    w = WORKLOADS["large_head_b2_h16_n8192_d256_causal"]
     inp = make_inputs(w)
     g, o, lse = P.gpu_forward(w, inp)
     grads = P.gpu_backward(w, g, o, lse)
