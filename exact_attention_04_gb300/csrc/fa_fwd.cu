@@ -3,9 +3,10 @@
 // One CTA per SM (persistent), 192 threads in four roles:
 //   warp 0      TMA producer: Q tile once per tile, then K_j and V_j into a
 //               STAGES-deep shared-memory ring (full/empty mbarriers).
-//   warp 1      MMA issuer (one thread): S = Q K_j^T into tensor memory,
-//               then O += P_j V_j with P read from tensor memory.  Also
-//               allocates and frees the tensor memory.
+//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two S
+//               buffers in tensor memory, issued two blocks ahead of the
+//               softmax, and O += P_j V_j with P read from tensor memory.
+//               Also allocates and frees the tensor memory.
 //   warps 2..5  softmax: thread r owns query row r of the tile (TMEM lane r).
 //               Reads its row of S, masks, updates the running max m and sum
 //               l, writes P = exp2(S*c - m) as bf16 into tensor memory,
@@ -25,8 +26,11 @@
 //
 // Loop order: outer over Q tiles, inner over key blocks (section 4.4.3);
 // key blocks entirely above the causal diagonal are never loaded (section
-// 4.3.2, last note).  Tensor memory columns: S [0,128), O [128, 128+D),
-// P double buffer [128+D, 256+D) as packed bf16 pairs (64 columns each).
+// 4.3.2, last note).  Tensor memory columns: S double buffer [0,256) (P of
+// each block as packed bf16 pairs over the first 64 columns of its S buffer),
+// O [256, 256+D).  Because S_{j+1} sits in the other buffer, the tensor core
+// computes it while the softmax works on S_j, and P_j V_j and S_{j+2} follow
+// without waiting for a round trip through the softmax warps.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -49,11 +53,12 @@ struct Cfg {
   static constexpr int NCH = D / 64;                 // 128-byte column chunks per row
   static constexpr int TILE_BYTES = NCH * CHUNK;     // one Q tile or one K/V block
   static constexpr int STAGES = D == 64 ? 4 : (D == 128 ? 3 : 1);
+  // S double buffer: block g uses columns [128*(g&1), +128); its P (packed
+  // bf16 pairs) is written over the first 64 of those columns.
   static constexpr uint32_t TM_S = 0;
-  static constexpr uint32_t TM_O = 128;
-  static constexpr uint32_t TM_P = 128 + D;
+  static constexpr uint32_t TM_O = 256;
   static constexpr uint32_t TM_COLS = 512;
-  static_assert(TM_P + 128 <= TM_COLS, "tensor memory budget");
+  static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
 };
 
 template <int D>
@@ -64,8 +69,9 @@ struct FwdSmem {
   uint64_t q_full, q_empty;
   uint64_t k_full[Cfg<D>::STAGES], k_empty[Cfg<D>::STAGES];
   uint64_t v_full[Cfg<D>::STAGES], v_empty[Cfg<D>::STAGES];
-  uint64_t s_full, s_free;
-  uint64_t p_full[2], p_free[2];
+  uint64_t s_full[2];          // S of block g is in buffer g & 1
+  uint64_t p_full[2];          // softmax is done with S buffer b and wrote its P
+  uint64_t pv_done[2];         // O += P V of block g (buffer g & 1) has completed
   uint64_t o_free;
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -158,11 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
     }
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.s_free, 4);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.s_full[b], 1);
       mbar_init(&sm.p_full[b], 4);
-      mbar_init(&sm.p_free[b], 1);
+      mbar_init(&sm.pv_done[b], 1);
     }
     mbar_init(&sm.o_free, 4);
     mbar_init(&sm.mma_done, 1);
@@ -256,15 +261,36 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q), 16, 1024);
       uint32_t q_it = 0, kv_it = 0, t_it = 0;
       bool ok = true;
-      // O += P_i V_i for global block index i; `first` starts a new accumulation.
-      auto issue_pv = [&](uint32_t i, bool first) -> bool {
-        const uint32_t b = i & 1;
-        if (!mbar_wait(&sm.p_full[b], (i >> 1) & 1, abort, kWaitTimeoutNs)) {
+      // S_g = Q K_g^T into S buffer g & 1 (tile's Q already in shared memory).
+      auto issue_s = [&](uint32_t g, bool last_of_tile) -> bool {
+        const int st = g % C::STAGES;
+        if (!mbar_wait(&sm.k_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+          record_failure(p.status, abort, kSiteMmaK);
+          return false;
+        }
+        tc_fence_after_sync();
+        const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[st]), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
+          mma_bf16_ss(tmem + C::TM_S + 128 * (g & 1), dq0 + (off >> 4), dk0 + (off >> 4), kIdescS,
+                      kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&sm.k_empty[st]);
+        mma_commit(&sm.s_full[g & 1]);
+        if (last_of_tile) mma_commit(&sm.q_empty);
+        return true;
+      };
+      // O += P_g V_g with P_g read from S buffer g & 1; `first` starts a new
+      // accumulation and must wait until the previous tile's O has been read.
+      auto issue_pv = [&](uint32_t g, bool first) -> bool {
+        const uint32_t b = g & 1;
+        if (!mbar_wait(&sm.p_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
           record_failure(p.status, abort, kSiteMmaP);
           return false;
         }
-        const int st = i % C::STAGES;
-        if (!mbar_wait(&sm.v_full[st], (i / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+        const int st = g % C::STAGES;
+        if (!mbar_wait(&sm.v_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
           record_failure(p.status, abort, kSiteMmaV);
           return false;
         }
@@ -278,12 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), BN * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_bf16_ts(tmem + C::TM_O, tmem + C::TM_P + 64 * b + kk * 8,
+          mma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + 128 * b + kk * 8,
                       dv0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescPV,
                       (first && kk == 0) ? 0u : 1u);
         }
         mma_commit(&sm.v_empty[st]);
-        mma_commit(&sm.p_free[b]);
+        mma_commit(&sm.pv_done[b]);
         return true;
       };
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
@@ -298,40 +324,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             break;
           }
           ++q_it;
-          for (int j = 0; j < nkv; ++j) {
-            const int st = kv_it % C::STAGES;
-            if (!mbar_wait(&sm.k_full[st], (kv_it / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaK);
-              ok = false;
-              break;
-            }
-            if (!mbar_wait(&sm.s_free, (kv_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaS);
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-            const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[st]), 16, 1024);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
-              mma_bf16_ss(tmem + C::TM_S, dq0 + (off >> 4), dk0 + (off >> 4), kIdescS,
-                          kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&sm.k_empty[st]);
-            mma_commit(&sm.s_full);
-            if (j == nkv - 1) mma_commit(&sm.q_empty);
-            if (j > 0 && !issue_pv(kv_it - 1, j == 1)) {
-              ok = false;
-              break;
-            }
-            ++kv_it;
+          // S_0 and S_1 first; then each P_j V_j is followed by S_{j+2}, whose
+          // buffer P_j V_j has just finished with (the tensor core runs the
+          // MMAs of one thread in issue order).
+          const uint32_t g0 = kv_it;
+          ok = issue_s(g0, nkv == 1) && (nkv == 1 || issue_s(g0 + 1, nkv == 2));
+          for (int j = 0; ok && j < nkv; ++j) {
+            ok = issue_pv(g0 + j, j == 0);
+            if (ok && j + 2 < nkv) ok = issue_s(g0 + j + 2, j + 2 == nkv - 1);
           }
-          if (!ok) break;
-          if (!issue_pv(kv_it - 1, nkv == 1)) {
-            ok = false;
-            break;
-          }
+          kv_it = g0 + nkv;
           ++t_it;
         }
       }
@@ -370,7 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         float m_ref = -INFINITY;    // reference maximum, base-2 units of S*scale
         float l = 0.f;
         for (int j = 0; j < nkv; ++j) {
-          if (!warp_wait(&sm.s_full, kv_it & 1, abort)) {
+          const uint32_t b = kv_it & 1;
+          const uint32_t t_s = t_lane + C::TM_S + 128 * b;      // this block's S buffer
+          if (!warp_wait(&sm.s_full[b], (kv_it >> 1) & 1, abort)) {
             if (lane == 0) record_failure(p.status, abort, kSiteSmS);
             ok = false;
             break;
@@ -378,12 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           tc_fence_after_sync();
           uint32_t sr[BN];
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) tmem_ld_x32(t_lane + C::TM_S + 32 * c, sr + 32 * c);
+          for (int c = 0; c < BN / 32; ++c) tmem_ld_x32(t_s + 32 * c, sr + 32 * c);
           tmem_wait_ld();
           reg_fence<BN>(sr);
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.s_free);
           float s[BN];
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
@@ -434,20 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             pk[c + 1] = pack_bf16x2(p2, p3);
           }
           l = l * alpha + ((rs0 + rs1) + (rs2 + rs3));
-          const uint32_t b = kv_it & 1;
-          if (!warp_wait(&sm.p_free[b], ((kv_it >> 1) & 1) ^ 1, abort)) {
-            if (lane == 0) record_failure(p.status, abort, kSiteSmP);
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          tmem_st_x32(t_lane + C::TM_P + 64 * b, pk);
-          tmem_st_x32(t_lane + C::TM_P + 64 * b + 32, pk + 32);
+          // P over the first 64 columns of this block's S buffer (S is in registers)
+          tmem_st_x32(t_s, pk);
+          tmem_st_x32(t_s + 32, pk + 32);
           if (__any_sync(0xffffffffu, rescale && j > 0)) {
             // O must hold every earlier P V before it is scaled: wait for the
             // previous block's P V to complete.
             const uint32_t prev = kv_it - 1;
-            if (!warp_wait(&sm.p_free[prev & 1], (prev >> 1) & 1, abort)) {
+            if (!warp_wait(&sm.pv_done[prev & 1], (prev >> 1) & 1, abort)) {
               if (lane == 0) record_failure(p.status, abort, kSiteSmO);
               ok = false;
               break;
@@ -473,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         if (!ok) break;
         // epilogue: wait for the tile's last P V, then O / l and LSE
         const uint32_t last = kv_it - 1;
-        if (!warp_wait(&sm.p_free[last & 1], (last >> 1) & 1, abort)) {
+        if (!warp_wait(&sm.pv_done[last & 1], (last >> 1) & 1, abort)) {
           if (lane == 0) record_failure(p.status, abort, kSiteSmEpi);
           ok = false;
           break;

@@ -68,9 +68,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase of `bar` with parity `parity` to complete.  Never
 // spins forever: gives up after `timeout_ns` of global time, or as soon as
-// another warp of the CTA has raised `*abort` (checked every 64 polls).
-// Returns false when it gave up; the caller then records the failure and
-// leaves its loop.
+// another warp of the CTA has raised `*abort` (checked every 64 polls; pass
+// nullptr for a wait that must not be cut short by the flag).  Returns false
+// when it gave up; the caller then records the failure and leaves its loop.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t timeout_ns) {
   const uint32_t a = smem_u32(bar);
@@ -79,7 +79,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(a, parity)) return true;
     if ((it & 63u) == 0u) {
-      if (*abort) return false;
+      if (abort != nullptr && *abort) return false;
       if (globaltimer_ns() - t0 > timeout_ns) return false;
     }
   }
