@@ -397,13 +397,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             for (int c = 0; c < BN; ++c)
               if (c >= lim_pad || c > lim_causal) s[c] = -INFINITY;
           }
+          // row maximum: four chains of three-input max
           float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-          for (int c = 4; c < BN; c += 4) {
-            mx0 = fmaxf(mx0, s[c]);
-            mx1 = fmaxf(mx1, s[c + 1]);
-            mx2 = fmaxf(mx2, s[c + 2]);
-            mx3 = fmaxf(mx3, s[c + 3]);
+          for (int c = 4; c < BN; c += 8) {
+            mx0 = fmax3(mx0, s[c], s[c + 1]);
+            mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+            mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+            mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
           }
           const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
           float alpha = 1.f;
@@ -419,21 +420,27 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             rescale = true;
           }
           const float base = (m_ref == -INFINITY) ? 0.f : m_ref;
-          float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+          // p = exp2(S*c - m) two lanes at a time: packed FMA for the argument,
+          // packed adds for the row sum, one bf16x2 convert per pair
+          const uint64_t c2x2 = f2_make(c2, c2);
+          const uint64_t nbx2 = f2_make(-base, -base);
+          uint64_t rsa = f2_make(0.f, 0.f), rsb = f2_make(0.f, 0.f);
           uint32_t pk[BN / 2];
 #pragma unroll
           for (int c = 0; c < BN / 2; c += 2) {
-            const float p0 = ex2_approx(fmaf(s[2 * c], c2, -base));
-            const float p1 = ex2_approx(fmaf(s[2 * c + 1], c2, -base));
-            const float p2 = ex2_approx(fmaf(s[2 * c + 2], c2, -base));
-            const float p3 = ex2_approx(fmaf(s[2 * c + 3], c2, -base));
-            rs0 += p0;
-            rs1 += p1;
-            rs2 += p2;
-            rs3 += p3;
+            float a0, a1, a2, a3;
+            f2_split(f2_fma(f2_make(s[2 * c], s[2 * c + 1]), c2x2, nbx2), a0, a1);
+            f2_split(f2_fma(f2_make(s[2 * c + 2], s[2 * c + 3]), c2x2, nbx2), a2, a3);
+            const float p0 = ex2_approx(a0), p1 = ex2_approx(a1);
+            const float p2 = ex2_approx(a2), p3 = ex2_approx(a3);
+            rsa = f2_add(rsa, f2_make(p0, p1));
+            rsb = f2_add(rsb, f2_make(p2, p3));
             pk[c] = pack_bf16x2(p0, p1);
             pk[c + 1] = pack_bf16x2(p2, p3);
           }
+          float rs0, rs1, rs2, rs3;
+          f2_split(rsa, rs0, rs1);
+          f2_split(rsb, rs2, rs3);
           l = l * alpha + ((rs0 + rs1) + (rs2 + rs3));
           // P over the first 64 columns of this block's S buffer (S is in registers)
           tmem_st_x32(t_s, pk);
