@@ -100,6 +100,22 @@ bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int box_ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [BH, N, d] accumulator as a 3-D tensor (d, N, BH): box of 128
+// columns x 64 rows, no swizzle (the target of bulk reduce-adds).
+bool make_acc_map(CUtensorMap* m, void* base, int d, int N, int BH) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(d) * N * 4};
+  const cuuint32_t box[3] = {128, 64, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t round_up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
@@ -212,6 +228,7 @@ fa_status_t bwd_main_impl(fa::BwdParams& p, const DeviceInfo* di, const void* q,
   if (!make_map(&p.tq, q, d, p.N, BH, qrows) || !make_map(&p.tk, k, d, p.N, BH) ||
       !make_map(&p.tv, v, d, p.N, BH) || !make_map(&p.tdo, dO, d, p.N, BH, qrows))
     return FA_ERR_CUDA;
+  if (dt && !make_acc_map(&p.tdq, p.dq_acc, d, p.N, BH)) return FA_ERR_CUDA;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = dt ? fa::launch_bwd_main_dt(p, d, di->num_sms, di->max_smem, s)
                            : fa::launch_bwd_main(p, d, di->num_sms, di->max_smem, s);

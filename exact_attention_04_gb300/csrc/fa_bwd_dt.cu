@@ -9,9 +9,11 @@
 //   P^T   = exp2(S^T*c - L2_i)  and  dS^T = P^T o (dP^T - D_i)   (row warps)
 //   dV_h += P^T dO_i[:, h]      dK_h += dS^T Q_i[:, h]           (A from tensor memory)
 //   dQ^T_h = K[:, h]^T dS^T     (128 head-dim rows x 64 queries)
-// dQ^T sits in tensor memory with one lane per head-dimension column, so the
-// four drain warps add it to the fp32 accumulator in global memory with
-// atomics that are contiguous across each warp (128 bytes per instruction).
+// dQ^T sits in tensor memory with one lane per head-dimension column.  For
+// d = 128 the four drain warps write it transposed into a shared staging tile
+// and one thread adds the tile to the fp32 accumulator in global memory with a
+// single bulk tensor reduce-add (the L2 does the adds); for d = 256 (no room
+// for the tile) they use atomics that are contiguous across each warp.
 // With d = 256 the two halves of a key block are separate work items; both
 // recompute S^T and dP^T (the price of fitting dK and dV in tensor memory).
 //
@@ -50,6 +52,9 @@ struct DtCfg {
   static constexpr int KV_BYTES = NCH * KCH;
   static constexpr int Q_BYTES = NCH * QCH;
   static constexpr int STAGES = D == 128 ? 3 : 1;
+  // d = 128 has room for a 64 x 128 fp32 staging tile: dQ^T goes to global
+  // memory as one bulk reduce-add per step.  d = 256 uses atomics.
+  static constexpr bool DQ_TMA = (D == 128);
   static constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DV = 128, TM_DK = 256, TM_DQ = 384;
   static constexpr uint32_t TM_COLS = 512;
 };
@@ -61,11 +66,13 @@ struct DtSmem {
   alignas(1024) uint8_t q[DtCfg<D>::STAGES][DtCfg<D>::Q_BYTES];
   alignas(1024) uint8_t dO[DtCfg<D>::STAGES][DtCfg<D>::Q_BYTES];
   alignas(1024) uint8_t ds[2][KCH];              // dS^T bf16, 128 keys x 64 queries, double buffer
+  alignas(1024) float dq_stage[DtCfg<D>::DQ_TMA ? BQ * DH : 4];   // dQ tile, [query][d]
   alignas(16) float lse2[DtCfg<D>::STAGES][BQ];
   alignas(16) float delta[DtCfg<D>::STAGES][BQ];
   uint64_t kv_full, kv_empty;
   uint64_t q_full[DtCfg<D>::STAGES], q_empty[DtCfg<D>::STAGES];
   uint64_t s_full, p_full, dp_full, ds_full, ds_free[2], dq_full, dq_free, acc_full, acc_free;
+  uint64_t stage_full, stage_free;
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -73,7 +80,8 @@ struct DtSmem {
 
 enum Site {
   kSiteProdKV = 64, kSiteProdQ, kSiteMmaKV, kSiteMmaQ, kSiteMmaP, kSiteMmaDs, kSiteMmaDq,
-  kSiteMmaAcc, kSiteRowS, kSiteRowDp, kSiteRowDsFree, kSiteRowAcc, kSiteDrainDq, kSiteDtDrain
+  kSiteMmaAcc, kSiteRowS, kSiteRowDp, kSiteRowDsFree, kSiteRowAcc, kSiteDrainDq, kSiteDtDrain,
+  kSiteStageFree, kSiteStageFull
 };
 
 __device__ __forceinline__ void record_failure(int* status, volatile int* abort, int site) {
@@ -167,6 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
     mbar_init(&sm.dq_free, 4);
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_free, 4);
+    mbar_init(&sm.stage_full, 4);
+    mbar_init(&sm.stage_free, 1);
     mbar_init(&sm.mma_done, 1);
     fence_mbar_init();
   }
@@ -418,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           const bool row_dead = key >= len;                       // whole row masked
           const int lim_causal = p.causal ? key - q0 : -BQ - 1;   // c < lim_causal masked
           float pr[BQ];
+          const uint64_t c2x2 = f2_make(c2, c2);
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             uint32_t sr[32];
@@ -427,11 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
               const float4 l4 = reinterpret_cast<const float4*>(sm.lse2[st])[8 * half + t];
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+              float a[4];
+              f2_split(f2_fma(f2_make(__uint_as_float(sr[4 * t]), __uint_as_float(sr[4 * t + 1])),
+                              c2x2, f2_make(-l4.x, -l4.y)),
+                       a[0], a[1]);
+              f2_split(f2_fma(f2_make(__uint_as_float(sr[4 * t + 2]), __uint_as_float(sr[4 * t + 3])),
+                              c2x2, f2_make(-l4.z, -l4.w)),
+                       a[2], a[3]);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int c = 32 * half + 4 * t + e;
-                float pv = ex2_approx(fmaf(__uint_as_float(sr[4 * t + e]), c2, -lv[e]));
+                float pv = ex2_approx(a[e]);
                 if (need_mask && (row_dead || c < lim_causal)) pv = 0.f;
                 pr[c] = pv;
               }
@@ -473,10 +490,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
             for (int t = 0; t < 8; ++t) {
               const float4 d4 = reinterpret_cast<const float4*>(sm.delta[st])[8 * half + t];
               const int c = 32 * half + 4 * t;
-              pk[2 * t] = pack_bf16x2(pr[c] * (__uint_as_float(sr[4 * t]) - d4.x),
-                                      pr[c + 1] * (__uint_as_float(sr[4 * t + 1]) - d4.y));
-              pk[2 * t + 1] = pack_bf16x2(pr[c + 2] * (__uint_as_float(sr[4 * t + 2]) - d4.z),
-                                          pr[c + 3] * (__uint_as_float(sr[4 * t + 3]) - d4.w));
+              float d0, d1, d2, d3;
+              f2_split(f2_mul(f2_add(f2_make(__uint_as_float(sr[4 * t]), __uint_as_float(sr[4 * t + 1])),
+                                     f2_make(-d4.x, -d4.y)),
+                              f2_make(pr[c], pr[c + 1])),
+                       d0, d1);
+              f2_split(f2_mul(f2_add(f2_make(__uint_as_float(sr[4 * t + 2]), __uint_as_float(sr[4 * t + 3])),
+                                     f2_make(-d4.z, -d4.w)),
+                              f2_make(pr[c + 2], pr[c + 3])),
+                       d2, d3);
+              pk[2 * t] = pack_bf16x2(d0, d1);
+              pk[2 * t + 1] = pack_bf16x2(d2, d3);
             }
             tmem_st_x16(t_lane + C::TM_DP + 16 * half, pk);
             // row = key r, 64 queries = 8 units of 16 bytes, XOR-swizzled by (r & 7)
@@ -537,6 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;            // head-dimension column within the half
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const bool issuer = (warp == 6 && lane == 0); // issues the bulk reduce-adds
+    if (C::DQ_TMA && issuer) prefetch_tmap(&p.tdq);
     uint32_t g = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
@@ -554,8 +580,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           }
           tc_fence_after_sync();
           const int q0 = i * BQ;
-          float* acc = p.dq_acc + (static_cast<size_t>(bh) * p.N + q0) * D + h * DH + r;
-          const int nq = p.N - q0 < BQ ? p.N - q0 : BQ;
           uint32_t v0[32], v1[32];
           tmem_ld_x32(t_lane + C::TM_DQ, v0);
           tmem_ld_x32(t_lane + C::TM_DQ + 32, v1);
@@ -566,15 +590,51 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.dq_free);
+          if constexpr (C::DQ_TMA) {
+            // staging tile [64 queries][128 columns]: this thread owns column r
+            if (!warp_wait(&sm.stage_free, (g & 1) ^ 1, abort)) {
+              if (lane == 0) record_failure(p.status, abort, kSiteStageFree);
+              ok = false;
+              break;
+            }
+            float* stg = sm.dq_stage + r;
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c < nq) atomicAdd(acc + static_cast<size_t>(c) * D, __uint_as_float(v0[c]));
+            for (int c = 0; c < 32; ++c) stg[c * DH] = __uint_as_float(v0[c]);
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (32 + c < nq) atomicAdd(acc + static_cast<size_t>(32 + c) * D, __uint_as_float(v1[c]));
+            for (int c = 0; c < 32; ++c) stg[(32 + c) * DH] = __uint_as_float(v1[c]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.stage_full);
+            if (issuer) {
+              if (!mbar_wait(&sm.stage_full, g & 1, abort, kWaitTimeoutNs)) {
+                record_failure(p.status, abort, kSiteStageFull);
+                ok = false;
+              } else {
+                // rows past N fall outside the tensor and are not written
+                tma_reduce_add_3d(&p.tdq, sm.dq_stage, h * DH, q0, bh);
+                bulk_commit_group();
+                bulk_wait_group_read<0>();
+                mbar_arrive(&sm.stage_free);
+              }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+          } else {
+            float* acc = p.dq_acc + (static_cast<size_t>(bh) * p.N + q0) * D + h * DH + r;
+            const int nq = p.N - q0 < BQ ? p.N - q0 : BQ;
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (c < nq) atomicAdd(acc + static_cast<size_t>(c) * D, __uint_as_float(v0[c]));
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (32 + c < nq)
+                atomicAdd(acc + static_cast<size_t>(32 + c) * D, __uint_as_float(v1[c]));
+          }
         }
       }
     }
+    // every reduce-add must have landed before the CTA exits
+    if (C::DQ_TMA && issuer) bulk_wait_group<0>();
   }
 
   tc_fence_before_sync();

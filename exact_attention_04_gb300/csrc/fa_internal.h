@@ -29,6 +29,7 @@ struct FwdParams {
 
 struct BwdParams {
   CUtensorMap tq, tk, tv, tdo; // bf16 [BH, N, d] as above
+  CUtensorMap tdq;             // fp32 dQ accumulator [BH, N, d], box (128, 64, 1), no swizzle
   const void* o;               // bf16 [B, H, N, d]
   const void* dO;              // bf16 [B, H, N, d]
   const float* lse;            // fp32 [B, H, N]
