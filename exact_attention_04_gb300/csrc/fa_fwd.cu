@@ -1,13 +1,17 @@
 // Attention forward for sm_103a.
 //
-// One CTA per SM (persistent), 192 threads in four roles:
+// One CTA per SM (persistent), 224 threads in four roles:
 //   warp 0      TMA producer: Q tile once per tile, then K_j and V_j into a
 //               STAGES-deep shared-memory ring (full/empty mbarriers).
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two S
-//               buffers in tensor memory, issued two blocks ahead of the
-//               softmax, and O += P_j V_j with P read from tensor memory.
-//               Also allocates and frees the tensor memory.
-//   warps 2..5  softmax: thread r owns query row r of the tile (TMEM lane r).
+//   warp 1      S issuer (one thread): S_j = Q K_j^T into one of NSB S
+//               buffers in tensor memory, running ahead of the softmax as far
+//               as the buffers allow.  Also allocates and frees the tensor
+//               memory.
+//   warp 2      P V issuer (one thread): O += P_j V_j with P read from tensor
+//               memory.  A tcgen05.mma holds its issuing thread for about as
+//               long as the tensor core needs to run it, so the two products
+//               are issued from two threads on different sub-partitions.
+//   warps 3..6  softmax: thread r owns query row r of the tile (TMEM lane r).
 //               Reads its row of S, masks, updates the running max m and sum
 //               l, writes P = exp2(S*c - m) as bf16 into tensor memory,
 //               rescales its row of O when m moved, and runs the epilogue
@@ -26,11 +30,10 @@
 //
 // Loop order: outer over Q tiles, inner over key blocks (section 4.4.3);
 // key blocks entirely above the causal diagonal are never loaded (section
-// 4.3.2, last note).  Tensor memory columns: S double buffer [0,256) (P of
-// each block as packed bf16 pairs over the first 64 columns of its S buffer),
-// O [256, 256+D).  Because S_{j+1} sits in the other buffer, the tensor core
-// computes it while the softmax works on S_j, and P_j V_j and S_{j+2} follow
-// without waiting for a round trip through the softmax warps.
+// 4.3.2, last note).  Tensor memory columns: NSB S buffers of 128 (P of each
+// block as packed bf16 pairs over the first 64 columns of its S buffer), then
+// O [128*NSB, 128*NSB + D).  S_{j+NSB} may overwrite S buffer j % NSB only
+// after P_j V_j has completed (pv_done), which the S issuer waits for.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -46,17 +49,19 @@ constexpr int BM = 128;          // query rows per tile = TMEM lanes = MMA M
 constexpr int BN = 128;          // keys per block = MMA N of S
 constexpr int CHUNK = 128 * 128; // bytes of one 128-row x 64-column bf16 chunk (SW128 atom rows)
 constexpr float kRescaleSlack = 8.0f;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 
 template <int D>
 struct Cfg {
   static constexpr int NCH = D / 64;                 // 128-byte column chunks per row
   static constexpr int TILE_BYTES = NCH * CHUNK;     // one Q tile or one K/V block
   static constexpr int STAGES = D == 64 ? 4 : (D == 128 ? 3 : 1);
-  // S double buffer: block g uses columns [128*(g&1), +128); its P (packed
-  // bf16 pairs) is written over the first 64 of those columns.
+  // NSB S buffers: block g uses columns [128*(g%NSB), +128); its P (packed
+  // bf16 pairs) is written over the first 64 of those columns.  Three
+  // buffers where O leaves room (d <= 128), two for d = 256.
+  static constexpr int NSB = D <= 128 ? 3 : 2;
   static constexpr uint32_t TM_S = 0;
-  static constexpr uint32_t TM_O = 256;
+  static constexpr uint32_t TM_O = 128 * NSB;
   static constexpr uint32_t TM_COLS = 512;
   static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
 };
@@ -69,11 +74,11 @@ struct FwdSmem {
   uint64_t q_full, q_empty;
   uint64_t k_full[Cfg<D>::STAGES], k_empty[Cfg<D>::STAGES];
   uint64_t v_full[Cfg<D>::STAGES], v_empty[Cfg<D>::STAGES];
-  uint64_t s_full[2];          // S of block g is in buffer g & 1
-  uint64_t p_full[2];          // softmax is done with S buffer b and wrote its P
-  uint64_t pv_done[2];         // O += P V of block g (buffer g & 1) has completed
+  uint64_t s_full[Cfg<D>::NSB];   // S of block g is in buffer g % NSB
+  uint64_t p_full[Cfg<D>::NSB];   // softmax is done with S buffer b and wrote its P
+  uint64_t pv_done[Cfg<D>::NSB];  // O += P V of block g (buffer g % NSB) has completed
   uint64_t o_free;
-  uint64_t mma_done;
+  uint64_t mma_done, pv_mma_done;
   uint32_t tmem_base;
   int abort;
 };
@@ -164,11 +169,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NSB; ++b) {
       mbar_init(&sm.s_full[b], 1);
       mbar_init(&sm.p_full[b], 4);
       mbar_init(&sm.pv_done[b], 1);
     }
+    mbar_init(&sm.pv_mma_done, 1);
     mbar_init(&sm.o_free, 4);
     mbar_init(&sm.mma_done, 1);
     fence_mbar_init();
@@ -254,64 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, 0, 0);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 0, 1);
       const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q), 16, 1024);
-      uint32_t q_it = 0, kv_it = 0, t_it = 0;
+      uint32_t q_it = 0, g = 0;
       bool ok = true;
-      // S_g = Q K_g^T into S buffer g & 1 (tile's Q already in shared memory).
-      auto issue_s = [&](uint32_t g, bool last_of_tile) -> bool {
-        const int st = g % C::STAGES;
-        if (!mbar_wait(&sm.k_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
-          record_failure(p.status, abort, kSiteMmaK);
-          return false;
-        }
-        tc_fence_after_sync();
-        const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[st]), 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
-          mma_bf16_ss(tmem + C::TM_S + 128 * (g & 1), dq0 + (off >> 4), dk0 + (off >> 4), kIdescS,
-                      kk > 0 ? 1u : 0u);
-        }
-        mma_commit(&sm.k_empty[st]);
-        mma_commit(&sm.s_full[g & 1]);
-        if (last_of_tile) mma_commit(&sm.q_empty);
-        return true;
-      };
-      // O += P_g V_g with P_g read from S buffer g & 1; `first` starts a new
-      // accumulation and must wait until the previous tile's O has been read.
-      auto issue_pv = [&](uint32_t g, bool first) -> bool {
-        const uint32_t b = g & 1;
-        if (!mbar_wait(&sm.p_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
-          record_failure(p.status, abort, kSiteMmaP);
-          return false;
-        }
-        const int st = g % C::STAGES;
-        if (!mbar_wait(&sm.v_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
-          record_failure(p.status, abort, kSiteMmaV);
-          return false;
-        }
-        if (first && !mbar_wait(&sm.o_free, (t_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
-          record_failure(p.status, abort, kSiteMmaO);
-          return false;
-        }
-        tc_fence_after_sync();
-        // V block: BN rows (keys) x D columns, MN-major B operand: 64-column
-        // chunks BN*128 bytes apart (LBO), 8-key groups 1024 bytes apart (SBO).
-        const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), BN * 128, 1024);
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + 128 * b + kk * 8,
-                      dv0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescPV,
-                      (first && kk == 0) ? 0u : 1u);
-        }
-        mma_commit(&sm.v_empty[st]);
-        mma_commit(&sm.pv_done[b]);
-        return true;
-      };
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
         for (int kt = 0; ok && kt < sched.ntiles(u); ++kt) {
           int bh, m;
@@ -324,22 +278,91 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             break;
           }
           ++q_it;
-          // S_0 and S_1 first; then each P_j V_j is followed by S_{j+2}, whose
-          // buffer P_j V_j has just finished with (the tensor core runs the
-          // MMAs of one thread in issue order).
-          const uint32_t g0 = kv_it;
-          ok = issue_s(g0, nkv == 1) && (nkv == 1 || issue_s(g0 + 1, nkv == 2));
-          for (int j = 0; ok && j < nkv; ++j) {
-            ok = issue_pv(g0 + j, j == 0);
-            if (ok && j + 2 < nkv) ok = issue_s(g0 + j + 2, j + 2 == nkv - 1);
+          for (int j = 0; j < nkv; ++j, ++g) {
+            const uint32_t b = g % C::NSB;
+            // buffer b last held block g - NSB: its P V must be complete
+            if (g >= static_cast<uint32_t>(C::NSB) &&
+                !mbar_wait(&sm.pv_done[b], ((g / C::NSB) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteMmaS);
+              ok = false;
+              break;
+            }
+            const int st = g % C::STAGES;
+            if (!mbar_wait(&sm.k_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteMmaK);
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[st]), 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
+              mma_bf16_ss(tmem + C::TM_S + 128 * b, dq0 + (off >> 4), dk0 + (off >> 4), kIdescS,
+                          kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&sm.k_empty[st]);
+            mma_commit(&sm.s_full[b]);
+            if (j == nkv - 1) mma_commit(&sm.q_empty);
           }
-          kv_it = g0 + nkv;
+        }
+      }
+      // every tcgen05 op issued by this thread must finish before exit
+      mma_commit(&sm.mma_done);
+      if (!mbar_wait(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
+        record_failure(p.status, abort, kSiteDrain);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ P V issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 0, 1);
+      uint32_t g = 0, t_it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+        for (int kt = 0; ok && kt < sched.ntiles(u); ++kt) {
+          int bh, m;
+          sched.tile(u, kt, bh, m);
+          const int nkv = kv_blocks(m, seq_len(p, bh), p.causal);
+          if (nkv == 0) continue;
+          for (int j = 0; j < nkv; ++j, ++g) {
+            const uint32_t b = g % C::NSB;
+            if (!mbar_wait(&sm.p_full[b], (g / C::NSB) & 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteMmaP);
+              ok = false;
+              break;
+            }
+            const int st = g % C::STAGES;
+            if (!mbar_wait(&sm.v_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteMmaV);
+              ok = false;
+              break;
+            }
+            // a tile's first P V starts a fresh O: the previous tile's epilogue
+            // must have read O out of tensor memory
+            if (j == 0 && !mbar_wait(&sm.o_free, (t_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteMmaO);
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            // V block: BN rows (keys) x D columns, MN-major B operand: 64-column
+            // chunks BN*128 bytes apart (LBO), 8-key groups 1024 bytes apart (SBO).
+            const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), BN * 128, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              mma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + 128 * b + kk * 8,
+                          dv0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescPV,
+                          (j == 0 && kk == 0) ? 0u : 1u);
+            }
+            mma_commit(&sm.v_empty[st]);
+            mma_commit(&sm.pv_done[b]);
+          }
           ++t_it;
         }
       }
-      // Every tcgen05 op issued above must finish before tensor memory is freed.
-      mma_commit(&sm.mma_done);
-      if (!mbar_wait(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
+      mma_commit(&sm.pv_mma_done);
+      if (!mbar_wait(&sm.pv_mma_done, 0, nullptr, kWaitTimeoutNs))
         record_failure(p.status, abort, kSiteDrain);
     }
     __syncwarp();
@@ -372,9 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         float m_ref = -INFINITY;    // reference maximum, base-2 units of S*scale
         float l = 0.f;
         for (int j = 0; j < nkv; ++j) {
-          const uint32_t b = kv_it & 1;
+          const uint32_t b = kv_it % C::NSB;
           const uint32_t t_s = t_lane + C::TM_S + 128 * b;      // this block's S buffer
-          if (!warp_wait(&sm.s_full[b], (kv_it >> 1) & 1, abort)) {
+          if (!warp_wait(&sm.s_full[b], (kv_it / C::NSB) & 1, abort)) {
             if (lane == 0) record_failure(p.status, abort, kSiteSmS);
             ok = false;
             break;
@@ -449,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             // O must hold every earlier P V before it is scaled: wait for the
             // previous block's P V to complete.
             const uint32_t prev = kv_it - 1;
-            if (!warp_wait(&sm.pv_done[prev & 1], (prev >> 1) & 1, abort)) {
+            if (!warp_wait(&sm.pv_done[prev % C::NSB], (prev / C::NSB) & 1, abort)) {
               if (lane == 0) record_failure(p.status, abort, kSiteSmO);
               ok = false;
               break;
@@ -475,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         if (!ok) break;
         // epilogue: wait for the tile's last P V, then O / l and LSE
         const uint32_t last = kv_it - 1;
-        if (!warp_wait(&sm.pv_done[last & 1], (last >> 1) & 1, abort)) {
+        if (!warp_wait(&sm.pv_done[last % C::NSB], (last / C::NSB) & 1, abort)) {
           if (lane == 0) record_failure(p.status, abort, kSiteSmEpi);
           ok = false;
           break;
