@@ -21,12 +21,17 @@
 // 算术强度与分块把 FlashAttention 推导清楚" section 八; "4. FlashAttention 深度
 // 剖析" section 4.3.4.  Gradient formulas: chain rule through the row softmax.
 //
-// Warps: 0 TMA producer, 1 MMA issuer (owns tensor memory), 2..5 key-row warps
-// (P^T, dS^T, dK/dV epilogue), 6..9 dQ drain warps.
-// Tensor memory columns: S^T [0,64) with P^T bf16 over [0,32), dP^T [64,128)
-// with dS^T bf16 over [64,96), dV_h [128,256), dK_h [256,384), dQ^T_h [384,448).
-// Successive tcgen05.mma issued by one thread execute in order, so an MMA that
-// overwrites columns an earlier MMA reads as an operand needs no extra wait.
+// Warps: 0 TMA producer; 1 issuer A (S^T, dP^T, dQ^T; owns tensor memory);
+// 2 issuer B (dV, dK); 3..6 key-row warps (P^T, dS^T, dK/dV epilogue); 7..10
+// dQ drain warps.  A tcgen05.mma holds its issuing thread about as long as
+// the tensor core runs it, so the products are split over two threads.
+// Tensor memory columns: two 64-column S buffers [0,128) (S^T of a step, then
+// its P^T as bf16, then its dQ^T), two dP buffers [128,256) (dP^T, then dS^T
+// as bf16), dV_h [256,384), dK_h [384,512).  With both S and dP double
+// buffered, issuer A can compute the next step's S^T and dP^T while the row
+// warps are still on the current step.  Where one issuer overwrites columns
+// the other issuer's MMA reads, it first waits for that MMA's commit
+// (dv_done, dk_done); within one issuer the tensor core keeps issue order.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -43,7 +48,7 @@ constexpr int BK = 128;            // keys per work item
 constexpr int DH = 128;            // head-dimension columns of dK, dV, dQ per work item
 constexpr int KCH = 128 * 128;     // 128 rows x 128 bytes
 constexpr int QCH = 64 * 128;      // 64 rows x 128 bytes
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 
 template <int D>
 struct DtCfg {
@@ -55,7 +60,11 @@ struct DtCfg {
   // d = 128 has room for a 64 x 128 fp32 staging tile: dQ^T goes to global
   // memory as one bulk reduce-add per step.  d = 256 uses atomics.
   static constexpr bool DQ_TMA = (D == 128);
-  static constexpr uint32_t TM_S = 0, TM_DP = 64, TM_DV = 128, TM_DK = 256, TM_DQ = 384;
+  // Two S buffers [0,64), [64,128): S^T of step g, then P^T (bf16, first 32
+  // columns), then dQ^T of the same step once dV has read P^T.  Two dP
+  // buffers [128,192), [192,256): dP^T, then dS^T (bf16, first 32 columns).
+  // dV [256,384), dK [384,512).
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384;
   static constexpr uint32_t TM_COLS = 512;
 };
 
@@ -71,7 +80,11 @@ struct DtSmem {
   alignas(16) float delta[DtCfg<D>::STAGES][BQ];
   uint64_t kv_full, kv_empty;
   uint64_t q_full[DtCfg<D>::STAGES], q_empty[DtCfg<D>::STAGES];
-  uint64_t s_full, p_full, dp_full, ds_full, ds_free[2], dq_full, dq_free, acc_full, acc_free;
+  // per step-parity buffer b = g & 1 wherever a producer can run a step ahead
+  uint64_t s_full[2], p_full[2], dp_full[2], ds_full[2], ds_free[2];
+  uint64_t dq_full, dq_free, acc_full, acc_free;
+  uint64_t dv_done[2], dk_done[2];  // cross-issuer: P^T / dS^T of a step consumed
+  uint64_t mma_done_b;
   uint64_t stage_full, stage_free;
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -163,14 +176,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
     mbar_init(&sm.kv_empty, 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&sm.q_full[s], 1);
-      mbar_init(&sm.q_empty[s], 1);
+      mbar_init(&sm.q_empty[s], 2);         // both MMA issuers read the stage
     }
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 4);
-    mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.ds_full, 4);
-    mbar_init(&sm.ds_free[0], 1);
-    mbar_init(&sm.ds_free[1], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.s_full[b], 1);
+      mbar_init(&sm.p_full[b], 4);
+      mbar_init(&sm.dp_full[b], 1);
+      mbar_init(&sm.ds_full[b], 4);
+      mbar_init(&sm.ds_free[b], 1);
+      mbar_init(&sm.dv_done[b], 1);
+      mbar_init(&sm.dk_done[b], 1);
+    }
+    mbar_init(&sm.mma_done_b, 1);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_free, 4);
     mbar_init(&sm.acc_full, 1);
@@ -253,44 +270,62 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ issuer A
+    // S^T(g) into S buffer g&1 once the drain has read dQ^T(g-2) out of it
+    // (waited as: the drain of the last dQ^T issued so far, which is g-2 or
+    // later, so the wait never runs behind the barrier's phase);
+    // dP^T(g) into dP buffer g&1 once dK(g-2) has read dS^T(g-2); dQ^T(g)
+    // into S buffer g&1 once dV(g) has read P^T(g) and the row warps wrote
+    // dS^T(g).  With two or more Q stages the next step's S^T and dP^T are
+    // issued before dQ^T(g).
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(BK, BQ, 0, 0);      // S^T, dP^T
-      constexpr uint32_t kIdAcc = idesc_bf16_f32(BK, DH, 0, 1);    // dV, dK (B MN-major)
       constexpr uint32_t kIdDq = idesc_bf16_f32(DH, BQ, 1, 1);     // dQ^T (A, B MN-major)
       const uint64_t dK0 = sdesc_sw128(smem_u32(sm.k), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sm.v), 16, 1024);
       uint32_t w_it = 0, g = 0;
+      uint32_t n_dq = 0;                       // dQ^T issued so far
       bool ok = true;
       auto fail = [&](int site) {
         record_failure(p.status, abort, site);
         ok = false;
       };
-      auto wait_q = [&](uint32_t gg) -> bool {
-        if (!mbar_wait(&sm.q_full[gg % C::STAGES], (gg / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+      auto issue_s = [&](uint32_t gg) -> bool {
+        const uint32_t b = gg & 1;
+        if (gg >= 2 && !mbar_wait(&sm.dq_free, (n_dq - 1) & 1, abort, kWaitTimeoutNs)) {
+          fail(kSiteMmaDq);
+          return false;
+        }
+        const int st = gg % C::STAGES;
+        if (!mbar_wait(&sm.q_full[st], (gg / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
           fail(kSiteMmaQ);
           return false;
         }
         tc_fence_after_sync();
-        return true;
-      };
-      auto issue_s = [&](uint32_t gg) {
-        const int st = gg % C::STAGES;
         const uint64_t dq = sdesc_sw128(smem_u32(sm.q[st]), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tmem + C::TM_S, dK0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
+          mma_bf16_ss(tmem + C::TM_S + 64 * b, dK0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
                       dq + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
-        mma_commit(&sm.s_full);
+        mma_commit(&sm.s_full[b]);
+        return true;
       };
-      auto issue_dp = [&](uint32_t gg) {
+      auto issue_dp = [&](uint32_t gg) -> bool {
+        const uint32_t b = gg & 1;
+        if (gg >= 2 && !mbar_wait(&sm.dk_done[b], ((gg >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+          fail(kSiteMmaDs);
+          return false;
+        }
         const int st = gg % C::STAGES;
+        tc_fence_after_sync();
         const uint64_t ddo = sdesc_sw128(smem_u32(sm.dO[st]), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tmem + C::TM_DP, dV0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
+          mma_bf16_ss(tmem + C::TM_DP + 64 * b, dV0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
                       ddo + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
-        mma_commit(&sm.dp_full);
+        mma_commit(&sm.dp_full[b]);
+        mma_commit(&sm.q_empty[st]);            // A's reads of this stage are done
+        return true;
       };
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
         int bh, pp, h;
@@ -307,14 +342,69 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
             fail(kSiteMmaKV);
             break;
           }
-          if (!wait_q(g)) break;
-          issue_s(g);
-          issue_dp(g);
+          if (!issue_s(g) || !issue_dp(g)) break;
+          for (int s = 0; s < nsteps; ++s, ++g) {
+            const bool ahead = C::STAGES >= 2 && s + 1 < nsteps;
+            if (ahead && (!issue_s(g + 1) || !issue_dp(g + 1))) break;
+            // dQ^T_h = K[:, h]^T dS^T into S buffer g&1
+            const uint32_t b = g & 1;
+            if (!mbar_wait(&sm.ds_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
+              fail(kSiteMmaDs);
+              break;
+            }
+            if (!mbar_wait(&sm.dv_done[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
+              fail(kSiteMmaP);
+              break;
+            }
+            tc_fence_after_sync();
+            const uint64_t dDS = sdesc_sw128(smem_u32(sm.ds[b]), KCH, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_bf16_ss(tmem + C::TM_S + 64 * b, dKmn + ((kk * 2048) >> 4),
+                          dDS + ((kk * 2048) >> 4), kIdDq, kk > 0 ? 1u : 0u);
+            mma_commit(&sm.dq_full);
+            mma_commit(&sm.ds_free[b]);
+            ++n_dq;
+            if (s + 1 < nsteps) {
+              if (!ahead && (!issue_s(g + 1) || !issue_dp(g + 1))) break;
+            } else {
+              mma_commit(&sm.kv_empty);
+            }
+          }
+          ++w_it;
+        }
+      }
+      // every tcgen05 op issued by this thread must finish before exit
+      mma_commit(&sm.mma_done);
+      if (!mbar_wait(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
+        record_failure(p.status, abort, kSiteDtDrain);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ issuer B
+    if (lane == 0) {
+      constexpr uint32_t kIdAcc = idesc_bf16_f32(BK, DH, 0, 1);    // dV, dK (B MN-major)
+      uint32_t w_it = 0, g = 0;
+      bool ok = true;
+      auto fail = [&](int site) {
+        record_failure(p.status, abort, site);
+        ok = false;
+      };
+      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+        int bh, pp, h;
+        sched.decode(u, bh, pp, h);
+        for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
+          const int n = sched.block(pp, kt);
+          int i0, i1;
+          dt_range(p, n, dt_len(p, bh), i0, i1);
+          if (i0 >= i1) continue;
+          const int nsteps = i1 - i0;
           for (int s = 0; s < nsteps; ++s, ++g) {
             const int st = g % C::STAGES;
+            const uint32_t b = g & 1;
             const bool first = (s == 0);
             // dV_h += P^T dO_i[:, h]
-            if (!mbar_wait(&sm.p_full, g & 1, abort, kWaitTimeoutNs)) {
+            if (!mbar_wait(&sm.p_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
               fail(kSiteMmaP);
               break;
             }
@@ -327,61 +417,32 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
             const uint64_t dQmn = sdesc_sw128(smem_u32(sm.q[st]) + 2 * h * QCH, QCH, 1024);
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
-              mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + kk * 8, dOmn + ((kk * 2048) >> 4),
-                          kIdAcc, (first && kk == 0) ? 0u : 1u);
-            // with a ring of two or more stages the next S^T goes ahead of dK
-            // and dQ^T, so the row warps can start on it while those run
-            const bool ahead = C::STAGES >= 2 && s + 1 < nsteps;
-            if (ahead) {
-              if (!wait_q(g + 1)) break;
-              issue_s(g + 1);
-            }
+              mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + 64 * b + kk * 8,
+                          dOmn + ((kk * 2048) >> 4), kIdAcc, (first && kk == 0) ? 0u : 1u);
+            mma_commit(&sm.dv_done[b]);
             // dK_h += dS^T Q_i[:, h]
-            if (!mbar_wait(&sm.ds_full, g & 1, abort, kWaitTimeoutNs)) {
+            if (!mbar_wait(&sm.ds_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
               fail(kSiteMmaDs);
               break;
             }
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
-              mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + kk * 8, dQmn + ((kk * 2048) >> 4),
-                          kIdAcc, (first && kk == 0) ? 0u : 1u);
-            mma_commit(&sm.q_empty[st]);
-            // dQ^T_h = K[:, h]^T dS^T, once the drain has emptied the previous one
-            if (g > 0 && !mbar_wait(&sm.dq_free, (g - 1) & 1, abort, kWaitTimeoutNs)) {
-              fail(kSiteMmaDq);
-              break;
-            }
-            tc_fence_after_sync();
-            const uint32_t b = g & 1;
-            const uint64_t dDS = sdesc_sw128(smem_u32(sm.ds[b]), KCH, 1024);
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              mma_bf16_ss(tmem + C::TM_DQ, dKmn + ((kk * 2048) >> 4), dDS + ((kk * 2048) >> 4),
-                          kIdDq, kk > 0 ? 1u : 0u);
-            mma_commit(&sm.dq_full);
-            mma_commit(&sm.ds_free[b]);
-            if (s + 1 < nsteps) {
-              if (!ahead) {
-                if (!wait_q(g + 1)) break;
-                issue_s(g + 1);
-              }
-              issue_dp(g + 1);
-            } else {
-              mma_commit(&sm.acc_full);
-              mma_commit(&sm.kv_empty);
-            }
+              mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + 64 * b + kk * 8,
+                          dQmn + ((kk * 2048) >> 4), kIdAcc, (first && kk == 0) ? 0u : 1u);
+            mma_commit(&sm.dk_done[b]);
+            mma_commit(&sm.q_empty[st]);          // B's reads of this stage are done
+            if (s + 1 == nsteps) mma_commit(&sm.acc_full);
           }
           ++w_it;
         }
       }
-      // every tcgen05 op issued above must finish before tensor memory is freed
-      mma_commit(&sm.mma_done);
-      if (!mbar_wait(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
+      mma_commit(&sm.mma_done_b);
+      if (!mbar_wait(&sm.mma_done_b, 0, nullptr, kWaitTimeoutNs))
         record_failure(p.status, abort, kSiteDtDrain);
     }
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 7) {
     // ------------------------------------------------------------ key-row warps
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;            // key row of the block = tensor-memory lane
@@ -418,7 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           const int st = g % C::STAGES;
           const int q0 = i * BQ;
           // ---- P^T = exp2(S^T * c - L2), masked; bf16 copy back to tensor memory
-          if (!warp_wait(&sm.s_full, g & 1, abort)) {
+          const uint32_t t_s = t_lane + C::TM_S + 64 * (g & 1);   // this step's S^T buffer
+          if (!warp_wait(&sm.s_full[g & 1], (g >> 1) & 1, abort)) {
             if (lane == 0) record_failure(p.status, abort, kSiteRowS);
             ok = false;
             break;
@@ -432,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             uint32_t sr[32];
-            tmem_ld_x32(t_lane + C::TM_S + 32 * half, sr);
+            tmem_ld_x32(t_s + 32 * half, sr);
             tmem_wait_ld();
             reg_fence<32>(sr);
 #pragma unroll
@@ -457,14 +519,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
 #pragma unroll
             for (int t = 0; t < 16; ++t)
               pk[t] = pack_bf16x2(pr[32 * half + 2 * t], pr[32 * half + 2 * t + 1]);
-            tmem_st_x16(t_lane + C::TM_S + 16 * half, pk);
+            tmem_st_x16(t_s + 16 * half, pk);
           }
           tmem_wait_st();
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.p_full);
+          if (lane == 0) mbar_arrive(&sm.p_full[g & 1]);
           // ---- dS^T = P^T o (dP^T - D)
-          if (!warp_wait(&sm.dp_full, g & 1, abort)) {
+          const uint32_t t_dp = t_lane + C::TM_DP + 64 * (g & 1);  // this step's dP^T buffer
+          if (!warp_wait(&sm.dp_full[g & 1], (g >> 1) & 1, abort)) {
             if (lane == 0) record_failure(p.status, abort, kSiteRowDp);
             ok = false;
             break;
@@ -482,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             uint32_t sr[32];
-            tmem_ld_x32(t_lane + C::TM_DP + 32 * half, sr);
+            tmem_ld_x32(t_dp + 32 * half, sr);
             tmem_wait_ld();
             reg_fence<32>(sr);
             uint32_t pk[16];
@@ -502,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
               pk[2 * t] = pack_bf16x2(d0, d1);
               pk[2 * t + 1] = pack_bf16x2(d2, d3);
             }
-            tmem_st_x16(t_lane + C::TM_DP + 16 * half, pk);
+            tmem_st_x16(t_dp + 16 * half, pk);
             // row = key r, 64 queries = 8 units of 16 bytes, XOR-swizzled by (r & 7)
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
@@ -515,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           tmem_wait_st();
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.ds_full);
+          if (lane == 0) mbar_arrive(&sm.ds_full[g & 1]);
         }
         if (!ok) break;
         // ---- dK_h, dV_h rows of this key block
@@ -561,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;            // head-dimension column within the half
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const bool issuer = (warp == 6 && lane == 0); // issues the bulk reduce-adds
+    const bool issuer = (warp == 7 && lane == 0); // issues the bulk reduce-adds
     if (C::DQ_TMA && issuer) prefetch_tmap(&p.tdq);
     uint32_t g = 0;
     bool ok = true;
@@ -581,8 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           tc_fence_after_sync();
           const int q0 = i * BQ;
           uint32_t v0[32], v1[32];
-          tmem_ld_x32(t_lane + C::TM_DQ, v0);
-          tmem_ld_x32(t_lane + C::TM_DQ + 32, v1);
+          tmem_ld_x32(t_lane + C::TM_S + 64 * (g & 1), v0);        // dQ^T(g) sits in S buffer g&1
+          tmem_ld_x32(t_lane + C::TM_S + 64 * (g & 1) + 32, v1);
           tmem_wait_ld();
           reg_fence<32>(v0);
           reg_fence<32>(v1);
