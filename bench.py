@@ -39,8 +39,16 @@ HEADLINE = "large_head_b2_h16_n8192_d128_causal"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd.cu", "sm103_ptx.cuh"],
-    "bwd_main_kernel": ["fa_bwd.cu", "fa_bwd_dt.cu", "fa_api.cu", "sm103_ptx.cuh"],
+    "bwd_main_kernel": ["fa_bwd.cu", "fa_api.cu", "sm103_ptx.cuh"],
+    "bwd_dt_kernel": ["fa_bwd_dt.cu", "fa_api.cu", "sm103_ptx.cuh"],
 }
+
+
+def bwd_kernel_names(d):
+    """Device names of the backward's main and dQ-conversion kernels: d = 64
+    runs the query-row kernel, d = 128 and 256 the transposed-dQ one."""
+    return ("bwd_main_kernel", "bwd_post_kernel") if d == 64 else ("bwd_dt_kernel",
+                                                                    "bwd_post_t_kernel")
 
 
 def parse_args():
@@ -203,9 +211,10 @@ class Runner:
         self.fa.fa_bwd_dq(self.dq, self.w.scale, self.ws)
 
     def phases(self):
+        main, post = bwd_kernel_names(self.w.d)
         return [("fa_fwd_kernel", self.fwd)] + ([("bwd_pre_kernel", self.prep),
-                                                 ("bwd_main_kernel", self.main),
-                                                 ("bwd_post_kernel", self.post)]
+                                                 (main, self.main),
+                                                 (post, self.post)]
                                                 if self.backward else [])
 
     def step(self):
@@ -286,7 +295,7 @@ def run_ours(args, dist):
     # dominant kernel and its roofline
     peaks, peak_src = load_peaks()
     kernel = max(per_phase, key=per_phase.get)
-    kflops = {"fa_fwd_kernel": flops_fwd, "bwd_main_kernel": flops_bwd}
+    kflops = {"fa_fwd_kernel": flops_fwd, bwd_kernel_names(w.d)[0]: flops_bwd}
     if kernel in kflops:
         achieved = kflops[kernel] / (per_phase[kernel] * 1e-3) / 1e12
         roof = {"kernel": kernel, "bound": "tensor", "achieved": round(achieved, 2),

@@ -100,19 +100,20 @@ bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int box_ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp32 [BH, N, d] accumulator as a 3-D tensor (d, N, BH): box of 128
-// columns x 64 rows, no swizzle (the target of bulk reduce-adds).
-bool make_acc_map(CUtensorMap* m, void* base, int d, int N, int BH) {
+// Transposed fp32 accumulator [BH, d, Npad] as a 3-D tensor (Npad, d, BH):
+// box of 32 queries (128 bytes) x 128 head-dimension rows, 128-byte swizzle
+// (the target of bulk reduce-adds).
+bool make_acc_map(CUtensorMap* m, void* base, int d, int npad, int BH) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(npad), static_cast<cuuint64_t>(d),
                               static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
-                                 static_cast<cuuint64_t>(d) * N * 4};
-  const cuuint32_t box[3] = {128, 64, 1};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(npad) * 4,
+                                 static_cast<cuuint64_t>(npad) * d * 4};
+  const cuuint32_t box[3] = {32, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -168,14 +169,15 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
   return FA_OK;
 }
 
-// Workspace layout: D [B*H, Npad] fp32, L2 [B*H, Npad] fp32, dQ_acc [B*H, N, d]
-// fp32, each region starting on a 256-byte boundary (Npad = N rounded up to 128).
+// Workspace layout: D [B*H, Npad] fp32, L2 [B*H, Npad] fp32, dQ_acc of
+// B*H*Npad*d fp32 ([B*H, Npad, d] for d = 64, [B*H, d, Npad] otherwise), each
+// region starting on a 256-byte boundary (Npad = N rounded up to 128).
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (check_sizes(B, H, N, d, 1.f) != FA_OK) return 0;
   const size_t npad = (static_cast<size_t>(N) + 127) / 128 * 128;
   const size_t padded_rows = static_cast<size_t>(B) * H * npad;
-  const size_t rows = static_cast<size_t>(B) * H * N;
-  return 2 * round_up256(padded_rows * sizeof(float)) + round_up256(rows * d * sizeof(float));
+  return 2 * round_up256(padded_rows * sizeof(float)) +
+         round_up256(padded_rows * d * sizeof(float));
 }
 
 }  // extern "C"
@@ -228,7 +230,7 @@ fa_status_t bwd_main_impl(fa::BwdParams& p, const DeviceInfo* di, const void* q,
   if (!make_map(&p.tq, q, d, p.N, BH, qrows) || !make_map(&p.tk, k, d, p.N, BH) ||
       !make_map(&p.tv, v, d, p.N, BH) || !make_map(&p.tdo, dO, d, p.N, BH, qrows))
     return FA_ERR_CUDA;
-  if (dt && !make_acc_map(&p.tdq, p.dq_acc, d, p.N, BH)) return FA_ERR_CUDA;
+  if (dt && !make_acc_map(&p.tdq, p.dq_acc, d, p.Npad, BH)) return FA_ERR_CUDA;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = dt ? fa::launch_bwd_main_dt(p, d, di->num_sms, di->max_smem, s)
                            : fa::launch_bwd_main(p, d, di->num_sms, di->max_smem, s);

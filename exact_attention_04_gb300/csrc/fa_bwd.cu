@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           tc_fence_after_sync();
           {
             const int q = q0 + r;
-            float* acc = p.dq_acc + (static_cast<size_t>(bh) * p.N + q) * D;
+            float* acc = p.dq_acc + (static_cast<size_t>(bh) * p.Npad + q) * D;
 #pragma unroll 1
             for (int c4 = 0; c4 < D / 32; ++c4) {
               uint32_t qr[32];
@@ -582,7 +582,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
       acc = fmaf(a.x, b.x, acc);
       acc = fmaf(a.y, b.y, acc);
     }
-    float4* z = reinterpret_cast<float4*>(p.dq_acc + off);
+  }
+  if (live) {
+    // the accumulator holds Npad * D floats per head in either layout: row
+    // `row` of this grid clears its D of them, padding included
+    float4* z = reinterpret_cast<float4*>(p.dq_acc + static_cast<size_t>(row) * D + sub * 8);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -595,12 +599,17 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
   }
 }
 
-// dQ = bf16(scale * dQ_acc), 8 elements per thread.
+// dQ = bf16(scale * dQ_acc) from the [BH, Npad, d] accumulator (d = 64), 8
+// elements per thread.
 __global__ void __launch_bounds__(256) bwd_post_kernel(const __grid_constant__ BwdParams p,
                                                        long long n8) {
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= n8) return;
-  const float4* src = reinterpret_cast<const float4*>(p.dq_acc) + 2 * t;
+  constexpr int D8 = 64 / 8;
+  const long long row = t / D8;                       // bh * N + q
+  const long long bh = row / p.N;
+  const long long src_row = bh * p.Npad + (row - bh * p.N);
+  const float4* src = reinterpret_cast<const float4*>(p.dq_acc + src_row * 64) + 2 * (t % D8);
   const float4 a = src[0], b = src[1];
   const float s = p.scale;
   uint4 out;
@@ -609,6 +618,31 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const __grid_constant__ B
   out.z = pack_bf16x2(b.x * s, b.y * s);
   out.w = pack_bf16x2(b.z * s, b.w * s);
   reinterpret_cast<uint4*>(p.dq)[t] = out;
+}
+
+// dQ = bf16(scale * dQ_acc^T) from the [BH, D, Npad] accumulator.  Thread
+// (bh, column group c8, query q): lanes run over q, so each of its 8 column
+// reads is a coalesced 128-byte row segment; it writes 8 bf16 of query q.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_post_t_kernel(const __grid_constant__ BwdParams p,
+                                                         long long total) {
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= total) return;
+  const int q = static_cast<int>(t % p.Npad);
+  const long long rest = t / p.Npad;
+  const int c8 = static_cast<int>(rest % (D / 8));
+  const long long bh = rest / (D / 8);
+  if (q >= p.N) return;
+  const float* src = p.dq_acc + (bh * D + c8 * 8) * p.Npad + q;
+  float a[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) a[j] = src[static_cast<size_t>(j) * p.Npad] * p.scale;
+  uint4 out;
+  out.x = pack_bf16x2(a[0], a[1]);
+  out.y = pack_bf16x2(a[2], a[3]);
+  out.z = pack_bf16x2(a[4], a[5]);
+  out.w = pack_bf16x2(a[6], a[7]);
+  reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + (bh * p.N + q) * D)[c8] = out;
 }
 
 template <int D>
@@ -654,8 +688,18 @@ cudaError_t launch_bwd_main(const BwdParams& p, int d, int num_sms, int max_smem
 }
 
 cudaError_t launch_bwd_post(const BwdParams& p, int d, cudaStream_t stream) {
-  const long long n8 = static_cast<long long>(p.B) * p.H * p.N * d / 8;
-  bwd_post_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(p, n8);
+  if (d == 64) {
+    const long long n8 = static_cast<long long>(p.B) * p.H * p.N * d / 8;
+    bwd_post_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(p, n8);
+    return cudaGetLastError();
+  }
+  const long long total = static_cast<long long>(p.B) * p.H * (d / 8) * p.Npad;
+  const unsigned grid = static_cast<unsigned>((total + 255) / 256);
+  switch (d) {
+    case 128: bwd_post_t_kernel<128><<<grid, 256, 0, stream>>>(p, total); break;
+    case 256: bwd_post_t_kernel<256><<<grid, 256, 0, stream>>>(p, total); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

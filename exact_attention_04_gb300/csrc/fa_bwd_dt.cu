@@ -9,11 +9,13 @@
 //   P^T   = exp2(S^T*c - L2_i)  and  dS^T = P^T o (dP^T - D_i)   (row warps)
 //   dV_h += P^T dO_i[:, h]      dK_h += dS^T Q_i[:, h]           (A from tensor memory)
 //   dQ^T_h = K[:, h]^T dS^T     (128 head-dim rows x 64 queries)
-// dQ^T sits in tensor memory with one lane per head-dimension column.  For
-// d = 128 the four drain warps write it transposed into a shared staging tile
-// and one thread adds the tile to the fp32 accumulator in global memory with a
-// single bulk tensor reduce-add (the L2 does the adds); for d = 256 (no room
-// for the tile) they use atomics that are contiguous across each warp.
+// dQ^T sits in tensor memory with one lane per head-dimension column, and the
+// fp32 accumulator in global memory is kept transposed too ([BH, d, Npad]), so
+// each drain thread owns one contiguous run of 64 queries.  For d = 128 the
+// four drain warps write the tile with 16-byte stores into a swizzled shared
+// staging buffer and one thread adds it to the accumulator with two bulk
+// tensor reduce-adds (the L2 does the adds); for d = 256 (no room for the
+// tile) each thread adds its run with 16-byte atomics.
 // With d = 256 the two halves of a key block are separate work items; both
 // recompute S^T and dP^T (the price of fitting dK and dV in tensor memory).
 //
@@ -75,7 +77,7 @@ struct DtSmem {
   alignas(1024) uint8_t q[DtCfg<D>::STAGES][DtCfg<D>::Q_BYTES];
   alignas(1024) uint8_t dO[DtCfg<D>::STAGES][DtCfg<D>::Q_BYTES];
   alignas(1024) uint8_t ds[2][KCH];              // dS^T bf16, 128 keys x 64 queries, double buffer
-  alignas(1024) float dq_stage[DtCfg<D>::DQ_TMA ? BQ * DH : 4];   // dQ tile, [query][d]
+  alignas(1024) float dq_stage[DtCfg<D>::DQ_TMA ? BQ * DH : 4];   // dQ^T tile, 2 x [d][32 queries]
   alignas(16) float lse2[DtCfg<D>::STAGES][BQ];
   alignas(16) float delta[DtCfg<D>::STAGES][BQ];
   uint64_t kv_full, kv_empty;
@@ -654,17 +656,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.dq_free);
           if constexpr (C::DQ_TMA) {
-            // staging tile [64 queries][128 columns]: this thread owns column r
+            // staging: two boxes of [128 columns][32 queries] fp32 in the
+            // 128-byte swizzle of the tensor map; this thread owns row r of
+            // each and writes it as eight 16-byte chunks, chunk j at j ^ (r & 7)
+            // (conflict-free: eight consecutive rows cover all 32 banks)
             if (!warp_wait(&sm.stage_free, (g & 1) ^ 1, abort)) {
               if (lane == 0) record_failure(p.status, abort, kSiteStageFree);
               ok = false;
               break;
             }
-            float* stg = sm.dq_stage + r;
+            uint4* row0 = reinterpret_cast<uint4*>(sm.dq_stage) + r * 8;
+            uint4* row1 = row0 + DH * 8;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) stg[c * DH] = __uint_as_float(v0[c]);
+            for (int j = 0; j < 8; ++j)
+              row0[j ^ (r & 7)] = make_uint4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) stg[(32 + c) * DH] = __uint_as_float(v1[c]);
+            for (int j = 0; j < 8; ++j)
+              row1[j ^ (r & 7)] = make_uint4(v1[4 * j], v1[4 * j + 1], v1[4 * j + 2], v1[4 * j + 3]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.stage_full);
@@ -673,8 +681,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
                 record_failure(p.status, abort, kSiteStageFull);
                 ok = false;
               } else {
-                // rows past N fall outside the tensor and are not written
-                tma_reduce_add_3d(&p.tdq, sm.dq_stage, h * DH, q0, bh);
+                // queries past N land in the padding up to Npad, never read
+                tma_reduce_add_3d(&p.tdq, sm.dq_stage, q0, h * DH, bh);
+                tma_reduce_add_3d(&p.tdq, sm.dq_stage + 32 * DH, q0 + 32, h * DH, bh);
                 bulk_commit_group();
                 bulk_wait_group_read<0>();
                 mbar_arrive(&sm.stage_free);
@@ -683,15 +692,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
           } else {
-            float* acc = p.dq_acc + (static_cast<size_t>(bh) * p.N + q0) * D + h * DH + r;
-            const int nq = p.N - q0 < BQ ? p.N - q0 : BQ;
+            // row h*DH + r of the transposed accumulator, queries q0 .. q0+63
+            // (q0 + 64 <= Npad: the tail lands in the padding)
+            float4* acc = reinterpret_cast<float4*>(
+                p.dq_acc + (static_cast<size_t>(bh) * D + h * DH + r) * p.Npad + q0);
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (c < nq) atomicAdd(acc + static_cast<size_t>(c) * D, __uint_as_float(v0[c]));
+            for (int j = 0; j < 8; ++j)
+              atomicAdd(acc + j, make_float4(__uint_as_float(v0[4 * j]), __uint_as_float(v0[4 * j + 1]),
+                                             __uint_as_float(v0[4 * j + 2]), __uint_as_float(v0[4 * j + 3])));
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (32 + c < nq)
-                atomicAdd(acc + static_cast<size_t>(32 + c) * D, __uint_as_float(v1[c]));
+            for (int j = 0; j < 8; ++j)
+              atomicAdd(acc + 8 + j, make_float4(__uint_as_float(v1[4 * j]), __uint_as_float(v1[4 * j + 1]),
+                                                 __uint_as_float(v1[4 * j + 2]), __uint_as_float(v1[4 * j + 3])));
           }
         }
       }

@@ -29,7 +29,7 @@ struct FwdParams {
 
 struct BwdParams {
   CUtensorMap tq, tk, tv, tdo; // bf16 [BH, N, d] as above
-  CUtensorMap tdq;             // fp32 dQ accumulator [BH, N, d], box (128, 64, 1), no swizzle
+  CUtensorMap tdq;             // fp32 dQ^T accumulator [BH, d, Npad], box (32, 128, 1), SW128
   const void* o;               // bf16 [B, H, N, d]
   const void* dO;              // bf16 [B, H, N, d]
   const float* lse;            // fp32 [B, H, N]
@@ -38,7 +38,7 @@ struct BwdParams {
   void* dv;                    // bf16
   float* delta;                // fp32 [B*H, Npad] workspace: D = rowsum(dO o O), 0 past N
   float* lse2;                 // fp32 [B*H, Npad] workspace: LSE * log2(e), +inf past N
-  float* dq_acc;               // fp32 [B, H, N, d] workspace
+  float* dq_acc;               // fp32 workspace: [BH, Npad, d] (d = 64) or [BH, d, Npad]
   const int* kv_len;
   int B, H, N;
   int Npad;                    // N rounded up to a multiple of 128

@@ -71,7 +71,8 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
 /*
  * Bytes of device workspace fa_bwd needs for these sizes: the fp32 row
  * statistics D = rowsum(dO o O) and LSE*log2(e), each [B*H, Npad] with Npad =
- * N rounded up to 128, and the fp32 dQ accumulator [B,H,N,d]; each region
+ * N rounded up to 128, and the fp32 dQ accumulator of B*H*Npad*d elements
+ * ([B*H, Npad, d] for d = 64, [B*H, d, Npad] for d = 128 and 256); each region
  * starts on a 256-byte boundary.  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);

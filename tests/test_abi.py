@@ -53,7 +53,7 @@ def test_workspace_bytes(lib):
     B, H, N, d = 2, 3, 200, 64
     npad = 256
     stat = -(-B * H * npad * 4 // 256) * 256
-    acc = -(-B * H * N * d * 4 // 256) * 256
+    acc = -(-B * H * npad * d * 4 // 256) * 256
     assert fa.fa_bwd_workspace_bytes(B, H, N, d) == 2 * stat + acc
     assert fa.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
     assert fa.fa_bwd_workspace_bytes(1, 1, 1, 96) == 0
