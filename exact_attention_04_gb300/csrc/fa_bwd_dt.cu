@@ -23,17 +23,19 @@
 // 算术强度与分块把 FlashAttention 推导清楚" section 八; "4. FlashAttention 深度
 // 剖析" section 4.3.4.  Gradient formulas: chain rule through the row softmax.
 //
-// Warps: 0 TMA producer; 1 issuer A (S^T, dP^T, dQ^T; owns tensor memory);
-// 2 issuer B (dV, dK); 3..6 key-row warps (P^T, dS^T, dK/dV epilogue); 7..10
-// dQ drain warps.  A tcgen05.mma holds its issuing thread about as long as
-// the tensor core runs it, so the products are split over two threads.
+// Warps: 0 TMA producer; 1 issuer A (S^T, dP^T; owns tensor memory); 2
+// issuer B (dV, dK, dQ^T); 3..6 key-row warps (P^T, dS^T, dK/dV epilogue);
+// 7..10 dQ drain warps.  A tcgen05.mma instruction holds its issuing thread
+// for about 100 cycles here, longer than the tensor core needs for these
+// shapes, so the 32 instructions of a step are split evenly over two threads.
 // Tensor memory columns: two 64-column S buffers [0,128) (S^T of a step, then
 // its P^T as bf16, then its dQ^T), two dP buffers [128,256) (dP^T, then dS^T
 // as bf16), dV_h [256,384), dK_h [384,512).  With both S and dP double
 // buffered, issuer A can compute the next step's S^T and dP^T while the row
-// warps are still on the current step.  Where one issuer overwrites columns
-// the other issuer's MMA reads, it first waits for that MMA's commit
-// (dv_done, dk_done); within one issuer the tensor core keeps issue order.
+// warps are still on the current step.  Where issuer A overwrites columns an
+// MMA of issuer B reads, it first waits for that MMA's commit (dk_done, and
+// the drain of dQ^T via dq_free); within one issuer the tensor core keeps
+// issue order, which orders dQ^T(g) after dV(g)'s reads of P^T(g).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -84,8 +86,8 @@ struct DtSmem {
   uint64_t q_full[DtCfg<D>::STAGES], q_empty[DtCfg<D>::STAGES];
   // per step-parity buffer b = g & 1 wherever a producer can run a step ahead
   uint64_t s_full[2], p_full[2], dp_full[2], ds_full[2], ds_free[2];
-  uint64_t dq_full, dq_free, acc_full, acc_free;
-  uint64_t dv_done[2], dk_done[2];  // cross-issuer: P^T / dS^T of a step consumed
+  uint64_t dq_full[2], dq_free[2], acc_full, acc_free;
+  uint64_t dk_done[2];              // cross-issuer: dS^T of a step consumed
   uint64_t mma_done_b;
   uint64_t stage_full, stage_free;
   uint64_t mma_done;
@@ -107,6 +109,18 @@ __device__ __forceinline__ void record_failure(int* status, volatile int* abort,
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   bool ok = mbar_wait(bar, parity, abort, kWaitTimeoutNs);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Issuer warps wait as a whole warp (the warp stays converged for the
+// elected MMA issue) and report a failure from lane 0.
+__device__ __forceinline__ bool warp_wait_t(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                            uint64_t timeout_ns) {
+  bool ok = mbar_wait(bar, parity, abort, timeout_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void issuer_fail(int* status, volatile int* abort, int lane, int site) {
+  if (lane == 0) record_failure(status, abort, site);
 }
 
 // Units are (bh, key-block pair or key block, half).  Causal: key block n
@@ -175,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     sm.abort = 0;
     mbar_init(&sm.kv_full, 1);
-    mbar_init(&sm.kv_empty, 1);
+    mbar_init(&sm.kv_empty, 2);             // both MMA issuers read K (and A reads V)
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 2);         // both MMA issuers read the stage
@@ -186,12 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
       mbar_init(&sm.dp_full[b], 1);
       mbar_init(&sm.ds_full[b], 4);
       mbar_init(&sm.ds_free[b], 1);
-      mbar_init(&sm.dv_done[b], 1);
       mbar_init(&sm.dk_done[b], 1);
+      mbar_init(&sm.dq_full[b], 1);
+      mbar_init(&sm.dq_free[b], 4);
     }
     mbar_init(&sm.mma_done_b, 1);
-    mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_free, 4);
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_free, 4);
     mbar_init(&sm.stage_full, 4);
@@ -273,61 +286,86 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ issuer A
-    // S^T(g) into S buffer g&1 once the drain has read dQ^T(g-2) out of it
-    // (waited as: the drain of the last dQ^T issued so far, which is g-2 or
-    // later, so the wait never runs behind the barrier's phase);
-    // dP^T(g) into dP buffer g&1 once dK(g-2) has read dS^T(g-2); dQ^T(g)
-    // into S buffer g&1 once dV(g) has read P^T(g) and the row warps wrote
-    // dS^T(g).  With two or more Q stages the next step's S^T and dP^T are
-    // issued before dQ^T(g).
-    if (lane == 0) {
+    // S^T(g) into S buffer g&1 once the drain has read dQ^T(g-2) out of it;
+    // dP^T(g) into dP buffer g&1 once dK(g-2) has read dS^T(g-2).  Runs
+    // ahead of the row warps as far as the Q ring and the two buffers allow.
+    {
       constexpr uint32_t kIdS = idesc_bf16_f32(BK, BQ, 0, 0);      // S^T, dP^T
-      constexpr uint32_t kIdDq = idesc_bf16_f32(DH, BQ, 1, 1);     // dQ^T (A, B MN-major)
       const uint64_t dK0 = sdesc_sw128(smem_u32(sm.k), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sm.v), 16, 1024);
       uint32_t w_it = 0, g = 0;
-      uint32_t n_dq = 0;                       // dQ^T issued so far
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
+        int bh, pp, h;
+        sched.decode(u, bh, pp, h);
+        for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
+          const int n = sched.block(pp, kt);
+          int i0, i1;
+          dt_range(p, n, dt_len(p, bh), i0, i1);
+          if (i0 >= i1) continue;
+          const int nsteps = i1 - i0;
+          if (!warp_wait_t(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
+            issuer_fail(p.status, abort, lane, kSiteMmaKV);
+            ok = false;
+            break;
+          }
+          for (int s = 0; s < nsteps; ++s, ++g) {
+            const uint32_t b = g & 1;
+            const int st = g % C::STAGES;
+            // S^T = K Q_i^T
+            if (g >= 2 && !warp_wait_t(&sm.dq_free[b], ((g >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaDq);
+              ok = false;
+              break;
+            }
+            if (!warp_wait_t(&sm.q_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaQ);
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint64_t dq = sdesc_sw128(smem_u32(sm.q[st]), 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_bf16_ss_w(tmem + C::TM_S + 64 * b, dK0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
+                          dq + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
+            mma_commit_w(&sm.s_full[b]);
+            // dP^T = V dO_i^T
+            if (g >= 2 && !warp_wait_t(&sm.dk_done[b], ((g >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaDs);
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint64_t ddo = sdesc_sw128(smem_u32(sm.dO[st]), 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_bf16_ss_w(tmem + C::TM_DP + 64 * b, dV0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
+                          ddo + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
+            mma_commit_w(&sm.dp_full[b]);
+            mma_commit_w(&sm.q_empty[st]);          // A's reads of this stage are done
+          }
+          if (!ok) break;
+          mma_commit_w(&sm.kv_empty);               // A's reads of K and V are done
+          ++w_it;
+        }
+      }
+      // every tcgen05 op issued by this thread must finish before exit
+      mma_commit_w(&sm.mma_done);
+      if (!warp_wait_t(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
+        issuer_fail(p.status, abort, lane, kSiteDtDrain);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ issuer B
+    {
+      constexpr uint32_t kIdAcc = idesc_bf16_f32(BK, DH, 0, 1);    // dV, dK (B MN-major)
+      constexpr uint32_t kIdDq = idesc_bf16_f32(DH, BQ, 1, 1);     // dQ^T (A, B MN-major)
+      uint32_t w_it = 0, g = 0;
       bool ok = true;
       auto fail = [&](int site) {
-        record_failure(p.status, abort, site);
+        issuer_fail(p.status, abort, lane, site);
         ok = false;
-      };
-      auto issue_s = [&](uint32_t gg) -> bool {
-        const uint32_t b = gg & 1;
-        if (gg >= 2 && !mbar_wait(&sm.dq_free, (n_dq - 1) & 1, abort, kWaitTimeoutNs)) {
-          fail(kSiteMmaDq);
-          return false;
-        }
-        const int st = gg % C::STAGES;
-        if (!mbar_wait(&sm.q_full[st], (gg / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
-          fail(kSiteMmaQ);
-          return false;
-        }
-        tc_fence_after_sync();
-        const uint64_t dq = sdesc_sw128(smem_u32(sm.q[st]), 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tmem + C::TM_S + 64 * b, dK0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
-                      dq + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
-        mma_commit(&sm.s_full[b]);
-        return true;
-      };
-      auto issue_dp = [&](uint32_t gg) -> bool {
-        const uint32_t b = gg & 1;
-        if (gg >= 2 && !mbar_wait(&sm.dk_done[b], ((gg >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
-          fail(kSiteMmaDs);
-          return false;
-        }
-        const int st = gg % C::STAGES;
-        tc_fence_after_sync();
-        const uint64_t ddo = sdesc_sw128(smem_u32(sm.dO[st]), 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tmem + C::TM_DP + 64 * b, dV0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
-                      ddo + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
-        mma_commit(&sm.dp_full[b]);
-        mma_commit(&sm.q_empty[st]);            // A's reads of this stage are done
-        return true;
       };
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
         int bh, pp, h;
@@ -340,77 +378,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           dt_range(p, n, dt_len(p, bh), i0, i1);
           if (i0 >= i1) continue;
           const int nsteps = i1 - i0;
-          if (!mbar_wait(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
-            fail(kSiteMmaKV);
-            break;
-          }
-          if (!issue_s(g) || !issue_dp(g)) break;
-          for (int s = 0; s < nsteps; ++s, ++g) {
-            const bool ahead = C::STAGES >= 2 && s + 1 < nsteps;
-            if (ahead && (!issue_s(g + 1) || !issue_dp(g + 1))) break;
-            // dQ^T_h = K[:, h]^T dS^T into S buffer g&1
-            const uint32_t b = g & 1;
-            if (!mbar_wait(&sm.ds_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
-              fail(kSiteMmaDs);
-              break;
-            }
-            if (!mbar_wait(&sm.dv_done[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
-              fail(kSiteMmaP);
-              break;
-            }
-            tc_fence_after_sync();
-            const uint64_t dDS = sdesc_sw128(smem_u32(sm.ds[b]), KCH, 1024);
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              mma_bf16_ss(tmem + C::TM_S + 64 * b, dKmn + ((kk * 2048) >> 4),
-                          dDS + ((kk * 2048) >> 4), kIdDq, kk > 0 ? 1u : 0u);
-            mma_commit(&sm.dq_full);
-            mma_commit(&sm.ds_free[b]);
-            ++n_dq;
-            if (s + 1 < nsteps) {
-              if (!ahead && (!issue_s(g + 1) || !issue_dp(g + 1))) break;
-            } else {
-              mma_commit(&sm.kv_empty);
-            }
-          }
-          ++w_it;
-        }
-      }
-      // every tcgen05 op issued by this thread must finish before exit
-      mma_commit(&sm.mma_done);
-      if (!mbar_wait(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
-        record_failure(p.status, abort, kSiteDtDrain);
-    }
-    __syncwarp();
-  } else if (warp == 2) {
-    // ------------------------------------------------------------ issuer B
-    if (lane == 0) {
-      constexpr uint32_t kIdAcc = idesc_bf16_f32(BK, DH, 0, 1);    // dV, dK (B MN-major)
-      uint32_t w_it = 0, g = 0;
-      bool ok = true;
-      auto fail = [&](int site) {
-        record_failure(p.status, abort, site);
-        ok = false;
-      };
-      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        int bh, pp, h;
-        sched.decode(u, bh, pp, h);
-        for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
-          const int n = sched.block(pp, kt);
-          int i0, i1;
-          dt_range(p, n, dt_len(p, bh), i0, i1);
-          if (i0 >= i1) continue;
-          const int nsteps = i1 - i0;
           for (int s = 0; s < nsteps; ++s, ++g) {
             const int st = g % C::STAGES;
             const uint32_t b = g & 1;
             const bool first = (s == 0);
+            const bool last = (s + 1 == nsteps);
             // dV_h += P^T dO_i[:, h]
-            if (!mbar_wait(&sm.p_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
+            if (!warp_wait_t(&sm.p_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
               fail(kSiteMmaP);
               break;
             }
-            if (first && !mbar_wait(&sm.acc_free, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+            if (first && !warp_wait_t(&sm.acc_free, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
               fail(kSiteMmaAcc);
               break;
             }
@@ -419,29 +397,39 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
             const uint64_t dQmn = sdesc_sw128(smem_u32(sm.q[st]) + 2 * h * QCH, QCH, 1024);
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
-              mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + 64 * b + kk * 8,
+              mma_bf16_ts_w(tmem + C::TM_DV, tmem + C::TM_S + 64 * b + kk * 8,
                           dOmn + ((kk * 2048) >> 4), kIdAcc, (first && kk == 0) ? 0u : 1u);
-            mma_commit(&sm.dv_done[b]);
             // dK_h += dS^T Q_i[:, h]
-            if (!mbar_wait(&sm.ds_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
+            if (!warp_wait_t(&sm.ds_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
               fail(kSiteMmaDs);
               break;
             }
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
-              mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + 64 * b + kk * 8,
+              mma_bf16_ts_w(tmem + C::TM_DK, tmem + C::TM_DP + 64 * b + kk * 8,
                           dQmn + ((kk * 2048) >> 4), kIdAcc, (first && kk == 0) ? 0u : 1u);
-            mma_commit(&sm.dk_done[b]);
-            mma_commit(&sm.q_empty[st]);          // B's reads of this stage are done
-            if (s + 1 == nsteps) mma_commit(&sm.acc_full);
+            mma_commit_w(&sm.dk_done[b]);
+            mma_commit_w(&sm.q_empty[st]);          // B's reads of this stage are done
+            if (last) mma_commit_w(&sm.acc_full);
+            // dQ^T_h = K[:, h]^T dS^T into S buffer g&1: issued after dV(g) by
+            // this thread, so it runs after dV(g) has read P^T(g) there
+            const uint64_t dDS = sdesc_sw128(smem_u32(sm.ds[b]), KCH, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_bf16_ss_w(tmem + C::TM_S + 64 * b, dKmn + ((kk * 2048) >> 4),
+                          dDS + ((kk * 2048) >> 4), kIdDq, kk > 0 ? 1u : 0u);
+            mma_commit_w(&sm.dq_full[b]);
+            mma_commit_w(&sm.ds_free[b]);
+            if (last) mma_commit_w(&sm.kv_empty);   // B's reads of K are done
           }
+          if (!ok) break;
           ++w_it;
         }
       }
-      mma_commit(&sm.mma_done_b);
-      if (!mbar_wait(&sm.mma_done_b, 0, nullptr, kWaitTimeoutNs))
-        record_failure(p.status, abort, kSiteDtDrain);
+      mma_commit_w(&sm.mma_done_b);
+      if (!warp_wait_t(&sm.mma_done_b, 0, nullptr, kWaitTimeoutNs))
+        issuer_fail(p.status, abort, lane, kSiteDtDrain);
     }
     __syncwarp();
   } else if (warp < 7) {
@@ -638,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
         int i0, i1;
         dt_range(p, n, dt_len(p, bh), i0, i1);
         for (int i = i0; i < i1; ++i, ++g) {
-          if (!warp_wait(&sm.dq_full, g & 1, abort)) {
+          if (!warp_wait(&sm.dq_full[g & 1], (g >> 1) & 1, abort)) {
             if (lane == 0) record_failure(p.status, abort, kSiteDrainDq);
             ok = false;
             break;
@@ -654,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           // the whole tile is in registers: tensor memory is free for the next dQ^T
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.dq_free);
+          if (lane == 0) mbar_arrive(&sm.dq_free[g & 1]);
           if constexpr (C::DQ_TMA) {
             // staging: two boxes of [128 columns][32 queries] fp32 in the
             // 128-byte swizzle of the tensor map; this thread owns row r of
