@@ -92,6 +92,10 @@ __device__ __forceinline__ void record_failure(int* status, volatile int* abort,
   *abort = 1;
 }
 
+__device__ __forceinline__ void issuer_fail(int* status, volatile int* abort, int lane, int site) {
+  if (lane == 0) record_failure(status, abort, site);
+}
+
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   bool ok = mbar_wait(bar, parity, abort, kWaitTimeoutNs);
   return __all_sync(0xffffffffu, ok);
@@ -251,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t kIdescS = idesc_bf16_f32(BN, BM, 0, 0);     // S^T, dP^T
       constexpr uint32_t kIdescAcc = idesc_bf16_f32(BN, D, 0, 1);    // dV, dK: B MN-major
       constexpr uint32_t kIdescDq = idesc_bf16_f32(BM, D, 1, 1);     // dQ: A and B MN-major
@@ -267,24 +271,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           sched.item(u, kt, bh, n);
           q_range(p, n, bwd_len(p, bh), i0, i1);
           if (i0 >= i1) continue;
-          if (!mbar_wait(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
-            record_failure(p.status, abort, kSiteMmaKV);
+          if (!mbar_wait_warp(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
+            issuer_fail(p.status, abort, lane, kSiteMmaKV);
             ok = false;
             break;
           }
           for (int i = i0; i < i1; ++i) {
             const int st = g % kStages;
             const bool first = (i == i0);
-            if (!mbar_wait(&sm.q_full[st], (g / kStages) & 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaQ);
+            if (!mbar_wait_warp(&sm.q_full[st], (g / kStages) & 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaQ);
               ok = false;
               break;
             }
             // dQ of the previous step must be out of tensor memory before the
             // columns it occupies are written again.
             if (C::DQ_ALIASES_S && g > 0 &&
-                !mbar_wait(&sm.dq_free, (g - 1) & 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaDq);
+                !mbar_wait_warp(&sm.dq_free, (g - 1) & 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaDq);
               ok = false;
               break;
             }
@@ -294,23 +298,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = ((kk / 4) * CHUNK + (kk % 4) * 32) >> 4;
-              mma_bf16_ss(tmem + C::TM_S, dK0 + off, dQ0 + off, kIdescS, kk > 0 ? 1u : 0u);
+              mma_bf16_ss_w(tmem + C::TM_S, dK0 + off, dQ0 + off, kIdescS, kk > 0 ? 1u : 0u);
             }
-            mma_commit(&sm.s_full);
+            mma_commit_w(&sm.s_full);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = ((kk / 4) * CHUNK + (kk % 4) * 32) >> 4;
-              mma_bf16_ss(tmem + C::TM_DP, dV0 + off, dO0 + off, kIdescS, kk > 0 ? 1u : 0u);
+              mma_bf16_ss_w(tmem + C::TM_DP, dV0 + off, dO0 + off, kIdescS, kk > 0 ? 1u : 0u);
             }
-            mma_commit(&sm.dp_full);
+            mma_commit_w(&sm.dp_full);
             // dV += P^T dO_i
-            if (!mbar_wait(&sm.p_full, g & 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaP);
+            if (!mbar_wait_warp(&sm.p_full, g & 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaP);
               ok = false;
               break;
             }
-            if (first && !mbar_wait(&sm.acc_free, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaAcc);
+            if (first && !mbar_wait_warp(&sm.acc_free, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaAcc);
               ok = false;
               break;
             }
@@ -319,43 +323,43 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             const uint64_t dQmn = sdesc_sw128(smem_u32(sm.q[st]), CHUNK, 1024);
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
-              mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + kk * 8, dOmn + ((kk * 2048) >> 4),
+              mma_bf16_ts_w(tmem + C::TM_DV, tmem + C::TM_S + kk * 8, dOmn + ((kk * 2048) >> 4),
                           kIdescAcc, (first && kk == 0) ? 0u : 1u);
             // dK += dS^T Q_i and dQ_i = dS K
-            if (!mbar_wait(&sm.ds_full, g & 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaDs);
+            if (!mbar_wait_warp(&sm.ds_full, g & 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaDs);
               ok = false;
               break;
             }
             if (!C::DQ_ALIASES_S && g > 0 &&
-                !mbar_wait(&sm.dq_free, (g - 1) & 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaDq);
+                !mbar_wait_warp(&sm.dq_free, (g - 1) & 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaDq);
               ok = false;
               break;
             }
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < BM / 16; ++kk)
-              mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + kk * 8, dQmn + ((kk * 2048) >> 4),
+              mma_bf16_ts_w(tmem + C::TM_DK, tmem + C::TM_DP + kk * 8, dQmn + ((kk * 2048) >> 4),
                           kIdescAcc, (first && kk == 0) ? 0u : 1u);
-            mma_commit(&sm.q_empty[st]);
+            mma_commit_w(&sm.q_empty[st]);
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-              mma_bf16_ss(tmem + C::TM_DQ, dDS + ((kk * 2048) >> 4), dKmn + ((kk * 2048) >> 4),
+              mma_bf16_ss_w(tmem + C::TM_DQ, dDS + ((kk * 2048) >> 4), dKmn + ((kk * 2048) >> 4),
                           kIdescDq, kk > 0 ? 1u : 0u);
-            mma_commit(&sm.dq_full);
+            mma_commit_w(&sm.dq_full);
             if (i == i1 - 1) {
-              mma_commit(&sm.acc_full);
-              mma_commit(&sm.kv_empty);
+              mma_commit_w(&sm.acc_full);
+              mma_commit_w(&sm.kv_empty);
             }
             ++g;
           }
           ++w_it;
         }
       }
-      mma_commit(&sm.mma_done);
-      if (!mbar_wait(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
-        record_failure(p.status, abort, kSiteBDrain);
+      mma_commit_w(&sm.mma_done);
+      if (!mbar_wait_warp(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
+        issuer_fail(p.status, abort, lane, kSiteBDrain);
     }
     __syncwarp();
   } else {

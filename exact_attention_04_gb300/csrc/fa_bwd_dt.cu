@@ -111,14 +111,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-// Issuer warps wait as a whole warp (the warp stays converged for the
-// elected MMA issue) and report a failure from lane 0.
-__device__ __forceinline__ bool warp_wait_t(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                            uint64_t timeout_ns) {
-  bool ok = mbar_wait(bar, parity, abort, timeout_ns);
-  return __all_sync(0xffffffffu, ok);
-}
-
+// Issuer warps wait as a whole warp (mbar_wait_warp) and report a failure
+// from lane 0.
 __device__ __forceinline__ void issuer_fail(int* status, volatile int* abort, int lane, int site) {
   if (lane == 0) record_failure(status, abort, site);
 }
@@ -304,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           dt_range(p, n, dt_len(p, bh), i0, i1);
           if (i0 >= i1) continue;
           const int nsteps = i1 - i0;
-          if (!warp_wait_t(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
+          if (!mbar_wait_warp(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
             issuer_fail(p.status, abort, lane, kSiteMmaKV);
             ok = false;
             break;
@@ -313,12 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
             const uint32_t b = g & 1;
             const int st = g % C::STAGES;
             // S^T = K Q_i^T
-            if (g >= 2 && !warp_wait_t(&sm.dq_free[b], ((g >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+            if (g >= 2 && !mbar_wait_warp(&sm.dq_free[b], ((g >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
               issuer_fail(p.status, abort, lane, kSiteMmaDq);
               ok = false;
               break;
             }
-            if (!warp_wait_t(&sm.q_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+            if (!mbar_wait_warp(&sm.q_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
               issuer_fail(p.status, abort, lane, kSiteMmaQ);
               ok = false;
               break;
@@ -331,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
                           dq + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
             mma_commit_w(&sm.s_full[b]);
             // dP^T = V dO_i^T
-            if (g >= 2 && !warp_wait_t(&sm.dk_done[b], ((g >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+            if (g >= 2 && !mbar_wait_warp(&sm.dk_done[b], ((g >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
               issuer_fail(p.status, abort, lane, kSiteMmaDs);
               ok = false;
               break;
@@ -352,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
       }
       // every tcgen05 op issued by this thread must finish before exit
       mma_commit_w(&sm.mma_done);
-      if (!warp_wait_t(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
+      if (!mbar_wait_warp(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
         issuer_fail(p.status, abort, lane, kSiteDtDrain);
     }
     __syncwarp();
@@ -384,11 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
             const bool first = (s == 0);
             const bool last = (s + 1 == nsteps);
             // dV_h += P^T dO_i[:, h]
-            if (!warp_wait_t(&sm.p_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
+            if (!mbar_wait_warp(&sm.p_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
               fail(kSiteMmaP);
               break;
             }
-            if (first && !warp_wait_t(&sm.acc_free, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+            if (first && !mbar_wait_warp(&sm.acc_free, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
               fail(kSiteMmaAcc);
               break;
             }
@@ -400,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
               mma_bf16_ts_w(tmem + C::TM_DV, tmem + C::TM_S + 64 * b + kk * 8,
                           dOmn + ((kk * 2048) >> 4), kIdAcc, (first && kk == 0) ? 0u : 1u);
             // dK_h += dS^T Q_i[:, h]
-            if (!warp_wait_t(&sm.ds_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
+            if (!mbar_wait_warp(&sm.ds_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
               fail(kSiteMmaDs);
               break;
             }
@@ -428,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
         }
       }
       mma_commit_w(&sm.mma_done_b);
-      if (!warp_wait_t(&sm.mma_done_b, 0, nullptr, kWaitTimeoutNs))
+      if (!mbar_wait_warp(&sm.mma_done_b, 0, nullptr, kWaitTimeoutNs))
         issuer_fail(p.status, abort, lane, kSiteDtDrain);
     }
     __syncwarp();

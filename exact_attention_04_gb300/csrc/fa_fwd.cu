@@ -3,14 +3,15 @@
 // One CTA per SM (persistent), 224 threads in four roles:
 //   warp 0      TMA producer: Q tile once per tile, then K_j and V_j into a
 //               STAGES-deep shared-memory ring (full/empty mbarriers).
-//   warp 1      S issuer (one thread): S_j = Q K_j^T into one of NSB S
-//               buffers in tensor memory, running ahead of the softmax as far
-//               as the buffers allow.  Also allocates and frees the tensor
-//               memory.
-//   warp 2      P V issuer (one thread): O += P_j V_j with P read from tensor
-//               memory.  A tcgen05.mma holds its issuing thread for about as
-//               long as the tensor core needs to run it, so the two products
-//               are issued from two threads on different sub-partitions.
+//   warp 1      S issuer: S_j = Q K_j^T into one of NSB S buffers in tensor
+//               memory, running ahead of the softmax as far as the buffers
+//               allow.  Also allocates and frees the tensor memory.
+//   warp 2      P V issuer: O += P_j V_j with P read from tensor memory.
+//               A tcgen05.mma holds its issuing thread for about as long as
+//               the tensor core needs to run it, so the two products are
+//               issued from two warps on different sub-partitions.  Each
+//               issuer warp runs converged and one lane chosen by elect.sync
+//               issues every MMA and commit.
 //   warps 3..6  softmax: thread r owns query row r of the tile (TMEM lane r).
 //               Reads its row of S, masks, updates the running max m and sum
 //               l, writes P = exp2(S*c - m) as bf16 into tensor memory,
@@ -138,6 +139,10 @@ __device__ __forceinline__ int kv_blocks(int m, int len, int causal) {
   return (end + BN - 1) / BN;
 }
 
+__device__ __forceinline__ void issuer_fail(int* status, volatile int* abort, int lane, int site) {
+  if (lane == 0) record_failure(status, abort, site);
+}
+
 // All 32 lanes wait; the decision is made uniform across the warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   bool ok = mbar_wait(bar, parity, abort, kWaitTimeoutNs);
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ S issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, 0, 0);
       const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q), 16, 1024);
       uint32_t q_it = 0, g = 0;
@@ -272,8 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           sched.tile(u, kt, bh, m);
           const int nkv = kv_blocks(m, seq_len(p, bh), p.causal);
           if (nkv == 0) continue;
-          if (!mbar_wait(&sm.q_full, q_it & 1, abort, kWaitTimeoutNs)) {
-            record_failure(p.status, abort, kSiteMmaQ);
+          if (!mbar_wait_warp(&sm.q_full, q_it & 1, abort, kWaitTimeoutNs)) {
+            issuer_fail(p.status, abort, lane, kSiteMmaQ);
             ok = false;
             break;
           }
@@ -282,14 +287,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             const uint32_t b = g % C::NSB;
             // buffer b last held block g - NSB: its P V must be complete
             if (g >= static_cast<uint32_t>(C::NSB) &&
-                !mbar_wait(&sm.pv_done[b], ((g / C::NSB) & 1) ^ 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaS);
+                !mbar_wait_warp(&sm.pv_done[b], ((g / C::NSB) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaS);
               ok = false;
               break;
             }
             const int st = g % C::STAGES;
-            if (!mbar_wait(&sm.k_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaK);
+            if (!mbar_wait_warp(&sm.k_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaK);
               ok = false;
               break;
             }
@@ -298,24 +303,24 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
-              mma_bf16_ss(tmem + C::TM_S + 128 * b, dq0 + (off >> 4), dk0 + (off >> 4), kIdescS,
+              mma_bf16_ss_w(tmem + C::TM_S + 128 * b, dq0 + (off >> 4), dk0 + (off >> 4), kIdescS,
                           kk > 0 ? 1u : 0u);
             }
-            mma_commit(&sm.k_empty[st]);
-            mma_commit(&sm.s_full[b]);
-            if (j == nkv - 1) mma_commit(&sm.q_empty);
+            mma_commit_w(&sm.k_empty[st]);
+            mma_commit_w(&sm.s_full[b]);
+            if (j == nkv - 1) mma_commit_w(&sm.q_empty);
           }
         }
       }
       // every tcgen05 op issued by this thread must finish before exit
-      mma_commit(&sm.mma_done);
-      if (!mbar_wait(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
-        record_failure(p.status, abort, kSiteDrain);
+      mma_commit_w(&sm.mma_done);
+      if (!mbar_wait_warp(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
+        issuer_fail(p.status, abort, lane, kSiteDrain);
     }
     __syncwarp();
   } else if (warp == 2) {
     // ------------------------------------------------------------ P V issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 0, 1);
       uint32_t g = 0, t_it = 0;
       bool ok = true;
@@ -327,21 +332,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           if (nkv == 0) continue;
           for (int j = 0; j < nkv; ++j, ++g) {
             const uint32_t b = g % C::NSB;
-            if (!mbar_wait(&sm.p_full[b], (g / C::NSB) & 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaP);
+            if (!mbar_wait_warp(&sm.p_full[b], (g / C::NSB) & 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaP);
               ok = false;
               break;
             }
             const int st = g % C::STAGES;
-            if (!mbar_wait(&sm.v_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaV);
+            if (!mbar_wait_warp(&sm.v_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaV);
               ok = false;
               break;
             }
             // a tile's first P V starts a fresh O: the previous tile's epilogue
             // must have read O out of tensor memory
-            if (j == 0 && !mbar_wait(&sm.o_free, (t_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
-              record_failure(p.status, abort, kSiteMmaO);
+            if (j == 0 && !mbar_wait_warp(&sm.o_free, (t_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaO);
               ok = false;
               break;
             }
@@ -351,19 +356,19 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), BN * 128, 1024);
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
-              mma_bf16_ts(tmem + C::TM_O, tmem + C::TM_S + 128 * b + kk * 8,
+              mma_bf16_ts_w(tmem + C::TM_O, tmem + C::TM_S + 128 * b + kk * 8,
                           dv0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescPV,
                           (j == 0 && kk == 0) ? 0u : 1u);
             }
-            mma_commit(&sm.v_empty[st]);
-            mma_commit(&sm.pv_done[b]);
+            mma_commit_w(&sm.v_empty[st]);
+            mma_commit_w(&sm.pv_done[b]);
           }
           ++t_it;
         }
       }
-      mma_commit(&sm.pv_mma_done);
-      if (!mbar_wait(&sm.pv_mma_done, 0, nullptr, kWaitTimeoutNs))
-        record_failure(p.status, abort, kSiteDrain);
+      mma_commit_w(&sm.pv_mma_done);
+      if (!mbar_wait_warp(&sm.pv_mma_done, 0, nullptr, kWaitTimeoutNs))
+        issuer_fail(p.status, abort, lane, kSiteDrain);
     }
     __syncwarp();
   } else {

@@ -85,6 +85,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// The bounded wait taken by every lane of a converged warp, with the outcome
+// made uniform (the warp stays converged for elect.sync issue after it).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort, uint64_t timeout_ns) {
+  const bool ok = mbar_wait(bar, parity, abort, timeout_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ------------------------------------------------------------------ proxies
 
 // Generic-proxy writes to shared memory made visible to the async proxy
@@ -235,7 +243,9 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 
 // Warp-collective forms of the two MMAs and the commit: every lane of a
 // converged warp executes them and one lane chosen by elect.sync issues, so
-// the operands stay warp-uniform.
+// the operands stay warp-uniform.  With the full mask elect.sync picks the
+// lowest lane every time, so the MMAs and commits of a warp all come from one
+// thread: a commit covers them and they run in issue order.
 __device__ __forceinline__ void mma_bf16_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
