@@ -24,18 +24,19 @@
 // 剖析" section 4.3.4.  Gradient formulas: chain rule through the row softmax.
 //
 // Warps: 0 TMA producer; 1 issuer A (S^T, dP^T; owns tensor memory); 2
-// issuer B (dV, dK, dQ^T); 3..6 key-row warps (P^T, dS^T, dK/dV epilogue);
-// 7..10 dQ drain warps.  A tcgen05.mma instruction holds its issuing thread
-// for about 100 cycles here, longer than the tensor core needs for these
-// shapes, so the 32 instructions of a step are split evenly over two threads.
+// issuer B (dV, dK, dQ^T); 3..10 key-row warps, two per sub-partition, one
+// per 32-query half (P^T, dS^T, dK/dV epilogue); 11..14 dQ drain warps.  A
+// tcgen05.mma instruction holds its issuing thread for about 100 cycles here,
+// longer than the tensor core needs for these shapes, so the 32 instructions
+// of a step are split evenly over two issuer warps.
 // Tensor memory columns: two 64-column S buffers [0,128) (S^T of a step, then
-// its P^T as bf16, then its dQ^T), two dP buffers [128,256) (dP^T, then dS^T
-// as bf16), dV_h [256,384), dK_h [384,512).  With both S and dP double
-// buffered, issuer A can compute the next step's S^T and dP^T while the row
-// warps are still on the current step.  Where issuer A overwrites columns an
-// MMA of issuer B reads, it first waits for that MMA's commit (dk_done, and
-// the drain of dQ^T via dq_free); within one issuer the tensor core keeps
-// issue order, which orders dQ^T(g) after dV(g)'s reads of P^T(g).
+// its P^T as bf16), two dP buffers [128,256) (dP^T, then dS^T as bf16, then
+// the step's dQ^T), dV_h [256,384), dK_h [384,512).  Issuer A writes S buffer
+// b again once dV has read P^T out of it (dv_done) and dP buffer b once the
+// drain has read dQ^T out of it (dq_free), and issues dP^T(g) before
+// S^T(g+1), so that the row warps can compute the next P^T while dQ^T(g) is
+// in flight.  Within one issuer the tensor core keeps issue order, which
+// orders dQ^T(g) after dK(g)'s reads of dS^T(g) in the same columns.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -52,7 +53,12 @@ constexpr int BK = 128;            // keys per work item
 constexpr int DH = 128;            // head-dimension columns of dK, dV, dQ per work item
 constexpr int KCH = 128 * 128;     // 128 rows x 128 bytes
 constexpr int QCH = 64 * 128;      // 64 rows x 128 bytes
-constexpr int kThreads = 352;
+constexpr int kRowWarps = 8;       // two per sub-partition, one per 32-query half
+constexpr int kDrainWarp0 = 3 + kRowWarps;   // four dQ drain warps
+constexpr int kThreads = 32 * (kDrainWarp0 + 4);   // 15 warps
+// With 15 warps one sub-partition holds four: 128 registers a thread at most
+// (the compiler is told 512 threads so that it plans for that).
+constexpr int kRegThreads = 512;
 
 template <int D>
 struct DtCfg {
@@ -62,12 +68,12 @@ struct DtCfg {
   static constexpr int Q_BYTES = NCH * QCH;
   static constexpr int STAGES = D == 128 ? 3 : 1;
   // d = 128 has room for a 64 x 128 fp32 staging tile: dQ^T goes to global
-  // memory as one bulk reduce-add per step.  d = 256 uses atomics.
+  // memory as bulk reduce-adds.  d = 256 uses atomics.
   static constexpr bool DQ_TMA = (D == 128);
-  // Two S buffers [0,64), [64,128): S^T of step g, then P^T (bf16, first 32
-  // columns), then dQ^T of the same step once dV has read P^T.  Two dP
-  // buffers [128,192), [192,256): dP^T, then dS^T (bf16, first 32 columns).
-  // dV [256,384), dK [384,512).
+  // Two S buffers [0,64), [64,128): S^T of step g, then P^T (bf16 pairs in
+  // columns [0,16) and [32,48), see pcol), then dQ^T of the same step once dV
+  // has read P^T.  Two dP buffers [128,192), [192,256): dP^T, then dS^T (bf16,
+  // same columns).  dV [256,384), dK [384,512).
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384;
   static constexpr uint32_t TM_COLS = 512;
 };
@@ -87,7 +93,7 @@ struct DtSmem {
   // per step-parity buffer b = g & 1 wherever a producer can run a step ahead
   uint64_t s_full[2], p_full[2], dp_full[2], ds_full[2], ds_free[2];
   uint64_t dq_full[2], dq_free[2], acc_full, acc_free;
-  uint64_t dk_done[2];              // cross-issuer: dS^T of a step consumed
+  uint64_t dv_done[2];              // cross-issuer: P^T of a step consumed
   uint64_t mma_done_b;
   uint64_t stage_full, stage_free;
   uint64_t mma_done;
@@ -109,6 +115,12 @@ __device__ __forceinline__ void record_failure(int* status, volatile int* abort,
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   bool ok = mbar_wait(bar, parity, abort, kWaitTimeoutNs);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Column of the packed bf16 P^T / dS^T for K-step kk (16 queries) within its
+// 64-column buffer: queries 32h .. 32h+31 sit in columns 32h .. 32h+15.
+__device__ __forceinline__ constexpr uint32_t pcol(int kk) {
+  return static_cast<uint32_t>((kk >> 1) * 32 + (kk & 1) * 8);
 }
 
 // Issuer warps wait as a whole warp (mbar_wait_warp) and report a failure
@@ -166,7 +178,7 @@ __device__ __forceinline__ void dt_range(const BwdParams& p, int n, int len, int
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_constant__ BwdParams p) {
   using C = DtCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
@@ -190,17 +202,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.s_full[b], 1);
-      mbar_init(&sm.p_full[b], 4);
+      mbar_init(&sm.p_full[b], kRowWarps);
       mbar_init(&sm.dp_full[b], 1);
-      mbar_init(&sm.ds_full[b], 4);
+      mbar_init(&sm.ds_full[b], kRowWarps);
       mbar_init(&sm.ds_free[b], 1);
-      mbar_init(&sm.dk_done[b], 1);
+      mbar_init(&sm.dv_done[b], 1);
       mbar_init(&sm.dq_full[b], 1);
       mbar_init(&sm.dq_free[b], 4);
     }
     mbar_init(&sm.mma_done_b, 1);
     mbar_init(&sm.acc_full, 1);
-    mbar_init(&sm.acc_free, 4);
+    mbar_init(&sm.acc_free, kRowWarps);
     mbar_init(&sm.stage_full, 4);
     mbar_init(&sm.stage_free, 1);
     mbar_init(&sm.mma_done, 1);
@@ -303,41 +315,50 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
             ok = false;
             break;
           }
-          for (int s = 0; s < nsteps; ++s, ++g) {
-            const uint32_t b = g & 1;
-            const int st = g % C::STAGES;
-            // S^T = K Q_i^T
-            if (g >= 2 && !mbar_wait_warp(&sm.dq_free[b], ((g >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
-              issuer_fail(p.status, abort, lane, kSiteMmaDq);
-              ok = false;
-              break;
+          // S^T(gg) = K Q^T into S buffer gg&1 once dV(gg-2) has read P^T(gg-2)
+          auto issue_s = [&](uint32_t gg) -> bool {
+            const uint32_t b = gg & 1;
+            const int st = gg % C::STAGES;
+            if (gg >= 2 && !mbar_wait_warp(&sm.dv_done[b], ((gg >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaP);
+              return false;
             }
-            if (!mbar_wait_warp(&sm.q_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+            if (!mbar_wait_warp(&sm.q_full[st], (gg / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
               issuer_fail(p.status, abort, lane, kSiteMmaQ);
-              ok = false;
-              break;
+              return false;
             }
             tc_fence_after_sync();
             const uint64_t dq = sdesc_sw128(smem_u32(sm.q[st]), 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
               mma_bf16_ss_w(tmem + C::TM_S + 64 * b, dK0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
-                          dq + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
+                            dq + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
             mma_commit_w(&sm.s_full[b]);
-            // dP^T = V dO_i^T
-            if (g >= 2 && !mbar_wait_warp(&sm.dk_done[b], ((g >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
-              issuer_fail(p.status, abort, lane, kSiteMmaDs);
-              ok = false;
-              break;
+            return true;
+          };
+          // dP^T(gg) = V dO^T into dP buffer gg&1 once the drain has read
+          // dQ^T(gg-2) out of it (which also means dK(gg-2) has read dS^T(gg-2))
+          auto issue_dp = [&](uint32_t gg) -> bool {
+            const uint32_t b = gg & 1;
+            const int st = gg % C::STAGES;
+            if (gg >= 2 && !mbar_wait_warp(&sm.dq_free[b], ((gg >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaDq);
+              return false;
             }
             tc_fence_after_sync();
             const uint64_t ddo = sdesc_sw128(smem_u32(sm.dO[st]), 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
               mma_bf16_ss_w(tmem + C::TM_DP + 64 * b, dV0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
-                          ddo + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
+                            ddo + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
             mma_commit_w(&sm.dp_full[b]);
             mma_commit_w(&sm.q_empty[st]);          // A's reads of this stage are done
+            return true;
+          };
+          // dP^T(g) goes ahead of S^T(g+1): the row warps need it first
+          ok = issue_s(g);
+          for (int s = 0; ok && s < nsteps; ++s, ++g) {
+            ok = issue_dp(g) && (s + 1 == nsteps || issue_s(g + 1));
           }
           if (!ok) break;
           mma_commit_w(&sm.kv_empty);               // A's reads of K and V are done
@@ -391,8 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
             const uint64_t dQmn = sdesc_sw128(smem_u32(sm.q[st]) + 2 * h * QCH, QCH, 1024);
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
-              mma_bf16_ts_w(tmem + C::TM_DV, tmem + C::TM_S + 64 * b + kk * 8,
+              mma_bf16_ts_w(tmem + C::TM_DV, tmem + C::TM_S + 64 * b + pcol(kk),
                           dOmn + ((kk * 2048) >> 4), kIdAcc, (first && kk == 0) ? 0u : 1u);
+            mma_commit_w(&sm.dv_done[b]);
             // dK_h += dS^T Q_i[:, h]
             if (!mbar_wait_warp(&sm.ds_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
               fail(kSiteMmaDs);
@@ -401,17 +423,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < BQ / 16; ++kk)
-              mma_bf16_ts_w(tmem + C::TM_DK, tmem + C::TM_DP + 64 * b + kk * 8,
+              mma_bf16_ts_w(tmem + C::TM_DK, tmem + C::TM_DP + 64 * b + pcol(kk),
                           dQmn + ((kk * 2048) >> 4), kIdAcc, (first && kk == 0) ? 0u : 1u);
-            mma_commit_w(&sm.dk_done[b]);
             mma_commit_w(&sm.q_empty[st]);          // B's reads of this stage are done
             if (last) mma_commit_w(&sm.acc_full);
-            // dQ^T_h = K[:, h]^T dS^T into S buffer g&1: issued after dV(g) by
-            // this thread, so it runs after dV(g) has read P^T(g) there
+            // dQ^T_h = K[:, h]^T dS^T into dP buffer g&1: issued after dK(g) by
+            // this thread, so it runs after dK(g) has read dS^T(g) there
             const uint64_t dDS = sdesc_sw128(smem_u32(sm.ds[b]), KCH, 1024);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              mma_bf16_ss_w(tmem + C::TM_S + 64 * b, dKmn + ((kk * 2048) >> 4),
+              mma_bf16_ss_w(tmem + C::TM_DP + 64 * b, dKmn + ((kk * 2048) >> 4),
                           dDS + ((kk * 2048) >> 4), kIdDq, kk > 0 ? 1u : 0u);
             mma_commit_w(&sm.dq_full[b]);
             mma_commit_w(&sm.ds_free[b]);
@@ -426,9 +447,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
         issuer_fail(p.status, abort, lane, kSiteDtDrain);
     }
     __syncwarp();
-  } else if (warp < 7) {
+  } else if (warp < 3 + kRowWarps) {
     // ------------------------------------------------------------ key-row warps
+    // Warp w owns key rows 32*(w%4) .. +31 (its tensor-memory lanes) and the
+    // query half hh = (w-3)/4: columns 32*hh .. 32*hh+31 of each step, and
+    // head-dimension columns 64*hh .. 64*hh+63 of the dK/dV epilogue.
     const int quarter = warp & 3;
+    const int hh = (warp - 3) >> 2;
     const int r = quarter * 32 + lane;            // key row of the block = tensor-memory lane
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c2 = p.scale_log2;
@@ -445,14 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
         int i0, i1;
         dt_range(p, n, len, i0, i1);
         const int key = n * BK + r;
-        const size_t out_off = (static_cast<size_t>(bh) * p.N + key) * D + h * DH;
+        const size_t out_off = (static_cast<size_t>(bh) * p.N + key) * D + h * DH + 64 * hh;
         if (i0 >= i1) {
           // key block entirely past the sequence: zero gradients
           if (key < p.N) {
             uint4* a = reinterpret_cast<uint4*>(dk_out + out_off);
             uint4* bq = reinterpret_cast<uint4*>(dv_out + out_off);
 #pragma unroll
-            for (int t = 0; t < DH / 8; ++t) {
+            for (int t = 0; t < 8; ++t) {
               a[t] = make_uint4(0, 0, 0, 0);
               bq[t] = make_uint4(0, 0, 0, 0);
             }
@@ -472,18 +497,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           tc_fence_after_sync();
           const bool need_mask = (n * BK + BK > len) || (p.causal && n * BK + BK - 1 > q0);
           const bool row_dead = key >= len;                       // whole row masked
-          const int lim_causal = p.causal ? key - q0 : -BQ - 1;   // c < lim_causal masked
-          float pr[BQ];
+          // column c (query q0 + 32*hh + c) is masked for c < lim_causal
+          const int lim_causal = p.causal ? key - q0 - 32 * hh : -BQ - 1;
+          float pr[32];
           const uint64_t c2x2 = f2_make(c2, c2);
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
+          {
             uint32_t sr[32];
-            tmem_ld_x32(t_s + 32 * half, sr);
+            tmem_ld_x32(t_s + 32 * hh, sr);
             tmem_wait_ld();
             reg_fence<32>(sr);
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-              const float4 l4 = reinterpret_cast<const float4*>(sm.lse2[st])[8 * half + t];
+              const float4 l4 = reinterpret_cast<const float4*>(sm.lse2[st])[8 * hh + t];
               float a[4];
               f2_split(f2_fma(f2_make(__uint_as_float(sr[4 * t]), __uint_as_float(sr[4 * t + 1])),
                               c2x2, f2_make(-l4.x, -l4.y)),
@@ -493,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
                        a[2], a[3]);
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const int c = 32 * half + 4 * t + e;
+                const int c = 4 * t + e;
                 float pv = ex2_approx(a[e]);
                 if (need_mask && (row_dead || c < lim_causal)) pv = 0.f;
                 pr[c] = pv;
@@ -501,9 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
             }
             uint32_t pk[16];
 #pragma unroll
-            for (int t = 0; t < 16; ++t)
-              pk[t] = pack_bf16x2(pr[32 * half + 2 * t], pr[32 * half + 2 * t + 1]);
-            tmem_st_x16(t_s + 16 * half, pk);
+            for (int t = 0; t < 16; ++t) pk[t] = pack_bf16x2(pr[2 * t], pr[2 * t + 1]);
+            // packed over the first 16 of this half's own 32 columns: the other
+            // half's warp may still be reading its fp32 columns
+            tmem_st_x16(t_s + 32 * hh, pk);
           }
           tmem_wait_st();
           tc_fence_before_sync();
@@ -526,17 +552,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           }
           tc_fence_after_sync();
           uint8_t* rowp = sm.ds[b] + r * 128;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
+          {
             uint32_t sr[32];
-            tmem_ld_x32(t_dp + 32 * half, sr);
+            tmem_ld_x32(t_dp + 32 * hh, sr);
             tmem_wait_ld();
             reg_fence<32>(sr);
             uint32_t pk[16];
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-              const float4 d4 = reinterpret_cast<const float4*>(sm.delta[st])[8 * half + t];
-              const int c = 32 * half + 4 * t;
+              const float4 d4 = reinterpret_cast<const float4*>(sm.delta[st])[8 * hh + t];
+              const int c = 4 * t;
               float d0, d1, d2, d3;
               f2_split(f2_mul(f2_add(f2_make(__uint_as_float(sr[4 * t]), __uint_as_float(sr[4 * t + 1])),
                                      f2_make(-d4.x, -d4.y)),
@@ -549,11 +574,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
               pk[2 * t] = pack_bf16x2(d0, d1);
               pk[2 * t + 1] = pack_bf16x2(d2, d3);
             }
-            tmem_st_x16(t_dp + 16 * half, pk);
+            tmem_st_x16(t_dp + 32 * hh, pk);
             // row = key r, 64 queries = 8 units of 16 bytes, XOR-swizzled by (r & 7)
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-              const int unit = 4 * half + t;
+              const int unit = 4 * hh + t;
               *reinterpret_cast<uint4*>(rowp + ((unit ^ (r & 7)) << 4)) =
                   make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
             }
@@ -565,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           if (lane == 0) mbar_arrive(&sm.ds_full[g & 1]);
         }
         if (!ok) break;
-        // ---- dK_h, dV_h rows of this key block
+        // ---- dK_h, dV_h rows of this key block, head-dimension columns of half hh
         if (!warp_wait(&sm.acc_full, w_it & 1, abort)) {
           if (lane == 0) record_failure(p.status, abort, kSiteRowAcc);
           ok = false;
@@ -573,10 +598,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
         }
         tc_fence_after_sync();
 #pragma unroll 1
-        for (int c4 = 0; c4 < DH / 32; ++c4) {
+        for (int c4 = 0; c4 < 2; ++c4) {
           uint32_t a[32], bb[32];
-          tmem_ld_x32(t_lane + C::TM_DV + 32 * c4, a);
-          tmem_ld_x32(t_lane + C::TM_DK + 32 * c4, bb);
+          tmem_ld_x32(t_lane + C::TM_DV + 64 * hh + 32 * c4, a);
+          tmem_ld_x32(t_lane + C::TM_DK + 64 * hh + 32 * c4, bb);
           tmem_wait_ld();
           reg_fence<32>(a);
           reg_fence<32>(bb);
@@ -608,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;            // head-dimension column within the half
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const bool issuer = (warp == 7 && lane == 0); // issues the bulk reduce-adds
+    const bool issuer = (warp == kDrainWarp0 && lane == 0);  // issues the bulk reduce-adds
     if (C::DQ_TMA && issuer) prefetch_tmap(&p.tdq);
     uint32_t g = 0;
     bool ok = true;
@@ -628,8 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dt_kernel(const __grid_consta
           tc_fence_after_sync();
           const int q0 = i * BQ;
           uint32_t v0[32], v1[32];
-          tmem_ld_x32(t_lane + C::TM_S + 64 * (g & 1), v0);        // dQ^T(g) sits in S buffer g&1
-          tmem_ld_x32(t_lane + C::TM_S + 64 * (g & 1) + 32, v1);
+          tmem_ld_x32(t_lane + C::TM_DP + 64 * (g & 1), v0);       // dQ^T(g) sits in dP buffer g&1
+          tmem_ld_x32(t_lane + C::TM_DP + 64 * (g & 1) + 32, v1);
           tmem_wait_ld();
           reg_fence<32>(v0);
           reg_fence<32>(v1);
