@@ -231,6 +231,7 @@ fa_status_t bwd_main_impl(fa::BwdParams& p, const DeviceInfo* di, const void* q,
       !make_map(&p.tv, v, d, p.N, BH) || !make_map(&p.tdo, dO, d, p.N, BH, qrows))
     return FA_ERR_CUDA;
   if (dt && !make_acc_map(&p.tdq, p.dq_acc, d, p.Npad, BH)) return FA_ERR_CUDA;
+  p.v = v;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = dt ? fa::launch_bwd_main_dt(p, d, di->num_sms, di->max_smem, s)
                            : fa::launch_bwd_main(p, d, di->num_sms, di->max_smem, s);

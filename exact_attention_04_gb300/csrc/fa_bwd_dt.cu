@@ -26,17 +26,21 @@
 // Warps: 0 TMA producer; 1 issuer A (S^T, dP^T; owns tensor memory); 2
 // issuer B (dV, dK, dQ^T); 3..10 key-row warps, two per sub-partition, one
 // per 32-query half (P^T, dS^T, dK/dV epilogue); 11..14 dQ drain warps.  A
-// tcgen05.mma instruction holds its issuing thread for about 100 cycles here,
-// longer than the tensor core needs for these shapes, so the 32 instructions
-// of a step are split evenly over two issuer warps.
-// Tensor memory columns: two 64-column S buffers [0,128) (S^T of a step, then
-// its P^T as bf16), two dP buffers [128,256) (dP^T, then dS^T as bf16, then
-// the step's dQ^T), dV_h [256,384), dK_h [384,512).  Issuer A writes S buffer
-// b again once dV has read P^T out of it (dv_done) and dP buffer b once the
-// drain has read dQ^T out of it (dq_free), and issues dP^T(g) before
-// S^T(g+1), so that the row warps can compute the next P^T while dQ^T(g) is
-// in flight.  Within one issuer the tensor core keeps issue order, which
-// orders dQ^T(g) after dK(g)'s reads of dS^T(g) in the same columns.
+// tcgen05.mma instruction holds its issuing warp for about 100 cycles here,
+// longer than the tensor core needs for these shapes, so the products of a
+// step are split over two issuer warps.  (A third issuer for dP^T measured
+// slower: products that run ahead queue in front of issuer B's.)
+// Tensor memory columns: NSB S buffers (S^T of a step, then its P^T as bf16),
+// NSB dP buffers (dP^T, then dS^T as bf16, then the step's dQ^T), dV_h
+// [256,384), dK_h [384,512); NSB = 2 for d = 128, and for d = 256 one of each
+// plus V in [128,256), written there by the row warps at each key block,
+// which frees the shared memory for a second Q/dO stage.
+// Issuer A writes S buffer b again once dV has read P^T out of it (dv_done)
+// and dP buffer b once the drain has read dQ^T out of it (dq_free), and
+// issues dP^T(g) before S^T(g+1), so that the row warps can compute the next
+// P^T while dQ^T(g) is in flight.  Within one issuer the tensor core keeps
+// issue order, which orders dQ^T(g) after dK(g)'s reads of dS^T(g) in the
+// same columns.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -66,34 +70,44 @@ struct DtCfg {
   static constexpr int NSPLIT = D / DH;
   static constexpr int KV_BYTES = NCH * KCH;
   static constexpr int Q_BYTES = NCH * QCH;
-  static constexpr int STAGES = D == 128 ? 3 : 1;
+  // d = 256: V lives in tensor memory (the A operand of dP^T), which frees
+  // its 64 KB of shared memory for a second Q/dO stage and leaves tensor
+  // memory for one S and one dP buffer.
+  static constexpr bool V_TMEM = (D == 256);
+  static constexpr int STAGES = D == 128 ? 3 : 2;
+  static constexpr int NSB = D == 128 ? 2 : 1;       // S and dP buffers
   // d = 128 has room for a 64 x 128 fp32 staging tile: dQ^T goes to global
   // memory as bulk reduce-adds.  d = 256 uses atomics.
   static constexpr bool DQ_TMA = (D == 128);
-  // Two S buffers [0,64), [64,128): S^T of step g, then P^T (bf16 pairs in
-  // columns [0,16) and [32,48), see pcol), then dQ^T of the same step once dV
-  // has read P^T.  Two dP buffers [128,192), [192,256): dP^T, then dS^T (bf16,
-  // same columns).  dV [256,384), dK [384,512).
-  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 384;
+  // NSB S buffers of 64 columns from TM_S: S^T of a step, then P^T (bf16
+  // pairs in columns [0,16) and [32,48), see pcol).  NSB dP buffers from
+  // TM_DP: dP^T, then dS^T (bf16, same columns), then dQ^T.  d = 256: V
+  // rows (bf16 pairs, 128 columns) from TM_V.  dV [256,384), dK [384,512).
+  static constexpr uint32_t TM_S = 0, TM_DP = 64 * NSB, TM_V = 128;
+  static constexpr uint32_t TM_DV = 256, TM_DK = 384;
   static constexpr uint32_t TM_COLS = 512;
+  static constexpr int V_SMEM_BYTES = V_TMEM ? 16 : KV_BYTES;
+  static_assert(!V_TMEM || (TM_DP + 64 * NSB <= TM_V && TM_V + D / 2 <= TM_DV),
+                "tensor-memory columns overlap");
 };
 
 template <int D>
 struct DtSmem {
   alignas(1024) uint8_t k[DtCfg<D>::KV_BYTES];
-  alignas(1024) uint8_t v[DtCfg<D>::KV_BYTES];
   alignas(1024) uint8_t q[DtCfg<D>::STAGES][DtCfg<D>::Q_BYTES];
   alignas(1024) uint8_t dO[DtCfg<D>::STAGES][DtCfg<D>::Q_BYTES];
   alignas(1024) uint8_t ds[2][KCH];              // dS^T bf16, 128 keys x 64 queries, double buffer
-  alignas(1024) float dq_stage[DtCfg<D>::DQ_TMA ? BQ * DH : 4];   // dQ^T tile, 2 x [d][32 queries]
+  alignas(DtCfg<D>::V_TMEM ? 16 : 1024) uint8_t v[DtCfg<D>::V_SMEM_BYTES];
+  alignas(DtCfg<D>::DQ_TMA ? 1024 : 16) float dq_stage[DtCfg<D>::DQ_TMA ? BQ * DH : 4];   // dQ^T tile, 2 x [d][32 queries]
   alignas(16) float lse2[DtCfg<D>::STAGES][BQ];
   alignas(16) float delta[DtCfg<D>::STAGES][BQ];
   uint64_t kv_full, kv_empty;
   uint64_t q_full[DtCfg<D>::STAGES], q_empty[DtCfg<D>::STAGES];
-  // per step-parity buffer b = g & 1 wherever a producer can run a step ahead
+  // per tensor-memory buffer (g % NSB) or per shared dS buffer (g & 1)
   uint64_t s_full[2], p_full[2], dp_full[2], ds_full[2], ds_free[2];
   uint64_t dq_full[2], dq_free[2], acc_full, acc_free;
   uint64_t dv_done[2];              // cross-issuer: P^T of a step consumed
+  uint64_t v_full, v_free;          // d = 256: V rows written to / read from tensor memory
   uint64_t mma_done_b;
   uint64_t stage_full, stage_free;
   uint64_t mma_done;
@@ -101,10 +115,14 @@ struct DtSmem {
   int abort;
 };
 
+// 227 KB of dynamic shared memory per block on sm_103a
+static_assert(sizeof(DtSmem<128>) <= 232448 && sizeof(DtSmem<256>) <= 232448,
+              "shared-memory layout exceeds the per-block limit");
+
 enum Site {
   kSiteProdKV = 64, kSiteProdQ, kSiteMmaKV, kSiteMmaQ, kSiteMmaP, kSiteMmaDs, kSiteMmaDq,
   kSiteMmaAcc, kSiteRowS, kSiteRowDp, kSiteRowDsFree, kSiteRowAcc, kSiteDrainDq, kSiteDtDrain,
-  kSiteStageFree, kSiteStageFull
+  kSiteStageFree, kSiteStageFull, kSiteRowV, kSiteMmaV
 };
 
 __device__ __forceinline__ void record_failure(int* status, volatile int* abort, int site) {
@@ -213,6 +231,8 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
     mbar_init(&sm.mma_done_b, 1);
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_free, kRowWarps);
+    mbar_init(&sm.v_full, kRowWarps);
+    mbar_init(&sm.v_free, 1);
     mbar_init(&sm.stage_full, 4);
     mbar_init(&sm.stage_free, 1);
     mbar_init(&sm.mma_done, 1);
@@ -251,11 +271,12 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.kv_full, 2 * C::KV_BYTES);
+          mbar_arrive_expect_tx(&sm.kv_full, (C::V_TMEM ? 1 : 2) * C::KV_BYTES);
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c) {
             tma_load_3d(sm.k + c * KCH, &p.tk, &sm.kv_full, 64 * c, n * BK, bh);
-            tma_load_3d(sm.v + c * KCH, &p.tv, &sm.kv_full, 64 * c, n * BK, bh);
+            if constexpr (!C::V_TMEM)
+              tma_load_3d(sm.v + c * KCH, &p.tv, &sm.kv_full, 64 * c, n * BK, bh);
           }
           ++w_it;
           for (int i = i0; i < i1; ++i) {
@@ -315,11 +336,13 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
             ok = false;
             break;
           }
-          // S^T(gg) = K Q^T into S buffer gg&1 once dV(gg-2) has read P^T(gg-2)
+          // S^T(gg) = K Q^T into S buffer gg%NSB once dV(gg-NSB) has read
+          // P^T(gg-NSB) out of it
           auto issue_s = [&](uint32_t gg) -> bool {
-            const uint32_t b = gg & 1;
+            const uint32_t b = gg % C::NSB;
+            const uint32_t ph = (gg / C::NSB) & 1;
             const int st = gg % C::STAGES;
-            if (gg >= 2 && !mbar_wait_warp(&sm.dv_done[b], ((gg >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+            if (gg >= C::NSB && !mbar_wait_warp(&sm.dv_done[b], ph ^ 1, abort, kWaitTimeoutNs)) {
               issuer_fail(p.status, abort, lane, kSiteMmaP);
               return false;
             }
@@ -336,32 +359,45 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
             mma_commit_w(&sm.s_full[b]);
             return true;
           };
-          // dP^T(gg) = V dO^T into dP buffer gg&1 once the drain has read
-          // dQ^T(gg-2) out of it (which also means dK(gg-2) has read dS^T(gg-2))
+          // dP^T(gg) = V dO^T into dP buffer gg%NSB once the drain has read
+          // dQ^T(gg-NSB) out of it (which also means dK(gg-NSB) has read
+          // dS^T(gg-NSB)).  d = 256: V (A operand) from tensor memory.
           auto issue_dp = [&](uint32_t gg) -> bool {
-            const uint32_t b = gg & 1;
+            const uint32_t b = gg % C::NSB;
+            const uint32_t ph = (gg / C::NSB) & 1;
             const int st = gg % C::STAGES;
-            if (gg >= 2 && !mbar_wait_warp(&sm.dq_free[b], ((gg >> 1) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+            if (gg >= C::NSB && !mbar_wait_warp(&sm.dq_free[b], ph ^ 1, abort, kWaitTimeoutNs)) {
               issuer_fail(p.status, abort, lane, kSiteMmaDq);
               return false;
             }
             tc_fence_after_sync();
             const uint64_t ddo = sdesc_sw128(smem_u32(sm.dO[st]), 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_bf16_ss_w(tmem + C::TM_DP + 64 * b, dV0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
-                            ddo + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t bk = ddo + (((kk / 4) * QCH + (kk % 4) * 32) >> 4);
+              if constexpr (C::V_TMEM)
+                mma_bf16_ts_w(tmem + C::TM_DP + 64 * b, tmem + C::TM_V + 8 * kk, bk, kIdS,
+                              kk > 0 ? 1u : 0u);
+              else
+                mma_bf16_ss_w(tmem + C::TM_DP + 64 * b, dV0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
+                              bk, kIdS, kk > 0 ? 1u : 0u);
+            }
             mma_commit_w(&sm.dp_full[b]);
             mma_commit_w(&sm.q_empty[st]);          // A's reads of this stage are done
             return true;
           };
           // dP^T(g) goes ahead of S^T(g+1): the row warps need it first
           ok = issue_s(g);
+          if (ok && C::V_TMEM && !mbar_wait_warp(&sm.v_full, w_it & 1, abort, kWaitTimeoutNs)) {
+            issuer_fail(p.status, abort, lane, kSiteMmaV);
+            ok = false;
+          }
           for (int s = 0; ok && s < nsteps; ++s, ++g) {
             ok = issue_dp(g) && (s + 1 == nsteps || issue_s(g + 1));
           }
           if (!ok) break;
           mma_commit_w(&sm.kv_empty);               // A's reads of K and V are done
+          if constexpr (C::V_TMEM) mma_commit_w(&sm.v_free);   // ... and of V in tensor memory
           ++w_it;
         }
       }
@@ -395,11 +431,13 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
           const int nsteps = i1 - i0;
           for (int s = 0; s < nsteps; ++s, ++g) {
             const int st = g % C::STAGES;
-            const uint32_t b = g & 1;
+            const uint32_t b = g % C::NSB;          // tensor-memory S / dP buffer
+            const uint32_t ph = (g / C::NSB) & 1;
+            const uint32_t bs = g & 1;              // shared dS buffer
             const bool first = (s == 0);
             const bool last = (s + 1 == nsteps);
             // dV_h += P^T dO_i[:, h]
-            if (!mbar_wait_warp(&sm.p_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
+            if (!mbar_wait_warp(&sm.p_full[b], ph, abort, kWaitTimeoutNs)) {
               fail(kSiteMmaP);
               break;
             }
@@ -416,7 +454,7 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
                           dOmn + ((kk * 2048) >> 4), kIdAcc, (first && kk == 0) ? 0u : 1u);
             mma_commit_w(&sm.dv_done[b]);
             // dK_h += dS^T Q_i[:, h]
-            if (!mbar_wait_warp(&sm.ds_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
+            if (!mbar_wait_warp(&sm.ds_full[bs], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
               fail(kSiteMmaDs);
               break;
             }
@@ -427,15 +465,15 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
                           dQmn + ((kk * 2048) >> 4), kIdAcc, (first && kk == 0) ? 0u : 1u);
             mma_commit_w(&sm.q_empty[st]);          // B's reads of this stage are done
             if (last) mma_commit_w(&sm.acc_full);
-            // dQ^T_h = K[:, h]^T dS^T into dP buffer g&1: issued after dK(g) by
+            // dQ^T_h = K[:, h]^T dS^T into dP buffer b: issued after dK(g) by
             // this thread, so it runs after dK(g) has read dS^T(g) there
-            const uint64_t dDS = sdesc_sw128(smem_u32(sm.ds[b]), KCH, 1024);
+            const uint64_t dDS = sdesc_sw128(smem_u32(sm.ds[bs]), KCH, 1024);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
               mma_bf16_ss_w(tmem + C::TM_DP + 64 * b, dKmn + ((kk * 2048) >> 4),
                           dDS + ((kk * 2048) >> 4), kIdDq, kk > 0 ? 1u : 0u);
             mma_commit_w(&sm.dq_full[b]);
-            mma_commit_w(&sm.ds_free[b]);
+            mma_commit_w(&sm.ds_free[bs]);
             if (last) mma_commit_w(&sm.kv_empty);   // B's reads of K are done
           }
           if (!ok) break;
@@ -484,12 +522,45 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
           }
           continue;
         }
+        if constexpr (C::V_TMEM) {
+          // V rows of this key block into tensor memory, the A operand of
+          // dP^T: row r, head-dimension elements 128*hh .. +127 as bf16 pairs in
+          // columns 64*hh .. +63, once the last dP^T of the previous item is done
+          if (!warp_wait(&sm.v_free, (w_it & 1) ^ 1, abort)) {
+            if (lane == 0) record_failure(p.status, abort, kSiteRowV);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint4* vrow = reinterpret_cast<const uint4*>(
+              static_cast<const __nv_bfloat16*>(p.v) + (static_cast<size_t>(bh) * p.N + key) * D +
+              128 * hh);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t vr[32];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const uint4 x = key < p.N ? __ldg(vrow + 8 * c + t) : make_uint4(0, 0, 0, 0);
+              vr[4 * t] = x.x;
+              vr[4 * t + 1] = x.y;
+              vr[4 * t + 2] = x.z;
+              vr[4 * t + 3] = x.w;
+            }
+            tmem_st_x32(t_lane + C::TM_V + 64 * hh + 32 * c, vr);
+          }
+          tmem_wait_st();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.v_full);
+        }
         for (int i = i0; i < i1; ++i, ++g) {
           const int st = g % C::STAGES;
           const int q0 = i * BQ;
+          const uint32_t tb = g % C::NSB;                          // tensor-memory S / dP buffer
+          const uint32_t tph = (g / C::NSB) & 1;
           // ---- P^T = exp2(S^T * c - L2), masked; bf16 copy back to tensor memory
-          const uint32_t t_s = t_lane + C::TM_S + 64 * (g & 1);   // this step's S^T buffer
-          if (!warp_wait(&sm.s_full[g & 1], (g >> 1) & 1, abort)) {
+          const uint32_t t_s = t_lane + C::TM_S + 64 * tb;         // this step's S^T buffer
+          if (!warp_wait(&sm.s_full[tb], tph, abort)) {
             if (lane == 0) record_failure(p.status, abort, kSiteRowS);
             ok = false;
             break;
@@ -534,10 +605,10 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
           tmem_wait_st();
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.p_full[g & 1]);
+          if (lane == 0) mbar_arrive(&sm.p_full[tb]);
           // ---- dS^T = P^T o (dP^T - D)
-          const uint32_t t_dp = t_lane + C::TM_DP + 64 * (g & 1);  // this step's dP^T buffer
-          if (!warp_wait(&sm.dp_full[g & 1], (g >> 1) & 1, abort)) {
+          const uint32_t t_dp = t_lane + C::TM_DP + 64 * tb;       // this step's dP^T buffer
+          if (!warp_wait(&sm.dp_full[tb], tph, abort)) {
             if (lane == 0) record_failure(p.status, abort, kSiteRowDp);
             ok = false;
             break;
@@ -645,7 +716,8 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         int i0, i1;
         dt_range(p, n, dt_len(p, bh), i0, i1);
         for (int i = i0; i < i1; ++i, ++g) {
-          if (!warp_wait(&sm.dq_full[g & 1], (g >> 1) & 1, abort)) {
+          const uint32_t tb = g % C::NSB;
+          if (!warp_wait(&sm.dq_full[tb], (g / C::NSB) & 1, abort)) {
             if (lane == 0) record_failure(p.status, abort, kSiteDrainDq);
             ok = false;
             break;
@@ -653,15 +725,15 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
           tc_fence_after_sync();
           const int q0 = i * BQ;
           uint32_t v0[32], v1[32];
-          tmem_ld_x32(t_lane + C::TM_DP + 64 * (g & 1), v0);       // dQ^T(g) sits in dP buffer g&1
-          tmem_ld_x32(t_lane + C::TM_DP + 64 * (g & 1) + 32, v1);
+          tmem_ld_x32(t_lane + C::TM_DP + 64 * tb, v0);            // dQ^T(g) sits in dP buffer tb
+          tmem_ld_x32(t_lane + C::TM_DP + 64 * tb + 32, v1);
           tmem_wait_ld();
           reg_fence<32>(v0);
           reg_fence<32>(v1);
           // the whole tile is in registers: tensor memory is free for the next dQ^T
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.dq_free[g & 1]);
+          if (lane == 0) mbar_arrive(&sm.dq_free[tb]);
           if constexpr (C::DQ_TMA) {
             // staging: two boxes of [128 columns][32 queries] fp32 in the
             // 128-byte swizzle of the tensor map; this thread owns row r of

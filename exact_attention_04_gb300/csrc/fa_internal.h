@@ -32,6 +32,7 @@ struct BwdParams {
   CUtensorMap tdq;             // fp32 dQ^T accumulator [BH, d, Npad], box (32, 128, 1), SW128
   const void* o;               // bf16 [B, H, N, d]
   const void* dO;              // bf16 [B, H, N, d]
+  const void* v;               // bf16 [B, H, N, d] (d = 256 reads V rows directly)
   const float* lse;            // fp32 [B, H, N]
   void* dq;                    // bf16 [B, H, N, d]
   void* dk;                    // bf16
