@@ -35,15 +35,15 @@ def _load():
         dp = ctypes.POINTER(ctypes.c_double)
         ip = ctypes.POINTER(ctypes.c_int)
         c_int, c_double = ctypes.c_int, ctypes.c_double
-        lib.fa_oracle_forward.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int,
-                                          c_double, c_int, ip, c_int]
-        lib.fa_oracle_forward.restype = c_int
-        lib.fa_oracle_forward_rows.argtypes = [dp, dp, dp, c_int, c_int, c_double, c_int, c_int,
-                                               ip, c_int, dp, dp, c_int]
-        lib.fa_oracle_forward_rows.restype = c_int
-        lib.fa_oracle_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int,
-                                           c_int, c_double, c_int, ip, c_int]
-        lib.fa_oracle_backward.restype = c_int
+        lib.fa_oracle_forward_v.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_int,
+                                            c_double, c_int, ip, c_int, c_int, c_int]
+        lib.fa_oracle_forward_v.restype = c_int
+        lib.fa_oracle_forward_rows_v.argtypes = [dp, dp, dp, c_int, c_int, c_double, c_int, c_int,
+                                                 c_int, c_int, ip, c_int, dp, dp, c_int]
+        lib.fa_oracle_forward_rows_v.restype = c_int
+        lib.fa_oracle_backward_v.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int,
+                                             c_int, c_int, c_double, c_int, ip, c_int, c_int, c_int]
+        lib.fa_oracle_backward_v.restype = c_int
         lib.fa_oracle_num_threads.argtypes = []
         lib.fa_oracle_num_threads.restype = c_int
         _lib = lib
@@ -76,49 +76,75 @@ def _kv(kv_len, B):
     return kv, _ptr(kv, ctypes.c_int)
 
 
-def attention_fwd(q, k, v, scale, causal=False, kv_len=None, threads=None):
-    """O [B,H,N,d] and LSE [B,H,N] of exact attention (float64 numpy arrays)."""
-    q, k, v = _f64(q), _f64(k), _f64(v)
+def _window(window):
+    wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    if wl < -1 or wr < -1:
+        raise ValueError("window sides are -1 (unbounded) or >= 0")
+    return wl, wr
+
+
+def _heads(q, k):
     B, H, N, d = q.shape
-    assert k.shape == q.shape and v.shape == q.shape
+    Hkv = k.shape[1]
+    if k.shape != (B, Hkv, N, d) or Hkv < 1 or H % Hkv:
+        raise ValueError(f"K/V shape {k.shape} does not group the {H} query heads")
+    return B, H, Hkv, N, d
+
+
+def attention_fwd(q, k, v, scale, causal=False, kv_len=None, threads=None, window=None):
+    """O [B,H,N,d] and LSE [B,H,N] of exact attention (float64 numpy arrays).
+
+    k, v are [B,H_kv,N,d] with H_kv dividing H (query head h reads K/V head
+    h // (H // H_kv)); window is flash-attn's (left, right), -1 = unbounded."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Hkv, N, d = _heads(q, k)
+    assert v.shape == k.shape
+    wl, wr = _window(window)
     o = np.empty_like(q)
     lse = np.empty((B, H, N), dtype=np.float64)
     kv, kvp = _kv(kv_len, B)
-    rc = _load().fa_oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                                   float(scale), int(bool(causal)), kvp,
-                                   threads or default_threads())
+    rc = _load().fa_oracle_forward_v(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv,
+                                     N, d, float(scale), int(bool(causal)), kvp, wl, wr,
+                                     threads or default_threads())
     if rc:
         raise RuntimeError(f"oracle forward failed ({rc})")
     return o, lse
 
 
-def attention_fwd_rows(q, k, v, rows, scale, causal=False, kv_len=None, threads=None):
+def attention_fwd_rows(q, k, v, rows, scale, causal=False, kv_len=None, threads=None,
+                       window=None):
     """Forward for selected query rows of one head; q, k, v are [N, d]."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     N, d = q.shape
+    wl, wr = _window(window)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
     o = np.empty((rows.size, d), dtype=np.float64)
     lse = np.empty(rows.size, dtype=np.float64)
     length = N if kv_len is None else int(kv_len)
-    rc = _load().fa_oracle_forward_rows(_ptr(q), _ptr(k), _ptr(v), N, d, float(scale),
-                                        int(bool(causal)), length, _ptr(rows, ctypes.c_int),
-                                        int(rows.size), _ptr(o), _ptr(lse),
-                                        threads or default_threads())
+    rc = _load().fa_oracle_forward_rows_v(_ptr(q), _ptr(k), _ptr(v), N, d, float(scale),
+                                          int(bool(causal)), length, wl, wr,
+                                          _ptr(rows, ctypes.c_int), int(rows.size), _ptr(o),
+                                          _ptr(lse), threads or default_threads())
     if rc:
         raise RuntimeError(f"oracle forward_rows failed ({rc})")
     return o, lse
 
 
-def attention_bwd(q, k, v, do, scale, causal=False, kv_len=None, threads=None):
-    """dQ, dK, dV [B,H,N,d] and D [B,H,N] (D_i = sum_j P_ij dP_ij)."""
+def attention_bwd(q, k, v, do, scale, causal=False, kv_len=None, threads=None, window=None):
+    """dQ [B,H,N,d], dK and dV [B,H_kv,N,d] (summed over each group's query
+    heads) and D [B,H,N] (D_i = sum_j P_ij dP_ij)."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
-    B, H, N, d = q.shape
-    dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
+    B, H, Hkv, N, d = _heads(q, k)
+    assert v.shape == k.shape and do.shape == q.shape
+    wl, wr = _window(window)
+    dq = np.empty_like(q)
+    dk, dv = np.empty_like(k), np.empty_like(k)
     D = np.empty((B, H, N), dtype=np.float64)
     kv, kvp = _kv(kv_len, B)
-    rc = _load().fa_oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
-                                    _ptr(dv), _ptr(D), B, H, N, d, float(scale),
-                                    int(bool(causal)), kvp, threads or default_threads())
+    rc = _load().fa_oracle_backward_v(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
+                                      _ptr(dv), _ptr(D), B, H, Hkv, N, d, float(scale),
+                                      int(bool(causal)), kvp, wl, wr,
+                                      threads or default_threads())
     if rc:
         raise RuntimeError(f"oracle backward failed ({rc})")
     return dq, dk, dv, D

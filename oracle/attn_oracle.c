@@ -36,12 +36,23 @@
  *   dQ_i  = scale * sum_j dS_ij k_j
  *   dK_j  = scale * sum_i dS_ij q_i
  *
- * Masks.  Key j is visible to query i iff j < kv_len[b] and, when causal,
- * j <= i (square attention, N queries and N keys, 0-based indices).  A row
- * with no visible key gets O = 0 and LSE = -inf (cannot occur with kv_len >= 1).
+ * Masks.  Key j is visible to query i iff j < kv_len[b], j <= i when causal,
+ * j >= i - window_left when window_left >= 0, and j <= i + window_right when
+ * window_right >= 0 (square attention, N queries and N keys, 0-based
+ * indices).  The window is the (left, right) pair of flash-attn's
+ * window_size argument, (-1, -1) meaning no window ("Flash Attention 详解",
+ * section 六; "4. FlashAttention 深度剖析" 4.8.1, sliding window).  A row
+ * with no visible key gets O = 0 and LSE = -inf.
  *
- * Layout: every tensor is a contiguous [B, H, N, d] array of doubles, LSE and
- * D are [B, H, N].  kv_len is NULL (no padding) or an int array of length B.
+ * Grouped K/V heads (GQA / MQA, "Flash Attention 详解" section 六 and the
+ * FlashAttention-2 summary in "注意力为什么受限于显存带宽…"): K and V have
+ * H_kv heads, H_kv divides H, and query head h reads K/V head
+ * h / (H / H_kv).  dK and dV of a K/V head are the sums over the query heads
+ * that read it.
+ *
+ * Layout: Q, O, dO, dQ are contiguous [B, H, N, d] arrays of doubles, K, V,
+ * dK, dV are [B, H_kv, N, d], LSE and D are [B, H, N].  kv_len is NULL (no
+ * padding) or an int array of length B.
  * Rows are spread over OpenMP threads when the file is built with -fopenmp;
  * the per-row arithmetic does not depend on the thread count, only the order
  * of the final dK/dV sums across threads does (a rounding-level effect).
@@ -57,10 +68,18 @@
 #define ORACLE_EINVAL 1
 #define ORACLE_ENOMEM 2
 
-static int key_visible(long i, long j, int causal, long len)
+typedef struct {
+    int causal;
+    long len;          /* kv_len of the batch entry */
+    long wl, wr;       /* window: -1 = unbounded on that side */
+} mask_t;
+
+static int key_visible(long i, long j, const mask_t *m)
 {
-    if (j >= len) return 0;
-    if (causal && j > i) return 0;
+    if (j >= m->len) return 0;
+    if (m->causal && j > i) return 0;
+    if (m->wl >= 0 && j < i - m->wl) return 0;
+    if (m->wr >= 0 && j > i + m->wr) return 0;
     return 1;
 }
 
@@ -74,12 +93,12 @@ static double dot(const double *a, const double *b, int d)
 /* One row of P for query i of one head: fills p[0..N) (0 for masked keys)
  * and returns the LSE of the row.  The three passes of the safe softmax. */
 static double softmax_row(const double *qi, const double *K, int N, int d,
-                          double scale, int causal, long len, long i, double *p)
+                          double scale, const mask_t *mk, long i, double *p)
 {
     double m = -INFINITY;
     int any = 0;
     for (long j = 0; j < N; ++j) {               /* S row and pass 1: max */
-        if (key_visible(i, j, causal, len)) {
+        if (key_visible(i, j, mk)) {
             p[j] = scale * dot(qi, K + j * (long)d, d);
             if (p[j] > m) m = p[j];
             any = 1;
@@ -93,7 +112,7 @@ static double softmax_row(const double *qi, const double *K, int N, int d,
     }
     double l = 0.0;
     for (long j = 0; j < N; ++j) {               /* pass 2: sum of exp(S - m) */
-        p[j] = key_visible(i, j, causal, len) ? exp(p[j] - m) : 0.0;
+        p[j] = key_visible(i, j, mk) ? exp(p[j] - m) : 0.0;
         l += p[j];
     }
     for (long j = 0; j < N; ++j) p[j] /= l;      /* pass 3: normalise */
@@ -107,6 +126,11 @@ static int check_args(const void *a, const void *b, const void *c, int B, int H,
     return 1;
 }
 
+static int check_heads(int H, int H_kv)
+{
+    return H_kv >= 1 && H_kv <= H && H % H_kv == 0;
+}
+
 int fa_oracle_num_threads(void)
 {
 #ifdef _OPENMP
@@ -116,20 +140,24 @@ int fa_oracle_num_threads(void)
 #endif
 }
 
-/* Forward over every (b, h) and every row. */
-int fa_oracle_forward(const double *q, const double *k, const double *v,
-                      double *o, double *lse,
-                      int B, int H, int N, int d, double scale, int causal,
-                      const int *kv_len, int nthreads)
+/* Forward over every (b, h) and every row; K/V head of query head h is
+ * h / (H / H_kv), window (wl, wr) as in the header. */
+int fa_oracle_forward_v(const double *q, const double *k, const double *v,
+                        double *o, double *lse,
+                        int B, int H, int H_kv, int N, int d, double scale, int causal,
+                        const int *kv_len, int wl, int wr, int nthreads)
 {
-    if (!check_args(q, k, v, B, H, N, d) || !o || !lse) return ORACLE_EINVAL;
+    if (!check_args(q, k, v, B, H, N, d) || !o || !lse || !check_heads(H, H_kv))
+        return ORACLE_EINVAL;
     if (nthreads < 1) nthreads = 1;
     const long hd = (long)N * d;
+    const int group = H / H_kv;
     int err = ORACLE_OK;
     for (long bh = 0; bh < (long)B * H; ++bh) {
         const long b = bh / H;
-        const long len = kv_len ? kv_len[b] : N;
-        const double *Q = q + bh * hd, *K = k + bh * hd, *V = v + bh * hd;
+        const long kvh = b * H_kv + (bh % H) / group;
+        const mask_t mk = {causal, kv_len ? kv_len[b] : N, wl, wr};
+        const double *Q = q + bh * hd, *K = k + kvh * hd, *V = v + kvh * hd;
         double *O = o + bh * hd, *L = lse + bh * (long)N;
 #pragma omp parallel num_threads(nthreads)
         {
@@ -143,7 +171,7 @@ int fa_oracle_forward(const double *q, const double *k, const double *v,
             for (long i = 0; i < N; ++i) {
                 if (!p) continue;
                 {
-                    L[i] = softmax_row(Q + i * d, K, N, d, scale, causal, len, i, p);
+                    L[i] = softmax_row(Q + i * d, K, N, d, scale, &mk, i, p);
                     double *oi = O + i * d;
                     for (int t = 0; t < d; ++t) oi[t] = 0.0;
                     for (long j = 0; j < N; ++j) {
@@ -160,13 +188,23 @@ int fa_oracle_forward(const double *q, const double *k, const double *v,
     return ORACLE_OK;
 }
 
+int fa_oracle_forward(const double *q, const double *k, const double *v,
+                      double *o, double *lse,
+                      int B, int H, int N, int d, double scale, int causal,
+                      const int *kv_len, int nthreads)
+{
+    return fa_oracle_forward_v(q, k, v, o, lse, B, H, H, N, d, scale, causal, kv_len, -1, -1,
+                               nthreads);
+}
+
 /* Forward for a chosen set of query rows of ONE head (q, k, v are [N, d]).
  * o_rows is [nrows, d], lse_rows is [nrows]; len is that head's kv_len. */
-int fa_oracle_forward_rows(const double *q, const double *k, const double *v,
-                           int N, int d, double scale, int causal, int len,
-                           const int *rows, int nrows,
-                           double *o_rows, double *lse_rows, int nthreads)
+int fa_oracle_forward_rows_v(const double *q, const double *k, const double *v,
+                             int N, int d, double scale, int causal, int len, int wl, int wr,
+                             const int *rows, int nrows,
+                             double *o_rows, double *lse_rows, int nthreads)
 {
+    const mask_t mk = {causal, len, wl, wr};
     if (!check_args(q, k, v, 1, 1, N, d) || !rows || !o_rows || !lse_rows || nrows < 0)
         return ORACLE_EINVAL;
     for (int r = 0; r < nrows; ++r)
@@ -185,7 +223,7 @@ int fa_oracle_forward_rows(const double *q, const double *k, const double *v,
             if (!p) continue;
             {
                 const long i = rows[r];
-                lse_rows[r] = softmax_row(q + i * d, k, N, d, scale, causal, len, i, p);
+                lse_rows[r] = softmax_row(q + i * d, k, N, d, scale, &mk, i, p);
                 double *oi = o_rows + (long)r * d;
                 for (int t = 0; t < d; ++t) oi[t] = 0.0;
                 for (long j = 0; j < N; ++j) {
@@ -200,29 +238,42 @@ int fa_oracle_forward_rows(const double *q, const double *k, const double *v,
     return err;
 }
 
-/* Backward over every (b, h): dq, dk, dv are [B,H,N,d]; D is [B,H,N]
+int fa_oracle_forward_rows(const double *q, const double *k, const double *v,
+                           int N, int d, double scale, int causal, int len,
+                           const int *rows, int nrows,
+                           double *o_rows, double *lse_rows, int nthreads)
+{
+    return fa_oracle_forward_rows_v(q, k, v, N, d, scale, causal, len, -1, -1, rows, nrows,
+                                    o_rows, lse_rows, nthreads);
+}
+
+/* Backward over every (b, h): dq is [B,H,N,d], dk and dv are [B,H_kv,N,d]
+ * (sums over the query heads of each group); D is [B,H,N]
  * (D_i = sum_j P_ij dP_ij).  P is rebuilt from its definition, not from a
  * stored LSE, so the oracle does not depend on the forward's outputs. */
-int fa_oracle_backward(const double *q, const double *k, const double *v,
-                       const double *dout,
-                       double *dq, double *dk, double *dv, double *D,
-                       int B, int H, int N, int d, double scale, int causal,
-                       const int *kv_len, int nthreads)
+int fa_oracle_backward_v(const double *q, const double *k, const double *v,
+                         const double *dout,
+                         double *dq, double *dk, double *dv, double *D,
+                         int B, int H, int H_kv, int N, int d, double scale, int causal,
+                         const int *kv_len, int wl, int wr, int nthreads)
 {
-    if (!check_args(q, k, v, B, H, N, d) || !dout || !dq || !dk || !dv || !D)
+    if (!check_args(q, k, v, B, H, N, d) || !dout || !dq || !dk || !dv || !D ||
+        !check_heads(H, H_kv))
         return ORACLE_EINVAL;
     if (nthreads < 1) nthreads = 1;
     const long hd = (long)N * d;
+    const int group = H / H_kv;
     int err = ORACLE_OK;
+    memset(dk, 0, sizeof(double) * (size_t)((long)B * H_kv * hd));
+    memset(dv, 0, sizeof(double) * (size_t)((long)B * H_kv * hd));
     for (long bh = 0; bh < (long)B * H; ++bh) {
         const long b = bh / H;
-        const long len = kv_len ? kv_len[b] : N;
-        const double *Q = q + bh * hd, *K = k + bh * hd, *V = v + bh * hd;
+        const long kvh = b * H_kv + (bh % H) / group;
+        const mask_t mk = {causal, kv_len ? kv_len[b] : N, wl, wr};
+        const double *Q = q + bh * hd, *K = k + kvh * hd, *V = v + kvh * hd;
         const double *dO = dout + bh * hd;
-        double *dQ = dq + bh * hd, *dK = dk + bh * hd, *dV = dv + bh * hd;
+        double *dQ = dq + bh * hd, *dK = dk + kvh * hd, *dV = dv + kvh * hd;
         double *Dh = D + bh * (long)N;
-        memset(dK, 0, sizeof(double) * (size_t)hd);
-        memset(dV, 0, sizeof(double) * (size_t)hd);
 #pragma omp parallel num_threads(nthreads)
         {
             double *p = (double *)malloc(sizeof(double) * (size_t)N);
@@ -239,7 +290,7 @@ int fa_oracle_backward(const double *q, const double *k, const double *v,
                 if (!ok) continue;
                 {
                     const double *qi = Q + i * d, *doi = dO + i * d;
-                    softmax_row(qi, K, N, d, scale, causal, len, i, p);
+                    softmax_row(qi, K, N, d, scale, &mk, i, p);
                     double Di = 0.0;
                     for (long j = 0; j < N; ++j) {        /* dP = dO V^T, D = rowsum(P o dP) */
                         dp[j] = (p[j] != 0.0) ? dot(doi, V + j * d, d) : 0.0;
@@ -278,4 +329,14 @@ int fa_oracle_backward(const double *q, const double *k, const double *v,
         if (err) return err;
     }
     return ORACLE_OK;
+}
+
+int fa_oracle_backward(const double *q, const double *k, const double *v,
+                       const double *dout,
+                       double *dq, double *dk, double *dv, double *D,
+                       int B, int H, int N, int d, double scale, int causal,
+                       const int *kv_len, int nthreads)
+{
+    return fa_oracle_backward_v(q, k, v, dout, dq, dk, dv, D, B, H, H, N, d, scale, causal,
+                                kv_len, -1, -1, nthreads);
 }
