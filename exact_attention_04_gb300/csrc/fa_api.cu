@@ -11,6 +11,7 @@
 
 #include "../../include/fa.h"
 #include "fa_internal.h"
+#include "fa_window.cuh"
 
 // Written by kernels that gave up waiting; read and cleared by fa_check.
 __device__ int g_fa_status;
@@ -119,6 +120,29 @@ bool make_acc_map(CUtensorMap* m, void* base, int d, int npad, int BH) {
 
 size_t round_up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// The variant as the kernels see it: K/V heads, and the window folded with
+// causal into the bounds wl, wr (key j visible to query i iff
+// i - wl <= j <= i + wr), unbounded sides as fa::kUnbounded.  `pair` is true
+// for plain causal attention, where the schedule pairs long and short tiles.
+struct Variant {
+  int H_kv, wl, wr;
+  bool pair;
+};
+
+fa_status_t resolve_variant(const fa_variant_t* var, int H, int causal, Variant* out) {
+  const int h_kv = var ? var->h_kv : H;
+  const int left = var ? var->window_left : -1;
+  const int right = var ? var->window_right : -1;
+  if (h_kv < 1 || h_kv > H || H % h_kv != 0 || left < -1 || right < -1)
+    return FA_ERR_INVALID_ARG;
+  out->H_kv = h_kv;
+  out->wl = left < 0 ? fa::kUnbounded : left;
+  out->wr = right < 0 ? fa::kUnbounded : right;
+  if (causal && out->wr > 0) out->wr = 0;
+  out->pair = causal && left < 0;
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -139,6 +163,12 @@ const char* fa_status_string(fa_status_t s) {
 fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                    int H, int N, int d, float scale, int causal, const int* kv_len,
                    void* stream) {
+  return fa_fwd_v(q, k, v, o, lse, B, H, N, d, scale, causal, kv_len, nullptr, stream);
+}
+
+fa_status_t fa_fwd_v(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, float scale, int causal, const int* kv_len,
+                     const fa_variant_t* variant, void* stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u))
@@ -146,14 +176,17 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
   if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
   const fa_status_t sz = check_sizes(B, H, N, d, scale);
   if (sz != FA_OK) return sz;
+  Variant var;
+  const fa_status_t vs = resolve_variant(variant, H, causal, &var);
+  if (vs != FA_OK) return vs;
   DeviceInfo* di = device_info(nullptr);
   if (!di || di->err != cudaSuccess) return FA_ERR_CUDA;
   if (!di->supported) return FA_ERR_UNSUPPORTED;
   fa::FwdParams p;
   std::memset(&p, 0, sizeof(p));
   const int BH = B * H;
-  if (!make_map(&p.tq, q, d, N, BH) || !make_map(&p.tk, k, d, N, BH) ||
-      !make_map(&p.tv, v, d, N, BH))
+  if (!make_map(&p.tq, q, d, N, BH) || !make_map(&p.tk, k, d, N, B * var.H_kv) ||
+      !make_map(&p.tv, v, d, N, B * var.H_kv))
     return FA_ERR_CUDA;
   p.o = o;
   p.lse = lse;
@@ -161,7 +194,10 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
   p.B = B;
   p.H = H;
   p.N = N;
-  p.causal = causal ? 1 : 0;
+  p.H_kv = var.H_kv;
+  p.wl = var.wl;
+  p.wr = var.wr;
+  p.causal = var.pair ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.status = di->status;
   if (fa::launch_fwd(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -187,11 +223,15 @@ namespace {
 // Common checks of the backward entry points and the parameter block they
 // share.  Pointer arguments are checked by each caller.
 fa_status_t bwd_setup(fa::BwdParams* p, DeviceInfo** di, int B, int H, int N, int d, float scale,
-                      int causal, const int* kv_len, void* workspace, size_t workspace_bytes) {
+                      int causal, const int* kv_len, const fa_variant_t* variant,
+                      void* workspace, size_t workspace_bytes) {
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return FA_ERR_INVALID_ARG;
   if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
   const fa_status_t sz = check_sizes(B, H, N, d, scale);
   if (sz != FA_OK) return sz;
+  Variant var;
+  const fa_status_t vs = resolve_variant(variant, H, causal, &var);
+  if (vs != FA_OK) return vs;
   if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
   *di = device_info(nullptr);
   if (!*di || (*di)->err != cudaSuccess) return FA_ERR_CUDA;
@@ -208,7 +248,10 @@ fa_status_t bwd_setup(fa::BwdParams* p, DeviceInfo** di, int B, int H, int N, in
   p->B = B;
   p->H = H;
   p->N = N;
-  p->causal = causal ? 1 : 0;
+  p->H_kv = var.H_kv;
+  p->wl = var.wl;
+  p->wr = var.wr;
+  p->causal = var.pair ? 1 : 0;
   p->scale = scale;
   p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p->status = (*di)->status;
@@ -227,8 +270,9 @@ fa_status_t bwd_main_impl(fa::BwdParams& p, const DeviceInfo* di, const void* q,
   // steps with dQ^T in head-dimension rows (fa_bwd_dt.cu).
   const bool dt = d != 64;
   const int qrows = dt ? 64 : 128;
-  if (!make_map(&p.tq, q, d, p.N, BH, qrows) || !make_map(&p.tk, k, d, p.N, BH) ||
-      !make_map(&p.tv, v, d, p.N, BH) || !make_map(&p.tdo, dO, d, p.N, BH, qrows))
+  const int BHkv = p.B * p.H_kv;
+  if (!make_map(&p.tq, q, d, p.N, BH, qrows) || !make_map(&p.tk, k, d, p.N, BHkv) ||
+      !make_map(&p.tv, v, d, p.N, BHkv) || !make_map(&p.tdo, dO, d, p.N, BH, qrows))
     return FA_ERR_CUDA;
   if (dt && !make_acc_map(&p.tdq, p.dq_acc, d, p.Npad, BH)) return FA_ERR_CUDA;
   p.v = v;
@@ -254,7 +298,7 @@ fa_status_t fa_bwd_prep(const void* o, const void* dO, const float* lse, int B, 
     return FA_ERR_INVALID_ARG;
   fa::BwdParams p;
   DeviceInfo* di = nullptr;
-  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, 1.f, 0, nullptr, workspace,
+  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, 1.f, 0, nullptr, nullptr, workspace,
                                    workspace_bytes);
   if (st != FA_OK) return st;
   p.o = o;
@@ -273,8 +317,8 @@ fa_status_t fa_bwd_dkdv(const void* q, const void* k, const void* v, const void*
     return FA_ERR_INVALID_ARG;
   fa::BwdParams p;
   DeviceInfo* di = nullptr;
-  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, causal, kv_len, workspace,
-                                   workspace_bytes);
+  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, causal, kv_len, nullptr,
+                                   workspace, workspace_bytes);
   if (st != FA_OK) return st;
   p.dk = dk;
   p.dv = dv;
@@ -286,7 +330,7 @@ fa_status_t fa_bwd_dq(void* dq, int B, int H, int N, int d, float scale, void* w
   if (!dq || !aligned16(dq)) return FA_ERR_INVALID_ARG;
   fa::BwdParams p;
   DeviceInfo* di = nullptr;
-  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, 0, nullptr, workspace,
+  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, 0, nullptr, nullptr, workspace,
                                    workspace_bytes);
   if (st != FA_OK) return st;
   p.dq = dq;
@@ -297,6 +341,15 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
                    const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                    float scale, int causal, const int* kv_len, void* workspace,
                    size_t workspace_bytes, void* stream) {
+  return fa_bwd_v(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, kv_len, nullptr,
+                  workspace, workspace_bytes, stream);
+}
+
+fa_status_t fa_bwd_v(const void* q, const void* k, const void* v, const void* o,
+                     const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                     int H, int N, int d, float scale, int causal, const int* kv_len,
+                     const fa_variant_t* variant, void* workspace, size_t workspace_bytes,
+                     void* stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) || !aligned16(dq) || !aligned16(dk) ||
@@ -304,8 +357,8 @@ fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o, c
     return FA_ERR_INVALID_ARG;
   fa::BwdParams p;
   DeviceInfo* di = nullptr;
-  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, causal, kv_len, workspace,
-                                   workspace_bytes);
+  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, causal, kv_len, variant,
+                                   workspace, workspace_bytes);
   if (st != FA_OK) return st;
   p.o = o;
   p.dO = dO;

@@ -38,6 +38,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_internal.h"
+#include "fa_window.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -101,9 +102,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-// Work items (bh, key block n).  Causal: key block n meets query blocks
-// n..T-1, so items n and T-1-n are paired (longest first) and every unit
-// costs T+1 steps.  Non-causal: one item per unit, bh-major.
+// Work items (K/V head kvbh, key block n); an item's steps run over the
+// query heads of kvbh's group and, for each, the query blocks the key block
+// is visible to.  Plain causal: key block n meets query blocks n..T-1, so
+// items n and T-1-n are paired (longest first) and every unit costs T+1
+// steps per query head.  Otherwise: one item per unit, head-major.
 struct BSched {
   int T, P, units, causal;
   __device__ BSched(int BH, int N, int causal_) : causal(causal_) {
@@ -128,25 +131,27 @@ struct BSched {
   }
 };
 
-__device__ __forceinline__ int bwd_len(const BwdParams& p, int bh) {
+// kv_len of K/V head kvbh's batch entry.
+__device__ __forceinline__ int bwd_len(const BwdParams& p, int kvbh) {
   int len = p.N;
   if (p.kv_len) {
-    len = __ldg(p.kv_len + bh / p.H);
+    len = __ldg(p.kv_len + kvbh / p.H_kv);
     len = len < 0 ? 0 : (len > p.N ? p.N : len);
   }
   return len;
 }
 
-// Query-block range [i0, i1) that key block n contributes to; empty when the
-// whole key block lies past the sequence.
+// Query-block range [i0, i1) that key block n is visible to (kv_len, causal
+// and window); empty when no query sees any of its keys.
 __device__ __forceinline__ void q_range(const BwdParams& p, int n, int len, int& i0, int& i1) {
-  const int T = (p.N + BM - 1) / BM;
-  if (n * BN >= len) {
+  int q_lo, q_hi;
+  visible_queries(n * BN, BN, len, p.N, p.wl, p.wr, q_lo, q_hi);
+  if (q_hi <= q_lo) {
     i0 = i1 = 0;
     return;
   }
-  i0 = p.causal ? (n * BN) / BM : 0;
-  i1 = T;
+  i0 = q_lo / BM;
+  i1 = (q_hi + BM - 1) / BM;
 }
 
 template <int D>
@@ -191,8 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-  const int BH = p.B * p.H;
-  const BSched sched(BH, p.N, p.causal);
+  const BSched sched(p.B * p.H_kv, p.N, p.causal);
+  const int G = p.H / p.H_kv;                     // query heads per K/V head
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -205,9 +210,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
         for (int kt = 0; ok && kt < sched.nitems(u); ++kt) {
-          int bh, n, i0, i1;
-          sched.item(u, kt, bh, n);
-          q_range(p, n, bwd_len(p, bh), i0, i1);
+          int kvbh, n, i0, i1;
+          sched.item(u, kt, kvbh, n);
+          q_range(p, n, bwd_len(p, kvbh), i0, i1);
           if (i0 >= i1) continue;
           if (!mbar_wait(&sm.kv_empty, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
             record_failure(p.status, abort, kSiteProdKV);
@@ -217,11 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           mbar_arrive_expect_tx(&sm.kv_full, 2 * C::TILE_BYTES);
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c) {
-            tma_load_3d(sm.k + c * CHUNK, &p.tk, &sm.kv_full, 64 * c, n * BN, bh);
-            tma_load_3d(sm.v + c * CHUNK, &p.tv, &sm.kv_full, 64 * c, n * BN, bh);
+            tma_load_3d(sm.k + c * CHUNK, &p.tk, &sm.kv_full, 64 * c, n * BN, kvbh);
+            tma_load_3d(sm.v + c * CHUNK, &p.tv, &sm.kv_full, 64 * c, n * BN, kvbh);
           }
           ++w_it;
-          for (int i = i0; i < i1; ++i) {
+          const int ni = i1 - i0;
+          for (int s = 0; s < ni * G; ++s) {
+            const int i = i0 + s % ni;
+            const int bh = q_head_of(kvbh, s / ni, p.H, p.H_kv);
             const int st = g % kStages;
             if (!mbar_wait(&sm.q_empty[st], ((g / kStages) & 1) ^ 1, abort, kWaitTimeoutNs)) {
               record_failure(p.status, abort, kSiteProdQ);
@@ -267,18 +275,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
         for (int kt = 0; ok && kt < sched.nitems(u); ++kt) {
-          int bh, n, i0, i1;
-          sched.item(u, kt, bh, n);
-          q_range(p, n, bwd_len(p, bh), i0, i1);
+          int kvbh, n, i0, i1;
+          sched.item(u, kt, kvbh, n);
+          q_range(p, n, bwd_len(p, kvbh), i0, i1);
           if (i0 >= i1) continue;
           if (!mbar_wait_warp(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
             issuer_fail(p.status, abort, lane, kSiteMmaKV);
             ok = false;
             break;
           }
-          for (int i = i0; i < i1; ++i) {
+          const int nsteps = (i1 - i0) * G;
+          for (int s = 0; s < nsteps; ++s) {
             const int st = g % kStages;
-            const bool first = (i == i0);
+            const bool first = (s == 0);
             if (!mbar_wait_warp(&sm.q_full[st], (g / kStages) & 1, abort, kWaitTimeoutNs)) {
               issuer_fail(p.status, abort, lane, kSiteMmaQ);
               ok = false;
@@ -348,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
               mma_bf16_ss_w(tmem + C::TM_DQ, dDS + ((kk * 2048) >> 4), dKmn + ((kk * 2048) >> 4),
                           kIdescDq, kk > 0 ? 1u : 0u);
             mma_commit_w(&sm.dq_full);
-            if (i == i1 - 1) {
+            if (s == nsteps - 1) {
               mma_commit_w(&sm.acc_full);
               mma_commit_w(&sm.kv_empty);
             }
@@ -374,12 +383,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     bool ok = true;
     for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
       for (int kt = 0; ok && kt < sched.nitems(u); ++kt) {
-        int bh, n, i0, i1;
-        sched.item(u, kt, bh, n);
-        const int len = bwd_len(p, bh);
+        int kvbh, n, i0, i1;
+        sched.item(u, kt, kvbh, n);
+        const int len = bwd_len(p, kvbh);
         q_range(p, n, len, i0, i1);
         const int key = n * BN + r;
-        const size_t key_off = static_cast<size_t>(bh) * p.N + key;
+        const size_t key_off = static_cast<size_t>(kvbh) * p.N + key;
         if (i0 >= i1) {
           // key block entirely past the sequence: zero gradients
           if (key < p.N) {
@@ -393,7 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           }
           continue;
         }
-        for (int i = i0; i < i1; ++i) {
+        const int ni = i1 - i0;
+        for (int s = 0; s < ni * G; ++s) {
+          const int i = i0 + s % ni;
+          const int bh = q_head_of(kvbh, s / ni, p.H, p.H_kv);
           const int st = g % kStages;
           // ---- P^T = exp2(S^T * c - L2), masked
           if (!warp_wait(&sm.s_full, g & 1, abort)) {
@@ -404,10 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           tc_fence_after_sync();
           const int q0 = i * BM;
           const bool need_mask = (n * BN + BN > len) || (q0 + BM > p.N) ||
-                                 (p.causal && n * BN + BN - 1 > q0);
-          // mask for column c (query q0+c): key past len, or key > query
-          const int lim_pad = (key < len) ? BM : -1;                 // all masked when key >= len
-          const int lim_causal = p.causal ? key - q0 : -BM - 1;      // c < lim_causal masked
+                                 (n * BN + BN - 1 > q0 + p.wr) || (n * BN < q0 + BM - 1 - p.wl);
+          // mask for column c (query q0+c): key past len, or the key outside
+          // the query's window [q - wl, q + wr]
+          const int lim_pad = (key < len) ? BM : -1;    // all masked when key >= len
+          const int lim_lo = key - p.wr - q0;           // c < lim_lo masked (key > q + wr)
+          const int lim_hi = key + p.wl - q0;           // c > lim_hi masked (key < q - wl)
           float pr[BM];
 #pragma unroll
           for (int c4 = 0; c4 < BM / 32; ++c4) {
@@ -424,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
               for (int e = 0; e < 4; ++e) {
                 const int c = 32 * c4 + 4 * t + e;
                 float pv = ex2_approx(fmaf(__uint_as_float(sr[4 * t + e]), c2, -lv[e]));
-                if (need_mask && (c >= lim_pad || c < lim_causal)) pv = 0.f;
+                if (need_mask && (c >= lim_pad || c < lim_lo || c > lim_hi)) pv = 0.f;
                 pr[c] = pv;
               }
             }
@@ -665,8 +679,8 @@ cudaError_t launch_main(const BwdParams& p, int num_sms, int max_smem, cudaStrea
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int T = (p.N + BN - 1) / BN;
-  const long long units = p.causal ? static_cast<long long>(p.B) * p.H * ((T + 1) / 2)
-                                   : static_cast<long long>(p.B) * p.H * T;
+  const long long units = p.causal ? static_cast<long long>(p.B) * p.H_kv * ((T + 1) / 2)
+                                   : static_cast<long long>(p.B) * p.H_kv * T;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   bwd_main_kernel<D><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();

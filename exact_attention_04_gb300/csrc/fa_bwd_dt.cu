@@ -1,8 +1,9 @@
 // Backward main kernel for head dimensions 128 and 256 ("dQ transposed").
 //
-// Work item: (bh, block of 128 keys, half h of the head dimension).  The CTA
-// keeps K and V of its key block in shared memory and streams the query
-// blocks of 64 rows (Q_i, dO_i, and the per-row statistics) through a ring.
+// Work item: (K/V head, block of 128 keys, half h of the head dimension).
+// The CTA keeps K and V of its key block on chip and streams the query blocks
+// of 64 rows (Q_i, dO_i, and the per-row statistics) of every query head that
+// shares the K/V head through a ring, so dK and dV sum over the group.
 // Per query block, on the tensor core (M = 128 everywhere):
 //   S^T   = K Q_i^T            (128 keys x 64 queries, contraction over all of d)
 //   dP^T  = V dO_i^T
@@ -45,6 +46,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_internal.h"
+#include "fa_window.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -147,8 +149,10 @@ __device__ __forceinline__ void issuer_fail(int* status, volatile int* abort, in
   if (lane == 0) record_failure(status, abort, site);
 }
 
-// Units are (bh, key-block pair or key block, half).  Causal: key block n
-// meets query blocks from its diagonal on, so blocks p and T-1-p are paired,
+// Units are (K/V head kvbh, key-block pair or key block, half); a work item
+// (one key block) steps over the query heads of kvbh's group and, for each,
+// the query blocks its keys are visible to.  Plain causal: key block n meets
+// query blocks from its diagonal on, so blocks p and T-1-p are paired,
 // longest first.  The halves of one key block are adjacent units so they run
 // at the same time and share K, V, Q, dO in L2.
 struct DtSched {
@@ -175,24 +179,27 @@ struct DtSched {
   }
 };
 
-__device__ __forceinline__ int dt_len(const BwdParams& p, int bh) {
+// kv_len of K/V head kvbh's batch entry.
+__device__ __forceinline__ int dt_len(const BwdParams& p, int kvbh) {
   int len = p.N;
   if (p.kv_len) {
-    len = __ldg(p.kv_len + bh / p.H);
+    len = __ldg(p.kv_len + kvbh / p.H_kv);
     len = len < 0 ? 0 : (len > p.N ? p.N : len);
   }
   return len;
 }
 
-// Query-step range [i0, i1) (blocks of 64) for key block n; empty when the
-// key block lies past the sequence.
+// Query-step range [i0, i1) (blocks of 64) that key block n is visible to
+// (kv_len, causal and window); empty when no query sees any of its keys.
 __device__ __forceinline__ void dt_range(const BwdParams& p, int n, int len, int& i0, int& i1) {
-  if (n * BK >= len) {
+  int q_lo, q_hi;
+  visible_queries(n * BK, BK, len, p.N, p.wl, p.wr, q_lo, q_hi);
+  if (q_hi <= q_lo) {
     i0 = i1 = 0;
     return;
   }
-  i0 = p.causal ? (n * BK) / BQ : 0;
-  i1 = (p.N + BQ - 1) / BQ;
+  i0 = q_lo / BQ;
+  i1 = (q_hi + BQ - 1) / BQ;
 }
 
 template <int D>
@@ -246,8 +253,8 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-  const int BH = p.B * p.H;
-  const DtSched sched(BH, p.N, p.causal, C::NSPLIT);
+  const DtSched sched(p.B * p.H_kv, p.N, p.causal, C::NSPLIT);
+  const int G = p.H / p.H_kv;                     // query heads per K/V head
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -259,12 +266,12 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
       uint32_t w_it = 0, g = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        int bh, pp, h;
-        sched.decode(u, bh, pp, h);
+        int kvbh, pp, h;
+        sched.decode(u, kvbh, pp, h);
         for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
           const int n = sched.block(pp, kt);
           int i0, i1;
-          dt_range(p, n, dt_len(p, bh), i0, i1);
+          dt_range(p, n, dt_len(p, kvbh), i0, i1);
           if (i0 >= i1) continue;
           if (!mbar_wait(&sm.kv_empty, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
             record_failure(p.status, abort, kSiteProdKV);
@@ -274,12 +281,15 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
           mbar_arrive_expect_tx(&sm.kv_full, (C::V_TMEM ? 1 : 2) * C::KV_BYTES);
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c) {
-            tma_load_3d(sm.k + c * KCH, &p.tk, &sm.kv_full, 64 * c, n * BK, bh);
+            tma_load_3d(sm.k + c * KCH, &p.tk, &sm.kv_full, 64 * c, n * BK, kvbh);
             if constexpr (!C::V_TMEM)
-              tma_load_3d(sm.v + c * KCH, &p.tv, &sm.kv_full, 64 * c, n * BK, bh);
+              tma_load_3d(sm.v + c * KCH, &p.tv, &sm.kv_full, 64 * c, n * BK, kvbh);
           }
           ++w_it;
-          for (int i = i0; i < i1; ++i) {
+          const int ni = i1 - i0;
+          for (int s = 0; s < ni * G; ++s) {
+            const int i = i0 + s % ni;
+            const int bh = q_head_of(kvbh, s / ni, p.H, p.H_kv);
             const int st = g % C::STAGES;
             if (!mbar_wait(&sm.q_empty[st], ((g / C::STAGES) & 1) ^ 1, abort, kWaitTimeoutNs)) {
               record_failure(p.status, abort, kSiteProdQ);
@@ -323,14 +333,14 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
       uint32_t w_it = 0, g = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        int bh, pp, h;
-        sched.decode(u, bh, pp, h);
+        int kvbh, pp, h;
+        sched.decode(u, kvbh, pp, h);
         for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
           const int n = sched.block(pp, kt);
           int i0, i1;
-          dt_range(p, n, dt_len(p, bh), i0, i1);
+          dt_range(p, n, dt_len(p, kvbh), i0, i1);
           if (i0 >= i1) continue;
-          const int nsteps = i1 - i0;
+          const int nsteps = (i1 - i0) * G;
           if (!mbar_wait_warp(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
             issuer_fail(p.status, abort, lane, kSiteMmaKV);
             ok = false;
@@ -419,16 +429,16 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         ok = false;
       };
       for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        int bh, pp, h;
-        sched.decode(u, bh, pp, h);
+        int kvbh, pp, h;
+        sched.decode(u, kvbh, pp, h);
         // K[:, h] as the MN-major A operand of dQ^T: 64-column chunks 2h, 2h+1
         const uint64_t dKmn = sdesc_sw128(smem_u32(sm.k) + 2 * h * KCH, KCH, 1024);
         for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
           const int n = sched.block(pp, kt);
           int i0, i1;
-          dt_range(p, n, dt_len(p, bh), i0, i1);
+          dt_range(p, n, dt_len(p, kvbh), i0, i1);
           if (i0 >= i1) continue;
-          const int nsteps = i1 - i0;
+          const int nsteps = (i1 - i0) * G;
           for (int s = 0; s < nsteps; ++s, ++g) {
             const int st = g % C::STAGES;
             const uint32_t b = g % C::NSB;          // tensor-memory S / dP buffer
@@ -500,15 +510,15 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
     uint32_t w_it = 0, g = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-      int bh, pp, h;
-      sched.decode(u, bh, pp, h);
+      int kvbh, pp, h;
+      sched.decode(u, kvbh, pp, h);
       for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
         const int n = sched.block(pp, kt);
-        const int len = dt_len(p, bh);
+        const int len = dt_len(p, kvbh);
         int i0, i1;
         dt_range(p, n, len, i0, i1);
         const int key = n * BK + r;
-        const size_t out_off = (static_cast<size_t>(bh) * p.N + key) * D + h * DH + 64 * hh;
+        const size_t out_off = (static_cast<size_t>(kvbh) * p.N + key) * D + h * DH + 64 * hh;
         if (i0 >= i1) {
           // key block entirely past the sequence: zero gradients
           if (key < p.N) {
@@ -533,7 +543,7 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
           }
           tc_fence_after_sync();
           const uint4* vrow = reinterpret_cast<const uint4*>(
-              static_cast<const __nv_bfloat16*>(p.v) + (static_cast<size_t>(bh) * p.N + key) * D +
+              static_cast<const __nv_bfloat16*>(p.v) + (static_cast<size_t>(kvbh) * p.N + key) * D +
               128 * hh);
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -553,7 +563,9 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.v_full);
         }
-        for (int i = i0; i < i1; ++i, ++g) {
+        const int ni = i1 - i0;
+        for (int s = 0; s < ni * G; ++s, ++g) {
+          const int i = i0 + s % ni;
           const int st = g % C::STAGES;
           const int q0 = i * BQ;
           const uint32_t tb = g % C::NSB;                          // tensor-memory S / dP buffer
@@ -566,10 +578,13 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
             break;
           }
           tc_fence_after_sync();
-          const bool need_mask = (n * BK + BK > len) || (p.causal && n * BK + BK - 1 > q0);
+          const bool need_mask = (n * BK + BK > len) || (n * BK + BK - 1 > q0 + p.wr) ||
+                                 (n * BK < q0 + BQ - 1 - p.wl);
           const bool row_dead = key >= len;                       // whole row masked
-          // column c (query q0 + 32*hh + c) is masked for c < lim_causal
-          const int lim_causal = p.causal ? key - q0 - 32 * hh : -BQ - 1;
+          // column c (query q = q0 + 32*hh + c) is masked outside the window
+          // [key - wr, key + wl] of queries that see this key
+          const int lim_lo = key - p.wr - q0 - 32 * hh;           // c < lim_lo masked
+          const int lim_hi = key + p.wl - q0 - 32 * hh;           // c > lim_hi masked
           float pr[32];
           const uint64_t c2x2 = f2_make(c2, c2);
           {
@@ -591,7 +606,7 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
               for (int e = 0; e < 4; ++e) {
                 const int c = 4 * t + e;
                 float pv = ex2_approx(a[e]);
-                if (need_mask && (row_dead || c < lim_causal)) pv = 0.f;
+                if (need_mask && (row_dead || c < lim_lo || c > lim_hi)) pv = 0.f;
                 pr[c] = pv;
               }
             }
@@ -709,13 +724,16 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
     uint32_t g = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-      int bh, pp, h;
-      sched.decode(u, bh, pp, h);
+      int kvbh, pp, h;
+      sched.decode(u, kvbh, pp, h);
       for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
         const int n = sched.block(pp, kt);
         int i0, i1;
-        dt_range(p, n, dt_len(p, bh), i0, i1);
-        for (int i = i0; i < i1; ++i, ++g) {
+        dt_range(p, n, dt_len(p, kvbh), i0, i1);
+        const int ni = i1 - i0;
+        for (int s = 0; s < ni * G; ++s, ++g) {
+          const int i = i0 + s % ni;
+          const int bh = q_head_of(kvbh, s / ni, p.H, p.H_kv);
           const uint32_t tb = g % C::NSB;
           if (!warp_wait(&sm.dq_full[tb], (g / C::NSB) & 1, abort)) {
             if (lane == 0) record_failure(p.status, abort, kSiteDrainDq);
@@ -807,7 +825,7 @@ cudaError_t launch(const BwdParams& p, int num_sms, int max_smem, cudaStream_t s
   if (e != cudaSuccess) return e;
   const int T = (p.N + BK - 1) / BK;
   const long long per_bh = p.causal ? (T + 1) / 2 : T;
-  const long long units = static_cast<long long>(p.B) * p.H * per_bh * DtCfg<D>::NSPLIT;
+  const long long units = static_cast<long long>(p.B) * p.H_kv * per_bh * DtCfg<D>::NSPLIT;
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
   bwd_dt_kernel<D><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();

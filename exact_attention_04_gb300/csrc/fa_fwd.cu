@@ -39,6 +39,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_internal.h"
+#include "fa_window.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -133,10 +134,14 @@ __device__ __forceinline__ int seq_len(const FwdParams& p, int bh) {
   return len;
 }
 
-__device__ __forceinline__ int kv_blocks(int m, int len, int causal) {
-  int end = len;
-  if (causal && m * BM + BM < end) end = m * BM + BM;
-  return (end + BN - 1) / BN;
+// Key blocks [jlo, jlo + count) that query tile m can see (causal, window
+// and kv_len); blocks outside are never loaded.  Returns the count.
+__device__ __forceinline__ int tile_blocks(const FwdParams& p, int m, int len, int& jlo) {
+  int k_lo, k_hi;
+  visible_keys(m * BM, BM, len, p.wl, p.wr, k_lo, k_hi);
+  jlo = k_lo / BN;
+  const int jhi = (k_hi + BN - 1) / BN;
+  return k_hi > k_lo ? jhi - jlo : 0;
 }
 
 __device__ __forceinline__ void issuer_fail(int* status, volatile int* abort, int lane, int site) {
@@ -207,8 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         for (int kt = 0; ok && kt < sched.ntiles(u); ++kt) {
           int bh, m;
           sched.tile(u, kt, bh, m);
-          const int nkv = kv_blocks(m, seq_len(p, bh), p.causal);
+          int jlo;
+          const int nkv = tile_blocks(p, m, seq_len(p, bh), jlo);
           if (nkv == 0) continue;
+          const int kvbh = kv_head_of(bh, p.H, p.H_kv);
           if (!mbar_wait(&sm.q_empty, (q_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
             record_failure(p.status, abort, kSiteProdQ);
             ok = false;
@@ -230,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             mbar_arrive_expect_tx(&sm.k_full[st], C::TILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c)
-              tma_load_3d(sm.k[st] + c * CHUNK, &p.tk, &sm.k_full[st], 64 * c, j * BN, bh);
+              tma_load_3d(sm.k[st] + c * CHUNK, &p.tk, &sm.k_full[st], 64 * c, (jlo + j) * BN, kvbh);
             ++k_it;
             if (!mbar_wait(&sm.v_empty[st], ph ^ 1, abort, kWaitTimeoutNs)) {
               record_failure(p.status, abort, kSiteProdV);
@@ -240,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             mbar_arrive_expect_tx(&sm.v_full[st], C::TILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c)
-              tma_load_3d(sm.v[st] + c * CHUNK, &p.tv, &sm.v_full[st], 64 * c, j * BN, bh);
+              tma_load_3d(sm.v[st] + c * CHUNK, &p.tv, &sm.v_full[st], 64 * c, (jlo + j) * BN, kvbh);
             ++v_it;
           }
         }
@@ -275,7 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         for (int kt = 0; ok && kt < sched.ntiles(u); ++kt) {
           int bh, m;
           sched.tile(u, kt, bh, m);
-          const int nkv = kv_blocks(m, seq_len(p, bh), p.causal);
+          int jlo;
+          const int nkv = tile_blocks(p, m, seq_len(p, bh), jlo);
           if (nkv == 0) continue;
           if (!mbar_wait_warp(&sm.q_full, q_it & 1, abort, kWaitTimeoutNs)) {
             issuer_fail(p.status, abort, lane, kSiteMmaQ);
@@ -328,7 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         for (int kt = 0; ok && kt < sched.ntiles(u); ++kt) {
           int bh, m;
           sched.tile(u, kt, bh, m);
-          const int nkv = kv_blocks(m, seq_len(p, bh), p.causal);
+          int jlo;
+          const int nkv = tile_blocks(p, m, seq_len(p, bh), jlo);
           if (nkv == 0) continue;
           for (int j = 0; j < nkv; ++j, ++g) {
             const uint32_t b = g % C::NSB;
@@ -385,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         int bh, m;
         sched.tile(u, kt, bh, m);
         const int len = seq_len(p, bh);
-        const int nkv = kv_blocks(m, len, p.causal);
+        int jlo;
+        const int nkv = tile_blocks(p, m, len, jlo);
         const int row = m * BM + row_local;
         const size_t row_off = static_cast<size_t>(bh) * p.N + row;
         if (nkv == 0) {
@@ -416,24 +426,31 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           float s[BN];
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
-          // masks: keys past the sequence (tail / padding) and above the diagonal
-          const int key0 = j * BN;
-          if (key0 + BN > len || (p.causal && key0 + BN - 1 > m * BM)) {
-            const int lim_pad = len - key0;                     // c >= lim_pad: past the sequence
-            const int lim_causal = p.causal ? row - key0 : BN;  // c > lim_causal: above the diagonal
+          // masks: keys past the sequence (tail / padding), right of the
+          // window (above the diagonal when causal) and left of the window;
+          // skipped when every key of the block is visible to every row
+          const int key0 = (jlo + j) * BN;
+          if (key0 + BN > len || key0 + BN - 1 > m * BM + p.wr ||
+              key0 < m * BM + BM - 1 - p.wl) {
+            const int lim_pad = len - key0;        // c >= lim_pad: past the sequence
+            const int lim_hi = row + p.wr - key0;  // c > lim_hi: right of the window
+            const int lim_lo = row - p.wl - key0;  // c < lim_lo: left of the window
 #pragma unroll
             for (int c = 0; c < BN; ++c)
-              if (c >= lim_pad || c > lim_causal) s[c] = -INFINITY;
+              if (c >= lim_pad || c > lim_hi || c < lim_lo) s[c] = -INFINITY;
           }
-          // row maximum: four chains of three-input max
+          // row maximum: four chains of three-input max over s[0 .. BN)
+          static_assert(BN % 8 == 0, "the max chains take 8 columns a step");
           float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-          for (int c = 4; c < BN; c += 8) {
+          for (int c = 4; c + 8 <= BN; c += 8) {
             mx0 = fmax3(mx0, s[c], s[c + 1]);
             mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
             mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
             mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
           }
+          mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
+          mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
           const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
           float alpha = 1.f;
           bool rescale = false;

@@ -22,7 +22,9 @@ struct FwdParams {
   float* lse;                  // fp32 [B, H, N]
   const int* kv_len;           // int32 [B] or nullptr
   int B, H, N;
-  int causal;
+  int H_kv;                    // K/V heads; query head h reads K/V head h / (H / H_kv)
+  int wl, wr;                  // key j visible to query i iff i - wl <= j <= i + wr (and j < len)
+  int causal;                  // causal pairing of tiles in the schedule (plain causal only)
   float scale_log2;            // scale * log2(e)
   int* status;                 // device status word
 };
@@ -42,8 +44,10 @@ struct BwdParams {
   float* dq_acc;               // fp32 workspace: [BH, Npad, d] (d = 64) or [BH, d, Npad]
   const int* kv_len;
   int B, H, N;
+  int H_kv;                    // K/V heads; query head h reads K/V head h / (H / H_kv)
+  int wl, wr;                  // key j visible to query i iff i - wl <= j <= i + wr (and j < len)
   int Npad;                    // N rounded up to a multiple of 128
-  int causal;
+  int causal;                  // causal pairing of key blocks in the schedule (plain causal only)
   float scale;
   float scale_log2;
   int* status;

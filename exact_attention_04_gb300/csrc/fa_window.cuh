@@ -1,0 +1,53 @@
+// Visibility of keys to queries, shared by the forward and backward kernels.
+//
+// Key j is visible to query i iff j < len (the batch entry's kv_len),
+// j >= i - wl and j <= i + wr.  The host folds the causal flag into wr
+// (wr = 0) and stores an unbounded side as kUnbounded, so every mask is the
+// same three comparisons.  The window is flash-attn's window_size=(left,
+// right) ("炉案与百步之外的仓库：Flash Attention 与注意力计算的工艺极限"
+// section 六; "4. FlashAttention 深度剖析" 4.8.1); blocks outside it are
+// skipped, not masked ("深入浅出 FlashAttention：快如闪电的精确注意力机制与
+// IO 感知计算" 第八部分, block-sparse skipping).
+#pragma once
+
+namespace fa {
+
+// An unbounded window side.  Query and key indices stay below 2^30, so
+// i +- kUnbounded never overflows an int.
+constexpr int kUnbounded = 1 << 30;
+
+// Key range [k_lo, k_hi) that query rows [r0, r0 + nrows) can see.
+__device__ __forceinline__ void visible_keys(int r0, int nrows, int len, int wl, int wr,
+                                             int& k_lo, int& k_hi) {
+  k_lo = r0 - wl;
+  if (k_lo < 0) k_lo = 0;
+  k_hi = r0 + nrows - 1 + wr + 1;
+  if (k_hi > len) k_hi = len;
+}
+
+// Query range [q_lo, q_hi) that keys [k0, k0 + nkeys) are visible to, among
+// N queries (empty when every key is past len).
+__device__ __forceinline__ void visible_queries(int k0, int nkeys, int len, int N, int wl,
+                                                int wr, int& q_lo, int& q_hi) {
+  if (k0 >= len) {
+    q_lo = q_hi = 0;
+    return;
+  }
+  const int k_last = (k0 + nkeys < len ? k0 + nkeys : len) - 1;
+  q_lo = k0 - wr;
+  if (q_lo < 0) q_lo = 0;
+  q_hi = k_last + wl + 1;
+  if (q_hi > N) q_hi = N;
+}
+
+// K/V head of query head (b, h) when H query heads share H_kv K/V heads.
+__device__ __forceinline__ int kv_head_of(int bh, int H, int H_kv) {
+  return (bh / H) * H_kv + (bh % H) / (H / H_kv);
+}
+
+// Query head (b, h) of member gi of K/V head kvbh's group.
+__device__ __forceinline__ int q_head_of(int kvbh, int gi, int H, int H_kv) {
+  return (kvbh / H_kv) * H + (kvbh % H_kv) * (H / H_kv) + gi;
+}
+
+}  // namespace fa

@@ -23,6 +23,12 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = ran
 _lib = None
 
 
+class FaVariant(ctypes.Structure):
+    """fa_variant_t: K/V heads and flash-attn's (left, right) window, -1 = unbounded."""
+    _fields_ = [("h_kv", ctypes.c_int), ("window_left", ctypes.c_int),
+                ("window_right", ctypes.c_int)]
+
+
 class FAError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
@@ -53,6 +59,12 @@ def load():
         lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp,
                                        vp]
         lib.fa_bwd_noalloc.restype = i
+        varp = ctypes.POINTER(FaVariant)
+        lib.fa_fwd_v.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, varp, vp]
+        lib.fa_fwd_v.restype = i
+        lib.fa_bwd_v.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, varp,
+                                 vp, sz, vp]
+        lib.fa_bwd_v.restype = i
         lib.fa_check.argtypes = [vp]
         lib.fa_check.restype = i
         lib.fa_status_string.argtypes = [i]
@@ -64,7 +76,8 @@ def load():
 
 
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_prep", "fa_bwd_dkdv",
-           "fa_bwd_dq", "fa_bwd_noalloc", "fa_check", "fa_status_string", "fa_version")
+           "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_v", "fa_bwd_v", "fa_check",
+           "fa_status_string", "fa_version")
 
 
 def fa_status_string(status: int) -> str:
@@ -204,6 +217,54 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, kv_len=
            "fa_bwd_noalloc")
 
 
+def _variant(q, k, window):
+    """fa_variant_t for K/V of k's head count and the (left, right) window."""
+    B, H, N, d = q.shape
+    if k.dim() != 4 or (k.shape[0], k.shape[2], k.shape[3]) != (B, N, d) or k.shape[1] < 1 \
+            or H % k.shape[1]:
+        raise ValueError(f"k: shape {tuple(k.shape)} does not group the {H} query heads")
+    wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    return FaVariant(int(k.shape[1]), wl, wr)
+
+
+def fa_fwd_v(q, k, v, o, lse, scale, causal=False, kv_len=None, window=None, stream=None):
+    """Calls fa_fwd_v: k, v are [B,H_kv,N,d] (H_kv divides H); window is
+    flash-attn's (left, right), -1 = unbounded."""
+    _check_qkv("q", q)
+    B, H, N, d = q.shape
+    var = _variant(q, k, window)
+    _check_qkv("k", k, k.shape)
+    _check_qkv("v", v, k.shape)
+    _check_qkv("o", o, q.shape)
+    if lse.dtype != torch.float32 or not lse.is_cuda or tuple(lse.shape) != (B, H, N) \
+            or not lse.is_contiguous():
+        raise ValueError("lse: expected a contiguous fp32 CUDA tensor [B,H,N]")
+    kv_len = _check_kv_len(kv_len, B)
+    st = load().fa_fwd_v(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(scale),
+                         int(bool(causal)), _ptr(kv_len), ctypes.byref(var), _stream_ptr(stream))
+    _raise(st, "fa_fwd_v")
+
+
+def fa_bwd_v(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, kv_len=None, window=None,
+             workspace=None, stream=None):
+    """Calls fa_bwd_v: k, v, dk, dv are [B,H_kv,N,d]; dk, dv sum over each group."""
+    _check_qkv("q", q)
+    B, H, N, d = q.shape
+    var = _variant(q, k, window)
+    for name, t in (("o", o), ("do", do), ("dq", dq)):
+        _check_qkv(name, t, q.shape)
+    for name, t in (("k", k), ("v", v), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, k.shape)
+    if lse.dtype != torch.float32 or not lse.is_cuda or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse: expected fp32 CUDA tensor [B,H,N]")
+    kv_len = _check_kv_len(kv_len, B)
+    wp, wn = _ws(workspace)
+    st = load().fa_bwd_v(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
+                         _ptr(kv_len), ctypes.byref(var), wp, wn, _stream_ptr(stream))
+    _raise(st, "fa_bwd_v")
+
+
 def fa_check(stream=None):
     """Waits for the stream; raises FAError if a kernel timed out or failed."""
     _raise(load().fa_check(_stream_ptr(stream)), "fa_check")
@@ -213,12 +274,17 @@ def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 
 
-def forward(q, k, v, scale=None, causal=False, kv_len=None, stream=None):
-    """(O, LSE) with outputs allocated by torch on q's device."""
+def forward(q, k, v, scale=None, causal=False, kv_len=None, window=None, stream=None):
+    """(O, LSE) with outputs allocated by torch on q's device.  K/V with fewer
+    heads than Q, or a window, go through fa_fwd_v."""
     B, H, N, d = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    fa_fwd(q, k, v, o, lse, default_scale(d) if scale is None else scale, causal, kv_len, stream)
+    sc = default_scale(d) if scale is None else scale
+    if window is None and k.shape == q.shape:
+        fa_fwd(q, k, v, o, lse, sc, causal, kv_len, stream)
+    else:
+        fa_fwd_v(q, k, v, o, lse, sc, causal, kv_len, window, stream)
     return o, lse
 
 
@@ -226,12 +292,17 @@ def workspace(B, H, N, d, device):
     return torch.empty(fa_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=device)
 
 
-def backward(q, k, v, o, lse, do, scale=None, causal=False, kv_len=None, ws=None, stream=None):
-    """(dQ, dK, dV) with outputs (and, if not given, the workspace) allocated by torch."""
+def backward(q, k, v, o, lse, do, scale=None, causal=False, kv_len=None, ws=None, window=None,
+             stream=None):
+    """(dQ, dK, dV) with outputs (and, if not given, the workspace) allocated by
+    torch; dK, dV are shaped like k."""
     B, H, N, d = q.shape
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
     if ws is None:
         ws = workspace(B, H, N, d, q.device)
-    fa_bwd(q, k, v, o, do, lse, dq, dk, dv, default_scale(d) if scale is None else scale,
-           causal, kv_len, ws, stream)
+    sc = default_scale(d) if scale is None else scale
+    if window is None and k.shape == q.shape:
+        fa_bwd(q, k, v, o, do, lse, dq, dk, dv, sc, causal, kv_len, ws, stream)
+    else:
+        fa_bwd_v(q, k, v, o, do, lse, dq, dk, dv, sc, causal, kv_len, window, ws, stream)
     return dq, dk, dv

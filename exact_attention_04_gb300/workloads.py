@@ -10,9 +10,10 @@ seeded as stated, then rounded to bf16; the same bf16 bytes go to the GPU
 and, widened exactly to float64, to the oracle):
 
 * Q, K, V ~ iid N(0, 1), drawn in that order from one generator seeded with
-  ``seed``; where ``qk_gain`` != 1 the fp32 Q and K are multiplied by it
-  before rounding (the large-head-dimension workload uses 3, which makes the
-  score standard deviation about 9 and stresses the max subtraction).
+  ``seed`` (Q with H heads, K and V with ``h_kv``); where ``qk_gain`` != 1 the
+  fp32 Q and K are multiplied by it before rounding (the large-head-dimension
+  workload uses 3, which makes the score standard deviation about 9 and
+  stresses the max subtraction).
 * dO ~ iid N(0, 1) from a generator seeded with ``seed + 100``.
 * key-padding lengths ~ uniform integers in [lo, hi] (inclusive) from a
   generator seeded with ``seed + 200``.
@@ -35,15 +36,38 @@ class Workload:
     backward: bool
     qk_gain: float = 1.0
     kv_len_range: tuple = None     # (lo, hi) inclusive, or None for no padding
+    h_kv: int = None               # K/V heads (grouped-query attention); None = H
+    window: tuple = None           # flash-attn (left, right), -1 = unbounded; None = no window
 
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.d)
 
+    @property
+    def kv_heads(self) -> int:
+        return self.H if self.h_kv is None else self.h_kv
+
+    def visible_pairs(self) -> float:
+        """(query, key) pairs one head computes: N^2, N^2/2 under the causal
+        mask, and with a window the exact count of keys in each row's window
+        (padding not discounted)."""
+        N = self.N
+        if self.window is None:
+            return N * N / 2 if self.causal else float(N * N)
+        wl, wr = self.window
+        total = 0
+        for i in range(N):
+            lo = 0 if wl < 0 else max(0, i - wl)
+            hi = N - 1 if wr < 0 else min(N - 1, i + wr)
+            if self.causal:
+                hi = min(hi, i)
+            total += max(0, hi - lo + 1)
+        return float(total)
+
     def fwd_flops(self) -> float:
-        """4*B*H*N^2*d, halved under the causal mask (padding not discounted)."""
-        f = 4.0 * self.B * self.H * self.N * self.N * self.d
-        return f / 2 if self.causal else f
+        """4*B*H*d per visible (query, key) pair: 4*B*H*N^2*d, halved under the
+        causal mask (padding not discounted)."""
+        return 4.0 * self.B * self.H * self.d * self.visible_pairs()
 
     def bwd_flops(self) -> float:
         """2.5 x the forward count."""
@@ -66,6 +90,13 @@ WORKLOADS = {w.name: w for w in [
              backward=True, qk_gain=3.0),
     Workload("large_head_b2_h16_n8192_d256_causal", 2, 16, 8192, 256, causal=True, seed=4,
              backward=True, qk_gain=3.0),
+    # grouped-query attention, four query heads per K/V head (the GQA note of
+    # the flash-attn API section names LLaMA 3 and Qwen)
+    Workload("gqa_b2_h32_kv8_n8192_d128_causal", 2, 32, 8192, 128, causal=True, seed=5,
+             backward=True, h_kv=8),
+    # causal sliding window of 4096 keys (Mistral, per the sliding-window note)
+    Workload("swa_b2_h32_n16384_d128_w4096_causal", 2, 32, 16384, 128, causal=True, seed=6,
+             backward=True, window=(4095, 0)),
 ]}
 
 
@@ -73,10 +104,11 @@ def make_inputs(w: Workload, with_grad_out: bool = None):
     """CPU tensors for workload ``w``: dict with q, k, v (bf16 [B,H,N,d]),
     optionally do (bf16) and kv_len (int32 [B] or None)."""
     shape = (w.B, w.H, w.N, w.d)
+    kv_shape = (w.B, w.kv_heads, w.N, w.d)
     g = torch.Generator().manual_seed(w.seed)
     q = torch.randn(shape, generator=g, dtype=torch.float32)
-    k = torch.randn(shape, generator=g, dtype=torch.float32)
-    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(kv_shape, generator=g, dtype=torch.float32)
+    v = torch.randn(kv_shape, generator=g, dtype=torch.float32)
     if w.qk_gain != 1.0:
         q.mul_(w.qk_gain)
         k.mul_(w.qk_gain)
@@ -95,7 +127,9 @@ def make_inputs(w: Workload, with_grad_out: bool = None):
     return out
 
 
-def random_case(B, H, N, d, seed, causal=False, kv_len_range=None, qk_gain=1.0, backward=True):
+def random_case(B, H, N, d, seed, causal=False, kv_len_range=None, qk_gain=1.0, backward=True,
+                h_kv=None, window=None):
     """An ad-hoc workload (edge-case tests) drawn with the same recipe."""
     return Workload(f"case_b{B}_h{H}_n{N}_d{d}", B, H, N, d, causal=causal, seed=seed,
-                    backward=backward, qk_gain=qk_gain, kv_len_range=kv_len_range)
+                    backward=backward, qk_gain=qk_gain, kv_len_range=kv_len_range, h_kv=h_kv,
+                    window=window)

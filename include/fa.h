@@ -117,6 +117,47 @@ fa_status_t fa_bwd_dq(void* dq, int B, int H, int N, int d, float scale, void* w
                       size_t workspace_bytes, void* stream);
 
 /*
+ * Attention variants: grouped K/V heads and a sliding window.
+ *
+ * h_kv: K/V heads.  K, V, dK, dV are bf16 [B, h_kv, N, d] and query head h
+ *   reads K/V head h / (H / h_kv); 1 <= h_kv <= H and H % h_kv == 0.
+ *   h_kv = H is multi-head attention, h_kv = 1 multi-query attention, values
+ *   in between grouped-query attention, as FlashAttention-2 supports them
+ *   ("注意力为什么受限于显存带宽…" section 九; "炉案与百步之外的仓库：Flash
+ *   Attention 与注意力计算的工艺极限" section 六).
+ * window_left, window_right: flash-attn's window_size=(left, right) (same
+ *   section 六; "4. FlashAttention 深度剖析" 4.8.1).  -1 leaves that side
+ *   unbounded; otherwise query i sees key j only when
+ *   i - window_left <= j <= i + window_right.  The window combines with
+ *   causal and kv_len; a row may then see no key at all (O = 0, LSE = -inf).
+ *   Key blocks outside every row's window are skipped, not masked
+ *   ("深入浅出 FlashAttention：快如闪电的精确注意力机制与 IO 感知计算"
+ *   第八部分).
+ * A NULL variant pointer means {H, -1, -1}.
+ */
+typedef struct fa_variant {
+  int h_kv;
+  int window_left;
+  int window_right;
+} fa_variant_t;
+
+/*
+ * fa_fwd and fa_bwd for a variant; every other argument is as in fa_fwd and
+ * fa_bwd, with K, V, dK, dV shaped [B, h_kv, N, d] and the workspace of
+ * fa_bwd_workspace_bytes(B, H, N, d).  dK and dV are the sums over each
+ * group's query heads.  FA_ERR_INVALID_ARG also for h_kv not dividing H or a
+ * window side below -1.  lse must come from fa_fwd_v with the same variant.
+ */
+fa_status_t fa_fwd_v(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int H, int N, int d, float scale, int causal,
+                     const int* kv_len, const fa_variant_t* variant, void* stream);
+fa_status_t fa_bwd_v(const void* q, const void* k, const void* v, const void* o,
+                     const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                     int B, int H, int N, int d, float scale, int causal, const int* kv_len,
+                     const fa_variant_t* variant, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/*
  * fa_bwd_noalloc: the backward pass for callers that cannot allocate device
  * memory.  Same arguments, results and errors as fa_bwd, minus the workspace:
  * the scratch fa_bwd needs (fa_bwd_workspace_bytes(B,H,N,d) bytes) comes from

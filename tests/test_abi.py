@@ -103,3 +103,33 @@ def test_binding_rejects_cpu_tensors(lib):
     lse = torch.zeros(1, 1, 128)
     with pytest.raises(ValueError):
         fa.fa_fwd(q, q, q, q, lse, 0.125)
+
+
+def test_variant_argument_errors(lib):
+    """fa_fwd_v / fa_bwd_v reject a K/V head count that does not divide H and
+    window sides below -1 before touching the device."""
+    ok = 0x1000
+
+    def fwd_v(h_kv, wl=-1, wr=-1, H=4):
+        var = fa.FaVariant(h_kv, wl, wr)
+        return lib.fa_fwd_v(P(ok), P(ok), P(ok), P(ok), P(ok), 1, H, 128, 64, 0.125, 0, None,
+                            ctypes.byref(var), None)
+
+    def bwd_v(h_kv, wl=-1, wr=-1, H=4):
+        var = fa.FaVariant(h_kv, wl, wr)
+        return lib.fa_bwd_v(P(ok), P(ok), P(ok), P(ok), P(ok), P(ok), P(ok), P(ok), P(ok), 1, H,
+                            128, 64, 0.125, 0, None, ctypes.byref(var), P(ok), 1 << 40, None)
+    for call in (fwd_v, bwd_v):
+        assert call(3) == fa.FA_ERR_INVALID_ARG          # 3 does not divide 4
+        assert call(0) == fa.FA_ERR_INVALID_ARG
+        assert call(8) == fa.FA_ERR_INVALID_ARG          # more K/V heads than query heads
+        assert call(2, wl=-2) == fa.FA_ERR_INVALID_ARG
+        assert call(2, wr=-5) == fa.FA_ERR_INVALID_ARG
+
+
+def test_variant_binding_checks_shapes(lib):
+    import torch
+    q = torch.zeros(1, 4, 128, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 3, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa._variant(q, k, None)
