@@ -193,19 +193,20 @@ class Runner:
         self.backward = w.backward
         if self.backward:
             self.do = inp["do"].to(d)
-            self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+            self.dq = torch.empty_like(self.q)
+            self.dk, self.dv = torch.empty_like(self.k), torch.empty_like(self.k)
             self.ws = fa.workspace(w.B, w.H, w.N, w.d, d)
 
     def fwd(self):
-        self.fa.fa_fwd(self.q, self.k, self.v, self.o, self.lse, self.w.scale, self.w.causal,
-                       self.kv)
+        self.fa.fa_fwd_v(self.q, self.k, self.v, self.o, self.lse, self.w.scale, self.w.causal,
+                         self.kv, self.w.window)
 
     def prep(self):
         self.fa.fa_bwd_prep(self.o, self.do, self.lse, self.ws)
 
     def main(self):
-        self.fa.fa_bwd_dkdv(self.q, self.k, self.v, self.do, self.dk, self.dv, self.w.scale,
-                            self.w.causal, self.kv, self.ws)
+        self.fa.fa_bwd_dkdv_v(self.q, self.k, self.v, self.do, self.dk, self.dv, self.w.scale,
+                              self.w.causal, self.kv, self.w.window, self.ws)
 
     def post(self):
         self.fa.fa_bwd_dq(self.dq, self.w.scale, self.ws)
@@ -382,7 +383,7 @@ def run_sweep(fa, peaks):
     for name, w in WORKLOADS.items():
         if name == HEADLINE:
             continue
-        key = (w.B, w.H, w.N, w.d, w.seed, w.qk_gain, w.kv_len_range, w.backward)
+        key = (w.B, w.H, w.kv_heads, w.N, w.d, w.seed, w.qk_gain, w.kv_len_range, w.backward)
         if key not in cache:
             cache.clear()
             cache[key] = make_inputs(w)
@@ -395,9 +396,11 @@ def run_sweep(fa, peaks):
         per_phase, _ = time_steps(r, steps, flush=lambda: flush_l2(flush_buf))
         fa.fa_check()
         fwd_ms = per_phase["fa_fwd_kernel"]
-        rowb = w.B * w.H * w.N
-        fwd_bytes = 8 * rowb * w.d + 4 * rowb
+        rowb = w.B * w.H * w.N               # query rows
+        kvrowb = w.B * w.kv_heads * w.N      # key rows
+        fwd_bytes = 4 * rowb * w.d + 4 * kvrowb * w.d + 4 * rowb     # Q, O; K, V; LSE
         entry = {"workload": name, "N": w.N, "d": w.d, "causal": w.causal,
+                 "h_kv": w.kv_heads, "window": list(w.window) if w.window else None,
                  "fwd_ms": round(fwd_ms, 4),
                  "fwd_tflops": round(w.fwd_flops() / (fwd_ms * 1e-3) / 1e12, 2),
                  "fwd_frac_of_peak": round(w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
@@ -405,7 +408,7 @@ def run_sweep(fa, peaks):
                  "fwd_gbs": round(fwd_bytes / (fwd_ms * 1e-3) / 1e9, 1)}
         if r.backward:
             bwd_ms = sum(v for k, v in per_phase.items() if k != "fa_fwd_kernel")
-            bwd_bytes = 16 * rowb * w.d + 12 * rowb
+            bwd_bytes = 8 * rowb * w.d + 8 * kvrowb * w.d + 12 * rowb   # Q,O,dO,dQ; K,V,dK,dV
             entry.update({"bwd_ms": round(bwd_ms, 4),
                           "bwd_tflops": round(w.bwd_flops() / (bwd_ms * 1e-3) / 1e12, 2),
                           "bwd_frac_of_peak": round(w.bwd_flops() / (bwd_ms * 1e-3) / 1e12

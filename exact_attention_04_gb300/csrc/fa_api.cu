@@ -311,13 +311,21 @@ fa_status_t fa_bwd_dkdv(const void* q, const void* k, const void* v, const void*
                         void* dv, int B, int H, int N, int d, float scale, int causal,
                         const int* kv_len, void* workspace, size_t workspace_bytes,
                         void* stream) {
+  return fa_bwd_dkdv_v(q, k, v, dO, dk, dv, B, H, N, d, scale, causal, kv_len, nullptr,
+                       workspace, workspace_bytes, stream);
+}
+
+fa_status_t fa_bwd_dkdv_v(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                          void* dv, int B, int H, int N, int d, float scale, int causal,
+                          const int* kv_len, const fa_variant_t* variant, void* workspace,
+                          size_t workspace_bytes, void* stream) {
   if (!q || !k || !v || !dO || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dk) ||
       !aligned16(dv))
     return FA_ERR_INVALID_ARG;
   fa::BwdParams p;
   DeviceInfo* di = nullptr;
-  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, causal, kv_len, nullptr,
+  const fa_status_t st = bwd_setup(&p, &di, B, H, N, d, scale, causal, kv_len, variant,
                                    workspace, workspace_bytes);
   if (st != FA_OK) return st;
   p.dk = dk;

@@ -226,10 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             tma_load_3d(sm.v + c * CHUNK, &p.tv, &sm.kv_full, 64 * c, n * BN, kvbh);
           }
           ++w_it;
-          const int ni = i1 - i0;
-          for (int s = 0; s < ni * G; ++s) {
-            const int i = i0 + s % ni;
-            const int bh = q_head_of(kvbh, s / ni, p.H, p.H_kv);
+          StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv));
+          for (int s = 0; s < (i1 - i0) * G; ++s, wk.next()) {
+            const int i = wk.i;
+            const int bh = wk.bh;
             const int st = g % kStages;
             if (!mbar_wait(&sm.q_empty[st], ((g / kStages) & 1) ^ 1, abort, kWaitTimeoutNs)) {
               record_failure(p.status, abort, kSiteProdQ);
@@ -402,10 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           }
           continue;
         }
-        const int ni = i1 - i0;
-        for (int s = 0; s < ni * G; ++s) {
-          const int i = i0 + s % ni;
-          const int bh = q_head_of(kvbh, s / ni, p.H, p.H_kv);
+        StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv));
+        for (int s = 0; s < (i1 - i0) * G; ++s, wk.next()) {
+          const int i = wk.i;
+          const int bh = wk.bh;
           const int st = g % kStages;
           // ---- P^T = exp2(S^T * c - L2), masked
           if (!warp_wait(&sm.s_full, g & 1, abort)) {
@@ -417,11 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           const int q0 = i * BM;
           const bool need_mask = (n * BN + BN > len) || (q0 + BM > p.N) ||
                                  (n * BN + BN - 1 > q0 + p.wr) || (n * BN < q0 + BM - 1 - p.wl);
-          // mask for column c (query q0+c): key past len, or the key outside
-          // the query's window [q - wl, q + wr]
-          const int lim_pad = (key < len) ? BM : -1;    // all masked when key >= len
-          const int lim_lo = key - p.wr - q0;           // c < lim_lo masked (key > q + wr)
-          const int lim_hi = key + p.wl - q0;           // c > lim_hi masked (key < q - wl)
+          // visible columns c (query q0 + c) of this key row: [c_lo, c_hi],
+          // the queries whose window [q - wl, q + wr] holds the key; none
+          // when the key is past len
+          const int c_lo = key - p.wr - q0;
+          const int c_hi = (key < len) ? key + p.wl - q0 : -1;
           float pr[BM];
 #pragma unroll
           for (int c4 = 0; c4 < BM / 32; ++c4) {
@@ -435,12 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
               const float4 l4 = l2v[t];
               const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int c = 32 * c4 + 4 * t + e;
-                float pv = ex2_approx(fmaf(__uint_as_float(sr[4 * t + e]), c2, -lv[e]));
-                if (need_mask && (c >= lim_pad || c < lim_lo || c > lim_hi)) pv = 0.f;
-                pr[c] = pv;
-              }
+              for (int e = 0; e < 4; ++e)
+                pr[32 * c4 + 4 * t + e] = ex2_approx(fmaf(__uint_as_float(sr[4 * t + e]), c2, -lv[e]));
+            }
+            if (need_mask) {      // diagonal and boundary steps only
+#pragma unroll
+              for (int c = 32 * c4; c < 32 * c4 + 32; ++c)
+                if (c < c_lo || c > c_hi) pr[c] = 0.f;
             }
             uint32_t pk[16];
 #pragma unroll

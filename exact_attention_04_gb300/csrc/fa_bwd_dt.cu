@@ -286,10 +286,10 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
               tma_load_3d(sm.v + c * KCH, &p.tv, &sm.kv_full, 64 * c, n * BK, kvbh);
           }
           ++w_it;
-          const int ni = i1 - i0;
-          for (int s = 0; s < ni * G; ++s) {
-            const int i = i0 + s % ni;
-            const int bh = q_head_of(kvbh, s / ni, p.H, p.H_kv);
+          StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv));
+          for (int s = 0; s < (i1 - i0) * G; ++s, wk.next()) {
+            const int i = wk.i;
+            const int bh = wk.bh;
             const int st = g % C::STAGES;
             if (!mbar_wait(&sm.q_empty[st], ((g / C::STAGES) & 1) ^ 1, abort, kWaitTimeoutNs)) {
               record_failure(p.status, abort, kSiteProdQ);
@@ -563,9 +563,9 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.v_full);
         }
-        const int ni = i1 - i0;
-        for (int s = 0; s < ni * G; ++s, ++g) {
-          const int i = i0 + s % ni;
+        StepWalk wk(i0, i1, 0);
+        for (int s = 0; s < (i1 - i0) * G; ++s, ++g, wk.next()) {
+          const int i = wk.i;
           const int st = g % C::STAGES;
           const int q0 = i * BQ;
           const uint32_t tb = g % C::NSB;                          // tensor-memory S / dP buffer
@@ -580,11 +580,11 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
           tc_fence_after_sync();
           const bool need_mask = (n * BK + BK > len) || (n * BK + BK - 1 > q0 + p.wr) ||
                                  (n * BK < q0 + BQ - 1 - p.wl);
-          const bool row_dead = key >= len;                       // whole row masked
-          // column c (query q = q0 + 32*hh + c) is masked outside the window
-          // [key - wr, key + wl] of queries that see this key
-          const int lim_lo = key - p.wr - q0 - 32 * hh;           // c < lim_lo masked
-          const int lim_hi = key + p.wl - q0 - 32 * hh;           // c > lim_hi masked
+          // visible columns c (query q = q0 + 32*hh + c) of this key row:
+          // [c_lo, c_hi], the queries whose window [q - wl, q + wr] holds the
+          // key; none when the key is past len
+          const int c_lo = key - p.wr - q0 - 32 * hh;
+          const int c_hi = (key < len) ? key + p.wl - q0 - 32 * hh : -1;
           float pr[32];
           const uint64_t c2x2 = f2_make(c2, c2);
           {
@@ -603,12 +603,12 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
                               c2x2, f2_make(-l4.z, -l4.w)),
                        a[2], a[3]);
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int c = 4 * t + e;
-                float pv = ex2_approx(a[e]);
-                if (need_mask && (row_dead || c < lim_lo || c > lim_hi)) pv = 0.f;
-                pr[c] = pv;
-              }
+              for (int e = 0; e < 4; ++e) pr[4 * t + e] = ex2_approx(a[e]);
+            }
+            if (need_mask) {      // diagonal and boundary steps only
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                if (c < c_lo || c > c_hi) pr[c] = 0.f;
             }
             uint32_t pk[16];
 #pragma unroll
@@ -730,10 +730,10 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         const int n = sched.block(pp, kt);
         int i0, i1;
         dt_range(p, n, dt_len(p, kvbh), i0, i1);
-        const int ni = i1 - i0;
-        for (int s = 0; s < ni * G; ++s, ++g) {
-          const int i = i0 + s % ni;
-          const int bh = q_head_of(kvbh, s / ni, p.H, p.H_kv);
+        StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv));
+        for (int s = 0; s < (i1 - i0) * G; ++s, ++g, wk.next()) {
+          const int i = wk.i;
+          const int bh = wk.bh;
           const uint32_t tb = g % C::NSB;
           if (!warp_wait(&sm.dq_full[tb], (g / C::NSB) & 1, abort)) {
             if (lane == 0) record_failure(p.status, abort, kSiteDrainDq);

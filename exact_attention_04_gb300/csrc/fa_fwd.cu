@@ -432,12 +432,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           const int key0 = (jlo + j) * BN;
           if (key0 + BN > len || key0 + BN - 1 > m * BM + p.wr ||
               key0 < m * BM + BM - 1 - p.wl) {
-            const int lim_pad = len - key0;        // c >= lim_pad: past the sequence
-            const int lim_hi = row + p.wr - key0;  // c > lim_hi: right of the window
-            const int lim_lo = row - p.wl - key0;  // c < lim_lo: left of the window
+            // visible columns [c_lo, c_hi]: before the sequence end and
+            // inside the window [row - wl, row + wr]
+            const int c_hi = min(len - key0 - 1, row + p.wr - key0);
+            const int c_lo = row - p.wl - key0;
 #pragma unroll
             for (int c = 0; c < BN; ++c)
-              if (c >= lim_pad || c > lim_hi || c < lim_lo) s[c] = -INFINITY;
+              if (c > c_hi || c < c_lo) s[c] = -INFINITY;
           }
           // row maximum: four chains of three-input max over s[0 .. BN)
           static_assert(BN % 8 == 0, "the max chains take 8 columns a step");

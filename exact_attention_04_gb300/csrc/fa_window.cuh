@@ -40,14 +40,32 @@ __device__ __forceinline__ void visible_queries(int k0, int nkeys, int len, int 
   if (q_hi > N) q_hi = N;
 }
 
-// K/V head of query head (b, h) when H query heads share H_kv K/V heads.
+// K/V head of query head (b, h) when H query heads share H_kv K/V heads
+// (the same index when they do not share).
 __device__ __forceinline__ int kv_head_of(int bh, int H, int H_kv) {
+  if (H_kv == H) return bh;
   return (bh / H) * H_kv + (bh % H) / (H / H_kv);
 }
 
 // Query head (b, h) of member gi of K/V head kvbh's group.
 __device__ __forceinline__ int q_head_of(int kvbh, int gi, int H, int H_kv) {
+  if (H_kv == H) return kvbh + gi;
   return (kvbh / H_kv) * H + (kvbh % H_kv) * (H / H_kv) + gi;
 }
+
+// The steps of a backward work item in order: query blocks [i0, i1) of the
+// group's first query head, then of the next, ...  Kept as counters so that a
+// step costs no integer division.
+struct StepWalk {
+  int i, bh, i0, i1;
+  __device__ __forceinline__ StepWalk(int i0_, int i1_, int bh0)
+      : i(i0_), bh(bh0), i0(i0_), i1(i1_) {}
+  __device__ __forceinline__ void next() {
+    if (++i == i1) {
+      i = i0;
+      ++bh;
+    }
+  }
+};
 
 }  // namespace fa

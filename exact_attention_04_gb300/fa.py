@@ -65,6 +65,9 @@ def load():
         lib.fa_bwd_v.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, varp,
                                  vp, sz, vp]
         lib.fa_bwd_v.restype = i
+        lib.fa_bwd_dkdv_v.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, varp, vp, sz,
+                                      vp]
+        lib.fa_bwd_dkdv_v.restype = i
         lib.fa_check.argtypes = [vp]
         lib.fa_check.restype = i
         lib.fa_status_string.argtypes = [i]
@@ -76,7 +79,7 @@ def load():
 
 
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_prep", "fa_bwd_dkdv",
-           "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_v", "fa_bwd_v", "fa_check",
+           "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_v", "fa_bwd_v", "fa_bwd_dkdv_v", "fa_check",
            "fa_status_string", "fa_version")
 
 
@@ -263,6 +266,22 @@ def fa_bwd_v(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, kv_len=None, 
                          _ptr(dk), _ptr(dv), B, H, N, d, float(scale), int(bool(causal)),
                          _ptr(kv_len), ctypes.byref(var), wp, wn, _stream_ptr(stream))
     _raise(st, "fa_bwd_v")
+
+
+def fa_bwd_dkdv_v(q, k, v, do, dk, dv, scale, causal=False, kv_len=None, window=None,
+                  workspace=None, stream=None):
+    """Second backward phase for a variant: k, v, dk, dv are [B,H_kv,N,d]."""
+    _check_qkv("q", q)
+    B, H, N, d = q.shape
+    var = _variant(q, k, window)
+    _check_qkv("do", do, q.shape)
+    for name, t in (("k", k), ("v", v), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, k.shape)
+    kv_len = _check_kv_len(kv_len, B)
+    wp, wn = _ws(workspace)
+    _raise(load().fa_bwd_dkdv_v(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dk), _ptr(dv), B, H,
+                                N, d, float(scale), int(bool(causal)), _ptr(kv_len),
+                                ctypes.byref(var), wp, wn, _stream_ptr(stream)), "fa_bwd_dkdv_v")
 
 
 def fa_check(stream=None):

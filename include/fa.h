@@ -157,6 +157,12 @@ fa_status_t fa_bwd_v(const void* q, const void* k, const void* v, const void* o,
                      const fa_variant_t* variant, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/* fa_bwd_dkdv for a variant (fa_bwd_v is fa_bwd_prep, fa_bwd_dkdv_v, fa_bwd_dq). */
+fa_status_t fa_bwd_dkdv_v(const void* q, const void* k, const void* v, const void* dO, void* dk,
+                          void* dv, int B, int H, int N, int d, float scale, int causal,
+                          const int* kv_len, const fa_variant_t* variant, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /*
  * fa_bwd_noalloc: the backward pass for callers that cannot allocate device
  * memory.  Same arguments, results and errors as fa_bwd, minus the workspace:
