@@ -44,6 +44,9 @@ def _load():
         lib.fa_oracle_backward_v.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int,
                                              c_int, c_int, c_double, c_int, ip, c_int, c_int, c_int]
         lib.fa_oracle_backward_v.restype = c_int
+        lib.fa_oracle_decode.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_int,
+                                         c_int, c_double, c_int, ip, c_int, c_int, c_int]
+        lib.fa_oracle_decode.restype = c_int
         lib.fa_oracle_num_threads.argtypes = []
         lib.fa_oracle_num_threads.restype = c_int
         _lib = lib
@@ -148,3 +151,24 @@ def attention_bwd(q, k, v, do, scale, causal=False, kv_len=None, threads=None, w
     if rc:
         raise RuntimeError(f"oracle backward failed ({rc})")
     return dq, dk, dv, D
+
+
+def attention_decode(q, k, v, scale, causal=False, kv_len=None, threads=None, window=None):
+    """O [B,H,Nq,d] and LSE [B,H,Nq] for Nq queries per head against Nk keys
+    (k, v [B,H_kv,Nk,d]); query t of batch entry b sits at position
+    kv_len[b] - Nq + t (kv_len None: Nk)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if k.shape != (B, Hkv, Nk, d) or v.shape != k.shape or Hkv < 1 or H % Hkv:
+        raise ValueError(f"K/V shape {k.shape} does not match Q {q.shape}")
+    wl, wr = _window(window)
+    o = np.empty_like(q)
+    lse = np.empty((B, H, Nq), dtype=np.float64)
+    kv, kvp = _kv(kv_len, B)
+    rc = _load().fa_oracle_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv, Nq,
+                                  Nk, d, float(scale), int(bool(causal)), kvp, wl, wr,
+                                  threads or default_threads())
+    if rc:
+        raise RuntimeError(f"oracle decode failed ({rc})")
+    return o, lse

@@ -40,12 +40,13 @@
  * j >= i - window_left when window_left >= 0, and j <= i + window_right when
  * window_right >= 0 (square attention, N queries and N keys, 0-based
  * indices).  The window is the (left, right) pair of flash-attn's
- * window_size argument, (-1, -1) meaning no window ("Flash Attention 详解",
- * section 六; "4. FlashAttention 深度剖析" 4.8.1, sliding window).  A row
- * with no visible key gets O = 0 and LSE = -inf.
+ * window_size argument, (-1, -1) meaning no window ("炉案与百步之外的仓库：
+ * Flash Attention 与注意力计算的工艺极限" section 六; "4. FlashAttention 深度
+ * 剖析" 4.8.1, sliding window).  A row with no visible key gets O = 0 and
+ * LSE = -inf.
  *
- * Grouped K/V heads (GQA / MQA, "Flash Attention 详解" section 六 and the
- * FlashAttention-2 summary in "注意力为什么受限于显存带宽…"): K and V have
+ * Grouped K/V heads (GQA / MQA, the same section 六 and the FlashAttention-2
+ * summary in "注意力为什么受限于显存带宽…" section 九): K and V have
  * H_kv heads, H_kv divides H, and query head h reads K/V head
  * h / (H / H_kv).  dK and dV of a K/V head are the sums over the query heads
  * that read it.
@@ -339,4 +340,60 @@ int fa_oracle_backward(const double *q, const double *k, const double *v,
 {
     return fa_oracle_backward_v(q, k, v, dout, dq, dk, dv, D, B, H, H, N, d, scale, causal,
                                 kv_len, -1, -1, nthreads);
+}
+
+/* Decode-shaped attention: Nq queries per head against Nk keys.  Query t of
+ * batch entry b sits at position pos = len_b - Nq + t of its sequence (the
+ * newest Nq tokens of a key/value cache of len_b entries), so under causal it
+ * sees keys j <= pos, and the window is taken around pos; keys j >= len_b are
+ * never visible.  This is the shape FlashDecoding splits across SMs
+ * ("4. FlashAttention 深度剖析" 4.8.3); the result is the plain definition, as
+ * for fa_oracle_forward_v.  q, o: [B, H, Nq, d]; k, v: [B, H_kv, Nk, d]; lse:
+ * [B, H, Nq]; kv_len NULL means len_b = Nk. */
+int fa_oracle_decode(const double *q, const double *k, const double *v,
+                     double *o, double *lse,
+                     int B, int H, int H_kv, int Nq, int Nk, int d, double scale, int causal,
+                     const int *kv_len, int wl, int wr, int nthreads)
+{
+    if (!check_args(q, k, v, B, H, Nq, d) || Nk < 1 || !o || !lse || !check_heads(H, H_kv))
+        return ORACLE_EINVAL;
+    if (nthreads < 1) nthreads = 1;
+    const long qd = (long)Nq * d, kd = (long)Nk * d;
+    const int group = H / H_kv;
+    int err = ORACLE_OK;
+    for (long bh = 0; bh < (long)B * H; ++bh) {
+        const long b = bh / H;
+        const long kvh = b * H_kv + (bh % H) / group;
+        long len = kv_len ? kv_len[b] : Nk;
+        if (len > Nk) len = Nk;
+        const mask_t mk = {causal, len, wl, wr};
+        const double *Q = q + bh * qd, *K = k + kvh * kd, *V = v + kvh * kd;
+        double *O = o + bh * qd, *L = lse + bh * (long)Nq;
+#pragma omp parallel num_threads(nthreads)
+        {
+            double *p = (double *)malloc(sizeof(double) * (size_t)Nk);
+            if (!p) {
+#pragma omp atomic write
+                err = ORACLE_ENOMEM;
+            }
+#pragma omp for schedule(dynamic, 1)
+            for (long t = 0; t < Nq; ++t) {
+                if (!p) continue;
+                {
+                    const long pos = len - Nq + t;
+                    L[t] = softmax_row(Q + t * d, K, Nk, d, scale, &mk, pos, p);
+                    double *ot = O + t * d;
+                    for (int c = 0; c < d; ++c) ot[c] = 0.0;
+                    for (long j = 0; j < Nk; ++j) {
+                        if (p[j] == 0.0) continue;
+                        const double *vj = V + j * d;
+                        for (int c = 0; c < d; ++c) ot[c] += p[j] * vj[c];
+                    }
+                }
+            }
+            free(p);
+        }
+        if (err) return err;
+    }
+    return ORACLE_OK;
 }
