@@ -223,6 +223,33 @@ class Runner:
             f()
 
 
+class DecodeRunner:
+    """Split-KV decoding (fa_decode: the split kernel and the merge) for one
+    decode workload."""
+
+    def __init__(self, w, inp, fa):
+        self.w, self.fa = w, fa
+        d = torch.device("cuda")
+        self.q, self.k, self.v = (inp[n].to(d) for n in ("q", "k", "v"))
+        self.kv = None if inp["kv_len"] is None else inp["kv_len"].to(d)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device=d)
+        self.splits = max(1, fa.fa_decode_splits(w.B, w.kv_heads, w.N))
+        self.ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.H, w.queries, w.d, self.splits),
+                              dtype=torch.uint8, device=d)
+        self.backward = False
+
+    def run(self):
+        self.fa.fa_decode(self.q, self.k, self.v, self.o, self.lse, self.w.scale, self.w.causal,
+                          self.kv, self.w.window, self.splits, self.ws)
+
+    def phases(self):
+        return [("fa_decode", self.run)]
+
+    def step(self):
+        self.run()
+
+
 def time_steps(runner, steps, flush=None):
     """Per-phase and per-step device times (ms) over `steps` timed steps."""
     phases = runner.phases()
@@ -383,11 +410,15 @@ def run_sweep(fa, peaks):
     for name, w in WORKLOADS.items():
         if name == HEADLINE:
             continue
-        key = (w.B, w.H, w.kv_heads, w.N, w.d, w.seed, w.qk_gain, w.kv_len_range, w.backward)
+        key = (w.B, w.H, w.kv_heads, w.queries, w.N, w.d, w.seed, w.qk_gain, w.kv_len_range,
+               w.backward)
         if key not in cache:
             cache.clear()
             cache[key] = make_inputs(w)
         inp = cache[key]
+        if w.nq is not None:
+            out.append(sweep_decode(w, inp, fa, peaks, flush_buf))
+            continue
         r = Runner(w, inp, fa)
         for _ in range(3):
             r.step()
@@ -420,6 +451,27 @@ def run_sweep(fa, peaks):
         del r
         torch.cuda.empty_cache()
     return out
+
+
+def sweep_decode(w, inp, fa, peaks, flush_buf):
+    """A decode workload: bound by reading K and V once, so GB/s against the
+    measured HBM peak is the figure that matters."""
+    r = DecodeRunner(w, inp, fa)
+    for _ in range(3):
+        r.step()
+    torch.cuda.synchronize()
+    per_phase, _ = time_steps(r, 20, flush=lambda: flush_l2(flush_buf))
+    fa.fa_check()
+    ms = per_phase["fa_decode"]
+    qrows = w.B * w.H * w.queries
+    kv_bytes = 4 * w.B * w.kv_heads * w.N * w.d           # K and V, bf16, read once
+    nbytes = kv_bytes + 4 * qrows * w.d + 4 * qrows       # + Q, O (bf16) and LSE
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "N": w.N, "nq": w.queries, "d": w.d, "causal": w.causal,
+            "h_kv": w.kv_heads, "splits": r.splits, "decode_ms": round(ms, 4),
+            "decode_gbs": round(gbs, 1), "decode_frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "decode_tflops": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 3),
+            "bytes": nbytes, "l2": "inputs larger than L2, flushed between steps"}
 
 
 # ------------------------------------------------------------------ the oracle as baseline

@@ -380,6 +380,92 @@ fa_status_t fa_bwd_v(const void* q, const void* k, const void* v, const void* o,
   return r;
 }
 
+int fa_decode_splits(int B, int H_kv, int Nk) {
+  if (B < 1 || H_kv < 1 || Nk < 1) return 0;
+  DeviceInfo* di = device_info(nullptr);
+  const int sms = (di && di->err == cudaSuccess && di->num_sms > 0) ? di->num_sms : 148;
+  const long long heads = static_cast<long long>(B) * H_kv;
+  const int nblk = (Nk + 127) / 128;
+  // Chunks of at least 8 key blocks; among those, the count whose units fill
+  // the SMs' waves best (ties: fewer chunks, less merging).
+  int best = 1;
+  double best_eff = -1.0;
+  for (int s = 1; s <= nblk; ++s) {
+    const int chunk = (nblk + s - 1) / s;
+    const int eff_s = (nblk + chunk - 1) / chunk;
+    if (eff_s != s || (s > 1 && chunk < 8)) continue;
+    const long long units = heads * s;
+    const long long waves = (units + sms - 1) / sms;
+    const double eff = static_cast<double>(units) / static_cast<double>(waves * sms);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
+    if (units >= 4ll * sms) break;
+  }
+  return best;
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int d, int splits) {
+  if (B < 1 || H < 1 || Nq < 1 || splits < 1 || (d != 64 && d != 128 && d != 256)) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * Nq * splits;
+  return round_up256(rows * d * sizeof(float)) + round_up256(rows * sizeof(float));
+}
+
+fa_status_t fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Nq, int Nk, int d, float scale, int causal, const int* kv_len,
+                      const fa_variant_t* variant, int splits, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FA_ERR_INVALID_ARG;
+  if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || splits < 1) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  Variant var;
+  const fa_status_t vs = resolve_variant(variant, H, causal, &var);
+  if (vs != FA_OK) return vs;
+  if (static_cast<long long>(B) * H * Nq * d >= (1ll << 31) ||
+      static_cast<long long>(B) * var.H_kv * Nk * d >= (1ll << 31))
+    return FA_ERR_INVALID_ARG;
+  if ((H / var.H_kv) * Nq > 128) return FA_ERR_UNSUPPORTED;   // one 128-row tile per K/V head
+  if (workspace_bytes < fa_decode_workspace_bytes(B, H, Nq, d, splits)) return FA_ERR_INVALID_ARG;
+  DeviceInfo* di = device_info(nullptr);
+  if (!di || di->err != cudaSuccess) return FA_ERR_CUDA;
+  if (!di->supported) return FA_ERR_UNSUPPORTED;
+  fa::FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int rows = B * H * Nq;
+  if (!make_map(&p.tq, q, d, rows, 1) || !make_map(&p.tk, k, d, Nk, B * var.H_kv) ||
+      !make_map(&p.tv, v, d, Nk, B * var.H_kv))
+    return FA_ERR_CUDA;
+  const int nblk = (Nk + 127) / 128;
+  const int chunk = (nblk + splits - 1) / splits;
+  p.kv_len = kv_len;
+  p.B = B;
+  p.H = H;
+  p.N = Nk;
+  p.H_kv = var.H_kv;
+  p.wl = var.wl;
+  p.wr = var.wr;
+  p.causal = 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.status = di->status;
+  p.Nq = Nq;
+  p.chunk_blocks = chunk;
+  p.splits = (nblk + chunk - 1) / chunk;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = reinterpret_cast<float*>(
+      static_cast<char*>(workspace) +
+      round_up256(static_cast<size_t>(rows) * splits * d * sizeof(float)));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (fa::launch_decode(p, d, di->num_sms, di->max_smem, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (fa::launch_decode_combine(p, d, o, lse, s) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 fa_status_t fa_check(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   DeviceInfo* di = device_info(nullptr);

@@ -148,13 +148,64 @@ __device__ __forceinline__ void issuer_fail(int* status, volatile int* abort, in
   if (lane == 0) record_failure(status, abort, site);
 }
 
+// One tile of the schedule as every role sees it.  Training: query tile m of
+// head bh (rows are the positions m*BM ..).  Decode: the H/H_kv query heads
+// of one K/V head stacked as rows (Nq rows each, row r at position
+// len - Nq + r % Nq) against one chunk of the keys; its outputs are partial
+// and merged later.
+struct Tile {
+  int qy, qz;          // Q tile coordinates in the tensor map (row, head)
+  int kvbh;            // K/V head
+  int len;             // keys of the batch entry (kv_len)
+  int qlo, qhi;        // query positions of the tile's first and last row
+  int jlo, nkv;        // key blocks [jlo, jlo + nkv)
+  long long out0;      // output row of tile row 0
+  int rows;            // rows of the tile that are real queries
+};
+
+template <bool DEC>
+__device__ __forceinline__ void make_tile(const FwdParams& p, const Sched& sched, int u, int kt,
+                                          Tile& t) {
+  if constexpr (!DEC) {
+    int bh, m;
+    sched.tile(u, kt, bh, m);
+    t.qy = m * BM;
+    t.qz = bh;
+    t.kvbh = kv_head_of(bh, p.H, p.H_kv);
+    t.len = seq_len(p, bh);
+    t.qlo = m * BM;
+    t.qhi = m * BM + BM - 1;
+    t.nkv = tile_blocks(p, m, t.len, t.jlo);
+    t.out0 = static_cast<long long>(bh) * p.N + m * BM;
+    t.rows = p.N - m * BM < BM ? p.N - m * BM : BM;
+  } else {
+    const int kvbh = u / p.splits, split = u % p.splits;
+    const int row0 = q_head_of(kvbh, 0, p.H, p.H_kv) * p.Nq;
+    t.qy = row0;
+    t.qz = 0;
+    t.kvbh = kvbh;
+    t.len = seq_len(p, (kvbh / p.H_kv) * p.H);
+    t.qlo = t.len - p.Nq;
+    t.qhi = t.len - 1;
+    int k_lo, k_hi;
+    visible_keys(t.qlo, p.Nq, t.len, p.wl, p.wr, k_lo, k_hi);
+    const int c0 = split * p.chunk_blocks * BN;
+    if (k_lo < c0) k_lo = c0;
+    if (k_hi > c0 + p.chunk_blocks * BN) k_hi = c0 + p.chunk_blocks * BN;
+    t.jlo = k_lo / BN;
+    t.nkv = k_hi > k_lo ? (k_hi + BN - 1) / BN - t.jlo : 0;
+    t.out0 = static_cast<long long>(split) * p.B * p.H * p.Nq + row0;
+    t.rows = (p.H / p.H_kv) * p.Nq;
+  }
+}
+
 // All 32 lanes wait; the decision is made uniform across the warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   bool ok = mbar_wait(bar, parity, abort, kWaitTimeoutNs);
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D>
+template <int D, bool DEC>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -199,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   const uint32_t tmem = sm.tmem_base;
   const int BH = p.B * p.H;
   const Sched sched(BH, p.N, p.causal);
+  const int nunits = DEC ? p.B * p.H_kv * p.splits : sched.units;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -208,14 +260,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       prefetch_tmap(&p.tv);
       uint32_t q_it = 0, k_it = 0, v_it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        for (int kt = 0; ok && kt < sched.ntiles(u); ++kt) {
-          int bh, m;
-          sched.tile(u, kt, bh, m);
-          int jlo;
-          const int nkv = tile_blocks(p, m, seq_len(p, bh), jlo);
+      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+        for (int kt = 0; ok && kt < (DEC ? 1 : sched.ntiles(u)); ++kt) {
+          Tile t;
+          make_tile<DEC>(p, sched, u, kt, t);
+          const int jlo = t.jlo, nkv = t.nkv;
           if (nkv == 0) continue;
-          const int kvbh = kv_head_of(bh, p.H, p.H_kv);
+          const int kvbh = t.kvbh;
           if (!mbar_wait(&sm.q_empty, (q_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
             record_failure(p.status, abort, kSiteProdQ);
             ok = false;
@@ -224,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           mbar_arrive_expect_tx(&sm.q_full, C::TILE_BYTES);
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(sm.q + c * CHUNK, &p.tq, &sm.q_full, 64 * c, m * BM, bh);
+            tma_load_3d(sm.q + c * CHUNK, &p.tq, &sm.q_full, 64 * c, t.qy, t.qz);
           ++q_it;
           for (int j = 0; j < nkv; ++j) {
             const int st = k_it % C::STAGES;
@@ -278,12 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q), 16, 1024);
       uint32_t q_it = 0, g = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        for (int kt = 0; ok && kt < sched.ntiles(u); ++kt) {
-          int bh, m;
-          sched.tile(u, kt, bh, m);
-          int jlo;
-          const int nkv = tile_blocks(p, m, seq_len(p, bh), jlo);
+      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+        for (int kt = 0; ok && kt < (DEC ? 1 : sched.ntiles(u)); ++kt) {
+          Tile t;
+          make_tile<DEC>(p, sched, u, kt, t);
+          const int nkv = t.nkv;
           if (nkv == 0) continue;
           if (!mbar_wait_warp(&sm.q_full, q_it & 1, abort, kWaitTimeoutNs)) {
             issuer_fail(p.status, abort, lane, kSiteMmaQ);
@@ -332,12 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 0, 1);
       uint32_t g = 0, t_it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        for (int kt = 0; ok && kt < sched.ntiles(u); ++kt) {
-          int bh, m;
-          sched.tile(u, kt, bh, m);
-          int jlo;
-          const int nkv = tile_blocks(p, m, seq_len(p, bh), jlo);
+      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+        for (int kt = 0; ok && kt < (DEC ? 1 : sched.ntiles(u)); ++kt) {
+          Tile t;
+          make_tile<DEC>(p, sched, u, kt, t);
+          const int nkv = t.nkv;
           if (nkv == 0) continue;
           for (int j = 0; j < nkv; ++j, ++g) {
             const uint32_t b = g % C::NSB;
@@ -389,21 +438,27 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o);
     uint32_t kv_it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-      for (int kt = 0; ok && kt < sched.ntiles(u); ++kt) {
-        int bh, m;
-        sched.tile(u, kt, bh, m);
-        const int len = seq_len(p, bh);
-        int jlo;
-        const int nkv = tile_blocks(p, m, len, jlo);
-        const int row = m * BM + row_local;
-        const size_t row_off = static_cast<size_t>(bh) * p.N + row;
+    for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+      for (int kt = 0; ok && kt < (DEC ? 1 : sched.ntiles(u)); ++kt) {
+        Tile t;
+        make_tile<DEC>(p, sched, u, kt, t);
+        const int len = t.len, jlo = t.jlo, nkv = t.nkv;
+        const int row = DEC ? t.qlo + row_local % p.Nq : t.qlo + row_local;   // query position
+        const bool row_valid = row_local < t.rows;
+        const size_t row_off = static_cast<size_t>(t.out0 + row_local);
         if (nkv == 0) {
-          if (row < p.N) {
-            uint4* dst = reinterpret_cast<uint4*>(out + row_off * D);
+          if (row_valid) {
+            if constexpr (DEC) {
+              float4* dst = reinterpret_cast<float4*>(p.o_part + row_off * D);
 #pragma unroll
-            for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-            p.lse[row_off] = -INFINITY;
+              for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+              p.lse_part[row_off] = -INFINITY;
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(out + row_off * D);
+#pragma unroll
+              for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+              p.lse[row_off] = -INFINITY;
+            }
           }
           continue;
         }
@@ -430,8 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           // window (above the diagonal when causal) and left of the window;
           // skipped when every key of the block is visible to every row
           const int key0 = (jlo + j) * BN;
-          if (key0 + BN > len || key0 + BN - 1 > m * BM + p.wr ||
-              key0 < m * BM + BM - 1 - p.wl) {
+          if (key0 + BN > len || key0 + BN - 1 > t.qlo + p.wr || key0 < t.qhi - p.wl) {
             // visible columns [c_lo, c_hi]: before the sequence end and
             // inside the window [row - wl, row + wr]
             const int c_hi = min(len - key0 - 1, row + p.wr - key0);
@@ -534,7 +588,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           tmem_ld_x32(t_lane + C::TM_O + 32 * c, orr);
           tmem_wait_ld();
           reg_fence<32>(orr);
-          if (row < p.N) {
+          if constexpr (DEC) {
+            if (row_valid) {
+              float4* dst = reinterpret_cast<float4*>(p.o_part + row_off * D + 32 * c);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(__uint_as_float(orr[4 * i]) * inv_l,
+                                     __uint_as_float(orr[4 * i + 1]) * inv_l,
+                                     __uint_as_float(orr[4 * i + 2]) * inv_l,
+                                     __uint_as_float(orr[4 * i + 3]) * inv_l);
+            }
+          } else if (row_valid) {
             uint32_t packed[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -550,8 +614,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.o_free);
-        if (row < p.N)
-          p.lse[row_off] = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if (row_valid) {
+          const float lse_row = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+          if constexpr (DEC)
+            p.lse_part[row_off] = lse_row;
+          else
+            p.lse[row_off] = lse_row;
+        }
       }
     }
   }
@@ -564,30 +633,97 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   }
 }
 
-template <int D>
+template <int D, bool DEC>
 cudaError_t launch(const FwdParams& p, int num_sms, int max_smem, cudaStream_t stream) {
   const size_t smem = smem_request(sizeof(FwdSmem<D>), max_smem);
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, DEC>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int T = (p.N + BM - 1) / BM;
-  const long long units = p.causal ? static_cast<long long>(p.B) * p.H * ((T + 1) / 2)
-                                   : static_cast<long long>(p.B) * p.H * T;
+  long long units;
+  if (DEC) {
+    units = static_cast<long long>(p.B) * p.H_kv * p.splits;
+  } else {
+    const int T = (p.N + BM - 1) / BM;
+    units = p.causal ? static_cast<long long>(p.B) * p.H * ((T + 1) / 2)
+                     : static_cast<long long>(p.B) * p.H * T;
+  }
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  fa_fwd_kernel<D><<<grid, kThreads, smem, stream>>>(p);
+  fa_fwd_kernel<D, DEC><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+// Merge of the split-KV partials (the associative block merge of "4.
+// FlashAttention 深度剖析" 4.2.4, in natural-log units): per row,
+// LSE = log sum_s exp(LSE_s) and O = sum_s exp(LSE_s - LSE) O_s, where each O_s
+// is already normalised by its own row sum.  One warp per row, D/32 columns a
+// lane; a row whose every chunk saw no key gets O = 0, LSE = -inf.
+template <int D>
+__global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_constant__ FwdParams p,
+                                                             __nv_bfloat16* o, float* lse,
+                                                             long long rows) {
+  const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= rows) return;
+  constexpr int PER = D / 32;
+  float m = -INFINITY;
+  for (int s = 0; s < p.splits; ++s) m = fmaxf(m, p.lse_part[s * rows + row]);
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float sum = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < p.splits; ++s) {
+      const float w = expf(p.lse_part[s * rows + row] - m);
+      sum += w;
+      const float* src = p.o_part + (s * rows + row) * D + lane * PER;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] = fmaf(w, src[i], acc[i]);
+    }
+  }
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  uint32_t packed[PER / 2];
+#pragma unroll
+  for (int i = 0; i < PER / 2; ++i) packed[i] = pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(o + row * D + lane * PER);
+#pragma unroll
+  for (int i = 0; i < PER / 2; ++i) dst[i] = packed[i];
+  if (lane == 0) lse[row] = sum > 0.f ? m + logf(sum) : -INFINITY;
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdParams& p, int d, int num_sms, int max_smem, cudaStream_t stream) {
   switch (d) {
-    case 64: return launch<64>(p, num_sms, max_smem, stream);
-    case 128: return launch<128>(p, num_sms, max_smem, stream);
-    case 256: return launch<256>(p, num_sms, max_smem, stream);
+    case 64: return launch<64, false>(p, num_sms, max_smem, stream);
+    case 128: return launch<128, false>(p, num_sms, max_smem, stream);
+    case 256: return launch<256, false>(p, num_sms, max_smem, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_decode(const FwdParams& p, int d, int num_sms, int max_smem,
+                          cudaStream_t stream) {
+  switch (d) {
+    case 64: return launch<64, true>(p, num_sms, max_smem, stream);
+    case 128: return launch<128, true>(p, num_sms, max_smem, stream);
+    case 256: return launch<256, true>(p, num_sms, max_smem, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode_combine(const FwdParams& p, int d, void* o, float* lse,
+                                  cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.B) * p.H * p.Nq;
+  const unsigned grid = static_cast<unsigned>((rows * 32 + 255) / 256);
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+  switch (d) {
+    case 64: decode_combine_kernel<64><<<grid, 256, 0, stream>>>(p, ob, lse, rows); break;
+    case 128: decode_combine_kernel<128><<<grid, 256, 0, stream>>>(p, ob, lse, rows); break;
+    case 256: decode_combine_kernel<256><<<grid, 256, 0, stream>>>(p, ob, lse, rows); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace fa

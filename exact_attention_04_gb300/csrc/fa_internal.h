@@ -27,6 +27,12 @@ struct FwdParams {
   int causal;                  // causal pairing of tiles in the schedule (plain causal only)
   float scale_log2;            // scale * log2(e)
   int* status;                 // device status word
+  // decode (split-KV) mode: N is the number of keys; Q is viewed as
+  // [B*H*Nq, d] and query t of a head sits at position len - Nq + t
+  int Nq;
+  int splits, chunk_blocks;    // key chunks per K/V head, key blocks per chunk
+  float* o_part;               // fp32 [splits, B*H*Nq, d] partial outputs (normalised)
+  float* lse_part;             // fp32 [splits, B*H*Nq] partial log-sum-exp (natural log)
 };
 
 struct BwdParams {
@@ -71,6 +77,10 @@ cudaError_t launch_bwd_main(const BwdParams& p, int d, int num_sms, int max_smem
 cudaError_t launch_bwd_post(const BwdParams& p, int d, cudaStream_t stream);
 // 64-query-step backward main kernel with dQ^T (head dimensions 128, 256);
 // its Q and dO tensor maps have a box of 64 rows.
+cudaError_t launch_decode(const FwdParams& p, int d, int num_sms, int max_smem,
+                          cudaStream_t stream);
+cudaError_t launch_decode_combine(const FwdParams& p, int d, void* o, float* lse,
+                                  cudaStream_t stream);
 cudaError_t launch_bwd_main_dt(const BwdParams& p, int d, int num_sms, int max_smem,
                                cudaStream_t stream);
 

@@ -68,6 +68,12 @@ def load():
         lib.fa_bwd_dkdv_v.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, varp, vp, sz,
                                       vp]
         lib.fa_bwd_dkdv_v.restype = i
+        lib.fa_decode_splits.argtypes = [i, i, i]
+        lib.fa_decode_splits.restype = i
+        lib.fa_decode_workspace_bytes.argtypes = [i, i, i, i, i]
+        lib.fa_decode_workspace_bytes.restype = sz
+        lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, varp, i, vp, sz, vp]
+        lib.fa_decode.restype = i
         lib.fa_check.argtypes = [vp]
         lib.fa_check.restype = i
         lib.fa_status_string.argtypes = [i]
@@ -79,7 +85,8 @@ def load():
 
 
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_prep", "fa_bwd_dkdv",
-           "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_v", "fa_bwd_v", "fa_bwd_dkdv_v", "fa_check",
+           "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_v", "fa_bwd_v", "fa_bwd_dkdv_v",
+           "fa_decode_splits", "fa_decode_workspace_bytes", "fa_decode", "fa_check",
            "fa_status_string", "fa_version")
 
 
@@ -282,6 +289,55 @@ def fa_bwd_dkdv_v(q, k, v, do, dk, dv, scale, causal=False, kv_len=None, window=
     _raise(load().fa_bwd_dkdv_v(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dk), _ptr(dv), B, H,
                                 N, d, float(scale), int(bool(causal)), _ptr(kv_len),
                                 ctypes.byref(var), wp, wn, _stream_ptr(stream)), "fa_bwd_dkdv_v")
+
+
+def fa_decode_splits(B, h_kv, Nk) -> int:
+    return int(load().fa_decode_splits(B, h_kv, Nk))
+
+
+def fa_decode_workspace_bytes(B, H, Nq, d, splits) -> int:
+    return int(load().fa_decode_workspace_bytes(B, H, Nq, d, splits))
+
+
+def fa_decode(q, k, v, o, lse, scale, causal=False, kv_len=None, window=None, splits=1,
+              workspace=None, stream=None):
+    """Calls fa_decode: q, o [B,H,Nq,d]; k, v [B,H_kv,Nk,d] (H_kv divides H);
+    lse fp32 [B,H,Nq]; workspace of fa_decode_workspace_bytes()."""
+    _check_qkv("q", q)
+    B, H, Nq, d = q.shape
+    _check_qkv("k", k)
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if (k.shape[0], k.shape[3]) != (B, d) or Hkv < 1 or H % Hkv:
+        raise ValueError(f"k: shape {tuple(k.shape)} does not match q {tuple(q.shape)}")
+    _check_qkv("v", v, k.shape)
+    _check_qkv("o", o, q.shape)
+    if lse.dtype != torch.float32 or not lse.is_cuda or tuple(lse.shape) != (B, H, Nq) \
+            or not lse.is_contiguous():
+        raise ValueError("lse: expected a contiguous fp32 CUDA tensor [B,H,Nq]")
+    kv_len = _check_kv_len(kv_len, B)
+    wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    var = FaVariant(int(Hkv), wl, wr)
+    wp, wn = _ws(workspace)
+    _raise(load().fa_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                            float(scale), int(bool(causal)), _ptr(kv_len), ctypes.byref(var),
+                            int(splits), wp, wn, _stream_ptr(stream)), "fa_decode")
+
+
+def decode(q, k, v, scale=None, causal=False, kv_len=None, window=None, splits=None,
+           stream=None):
+    """(O, LSE) of split-KV decoding with outputs and workspace allocated by
+    torch; splits defaults to the library's choice for this GPU."""
+    B, H, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if splits is None:
+        splits = max(1, fa_decode_splits(B, Hkv, Nk))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    ws = torch.empty(fa_decode_workspace_bytes(B, H, Nq, d, splits), dtype=torch.uint8,
+                     device=q.device)
+    fa_decode(q, k, v, o, lse, default_scale(d) if scale is None else scale, causal, kv_len,
+              window, splits, ws, stream)
+    return o, lse
 
 
 def fa_check(stream=None):

@@ -38,6 +38,7 @@ class Workload:
     kv_len_range: tuple = None     # (lo, hi) inclusive, or None for no padding
     h_kv: int = None               # K/V heads (grouped-query attention); None = H
     window: tuple = None           # flash-attn (left, right), -1 = unbounded; None = no window
+    nq: int = None                 # decode: queries per head at the end of an N-key cache
 
     @property
     def scale(self) -> float:
@@ -47,11 +48,27 @@ class Workload:
     def kv_heads(self) -> int:
         return self.H if self.h_kv is None else self.h_kv
 
+    @property
+    def queries(self) -> int:
+        return self.N if self.nq is None else self.nq
+
     def visible_pairs(self) -> float:
         """(query, key) pairs one head computes: N^2, N^2/2 under the causal
         mask, and with a window the exact count of keys in each row's window
-        (padding not discounted)."""
+        (padding not discounted).  Decode: query t sits at position
+        N - nq + t of the N-key cache."""
         N = self.N
+        if self.nq is not None:
+            wl, wr = self.window if self.window is not None else (-1, -1)
+            total = 0
+            for t in range(self.nq):
+                pos = N - self.nq + t
+                lo = 0 if wl < 0 else max(0, pos - wl)
+                hi = N - 1 if wr < 0 else min(N - 1, pos + wr)
+                if self.causal:
+                    hi = min(hi, pos)
+                total += max(0, hi - lo + 1)
+            return float(total)
         if self.window is None:
             return N * N / 2 if self.causal else float(N * N)
         wl, wr = self.window
@@ -97,13 +114,17 @@ WORKLOADS = {w.name: w for w in [
     # causal sliding window of 4096 keys (Mistral, per the sliding-window note)
     Workload("swa_b2_h32_n16384_d128_w4096_causal", 2, 32, 16384, 128, causal=True, seed=6,
              backward=True, window=(4095, 0)),
+    # decoding one token per sequence against a 32K-key cache with four query
+    # heads per K/V head (split-KV, the FlashDecoding note)
+    Workload("decode_b4_h32_kv8_nq1_nk32768_d128", 4, 32, 32768, 128, causal=True, seed=7,
+             backward=False, h_kv=8, nq=1),
 ]}
 
 
 def make_inputs(w: Workload, with_grad_out: bool = None):
     """CPU tensors for workload ``w``: dict with q, k, v (bf16 [B,H,N,d]),
     optionally do (bf16) and kv_len (int32 [B] or None)."""
-    shape = (w.B, w.H, w.N, w.d)
+    shape = (w.B, w.H, w.queries, w.d)
     kv_shape = (w.B, w.kv_heads, w.N, w.d)
     g = torch.Generator().manual_seed(w.seed)
     q = torch.randn(shape, generator=g, dtype=torch.float32)
@@ -133,3 +154,15 @@ def random_case(B, H, N, d, seed, causal=False, kv_len_range=None, qk_gain=1.0, 
     return Workload(f"case_b{B}_h{H}_n{N}_d{d}", B, H, N, d, causal=causal, seed=seed,
                     backward=backward, qk_gain=qk_gain, kv_len_range=kv_len_range, h_kv=h_kv,
                     window=window)
+
+
+def decode_case(B, H, h_kv, Nq, Nk, d, seed, causal=True, kv_len_range=None, window=None):
+    """An ad-hoc decode workload: Nq queries per head, Nk keys."""
+    return Workload(f"decode_b{B}_h{H}_kv{h_kv}_nq{Nq}_nk{Nk}_d{d}", B, H, Nk, d, causal=causal,
+                    seed=seed, backward=False, kv_len_range=kv_len_range, h_kv=h_kv,
+                    window=window, nq=Nq)
+
+
+def make_decode_inputs(w: Workload):
+    """q [B,H,Nq,d], k and v [B,H_kv,Nk,d], kv_len: make_inputs for a decode workload."""
+    return make_inputs(w, with_grad_out=False)

@@ -164,6 +164,35 @@ fa_status_t fa_bwd_dkdv_v(const void* q, const void* k, const void* v, const voi
                           size_t workspace_bytes, void* stream);
 
 /*
+ * Split-KV decoding: Nq new queries per head against a long key/value cache
+ * (FlashDecoding, "4. FlashAttention 深度剖析" 4.8.3).  The keys of every K/V
+ * head are cut into `splits` chunks that different SMs process at once; each
+ * chunk yields a partial (O_s normalised by its own row sum, LSE_s), and a
+ * second kernel merges the chunks with the associative rule of 4.2.4:
+ *   LSE = log sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s.
+ *
+ * q, o: bf16 [B, H, Nq, d]; k, v: bf16 [B, h_kv, Nk, d] (h_kv from the
+ * variant, H when NULL); lse: fp32 [B, H, Nq].  kv_len: NULL (every entry has
+ * Nk valid keys) or a device int32[B] of cache lengths, clamped to [0, Nk].
+ * Query t of batch entry b is the token at position kv_len[b] - Nq + t:
+ * with causal it sees keys j <= that position, the variant's window is taken
+ * around it, and keys j >= kv_len[b] are never seen.  A query that sees no
+ * key gets O = 0, LSE = -inf.  The query heads of one K/V head are processed
+ * together: (H / h_kv) * Nq must be at most 128 (else FA_ERR_UNSUPPORTED).
+ * workspace: device memory of fa_decode_workspace_bytes(B, H, Nq, d, splits)
+ * bytes, 256-byte aligned, for the fp32 partials.  splits >= 1; chunks are
+ * whole 128-key blocks, so at most ceil(Nk / 128) chunks are used.
+ * fa_decode_splits returns the library's choice for this GPU (0 for invalid
+ * sizes).  Other arguments and errors as for fa_fwd_v.
+ */
+int fa_decode_splits(int B, int h_kv, int Nk);
+size_t fa_decode_workspace_bytes(int B, int H, int Nq, int d, int splits);
+fa_status_t fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                      const int* kv_len, const fa_variant_t* variant, int splits,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * fa_bwd_noalloc: the backward pass for callers that cannot allocate device
  * memory.  Same arguments, results and errors as fa_bwd, minus the workspace:
  * the scratch fa_bwd needs (fa_bwd_workspace_bytes(B,H,N,d) bytes) comes from
