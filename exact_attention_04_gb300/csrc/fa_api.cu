@@ -466,6 +466,17 @@ fa_status_t fa_decode(const void* q, const void* k, const void* v, void* o, floa
   return FA_OK;
 }
 
+fa_status_t fa_selftest_wait_timeout(unsigned int timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 1000000u) return FA_ERR_INVALID_ARG;
+  DeviceInfo* di = device_info(nullptr);
+  if (!di || di->err != cudaSuccess) return FA_ERR_CUDA;
+  if (!di->supported) return FA_ERR_UNSUPPORTED;
+  return fa::launch_wait_selftest(di->status, 1000ull * timeout_us,
+                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
 fa_status_t fa_check(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
   DeviceInfo* di = device_info(nullptr);

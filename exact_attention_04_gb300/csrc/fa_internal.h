@@ -77,6 +77,7 @@ cudaError_t launch_bwd_main(const BwdParams& p, int d, int num_sms, int max_smem
 cudaError_t launch_bwd_post(const BwdParams& p, int d, cudaStream_t stream);
 // 64-query-step backward main kernel with dQ^T (head dimensions 128, 256);
 // its Q and dO tensor maps have a box of 64 rows.
+cudaError_t launch_wait_selftest(int* status, unsigned long long timeout_ns, cudaStream_t s);
 cudaError_t launch_decode(const FwdParams& p, int d, int num_sms, int max_smem,
                           cudaStream_t stream);
 cudaError_t launch_decode_combine(const FwdParams& p, int d, void* o, float* lse,

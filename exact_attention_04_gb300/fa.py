@@ -74,6 +74,8 @@ def load():
         lib.fa_decode_workspace_bytes.restype = sz
         lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, varp, i, vp, sz, vp]
         lib.fa_decode.restype = i
+        lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+        lib.fa_selftest_wait_timeout.restype = i
         lib.fa_check.argtypes = [vp]
         lib.fa_check.restype = i
         lib.fa_status_string.argtypes = [i]
@@ -86,7 +88,8 @@ def load():
 
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_prep", "fa_bwd_dkdv",
            "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_v", "fa_bwd_v", "fa_bwd_dkdv_v",
-           "fa_decode_splits", "fa_decode_workspace_bytes", "fa_decode", "fa_check",
+           "fa_decode_splits", "fa_decode_workspace_bytes", "fa_decode",
+           "fa_selftest_wait_timeout", "fa_check",
            "fa_status_string", "fa_version")
 
 
@@ -338,6 +341,13 @@ def decode(q, k, v, scale=None, causal=False, kv_len=None, window=None, splits=N
     fa_decode(q, k, v, o, lse, default_scale(d) if scale is None else scale, causal, kv_len,
               window, splits, ws, stream)
     return o, lse
+
+
+def fa_selftest_wait_timeout(timeout_us, stream=None):
+    """Enqueues the bounded-wait self-test (see include/fa.h); the next
+    fa_check() must raise FAError with FA_ERR_TIMEOUT."""
+    _raise(load().fa_selftest_wait_timeout(int(timeout_us), _stream_ptr(stream)),
+           "fa_selftest_wait_timeout")
 
 
 def fa_check(stream=None):

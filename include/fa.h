@@ -193,6 +193,16 @@ fa_status_t fa_decode(const void* q, const void* k, const void* v, void* o, floa
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Self-test of the bounded waits: enqueues one tiny kernel that waits on a
+ * barrier nothing ever completes, with a limit of timeout_us microseconds
+ * (1 .. 1000000) instead of the kernels' two seconds.  The wait gives up,
+ * the kernel records FA_ERR_TIMEOUT in the status word and returns, so the
+ * following fa_check() returns FA_ERR_TIMEOUT (and clears it) and the
+ * device stays usable.  Returns FA_ERR_INVALID_ARG for a limit out of range.
+ */
+fa_status_t fa_selftest_wait_timeout(unsigned int timeout_us, void* stream);
+
+/*
  * fa_bwd_noalloc: the backward pass for callers that cannot allocate device
  * memory.  Same arguments, results and errors as fa_bwd, minus the workspace:
  * the scratch fa_bwd needs (fa_bwd_workspace_bytes(B,H,N,d) bytes) comes from

@@ -133,3 +133,8 @@ def test_variant_binding_checks_shapes(lib):
     k = torch.zeros(1, 3, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa._variant(q, k, None)
+
+
+def test_selftest_rejects_limits_out_of_range(lib):
+    assert lib.fa_selftest_wait_timeout(0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_selftest_wait_timeout(2000000, None) == fa.FA_ERR_INVALID_ARG
