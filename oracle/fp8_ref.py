@@ -10,7 +10,8 @@ readings used here (and by the GPU path, which is checked against this file):
 
 * E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits, subnormals, largest
   finite 448, no infinities.  Conversion from fp32 rounds to nearest, ties
-  to even, and saturates to +-448.
+  to even, saturates to +-448, and keeps the sign (a negative value that
+  rounds to zero becomes -0, as IEEE conversions do).
 * Q is scaled per 128-row tile of a head, K per 128-key block of a K/V head,
   V per K/V head: scale = amax / 448 (fp32), stored value = E4M3(x * (448 /
   amax)) with that product and quotient rounded to fp32; an all-zero block
@@ -66,7 +67,7 @@ def e4m3_round(x):
     mcode = np.round(mant * 8).astype(np.int64)
     ecode = np.where(normal, en.astype(np.int64) + 7, 0)
     codes = (ecode << 3) | mcode
-    codes = np.where(np.signbit(x) & (q > 0), codes | 0x80, codes)
+    codes = np.where(np.signbit(x), codes | 0x80, codes)
     return codes.astype(np.uint8)
 
 
@@ -115,11 +116,13 @@ def quantize_v_transposed(v):
     return codes, scales
 
 
-def attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=False, kv_len=None, H_kv=None):
+def attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=False, kv_len=None, H_kv=None,
+                  rows=None):
     """O [B,H,N,d] and LSE [B,H,N] of the FP8 forward, step by step.
 
     q8 [B,H,N,d] codes with sq [B,H,ceil(N/128)]; k8 [B,H_kv,N,d] with
-    sk [B,H_kv,ceil(N/128)]; v8t [B,H_kv,d,Npad] with sv [B,H_kv]."""
+    sk [B,H_kv,ceil(N/128)]; v8t [B,H_kv,d,Npad] with sv [B,H_kv].  rows: a
+    list of query rows to compute (the others are left 0 / -inf)."""
     B, H, N, d = q8.shape
     Hkv = k8.shape[1] if H_kv is None else H_kv
     G = H // Hkv
@@ -133,7 +136,7 @@ def attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=False, kv_len=None, H_k
         ln = N if kv_len is None else int(min(max(kv_len[b], 0), N))
         for h in range(H):
             hk = h // G
-            for i in range(N):
+            for i in (range(N) if rows is None else rows):
                 m = -np.inf
                 l = 0.0
                 acc = np.zeros(d)

@@ -25,8 +25,9 @@ def brute_round(x):
             continue
         d = np.abs(vals[finite] - v)
         best = finite[d == d.min()]
-        # ties: the code with an even mantissa; +0 for zero
-        best = [c for c in best if vals[c] != 0 or c == 0] or list(best)
+        # ties: the code with an even mantissa; a zero carries the input's sign
+        zero = 0x80 if np.signbit(v) else 0x00
+        best = [c for c in best if vals[c] != 0 or c == zero] or list(best)
         even = [c for c in best if c % 2 == 0]
         out.append((even or best)[0])
     return np.array(out, dtype=np.uint8)
@@ -41,18 +42,24 @@ def test_known_codes():
     assert np.isnan(F.e4m3_decode(0x7F))
 
 
+def test_sign_is_kept_through_rounding_to_zero():
+    assert F.e4m3_round(np.float32(-1e-6)) == 0x80
+    assert F.e4m3_round(np.float32(1e-6)) == 0x00
+    assert F.e4m3_round(np.float32(-0.0)) == 0x80
+
+
 def test_rounding_matches_nearest_code_with_even_ties():
     rng = np.random.default_rng(50)
     vals = F.e4m3_values()
     finite = np.sort(np.unique(vals[~np.isnan(vals)]))
     mids = (finite[1:] + finite[:-1]) / 2                  # every tie
     x = np.concatenate([rng.standard_normal(3000) * 10, rng.standard_normal(1000) * 0.01,
-                        mids, [500.0, -1000.0, 447.0, 460.0, 0.0, 2.0 ** -11, -2.0 ** -10]])
+                        mids, -mids, [500.0, -1000.0, 447.0, 460.0, 0.0, -0.0, 2.0 ** -11,
+                                      -2.0 ** -10, -2.0 ** -11, -1e-7]])
     x = x.astype(np.float32)
     got = F.e4m3_round(x)
     ref = brute_round(x)
-    gv, rv = F.e4m3_decode(got), F.e4m3_decode(ref)
-    assert np.array_equal(gv, rv), x[gv != rv][:10]
+    assert np.array_equal(got, ref), (x[got != ref][:10], got[got != ref][:10], ref[got != ref][:10])
 
 
 def test_quantize_round_trip_bound():
