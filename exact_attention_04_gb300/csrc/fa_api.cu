@@ -101,6 +101,25 @@ bool make_map(CUtensorMap* m, const void* base, int d, int N, int BH, int box_ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Byte tensor (E4M3) [depth, rows, inner] as 3-D (inner, rows, depth): box of
+// box_inner bytes x box_rows rows, 128-byte swizzle, out-of-range reads zero.
+bool make_map_u8(CUtensorMap* m, const void* base, int inner, int rows, int depth, int box_inner,
+                 int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(depth)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner),
+                                 static_cast<cuuint64_t>(inner) * rows};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner),
+                             static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Transposed fp32 accumulator [BH, d, Npad] as a 3-D tensor (Npad, d, BH):
 // box of 32 queries (128 bytes) x 128 head-dimension rows, 128-byte swizzle
 // (the target of bulk reduce-adds).
@@ -464,6 +483,79 @@ fa_status_t fa_decode(const void* q, const void* k, const void* v, void* o, floa
   if (fa::launch_decode(p, d, di->num_sms, di->max_smem, s) != cudaSuccess) return FA_ERR_CUDA;
   if (fa::launch_decode_combine(p, d, o, lse, s) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
+}
+
+fa_status_t fa_fp8_quantize(const void* q, const void* k, const void* v, int B, int H, int N,
+                            int d, const fa_variant_t* variant, void* q8, float* q_scale,
+                            void* k8, float* k_scale, void* v8t, float* v_scale, void* stream) {
+  if (!q || !k || !v || !q8 || !q_scale || !k8 || !k_scale || !v8t || !v_scale)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q8) || !aligned16(k8) ||
+      !aligned16(v8t) || (reinterpret_cast<uintptr_t>(q_scale) & 3u) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return FA_ERR_INVALID_ARG;
+  const fa_status_t sz = check_sizes(B, H, N, d, 1.f);
+  if (sz != FA_OK) return sz;
+  if (d == 64) return FA_ERR_UNSUPPORTED;
+  Variant var;
+  const fa_status_t vs = resolve_variant(variant, H, 0, &var);
+  if (vs != FA_OK) return vs;
+  DeviceInfo* di = device_info(nullptr);
+  if (!di || di->err != cudaSuccess) return FA_ERR_CUDA;
+  if (!di->supported) return FA_ERR_UNSUPPORTED;
+  fa::Fp8QuantArgs a{q, k, v, B, H, var.H_kv, N, q8, q_scale, k8, k_scale, v8t, v_scale};
+  return fa::launch_fp8_quantize(a, d, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
+}
+
+fa_status_t fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8,
+                       const float* k_scale, const void* v8t, const float* v_scale, void* o,
+                       float* lse, int B, int H, int N, int d, float scale, int causal,
+                       const int* kv_len, const fa_variant_t* variant, void* stream) {
+  if (!q8 || !q_scale || !k8 || !k_scale || !v8t || !v_scale || !o || !lse)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8t) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(q_scale) & 3u) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return FA_ERR_INVALID_ARG;
+  if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+  const fa_status_t sz = check_sizes(B, H, N, d, scale);
+  if (sz != FA_OK) return sz;
+  if (d == 64) return FA_ERR_UNSUPPORTED;
+  Variant var;
+  const fa_status_t vs = resolve_variant(variant, H, causal, &var);
+  if (vs != FA_OK) return vs;
+  DeviceInfo* di = device_info(nullptr);
+  if (!di || di->err != cudaSuccess) return FA_ERR_CUDA;
+  if (!di->supported) return FA_ERR_UNSUPPORTED;
+  fa::FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int nb = (N + 127) / 128;
+  if (!make_map_u8(&p.tq, q8, d, N, B * H, 128, 128) ||
+      !make_map_u8(&p.tk, k8, d, N, B * var.H_kv, 128, 128) ||
+      !make_map_u8(&p.tv, v8t, nb * 128, d, B * var.H_kv, 128, d))
+    return FA_ERR_CUDA;
+  p.o = o;
+  p.lse = lse;
+  p.kv_len = kv_len;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.H_kv = var.H_kv;
+  p.wl = var.wl;
+  p.wr = var.wr;
+  p.causal = var.pair ? 1 : 0;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.status = di->status;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.nb = nb;
+  return fa::launch_fwd_fp8(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FA_OK
+             : FA_ERR_CUDA;
 }
 
 fa_status_t fa_selftest_wait_timeout(unsigned int timeout_us, void* stream) {

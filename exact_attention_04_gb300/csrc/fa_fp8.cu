@@ -1,0 +1,195 @@
+// E4M3 quantisation of Q, K and V for the FP8 forward.
+//
+// "4. FlashAttention 深度剖析" 4.5.4: FP8 (E4M3) operands for the forward
+// pass, a scale per block applied when the block is loaded, FP32
+// accumulation.  The scales here: Q per 128-row tile of a head, K per
+// 128-key block of a K/V head, V per K/V head (so the P V sum is scaled once
+// at the end).  For a block with largest magnitude amax the stored value is
+// E4M3(x * (448 / amax)), rounded to nearest even and saturated, and the
+// dequantisation scale is amax / 448 (both quotients and the product rounded
+// to fp32); an all-zero block has scale 1.  V is written transposed per head,
+// [d, keys] with the keys padded to a multiple of 128, so that a V block is
+// the K-major B operand of the P V product.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kRowsPerBlock = 128;
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float block_max(float m) {
+  __shared__ float red[kThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < kThreads / 32 ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  }
+  return m;   // valid in thread 0
+}
+
+__device__ __forceinline__ void unpack8(uint4 u, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+// Largest |x| of each 128-row block of G heads ([G, N, D] bf16): written to
+// out[g * nb + b], or (PER_HEAD) folded into out[g] with an integer max on
+// the bit patterns, which orders non-negative floats correctly.
+template <int D, bool PER_HEAD>
+__global__ void __launch_bounds__(kThreads) amax_kernel(const __nv_bfloat16* x, int N, int nb,
+                                                        float* out) {
+  const int blk = blockIdx.x;
+  const int g = blk / nb, b = blk % nb;
+  const int r0 = b * kRowsPerBlock;
+  const int r1 = r0 + kRowsPerBlock < N ? r0 + kRowsPerBlock : N;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (static_cast<size_t>(g) * N + r0) * D);
+  const int n8 = (r1 - r0) * (D / 8);
+  float m = 0.f;
+  for (int i = threadIdx.x; i < n8; i += kThreads) {
+    float f[8];
+    unpack8(src[i], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
+  }
+  m = block_max(m);
+  if (threadIdx.x == 0) {
+    if (PER_HEAD)
+      atomicMax(reinterpret_cast<int*>(out + g), __float_as_int(m));
+    else
+      out[blk] = m;
+  }
+}
+
+__device__ __forceinline__ void scale_of(float amax, float& s, float& mul) {
+  s = 1.f;
+  mul = 1.f;
+  if (amax > 0.f) {
+    s = __fdiv_rn(amax, 448.f);
+    mul = __fdiv_rn(448.f, amax);
+  }
+}
+
+// Rows of each 128-row block to E4M3; io holds the block's amax on entry and
+// its dequantisation scale on exit.
+template <int D>
+__global__ void __launch_bounds__(kThreads) quant_rows_kernel(const __nv_bfloat16* x, int N,
+                                                              int nb, float* io,
+                                                              uint8_t* codes) {
+  const int blk = blockIdx.x;
+  const int g = blk / nb, b = blk % nb;
+  float s, mul;
+  scale_of(io[blk], s, mul);
+  __syncthreads();                       // every thread has read the amax
+  if (threadIdx.x == 0) io[blk] = s;
+  const int r0 = b * kRowsPerBlock;
+  const int r1 = r0 + kRowsPerBlock < N ? r0 + kRowsPerBlock : N;
+  const size_t off = (static_cast<size_t>(g) * N + r0) * D;
+  const uint4* src = reinterpret_cast<const uint4*>(x + off);
+  uint2* dst = reinterpret_cast<uint2*>(codes + off);
+  const int n8 = (r1 - r0) * (D / 8);
+  for (int i = threadIdx.x; i < n8; i += kThreads) {
+    float f[8];
+    unpack8(src[i], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = __fmul_rn(f[e], mul);
+    dst[i] = make_uint2(ptx::pack_e4m3x4(f[0], f[1], f[2], f[3]),
+                        ptx::pack_e4m3x4(f[4], f[5], f[6], f[7]));
+  }
+}
+
+// One 128-key block of V to E4M3, transposed: vt[(g*D + c) * npad + key].
+template <int D>
+__global__ void __launch_bounds__(kThreads) quant_vt_kernel(const __nv_bfloat16* v, int N,
+                                                            int npad, int nb,
+                                                            const float* head_amax,
+                                                            uint8_t* vt) {
+  __shared__ __align__(16) uint8_t tile[D][kRowsPerBlock + 16];
+  const int blk = blockIdx.x;
+  const int g = blk / nb, b = blk % nb;
+  float s, mul;
+  scale_of(head_amax[g], s, mul);
+  for (int it = threadIdx.x; it < kRowsPerBlock * (D / 8); it += kThreads) {
+    const int k = it / (D / 8), c8 = it % (D / 8);
+    const int key = b * kRowsPerBlock + k;
+    float f[8];
+    if (key < N) {
+      unpack8(*reinterpret_cast<const uint4*>(v + (static_cast<size_t>(g) * N + key) * D + c8 * 8), f);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = __fmul_rn(f[e], mul);
+    const uint32_t lo = ptx::pack_e4m3x4(f[0], f[1], f[2], f[3]);
+    const uint32_t hi = ptx::pack_e4m3x4(f[4], f[5], f[6], f[7]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      tile[c8 * 8 + e][k] = static_cast<uint8_t>(lo >> (8 * e));
+      tile[c8 * 8 + 4 + e][k] = static_cast<uint8_t>(hi >> (8 * e));
+    }
+  }
+  __syncthreads();
+  for (int it = threadIdx.x; it < D * (kRowsPerBlock / 16); it += kThreads) {
+    const int c = it / (kRowsPerBlock / 16), k16 = it % (kRowsPerBlock / 16);
+    *reinterpret_cast<uint4*>(vt + (static_cast<size_t>(g) * D + c) * npad + b * kRowsPerBlock +
+                              16 * k16) = *reinterpret_cast<const uint4*>(&tile[c][16 * k16]);
+  }
+}
+
+// amax -> dequantisation scale, one value per head.
+__global__ void head_scale_kernel(float* io, int G) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= G) return;
+  float s, mul;
+  scale_of(io[g], s, mul);
+  io[g] = s;
+}
+
+template <int D>
+cudaError_t quantize(const Fp8QuantArgs& a, cudaStream_t st) {
+  const int nb = (a.N + kRowsPerBlock - 1) / kRowsPerBlock;
+  const int npad = nb * kRowsPerBlock;
+  const int gq = a.B * a.H, gk = a.B * a.H_kv;
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
+  amax_kernel<D, false><<<gq * nb, kThreads, 0, st>>>(q, a.N, nb, a.q_scale);
+  amax_kernel<D, false><<<gk * nb, kThreads, 0, st>>>(k, a.N, nb, a.k_scale);
+  cudaError_t e = cudaMemsetAsync(a.v_scale, 0, sizeof(float) * gk, st);
+  if (e != cudaSuccess) return e;
+  amax_kernel<D, true><<<gk * nb, kThreads, 0, st>>>(v, a.N, nb, a.v_scale);
+  quant_rows_kernel<D><<<gq * nb, kThreads, 0, st>>>(q, a.N, nb, a.q_scale,
+                                                     static_cast<uint8_t*>(a.q8));
+  quant_rows_kernel<D><<<gk * nb, kThreads, 0, st>>>(k, a.N, nb, a.k_scale,
+                                                     static_cast<uint8_t*>(a.k8));
+  quant_vt_kernel<D><<<gk * nb, kThreads, 0, st>>>(v, a.N, npad, nb, a.v_scale,
+                                                   static_cast<uint8_t*>(a.v8t));
+  head_scale_kernel<<<(gk + 127) / 128, 128, 0, st>>>(a.v_scale, gk);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, int d, cudaStream_t stream) {
+  switch (d) {
+    case 128: return quantize<128>(a, stream);
+    case 256: return quantize<256>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

@@ -53,11 +53,18 @@ constexpr int CHUNK = 128 * 128; // bytes of one 128-row x 64-column bf16 chunk 
 constexpr float kRescaleSlack = 8.0f;
 constexpr int kThreads = 224;
 
-template <int D>
+// FP8 = true: E4M3 Q and K (one byte an element, so a 128-byte swizzle row
+// holds 128 of them) and V transposed per K/V head ([d, keys]: a V block is d
+// rows of 128 keys, the K-major B operand of P V).
+template <int D, bool FP8 = false>
 struct Cfg {
-  static constexpr int NCH = D / 64;                 // 128-byte column chunks per row
-  static constexpr int TILE_BYTES = NCH * CHUNK;     // one Q tile or one K/V block
-  static constexpr int STAGES = D == 64 ? 4 : (D == 128 ? 3 : 1);
+  static_assert(!FP8 || D >= 128, "E4M3 rows need at least 128 bytes");
+  static constexpr int BOX_COLS = FP8 ? 128 : 64;    // elements in one 128-byte swizzle row
+  static constexpr int NCH = D / BOX_COLS;           // 128-byte column chunks per row
+  static constexpr int TILE_BYTES = NCH * CHUNK;     // one Q tile or one K block
+  static constexpr int V_BYTES = FP8 ? D * 128 : TILE_BYTES;
+  static constexpr int STAGES =
+      FP8 ? (D == 128 ? 6 : 3) : (D == 64 ? 4 : (D == 128 ? 3 : 1));
   // NSB S buffers: block g uses columns [128*(g%NSB), +128); its P (packed
   // bf16 pairs) is written over the first 64 of those columns.  Three
   // buffers where O leaves room (d <= 128), two for d = 256.
@@ -68,17 +75,18 @@ struct Cfg {
   static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
 };
 
-template <int D>
+template <int D, bool FP8 = false>
 struct FwdSmem {
-  alignas(1024) uint8_t q[Cfg<D>::TILE_BYTES];
-  alignas(1024) uint8_t k[Cfg<D>::STAGES][Cfg<D>::TILE_BYTES];
-  alignas(1024) uint8_t v[Cfg<D>::STAGES][Cfg<D>::TILE_BYTES];
+  using C = Cfg<D, FP8>;
+  alignas(1024) uint8_t q[C::TILE_BYTES];
+  alignas(1024) uint8_t k[C::STAGES][C::TILE_BYTES];
+  alignas(1024) uint8_t v[C::STAGES][C::V_BYTES];
   uint64_t q_full, q_empty;
-  uint64_t k_full[Cfg<D>::STAGES], k_empty[Cfg<D>::STAGES];
-  uint64_t v_full[Cfg<D>::STAGES], v_empty[Cfg<D>::STAGES];
-  uint64_t s_full[Cfg<D>::NSB];   // S of block g is in buffer g % NSB
-  uint64_t p_full[Cfg<D>::NSB];   // softmax is done with S buffer b and wrote its P
-  uint64_t pv_done[Cfg<D>::NSB];  // O += P V of block g (buffer g % NSB) has completed
+  uint64_t k_full[C::STAGES], k_empty[C::STAGES];
+  uint64_t v_full[C::STAGES], v_empty[C::STAGES];
+  uint64_t s_full[C::NSB];   // S of block g is in buffer g % NSB
+  uint64_t p_full[C::NSB];   // softmax is done with S buffer b and wrote its P
+  uint64_t pv_done[C::NSB];  // O += P V of block g (buffer g % NSB) has completed
   uint64_t o_free;
   uint64_t mma_done, pv_mma_done;
   uint32_t tmem_base;
@@ -161,6 +169,7 @@ struct Tile {
   int jlo, nkv;        // key blocks [jlo, jlo + nkv)
   long long out0;      // output row of tile row 0
   int rows;            // rows of the tile that are real queries
+  int qs;              // index of the tile's Q scale (FP8)
 };
 
 template <bool DEC>
@@ -178,6 +187,7 @@ __device__ __forceinline__ void make_tile(const FwdParams& p, const Sched& sched
     t.nkv = tile_blocks(p, m, t.len, t.jlo);
     t.out0 = static_cast<long long>(bh) * p.N + m * BM;
     t.rows = p.N - m * BM < BM ? p.N - m * BM : BM;
+    t.qs = bh * p.nb + m;
   } else {
     const int kvbh = u / p.splits, split = u % p.splits;
     const int row0 = q_head_of(kvbh, 0, p.H, p.H_kv) * p.Nq;
@@ -196,6 +206,7 @@ __device__ __forceinline__ void make_tile(const FwdParams& p, const Sched& sched
     t.nkv = k_hi > k_lo ? (k_hi + BN - 1) / BN - t.jlo : 0;
     t.out0 = static_cast<long long>(split) * p.B * p.H * p.Nq + row0;
     t.rows = (p.H / p.H_kv) * p.Nq;
+    t.qs = 0;
   }
 }
 
@@ -205,17 +216,19 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, bool DEC>
+template <int D, bool DEC, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using C = Cfg<D>;
+  static_assert(!(DEC && FP8), "decode runs in bf16");
+  using C = Cfg<D, FP8>;
+  using Smem = FwdSmem<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
   const uintptr_t aligned = (raw + 1023) & ~static_cast<uintptr_t>(1023);
-  if (aligned - raw + sizeof(FwdSmem<D>) > dynamic_smem_size()) {
+  if (aligned - raw + sizeof(Smem) > dynamic_smem_size()) {
     if (threadIdx.x == 0) atomicCAS(p.status, 0, status_code(kSiteSmemLayout));
     return;
   }
-  FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(aligned);
+  Smem& sm = *reinterpret_cast<Smem*>(aligned);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   volatile int* abort = &sm.abort;
@@ -275,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           mbar_arrive_expect_tx(&sm.q_full, C::TILE_BYTES);
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(sm.q + c * CHUNK, &p.tq, &sm.q_full, 64 * c, t.qy, t.qz);
+            tma_load_3d(sm.q + c * CHUNK, &p.tq, &sm.q_full, C::BOX_COLS * c, t.qy, t.qz);
           ++q_it;
           for (int j = 0; j < nkv; ++j) {
             const int st = k_it % C::STAGES;
@@ -288,17 +301,23 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             mbar_arrive_expect_tx(&sm.k_full[st], C::TILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c)
-              tma_load_3d(sm.k[st] + c * CHUNK, &p.tk, &sm.k_full[st], 64 * c, (jlo + j) * BN, kvbh);
+              tma_load_3d(sm.k[st] + c * CHUNK, &p.tk, &sm.k_full[st], C::BOX_COLS * c, (jlo + j) * BN,
+                          kvbh);
             ++k_it;
             if (!mbar_wait(&sm.v_empty[st], ph ^ 1, abort, kWaitTimeoutNs)) {
               record_failure(p.status, abort, kSiteProdV);
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&sm.v_full[st], C::TILE_BYTES);
+            mbar_arrive_expect_tx(&sm.v_full[st], C::V_BYTES);
+            if constexpr (FP8) {
+              // transposed V: one box of D rows x 128 keys
+              tma_load_3d(sm.v[st], &p.tv, &sm.v_full[st], (jlo + j) * BN, 0, kvbh);
+            } else {
 #pragma unroll
-            for (int c = 0; c < C::NCH; ++c)
-              tma_load_3d(sm.v[st] + c * CHUNK, &p.tv, &sm.v_full[st], 64 * c, (jlo + j) * BN, kvbh);
+              for (int c = 0; c < C::NCH; ++c)
+                tma_load_3d(sm.v[st] + c * CHUNK, &p.tv, &sm.v_full[st], 64 * c, (jlo + j) * BN, kvbh);
+            }
             ++v_it;
           }
         }
@@ -325,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   } else if (warp == 1) {
     // ------------------------------------------------------------ S issuer
     {
-      constexpr uint32_t kIdescS = idesc_bf16_f32(BM, BN, 0, 0);
+      constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(BM, BN, 0, 0) : idesc_bf16_f32(BM, BN, 0, 0);
       const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q), 16, 1024);
       uint32_t q_it = 0, g = 0;
       bool ok = true;
@@ -358,11 +377,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             }
             tc_fence_after_sync();
             const uint64_t dk0 = sdesc_sw128(smem_u32(sm.k[st]), 16, 1024);
+            // one K step is 32 bytes of a row: 16 bf16 or 32 E4M3 values
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < C::NCH * 4; ++kk) {
               const uint32_t off = (kk / 4) * CHUNK + (kk % 4) * 32;
-              mma_bf16_ss_w(tmem + C::TM_S + 128 * b, dq0 + (off >> 4), dk0 + (off >> 4), kIdescS,
-                          kk > 0 ? 1u : 0u);
+              if constexpr (FP8)
+                mma_e4m3_ss_w(tmem + C::TM_S + 128 * b, dq0 + (off >> 4), dk0 + (off >> 4), kIdescS,
+                              kk > 0 ? 1u : 0u);
+              else
+                mma_bf16_ss_w(tmem + C::TM_S + 128 * b, dq0 + (off >> 4), dk0 + (off >> 4), kIdescS,
+                              kk > 0 ? 1u : 0u);
             }
             mma_commit_w(&sm.k_empty[st]);
             mma_commit_w(&sm.s_full[b]);
@@ -379,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   } else if (warp == 2) {
     // ------------------------------------------------------------ P V issuer
     {
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(BM, D, 0, 1);
+      constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3_f32(BM, D, 0, 0) : idesc_bf16_f32(BM, D, 0, 1);
       uint32_t g = 0, t_it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
@@ -409,14 +433,25 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               break;
             }
             tc_fence_after_sync();
-            // V block: BN rows (keys) x D columns, MN-major B operand: 64-column
-            // chunks BN*128 bytes apart (LBO), 8-key groups 1024 bytes apart (SBO).
-            const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), BN * 128, 1024);
+            if constexpr (FP8) {
+              // transposed V block: D rows x 128 keys, the K-major B operand;
+              // P as E4M3, four keys a tensor-memory column, 32 keys a step
+              const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), 16, 1024);
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              mma_bf16_ts_w(tmem + C::TM_O, tmem + C::TM_S + 128 * b + kk * 8,
-                          dv0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescPV,
-                          (j == 0 && kk == 0) ? 0u : 1u);
+              for (int kk = 0; kk < BN / 32; ++kk)
+                mma_e4m3_ts_w(tmem + C::TM_O, tmem + C::TM_S + 128 * b + kk * 8,
+                              dv0 + static_cast<uint64_t>((kk * 32) >> 4), kIdescPV,
+                              (j == 0 && kk == 0) ? 0u : 1u);
+            } else {
+              // V block: BN rows (keys) x D columns, MN-major B operand: 64-column
+              // chunks BN*128 bytes apart (LBO), 8-key groups 1024 bytes apart (SBO).
+              const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), BN * 128, 1024);
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk) {
+                mma_bf16_ts_w(tmem + C::TM_O, tmem + C::TM_S + 128 * b + kk * 8,
+                            dv0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescPV,
+                            (j == 0 && kk == 0) ? 0u : 1u);
+              }
             }
             mma_commit_w(&sm.v_empty[st]);
             mma_commit_w(&sm.pv_done[b]);
@@ -444,6 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         make_tile<DEC>(p, sched, u, kt, t);
         const int len = t.len, jlo = t.jlo, nkv = t.nkv;
         const int row = DEC ? t.qlo + row_local % p.Nq : t.qlo + row_local;   // query position
+        // FP8: scores come out of the MMA in units of sq * sk
+        const float q_sc = FP8 ? __ldg(p.q_scale + t.qs) : 1.f;
         const bool row_valid = row_local < t.rows;
         const size_t row_off = static_cast<size_t>(t.out0 + row_local);
         if (nkv == 0) {
@@ -506,7 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           }
           mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
           mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
-          const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c2;
+          // this block's multiplier from MMA output to base-2 units of S*scale
+          const float cb = FP8 ? c2 * q_sc * __ldg(p.k_scale + t.kvbh * p.nb + jlo + j) : c2;
+          const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cb;
           float alpha = 1.f;
           bool rescale = false;
           if (m_ref == -INFINITY) {
@@ -514,7 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               alpha = 0.f;
               m_ref = m_blk;
             }
-          } else if (m_blk > m_ref + kRescaleSlack) {
+          } else if (m_blk > m_ref + (FP8 ? 0.f : kRescaleSlack)) {
+            // (FP8: no slack, so 256 P <= 256 stays inside E4M3's range)
             alpha = ex2_approx(m_ref - m_blk);
             m_ref = m_blk;
             rescale = true;
@@ -522,10 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           const float base = (m_ref == -INFINITY) ? 0.f : m_ref;
           // p = exp2(S*c - m) two lanes at a time: packed FMA for the argument,
           // packed adds for the row sum, one bf16x2 convert per pair
-          const uint64_t c2x2 = f2_make(c2, c2);
+          const uint64_t c2x2 = f2_make(cb, cb);
           const uint64_t nbx2 = f2_make(-base, -base);
           uint64_t rsa = f2_make(0.f, 0.f), rsb = f2_make(0.f, 0.f);
-          uint32_t pk[BN / 2];
+          uint32_t pk[FP8 ? BN / 4 : BN / 2];
 #pragma unroll
           for (int c = 0; c < BN / 2; c += 2) {
             float a0, a1, a2, a3;
@@ -535,16 +575,21 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             const float p2 = ex2_approx(a2), p3 = ex2_approx(a3);
             rsa = f2_add(rsa, f2_make(p0, p1));
             rsb = f2_add(rsb, f2_make(p2, p3));
-            pk[c] = pack_bf16x2(p0, p1);
-            pk[c + 1] = pack_bf16x2(p2, p3);
+            if constexpr (FP8) {
+              pk[c / 2] = pack_e4m3x4(256.f * p0, 256.f * p1, 256.f * p2, 256.f * p3);
+            } else {
+              pk[c] = pack_bf16x2(p0, p1);
+              pk[c + 1] = pack_bf16x2(p2, p3);
+            }
           }
           float rs0, rs1, rs2, rs3;
           f2_split(rsa, rs0, rs1);
           f2_split(rsb, rs2, rs3);
           l = l * alpha + ((rs0 + rs1) + (rs2 + rs3));
-          // P over the first 64 columns of this block's S buffer (S is in registers)
+          // P over the first columns of this block's S buffer (S is in registers):
+          // 64 columns of bf16 pairs, or 32 of E4M3 quads
           tmem_st_x32(t_s, pk);
-          tmem_st_x32(t_s + 32, pk + 32);
+          if constexpr (!FP8) tmem_st_x32(t_s + 32, pk + 32);
           if (__any_sync(0xffffffffu, rescale && j > 0)) {
             // O must hold every earlier P V before it is scaled: wait for the
             // previous block's P V to complete.
@@ -581,7 +626,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           break;
         }
         tc_fence_after_sync();
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        // FP8: P entered the product as 256 P and V in units of its head scale
+        const float inv_l =
+            l > 0.f ? (FP8 ? __ldg(p.v_scale + t.kvbh) / (256.f * l) : 1.f / l) : 0.f;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t orr[32];
@@ -633,10 +680,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   }
 }
 
-template <int D, bool DEC>
+template <int D, bool DEC, bool FP8 = false>
 cudaError_t launch(const FwdParams& p, int num_sms, int max_smem, cudaStream_t stream) {
-  const size_t smem = smem_request(sizeof(FwdSmem<D>), max_smem);
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, DEC>,
+  const size_t smem = smem_request(sizeof(FwdSmem<D, FP8>), max_smem);
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, DEC, FP8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -649,7 +696,7 @@ cudaError_t launch(const FwdParams& p, int num_sms, int max_smem, cudaStream_t s
                      : static_cast<long long>(p.B) * p.H * T;
   }
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  fa_fwd_kernel<D, DEC><<<grid, kThreads, smem, stream>>>(p);
+  fa_fwd_kernel<D, DEC, FP8><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -698,6 +745,15 @@ cudaError_t launch_fwd(const FwdParams& p, int d, int num_sms, int max_smem, cud
     case 64: return launch<64, false>(p, num_sms, max_smem, stream);
     case 128: return launch<128, false>(p, num_sms, max_smem, stream);
     case 256: return launch<256, false>(p, num_sms, max_smem, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_fwd_fp8(const FwdParams& p, int d, int num_sms, int max_smem,
+                           cudaStream_t stream) {
+  switch (d) {
+    case 128: return launch<128, false, true>(p, num_sms, max_smem, stream);
+    case 256: return launch<256, false, true>(p, num_sms, max_smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -33,6 +33,11 @@ struct FwdParams {
   int splits, chunk_blocks;    // key chunks per K/V head, key blocks per chunk
   float* o_part;               // fp32 [splits, B*H*Nq, d] partial outputs (normalised)
   float* lse_part;             // fp32 [splits, B*H*Nq] partial log-sum-exp (natural log)
+  // FP8 mode: E4M3 Q, K and transposed V with their dequantisation scales
+  const float* q_scale;        // [B*H, nb], one per 128-row tile
+  const float* k_scale;        // [B*H_kv, nb], one per 128-key block
+  const float* v_scale;        // [B*H_kv]
+  int nb;                      // ceil(N / 128)
 };
 
 struct BwdParams {
@@ -78,6 +83,22 @@ cudaError_t launch_bwd_post(const BwdParams& p, int d, cudaStream_t stream);
 // 64-query-step backward main kernel with dQ^T (head dimensions 128, 256);
 // its Q and dO tensor maps have a box of 64 rows.
 cudaError_t launch_wait_selftest(int* status, unsigned long long timeout_ns, cudaStream_t s);
+struct Fp8QuantArgs {
+  const void* q;               // bf16 [B*H, N, d]
+  const void* k;               // bf16 [B*H_kv, N, d]
+  const void* v;               // bf16 [B*H_kv, N, d]
+  int B, H, H_kv, N;
+  void* q8;                    // E4M3 [B*H, N, d]
+  float* q_scale;              // [B*H, nb]
+  void* k8;                    // E4M3 [B*H_kv, N, d]
+  float* k_scale;              // [B*H_kv, nb]
+  void* v8t;                   // E4M3 [B*H_kv, d, nb*128]
+  float* v_scale;              // [B*H_kv]
+};
+
+cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, int d, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const FwdParams& p, int d, int num_sms, int max_smem,
+                           cudaStream_t stream);
 cudaError_t launch_decode(const FwdParams& p, int d, int num_sms, int max_smem,
                           cudaStream_t stream);
 cudaError_t launch_decode_combine(const FwdParams& p, int d, void* o, float* lse,

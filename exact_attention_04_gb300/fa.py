@@ -74,6 +74,11 @@ def load():
         lib.fa_decode_workspace_bytes.restype = sz
         lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, varp, i, vp, sz, vp]
         lib.fa_decode.restype = i
+        fp = ctypes.POINTER(ctypes.c_float)
+        lib.fa_fp8_quantize.argtypes = [vp, vp, vp, i, i, i, i, varp, vp, vp, vp, vp, vp, vp, vp]
+        lib.fa_fp8_quantize.restype = i
+        lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp, varp, vp]
+        lib.fa_fwd_fp8.restype = i
         lib.fa_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
         lib.fa_selftest_wait_timeout.restype = i
         lib.fa_check.argtypes = [vp]
@@ -89,7 +94,7 @@ def load():
 EXPORTS = ("fa_fwd", "fa_bwd_workspace_bytes", "fa_bwd", "fa_bwd_prep", "fa_bwd_dkdv",
            "fa_bwd_dq", "fa_bwd_noalloc", "fa_fwd_v", "fa_bwd_v", "fa_bwd_dkdv_v",
            "fa_decode_splits", "fa_decode_workspace_bytes", "fa_decode",
-           "fa_selftest_wait_timeout", "fa_check",
+           "fa_fp8_quantize", "fa_fwd_fp8", "fa_selftest_wait_timeout", "fa_check",
            "fa_status_string", "fa_version")
 
 
@@ -341,6 +346,57 @@ def decode(q, k, v, scale=None, causal=False, kv_len=None, window=None, splits=N
     fa_decode(q, k, v, o, lse, default_scale(d) if scale is None else scale, causal, kv_len,
               window, splits, ws, stream)
     return o, lse
+
+
+def fp8_buffers(B, H, Hkv, N, d, device):
+    """Empty E4M3 buffers and scales in the layouts fa_fp8_quantize writes."""
+    nb = -(-N // 128)
+    u8 = dict(dtype=torch.uint8, device=device)
+    f32 = dict(dtype=torch.float32, device=device)
+    return {"q8": torch.empty(B, H, N, d, **u8), "q_scale": torch.empty(B, H, nb, **f32),
+            "k8": torch.empty(B, Hkv, N, d, **u8), "k_scale": torch.empty(B, Hkv, nb, **f32),
+            "v8t": torch.zeros(B, Hkv, d, nb * 128, **u8), "v_scale": torch.empty(B, Hkv, **f32)}
+
+
+def fa_fp8_quantize(q, k, v, buf, stream=None):
+    """Calls fa_fp8_quantize into buf (from fp8_buffers)."""
+    _check_qkv("q", q)
+    B, H, N, d = q.shape
+    var = _variant(q, k, None)
+    _check_qkv("k", k, k.shape)
+    _check_qkv("v", v, k.shape)
+    _raise(load().fa_fp8_quantize(_ptr(q), _ptr(k), _ptr(v), B, H, N, d, ctypes.byref(var),
+                                  _ptr(buf["q8"]), _ptr(buf["q_scale"]), _ptr(buf["k8"]),
+                                  _ptr(buf["k_scale"]), _ptr(buf["v8t"]), _ptr(buf["v_scale"]),
+                                  _stream_ptr(stream)), "fa_fp8_quantize")
+
+
+def fa_fwd_fp8(buf, o, lse, scale, causal=False, kv_len=None, window=None, stream=None):
+    """Calls fa_fwd_fp8 on E4M3 buffers (from fp8_buffers / fa_fp8_quantize)."""
+    B, H, N, d = buf["q8"].shape
+    Hkv = buf["k8"].shape[1]
+    _check_qkv("o", o, (B, H, N, d))
+    if lse.dtype != torch.float32 or not lse.is_cuda or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse: expected fp32 CUDA tensor [B,H,N]")
+    kv_len = _check_kv_len(kv_len, B)
+    wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    var = FaVariant(int(Hkv), wl, wr)
+    _raise(load().fa_fwd_fp8(_ptr(buf["q8"]), _ptr(buf["q_scale"]), _ptr(buf["k8"]),
+                             _ptr(buf["k_scale"]), _ptr(buf["v8t"]), _ptr(buf["v_scale"]),
+                             _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
+                             _ptr(kv_len), ctypes.byref(var), _stream_ptr(stream)), "fa_fwd_fp8")
+
+
+def forward_fp8(q, k, v, scale=None, causal=False, kv_len=None, window=None, stream=None):
+    """(O, LSE, E4M3 buffers): quantise bf16 Q, K, V and run the FP8 forward."""
+    B, H, N, d = q.shape
+    buf = fp8_buffers(B, H, k.shape[1], N, d, q.device)
+    fa_fp8_quantize(q, k, v, buf, stream)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fa_fwd_fp8(buf, o, lse, default_scale(d) if scale is None else scale, causal, kv_len, window,
+               stream)
+    return o, lse, buf
 
 
 def fa_selftest_wait_timeout(timeout_us, stream=None):

@@ -193,6 +193,37 @@ fa_status_t fa_decode(const void* q, const void* k, const void* v, void* o, floa
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * FP8 (E4M3) forward ("4. FlashAttention 深度剖析" 4.5.4: E4M3 operands for
+ * the forward, a scale per block applied at load, FP32 accumulation).
+ *
+ * Layouts, with nb = ceil(N / 128) and h_kv from the variant:
+ *   q8  E4M3 [B, H, N, d]        q_scale fp32 [B, H, nb]     (per 128-row tile)
+ *   k8  E4M3 [B, h_kv, N, d]     k_scale fp32 [B, h_kv, nb]  (per 128-key block)
+ *   v8t E4M3 [B, h_kv, d, nb*128] (V transposed, keys padded with zeros)
+ *                                v_scale fp32 [B, h_kv]      (per head)
+ * A stored value x8 stands for x8 * scale.  d = 128 or 256 (64:
+ * FA_ERR_UNSUPPORTED); E4M3 buffers 16-byte aligned.
+ *
+ * fa_fp8_quantize writes these from bf16 Q, K, V ([B,H,N,d], [B,h_kv,N,d]):
+ * scale = amax / 448 of the block (1 for an all-zero block) and
+ * x8 = E4M3(x * (448 / amax)), rounded to nearest even and saturated.
+ *
+ * fa_fwd_fp8 computes O (bf16 [B,H,N,d]) and LSE (fp32 [B,H,N]) from them:
+ * S = (q8 k8^T) * q_scale * k_scale * scale on the tensor core in FP32; the
+ * online softmax of fa_fwd over 128-key blocks, with the reference maximum
+ * raised at every new block maximum; P enters the P V product as E4M3(256 P)
+ * against v8t, the row sum adds the unrounded P; O = v_scale * (P V) /
+ * (256 * l).  causal, kv_len and the variant as for fa_fwd_v.
+ */
+fa_status_t fa_fp8_quantize(const void* q, const void* k, const void* v, int B, int H, int N,
+                            int d, const fa_variant_t* variant, void* q8, float* q_scale,
+                            void* k8, float* k_scale, void* v8t, float* v_scale, void* stream);
+fa_status_t fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8,
+                       const float* k_scale, const void* v8t, const float* v_scale, void* o,
+                       float* lse, int B, int H, int N, int d, float scale, int causal,
+                       const int* kv_len, const fa_variant_t* variant, void* stream);
+
+/*
  * Self-test of the bounded waits: enqueues one tiny kernel that waits on a
  * barrier nothing ever completes, with a limit of timeout_us microseconds
  * (1 .. 1000000) instead of the kernels' two seconds.  The wait gives up,

@@ -138,3 +138,31 @@ def test_variant_binding_checks_shapes(lib):
 def test_selftest_rejects_limits_out_of_range(lib):
     assert lib.fa_selftest_wait_timeout(0, None) == fa.FA_ERR_INVALID_ARG
     assert lib.fa_selftest_wait_timeout(2000000, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_fp8_argument_errors(lib):
+    """fa_fp8_quantize / fa_fwd_fp8: null or misaligned buffers, d = 64 (no
+    E4M3 kernel) and bad K/V head counts are refused before the device."""
+    ok = 0x1000
+
+    def quant(q8=ok, qs=ok, d=128, h_kv=1, H=2):
+        var = fa.FaVariant(h_kv, -1, -1)
+        return lib.fa_fp8_quantize(P(ok), P(ok), P(ok), 1, H, 128, d, ctypes.byref(var), P(q8),
+                                   P(qs), P(ok), P(ok), P(ok), P(ok), None)
+
+    def fwd8(v8t=ok, lse=ok, d=128, N=128, scale=0.125, h_kv=1, H=2):
+        var = fa.FaVariant(h_kv, -1, -1)
+        return lib.fa_fwd_fp8(P(ok), P(ok), P(ok), P(ok), P(v8t), P(ok), P(ok), P(lse), 1, H, N,
+                              d, scale, 1, None, ctypes.byref(var), None)
+    assert quant(q8=0) == fa.FA_ERR_INVALID_ARG
+    assert quant(q8=0x1008) == fa.FA_ERR_INVALID_ARG       # codes must be 16-byte aligned
+    assert quant(qs=0x1002) == fa.FA_ERR_INVALID_ARG       # scales must be 4-byte aligned
+    assert quant(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert quant(h_kv=3) == fa.FA_ERR_INVALID_ARG
+    assert fwd8(v8t=0) == fa.FA_ERR_INVALID_ARG
+    assert fwd8(lse=0x1001) == fa.FA_ERR_INVALID_ARG
+    assert fwd8(d=64) == fa.FA_ERR_UNSUPPORTED
+    assert fwd8(d=96) == fa.FA_ERR_UNSUPPORTED
+    assert fwd8(N=0) == fa.FA_ERR_INVALID_ARG
+    assert fwd8(scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert fwd8(h_kv=4) == fa.FA_ERR_INVALID_ARG
