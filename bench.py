@@ -60,6 +60,10 @@ def parse_args():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (small cases for profiling)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the E4M3 forward (quantiser + FP8 kernel) of the workload instead")
     return ap.parse_args()
 
 
@@ -250,6 +254,34 @@ class DecodeRunner:
         self.run()
 
 
+class Fp8Runner:
+    """The E4M3 forward (fa_fp8_quantize, then fa_fwd_fp8) for one workload."""
+
+    def __init__(self, w, inp, fa):
+        self.w, self.fa = w, fa
+        d = torch.device("cuda")
+        self.q, self.k, self.v = (inp[n].to(d) for n in ("q", "k", "v"))
+        self.kv = None if inp["kv_len"] is None else inp["kv_len"].to(d)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device=d)
+        self.buf = fa.fp8_buffers(w.B, w.H, w.kv_heads, w.N, w.d, d)
+        self.backward = False
+
+    def quant(self):
+        self.fa.fa_fp8_quantize(self.q, self.k, self.v, self.buf)
+
+    def fwd(self):
+        self.fa.fa_fwd_fp8(self.buf, self.o, self.lse, self.w.scale, self.w.causal, self.kv,
+                           self.w.window)
+
+    def phases(self):
+        return [("fp8_quantize", self.quant), ("fa_fwd_kernel", self.fwd)]
+
+    def step(self):
+        for _, f in self.phases():
+            f()
+
+
 def time_steps(runner, steps, flush=None):
     """Per-phase and per-step device times (ms) over `steps` timed steps."""
     phases = runner.phases()
@@ -284,10 +316,12 @@ def run_ours(args, dist):
     fa.load()
     torch.cuda.set_device(dist.local_rank)
     w = WORKLOADS[args.workload]
+    if args.batch:
+        w = dataclasses.replace(w, B=args.batch, name=f"{w.name}@B{args.batch}")
     if dist.rank:
         w = dataclasses.replace(w, seed=w.seed + 1000 * dist.rank)
-    inp = make_inputs(w)
-    r = Runner(w, inp, fa)
+    inp = make_inputs(w, with_grad_out=None if not args.fp8 else False)
+    r = Fp8Runner(w, inp, fa) if args.fp8 else Runner(w, inp, fa)
     flops_fwd = w.fwd_flops()
     flops_bwd = w.bwd_flops() if r.backward else 0.0
     flops_step = flops_fwd + flops_bwd
@@ -326,11 +360,13 @@ def run_ours(args, dist):
     kflops = {"fa_fwd_kernel": flops_fwd, bwd_kernel_names(w.d)[0]: flops_bwd}
     if kernel in kflops:
         achieved = kflops[kernel] / (per_phase[kernel] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"] * (2 if args.fp8 else 1)
         roof = {"kernel": kernel, "bound": "tensor", "achieved": round(achieved, 2),
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": committed_traffic(kernel, w.name),
-                "peak_source": f"{peak_src} bf16 dense, burst",
+                "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": None if args.fp8 else committed_traffic(kernel, w.name),
+                "peak_source": (f"{peak_src} bf16 dense, burst"
+                                + (" x 2 (nominal E4M3 : BF16 dense ratio)" if args.fp8 else "")),
                 "avg_launch_ms": round(per_phase[kernel], 4)}
     else:
         roof = {"kernel": kernel, "bound": "hbm", "achieved": None, "peak": peaks["hbm_gbs"],
@@ -342,10 +378,12 @@ def run_ours(args, dist):
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if args.fp8 else "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal, "pass": "fwd+bwd" if w.backward else "fwd",
+                   "causal": w.causal,
+                   "pass": "fwd (E4M3)" if args.fp8 else ("fwd+bwd" if w.backward else "fwd"),
                    "parallelism": f"replica x{dist.world} (weak scaling, no collective)",
                    "l2": "inputs larger than L2, no flush"},
         "fwd_tflops": round(flops_fwd / (per_phase["fa_fwd_kernel"] * 1e-3) / 1e12, 2),
@@ -363,7 +401,7 @@ def run_ours(args, dist):
     torch.cuda.empty_cache()
     if not args.no_sweep:
         result["sweep"] = run_sweep(fa, peaks)
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and not args.fp8:
         result["cpu_baseline"] = cpu_baseline(w, inp)
     return result
 
@@ -409,6 +447,10 @@ def run_sweep(fa, peaks):
     cache = {}
     for name, w in WORKLOADS.items():
         if name == HEADLINE:
+            inp = make_inputs(w, with_grad_out=False)
+            out.append({"workload": name, "N": w.N, "d": w.d, "causal": w.causal,
+                        "fp8": sweep_fp8(w, inp, fa, peaks, flush_buf)})
+            del inp
             continue
         key = (w.B, w.H, w.kv_heads, w.queries, w.N, w.d, w.seed, w.qk_gain, w.kv_len_range,
                w.backward)
@@ -447,10 +489,38 @@ def run_sweep(fa, peaks):
                           "bwd_gbs": round(bwd_bytes / (bwd_ms * 1e-3) / 1e9, 1)})
         if w.backward and not r.backward:
             entry["bwd"] = "not built for this head dimension"
-        out.append(entry)
         del r
         torch.cuda.empty_cache()
+        if w.d in (128, 256):
+            entry["fp8"] = sweep_fp8(w, inp, fa, peaks, flush_buf)
+        out.append(entry)
     return out
+
+
+def sweep_fp8(w, inp, fa, peaks, flush_buf):
+    """The E4M3 forward of a workload: the quantiser (HBM-bound: reads Q, K, V
+    in bf16, writes them in E4M3) and the FP8 attention kernel, whose FLOPs
+    are the bf16 forward's, against an E4M3 peak of twice the measured bf16
+    one (the nominal dense ratio, 4.5 / 2.25 PFLOP/s)."""
+    r = Fp8Runner(w, inp, fa)
+    for _ in range(3):
+        r.step()
+    torch.cuda.synchronize()
+    per_phase, _ = time_steps(r, 10, flush=lambda: flush_l2(flush_buf))
+    fa.fa_check()
+    qb = w.B * w.H * w.N * w.d
+    kb = w.B * w.kv_heads * w.N * w.d
+    qbytes = 3 * qb + 6 * kb                  # bf16 read (2 B) + E4M3 write (1 B) per element
+    fwd_ms, q_ms = per_phase["fa_fwd_kernel"], per_phase["fp8_quantize"]
+    tfl = w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
+    peak = 2 * peaks["bf16_tflops"]
+    del r
+    torch.cuda.empty_cache()
+    return {"fwd_ms": round(fwd_ms, 4), "fwd_tflops": round(tfl, 2),
+            "fwd_frac_of_peak": round(tfl / peak, 4), "peak_tflops": round(peak, 1),
+            "peak": "2 x measured bf16 burst (nominal E4M3 : BF16 dense ratio)",
+            "quantize_ms": round(q_ms, 4),
+            "quantize_gbs": round(qbytes / (q_ms * 1e-3) / 1e9, 1)}
 
 
 def sweep_decode(w, inp, fa, peaks, flush_buf):

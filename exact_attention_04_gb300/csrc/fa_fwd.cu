@@ -559,7 +559,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             m_ref = m_blk;
             rescale = true;
           }
-          const float base = (m_ref == -INFINITY) ? 0.f : m_ref;
+          // FP8 takes 256 p, the E4M3 operand, straight from the exponent
+          // (exp2(x + 8) = 256 exp2(x)); its row sum l is then 256 times the
+          // sum of p, and the epilogue divides the 256 back out.
+          const float base = ((m_ref == -INFINITY) ? 0.f : m_ref) - (FP8 ? 8.f : 0.f);
           // p = exp2(S*c - m) two lanes at a time: packed FMA for the argument,
           // packed adds for the row sum, one bf16x2 convert per pair
           const uint64_t c2x2 = f2_make(cb, cb);
@@ -576,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             rsa = f2_add(rsa, f2_make(p0, p1));
             rsb = f2_add(rsb, f2_make(p2, p3));
             if constexpr (FP8) {
-              pk[c / 2] = pack_e4m3x4(256.f * p0, 256.f * p1, 256.f * p2, 256.f * p3);
+              pk[c / 2] = pack_e4m3x4(p0, p1, p2, p3);
             } else {
               pk[c] = pack_bf16x2(p0, p1);
               pk[c + 1] = pack_bf16x2(p2, p3);
@@ -600,15 +603,27 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               break;
             }
             tc_fence_after_sync();
+            // up to 128 columns of O per round trip (S is no longer live),
+            // scaled two at a time
+            constexpr int RC = D < 128 ? D / 32 : 4;
+            const uint64_t a2 = f2_make(alpha, alpha);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t orr[32];
-              tmem_ld_x32(t_lane + C::TM_O + 32 * c, orr);
-              tmem_wait_ld();
-              reg_fence<32>(orr);
+            for (int c0 = 0; c0 < D / 32; c0 += RC) {
+              uint32_t orr[RC * 32];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-              tmem_st_x32(t_lane + C::TM_O + 32 * c, orr);
+              for (int c = 0; c < RC; ++c) tmem_ld_x32(t_lane + C::TM_O + 32 * (c0 + c), orr + 32 * c);
+              tmem_wait_ld();
+              reg_fence<RC * 32>(orr);
+#pragma unroll
+              for (int i = 0; i < RC * 16; ++i) {
+                float lo, hi;
+                f2_split(f2_mul(f2_make(__uint_as_float(orr[2 * i]), __uint_as_float(orr[2 * i + 1])), a2),
+                         lo, hi);
+                orr[2 * i] = __float_as_uint(lo);
+                orr[2 * i + 1] = __float_as_uint(hi);
+              }
+#pragma unroll
+              for (int c = 0; c < RC; ++c) tmem_st_x32(t_lane + C::TM_O + 32 * (c0 + c), orr + 32 * c);
             }
           }
           tmem_wait_st();
@@ -626,9 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           break;
         }
         tc_fence_after_sync();
-        // FP8: P entered the product as 256 P and V in units of its head scale
-        const float inv_l =
-            l > 0.f ? (FP8 ? __ldg(p.v_scale + t.kvbh) / (256.f * l) : 1.f / l) : 0.f;
+        // FP8: P entered the product as 256 P (and l sums 256 P), V in units
+        // of its head scale
+        const float inv_l = l > 0.f ? (FP8 ? __ldg(p.v_scale + t.kvbh) / l : 1.f / l) : 0.f;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t orr[32];
@@ -662,7 +677,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.o_free);
         if (row_valid) {
-          const float lse_row = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+          const float lse_row =
+              l > 0.f ? (m_ref + (log2f(l) - (FP8 ? 8.f : 0.f))) * 0.69314718055994531f : -INFINITY;
           if constexpr (DEC)
             p.lse_part[row_off] = lse_row;
           else

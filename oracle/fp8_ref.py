@@ -117,12 +117,17 @@ def quantize_v_transposed(v):
 
 
 def attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=False, kv_len=None, H_kv=None,
-                  rows=None):
+                  rows=None, window=None):
     """O [B,H,N,d] and LSE [B,H,N] of the FP8 forward, step by step.
 
     q8 [B,H,N,d] codes with sq [B,H,ceil(N/128)]; k8 [B,H_kv,N,d] with
     sk [B,H_kv,ceil(N/128)]; v8t [B,H_kv,d,Npad] with sv [B,H_kv].  rows: a
-    list of query rows to compute (the others are left 0 / -inf)."""
+    list of query rows to compute (the others are left 0 / -inf).  window:
+    (left, right), query i sees keys i-left..i+right (-1: unbounded side),
+    the same visibility rule as the bf16 oracle; causal caps right at 0."""
+    wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
+    if causal:
+        wr = 0
     B, H, N, d = q8.shape
     Hkv = k8.shape[1] if H_kv is None else H_kv
     G = H // Hkv
@@ -143,10 +148,11 @@ def attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=False, kv_len=None, H_k
                 sqi = float(sq[b, h, i // BLOCK])
                 for j in range(nb):
                     k0, k1 = j * BLOCK, min((j + 1) * BLOCK, N)
-                    hi = min(k1, ln, i + 1 if causal else k1)
-                    if hi <= k0:
+                    lo = k0 if wl < 0 else max(k0, i - wl)
+                    hi = min(k1, ln, k1 if wr < 0 else i + wr + 1)
+                    if hi <= lo:
                         continue
-                    s = (K[b, hk, k0:hi] @ Q[b, h, i]) * (sqi * float(sk[b, hk, j])) * scale
+                    s = (K[b, hk, lo:hi] @ Q[b, h, i]) * (sqi * float(sk[b, hk, j])) * scale
                     mb = s.max()
                     if mb > m:                         # raise the reference to the new max
                         if m > -np.inf:
@@ -157,7 +163,7 @@ def attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=False, kv_len=None, H_k
                     p = np.exp(s - m)
                     p8 = e4m3_decode(e4m3_round((p * 256.0).astype(np.float32)))
                     l += p.sum()
-                    acc += V[b, hk, :, k0:hi] @ p8
+                    acc += V[b, hk, :, lo:hi] @ p8
                 if l > 0:
                     O[b, h, i] = float(sv[b, hk]) * acc / (256.0 * l)
                     LSE[b, h, i] = m + np.log(l)

@@ -67,24 +67,29 @@ def test_quantizer_is_bit_exact(B, H, Hkv, N, d):
 
 
 CASES = [
-    # B, H, H_kv, N, d, causal, kv_len range
-    (2, 2, 2, 300, 128, False, None),
-    (1, 4, 2, 520, 128, True, None),
-    (2, 2, 1, 257, 256, True, (100, 257)),
-    (1, 2, 2, 384, 256, False, None),
-    (2, 3, 3, 129, 128, True, (1, 129)),
+    # B, H, H_kv, N, d, causal, kv_len range, window
+    (2, 2, 2, 300, 128, False, None, None),
+    (1, 4, 2, 520, 128, True, None, None),
+    (2, 2, 1, 257, 256, True, (100, 257), None),
+    (1, 2, 2, 384, 256, False, None, None),
+    (2, 3, 3, 129, 128, True, (1, 129), None),
+    (1, 4, 1, 700, 128, True, None, (255, 0)),            # causal sliding window, MQA
+    (2, 2, 2, 600, 128, False, (300, 600), (100, 200)),   # two-sided window, ragged lengths
+    (1, 2, 1, 400, 256, True, None, (0, 0)),              # each query sees only its own key
 ]
 
 
-@pytest.mark.parametrize("B,H,Hkv,N,d,causal,kv", CASES)
-def test_fp8_forward_against_oracle(B, H, Hkv, N, d, causal, kv):
-    w = random_case(B, H, N, d, seed=3 * N + d, causal=causal, kv_len_range=kv, h_kv=Hkv)
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal,kv,window", CASES)
+def test_fp8_forward_against_oracle(B, H, Hkv, N, d, causal, kv, window):
+    w = random_case(B, H, N, d, seed=3 * N + d, causal=causal, kv_len_range=kv, h_kv=Hkv,
+                    window=window)
     inp = make_inputs(w, with_grad_out=False)
     o, lse, _ = run(w, inp)
     r = oracle_quantize(inp)
     kvn = None if inp["kv_len"] is None else inp["kv_len"].numpy()
     o_ref, lse_ref = F.attention_fp8(r["q8"], r["q_scale"], r["k8"], r["k_scale"], r["v8t"],
-                                     r["v_scale"], w.scale, causal=causal, kv_len=kvn)
+                                     r["v_scale"], w.scale, causal=causal, kv_len=kvn,
+                                     window=window)
     P.check_o(P.f64(o), o_ref, w.name + " O (fp8)")
     P.check_lse(P.f64(lse), lse_ref, w.name + " LSE (fp8)")
 

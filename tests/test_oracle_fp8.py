@@ -78,8 +78,11 @@ def test_quantize_round_trip_bound():
     assert np.all(np.abs(deqv - x) <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * sv[:, None, None]) * (1 + 1e-6))
 
 
-@pytest.mark.parametrize("causal,kv,Hkv", [(False, None, 2), (True, None, 2), (True, [150, 300], 1)])
-def test_fp8_attention_against_exact_attention_of_dequantised_inputs(causal, kv, Hkv):
+@pytest.mark.parametrize("causal,kv,Hkv,window", [(False, None, 2, None), (True, None, 2, None),
+                                                  (True, [150, 300], 1, None),
+                                                  (True, None, 1, (70, 0)),
+                                                  (False, [200, 300], 2, (40, 130))])
+def test_fp8_attention_against_exact_attention_of_dequantised_inputs(causal, kv, Hkv, window):
     rng = np.random.default_rng(52)
     B, H, N, d = 2, 2, 300, 32
     q = (rng.standard_normal((B, H, N, d)) * 2).astype(np.float32)
@@ -92,11 +95,13 @@ def test_fp8_attention_against_exact_attention_of_dequantised_inputs(causal, kv,
     k8, sk = k8.reshape(B, Hkv, N, d), sk.reshape(B, Hkv, -1)
     v8t, sv = v8t.reshape(B, Hkv, d, -1), sv.reshape(B, Hkv)
     scale = 1 / np.sqrt(d)
-    o, lse = F.attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=causal, kv_len=kv)
+    o, lse = F.attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=causal, kv_len=kv,
+                             window=window)
     qd = F.e4m3_decode(q8) * np.repeat(sq, 128, axis=2)[:, :, :N, None]
     kd = F.e4m3_decode(k8) * np.repeat(sk, 128, axis=2)[:, :, :N, None]
     vd = F.e4m3_decode(v8t[..., :N]).transpose(0, 1, 3, 2) * sv[:, :, None, None]
-    o_ref, lse_ref = oracle.attention_fwd(qd, kd, vd, scale, causal=causal, kv_len=kv)
+    o_ref, lse_ref = oracle.attention_fwd(qd, kd, vd, scale, causal=causal, kv_len=kv,
+                                          window=window)
     np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-10)
     err = np.abs(o - o_ref)
     assert err.max() <= 2.0 ** -4 * np.abs(vd).max()           # P rounded to E4M3
