@@ -1,11 +1,19 @@
 // Attention forward for sm_103a.
 //
-// One CTA per SM (persistent), 224 threads in four roles:
-//   warp 0      TMA producer: Q tile once per tile, then K_j and V_j into a
-//               STAGES-deep shared-memory ring (full/empty mbarriers).
+// One CTA per SM (persistent), 256 threads in five roles:
+//   warp 0      TMA producer: Q tile once per tile, then K_j (and, for
+//               d <= 128, V_j) into STAGES-deep shared-memory rings
+//               (full/empty mbarriers).
+//   warp 7      bf16 d = 256: TMA producer of V_j.  There the tensor core is the
+//               bound (2048 cycles of products per block), and separate K
+//               and V producers keep both rings full; for d <= 128 one
+//               producer loading K_j then V_j measured faster (it paces the
+//               S products against the P V products on the in-order tensor
+//               pipe), and warp 7 idles.
 //   warp 1      S issuer: S_j = Q K_j^T into one of NSB S buffers in tensor
 //               memory, running ahead of the softmax as far as the buffers
-//               allow.  Also allocates and frees the tensor memory.
+//               allow (a buffer is free again once the softmax has loaded
+//               it).  Also allocates and frees the tensor memory.
 //   warp 2      P V issuer: O += P_j V_j with P read from tensor memory.
 //               A tcgen05.mma holds its issuing thread for about as long as
 //               the tensor core needs to run it, so the two products are
@@ -14,7 +22,8 @@
 //               issues every MMA and commit.
 //   warps 3..6  softmax: thread r owns query row r of the tile (TMEM lane r).
 //               Reads its row of S, masks, updates the running max m and sum
-//               l, writes P = exp2(S*c - m) as bf16 into tensor memory,
+//               l, writes P = exp2(S*c - m) as bf16 into one of NPB P
+//               buffers in tensor memory,
 //               rescales its row of O when m moved, and runs the epilogue
 //               O / l, LSE = (m + log2 l) * ln 2.
 //
@@ -31,10 +40,14 @@
 //
 // Loop order: outer over Q tiles, inner over key blocks (section 4.4.3);
 // key blocks entirely above the causal diagonal are never loaded (section
-// 4.3.2, last note).  Tensor memory columns: NSB S buffers of 128 (P of each
-// block as packed bf16 pairs over the first 64 columns of its S buffer), then
-// O [128*NSB, 128*NSB + D).  S_{j+NSB} may overwrite S buffer j % NSB only
-// after P_j V_j has completed (pv_done), which the S issuer waits for.
+// 4.3.2, last note).  Tensor memory columns: NSB S buffers of 128 (3 for
+// d <= 128, 2 for E4M3 d = 256), a block's P (packed bf16 pairs, or E4M3
+// quads) written over the first columns of its own S buffer, then O;
+// S_{j+NSB} may overwrite S buffer j % NSB only after P_j V_j has completed
+// (pv_done).  bf16 d = 256 (O takes 256 columns): one S buffer and two P
+// buffers of their own (SEP), so that the S buffer is free as soon as the
+// softmax has read S out of it (s_free); the softmax writes P buffer j % NPB
+// once P_{j-NPB} V has completed.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -51,7 +64,7 @@ constexpr int BM = 128;          // query rows per tile = TMEM lanes = MMA M
 constexpr int BN = 128;          // keys per block = MMA N of S
 constexpr int CHUNK = 128 * 128; // bytes of one 128-row x 64-column bf16 chunk (SW128 atom rows)
 constexpr float kRescaleSlack = 8.0f;
-constexpr int kThreads = 224;
+constexpr int kThreads = 256;
 
 // FP8 = true: E4M3 Q and K (one byte an element, so a 128-byte swizzle row
 // holds 128 of them) and V transposed per K/V head ([d, keys]: a V block is d
@@ -65,12 +78,19 @@ struct Cfg {
   static constexpr int V_BYTES = FP8 ? D * 128 : TILE_BYTES;
   static constexpr int STAGES =
       FP8 ? (D == 128 ? 6 : 3) : (D == 64 ? 4 : (D == 128 ? 3 : 1));
-  // NSB S buffers: block g uses columns [128*(g%NSB), +128); its P (packed
-  // bf16 pairs) is written over the first 64 of those columns.  Three
-  // buffers where O leaves room (d <= 128), two for d = 256.
-  static constexpr int NSB = D <= 128 ? 3 : 2;
+  // SEP: P in buffers of its own, with V from a separate producer (bf16
+  // d = 256, where the products bound the kernel; E4M3 halves them and
+  // measured faster with P over S).
+  static constexpr bool SEP = (D == 256 && !FP8);
+  // NSB S buffers: block g uses columns [128*(g%NSB), +128).  NPB P buffers
+  // (without SEP, P buffer b is the start of S buffer b).
+  static constexpr int NSB = SEP ? 1 : (D <= 128 ? 3 : 2);
+  static constexpr int NPB = SEP ? 2 : NSB;
+  static constexpr int PW = FP8 ? BN / 4 : BN / 2;   // columns of one block's P
   static constexpr uint32_t TM_S = 0;
-  static constexpr uint32_t TM_O = 128 * NSB;
+  static constexpr uint32_t TM_P = SEP ? 128 * NSB : TM_S;
+  static constexpr uint32_t P_STRIDE = SEP ? PW : 128;
+  static constexpr uint32_t TM_O = SEP ? TM_P + PW * NPB : 128 * NSB;
   static constexpr uint32_t TM_COLS = 512;
   static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
 };
@@ -84,9 +104,10 @@ struct FwdSmem {
   uint64_t q_full, q_empty;
   uint64_t k_full[C::STAGES], k_empty[C::STAGES];
   uint64_t v_full[C::STAGES], v_empty[C::STAGES];
-  uint64_t s_full[C::NSB];   // S of block g is in buffer g % NSB
-  uint64_t p_full[C::NSB];   // softmax is done with S buffer b and wrote its P
-  uint64_t pv_done[C::NSB];  // O += P V of block g (buffer g % NSB) has completed
+  uint64_t s_full[C::NSB];   // S of block g is in S buffer g % NSB
+  uint64_t s_free[C::NSB];   // SEP: the softmax has loaded S buffer b
+  uint64_t p_full[C::NPB];   // the softmax wrote P of block g into P buffer g % NPB
+  uint64_t pv_done[C::NPB];  // O += P V of block g (P buffer g % NPB) has completed
   uint64_t o_free;
   uint64_t mma_done, pv_mma_done;
   uint32_t tmem_base;
@@ -245,6 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     }
     for (int b = 0; b < C::NSB; ++b) {
       mbar_init(&sm.s_full[b], 1);
+      mbar_init(&sm.s_free[b], 4);
+    }
+    for (int b = 0; b < C::NPB; ++b) {
       mbar_init(&sm.p_full[b], 4);
       mbar_init(&sm.pv_done[b], 1);
     }
@@ -270,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
     if (lane == 0) {
       prefetch_tmap(&p.tq);
       prefetch_tmap(&p.tk);
-      prefetch_tmap(&p.tv);
+      if constexpr (!C::SEP) prefetch_tmap(&p.tv);
       uint32_t q_it = 0, k_it = 0, v_it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
@@ -304,6 +328,60 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               tma_load_3d(sm.k[st] + c * CHUNK, &p.tk, &sm.k_full[st], C::BOX_COLS * c, (jlo + j) * BN,
                           kvbh);
             ++k_it;
+            if constexpr (!C::SEP) {
+              if (!mbar_wait(&sm.v_empty[st], ph ^ 1, abort, kWaitTimeoutNs)) {
+                record_failure(p.status, abort, kSiteProdV);
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&sm.v_full[st], C::V_BYTES);
+              if constexpr (FP8) {
+                tma_load_3d(sm.v[st], &p.tv, &sm.v_full[st], (jlo + j) * BN, 0, kvbh);
+              } else {
+#pragma unroll
+                for (int c = 0; c < C::NCH; ++c)
+                  tma_load_3d(sm.v[st] + c * CHUNK, &p.tv, &sm.v_full[st], 64 * c, (jlo + j) * BN,
+                              kvbh);
+              }
+              ++v_it;
+            }
+          }
+        }
+      }
+      // No copy may still be landing in shared memory when the CTA exits:
+      // wait (bounded, ignoring the abort flag) for the last phase issued on
+      // every full barrier.  In a normal run these phases completed long ago.
+      if (q_it > 0 && !mbar_wait(&sm.q_full, (q_it - 1) & 1, nullptr, kWaitTimeoutNs))
+        record_failure(p.status, abort, kSiteDrain);
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (k_it > static_cast<uint32_t>(s)) {
+          const uint32_t n = (k_it - 1 - s) / C::STAGES;
+          if (!mbar_wait(&sm.k_full[s], n & 1, nullptr, kWaitTimeoutNs))
+            record_failure(p.status, abort, kSiteDrain);
+        }
+        if (v_it > static_cast<uint32_t>(s)) {      // (SEP: v_it stays 0 here)
+          const uint32_t n = (v_it - 1 - s) / C::STAGES;
+          if (!mbar_wait(&sm.v_full[s], n & 1, nullptr, kWaitTimeoutNs))
+            record_failure(p.status, abort, kSiteDrain);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 7) {
+    // ------------------------------------------------------------ V producer (SEP)
+    if (C::SEP && lane == 0) {
+      prefetch_tmap(&p.tv);
+      uint32_t v_it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
+        for (int kt = 0; ok && kt < (DEC ? 1 : sched.ntiles(u)); ++kt) {
+          Tile t;
+          make_tile<DEC>(p, sched, u, kt, t);
+          const int jlo = t.jlo, nkv = t.nkv;
+          const int kvbh = t.kvbh;
+          for (int j = 0; j < nkv; ++j) {
+            const int st = v_it % C::STAGES;
+            const uint32_t ph = (v_it / C::STAGES) & 1;
             if (!mbar_wait(&sm.v_empty[st], ph ^ 1, abort, kWaitTimeoutNs)) {
               record_failure(p.status, abort, kSiteProdV);
               ok = false;
@@ -322,17 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           }
         }
       }
-      // No copy may still be landing in shared memory when the CTA exits:
-      // wait (bounded, ignoring the abort flag) for the last phase issued on
-      // every full barrier.  In a normal run these phases completed long ago.
-      if (q_it > 0 && !mbar_wait(&sm.q_full, (q_it - 1) & 1, nullptr, kWaitTimeoutNs))
-        record_failure(p.status, abort, kSiteDrain);
+      // as for K: no V copy may still be landing when the CTA exits
       for (int s = 0; s < C::STAGES; ++s) {
-        if (k_it > static_cast<uint32_t>(s)) {
-          const uint32_t n = (k_it - 1 - s) / C::STAGES;
-          if (!mbar_wait(&sm.k_full[s], n & 1, nullptr, kWaitTimeoutNs))
-            record_failure(p.status, abort, kSiteDrain);
-        }
         if (v_it > static_cast<uint32_t>(s)) {
           const uint32_t n = (v_it - 1 - s) / C::STAGES;
           if (!mbar_wait(&sm.v_full[s], n & 1, nullptr, kWaitTimeoutNs))
@@ -362,9 +431,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           ++q_it;
           for (int j = 0; j < nkv; ++j, ++g) {
             const uint32_t b = g % C::NSB;
-            // buffer b last held block g - NSB: its P V must be complete
+            // buffer b last held block g - NSB: the softmax must have loaded
+            // it (SEP), or its P V must be complete (P over S)
             if (g >= static_cast<uint32_t>(C::NSB) &&
-                !mbar_wait_warp(&sm.pv_done[b], ((g / C::NSB) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+                !mbar_wait_warp(C::SEP ? &sm.s_free[b] : &sm.pv_done[b], ((g / C::NSB) & 1) ^ 1,
+                                abort, kWaitTimeoutNs)) {
               issuer_fail(p.status, abort, lane, kSiteMmaS);
               ok = false;
               break;
@@ -413,8 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           const int nkv = t.nkv;
           if (nkv == 0) continue;
           for (int j = 0; j < nkv; ++j, ++g) {
-            const uint32_t b = g % C::NSB;
-            if (!mbar_wait_warp(&sm.p_full[b], (g / C::NSB) & 1, abort, kWaitTimeoutNs)) {
+            const uint32_t b = g % C::NPB;
+            if (!mbar_wait_warp(&sm.p_full[b], (g / C::NPB) & 1, abort, kWaitTimeoutNs)) {
               issuer_fail(p.status, abort, lane, kSiteMmaP);
               ok = false;
               break;
@@ -439,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), 16, 1024);
 #pragma unroll
               for (int kk = 0; kk < BN / 32; ++kk)
-                mma_e4m3_ts_w(tmem + C::TM_O, tmem + C::TM_S + 128 * b + kk * 8,
+                mma_e4m3_ts_w(tmem + C::TM_O, tmem + C::TM_P + C::P_STRIDE * b + kk * 8,
                               dv0 + static_cast<uint64_t>((kk * 32) >> 4), kIdescPV,
                               (j == 0 && kk == 0) ? 0u : 1u);
             } else {
@@ -448,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), BN * 128, 1024);
 #pragma unroll
               for (int kk = 0; kk < BN / 16; ++kk) {
-                mma_bf16_ts_w(tmem + C::TM_O, tmem + C::TM_S + 128 * b + kk * 8,
+                mma_bf16_ts_w(tmem + C::TM_O, tmem + C::TM_P + C::P_STRIDE * b + kk * 8,
                             dv0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescPV,
                             (j == 0 && kk == 0) ? 0u : 1u);
               }
@@ -515,6 +586,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           for (int c = 0; c < BN / 32; ++c) tmem_ld_x32(t_s + 32 * c, sr + 32 * c);
           tmem_wait_ld();
           reg_fence<BN>(sr);
+          if constexpr (C::SEP) {
+            // S is in registers: the S issuer may reuse the buffer
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.s_free[b]);
+          }
           float s[BN];
 #pragma unroll
           for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
@@ -589,15 +666,25 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           f2_split(rsa, rs0, rs1);
           f2_split(rsb, rs2, rs3);
           l = l * alpha + ((rs0 + rs1) + (rs2 + rs3));
-          // P over the first columns of this block's S buffer (S is in registers):
-          // 64 columns of bf16 pairs, or 32 of E4M3 quads
-          tmem_st_x32(t_s, pk);
-          if constexpr (!FP8) tmem_st_x32(t_s + 32, pk + 32);
+          // P: 64 columns of bf16 pairs, or 32 of E4M3 quads, over the start of
+          // this block's S buffer (S is in registers), or (SEP) into P buffer
+          // kv_it % NPB once P_{kv_it-NPB} V has read it
+          const uint32_t pb = kv_it % C::NPB;
+          if (C::SEP && kv_it >= static_cast<uint32_t>(C::NPB) &&
+              !warp_wait(&sm.pv_done[pb], ((kv_it / C::NPB) & 1) ^ 1, abort)) {
+            if (lane == 0) record_failure(p.status, abort, kSiteSmP);
+            ok = false;
+            break;
+          }
+          if constexpr (C::SEP) tc_fence_after_sync();
+          const uint32_t t_p = t_lane + C::TM_P + C::P_STRIDE * pb;
+          tmem_st_x32(t_p, pk);
+          if constexpr (!FP8) tmem_st_x32(t_p + 32, pk + 32);
           if (__any_sync(0xffffffffu, rescale && j > 0)) {
             // O must hold every earlier P V before it is scaled: wait for the
             // previous block's P V to complete.
             const uint32_t prev = kv_it - 1;
-            if (!warp_wait(&sm.pv_done[prev % C::NSB], (prev / C::NSB) & 1, abort)) {
+            if (!warp_wait(&sm.pv_done[prev % C::NPB], (prev / C::NPB) & 1, abort)) {
               if (lane == 0) record_failure(p.status, abort, kSiteSmO);
               ok = false;
               break;
@@ -629,13 +716,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           tmem_wait_st();
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.p_full[b]);
+          if (lane == 0) mbar_arrive(&sm.p_full[pb]);
           ++kv_it;
         }
         if (!ok) break;
         // epilogue: wait for the tile's last P V, then O / l and LSE
         const uint32_t last = kv_it - 1;
-        if (!warp_wait(&sm.pv_done[last % C::NSB], (last / C::NSB) & 1, abort)) {
+        if (!warp_wait(&sm.pv_done[last % C::NPB], (last / C::NPB) & 1, abort)) {
           if (lane == 0) record_failure(p.status, abort, kSiteSmEpi);
           ok = false;
           break;
