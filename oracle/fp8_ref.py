@@ -18,10 +18,14 @@ readings used here (and by the GPU path, which is checked against this file):
   has scale 1.  V gets one scale per head so that the P V sum can be scaled
   once at the end.
 * The softmax is the block-online recurrence of 4.3.2 over 128-key blocks
-  in order.  Within a block, S = sq * sk * (Q8 K8^T) * scale; the running
-  maximum m is raised to every new block maximum (no slack); P = exp(S - m)
-  is stored as E4M3(256 * P) for the P V product and the row sum l adds the
-  unrounded P.  O = sv * (sum of P8 V8) / (256 * l), LSE = m + ln l.
+  in order.  Within a block, S = sq * sk * (Q8 K8^T) * scale.  The reference
+  maximum m starts at the first block's maximum and is raised to a block's
+  maximum only when that exceeds m by more than 4 ln 2 (a factor 2^4), so
+  P = exp(S - m) <= 16 and is stored as E4M3(16 * P) <= 256 for the P V
+  product; the row sum l adds the unrounded P.  O = sv * (sum of P8 V8) /
+  (16 * l), LSE = m + ln l.  (16 P keeps the normal range, relative to the
+  row maximum, that 256 P has when m follows every new maximum; the slack
+  spares the rescale of O on most blocks.)
 
 Unlike attn_oracle.c this is an algorithm, not a definition: its blocks and
 rounding are part of the result, so they are written out step by step.
@@ -30,6 +34,8 @@ import numpy as np
 
 E4M3_MAX = 448.0
 BLOCK = 128
+SLACK = 4.0 * np.log(2.0)     # the reference maximum moves past 2^4 growth
+P_MULT = 16.0                 # E4M3 operand = 16 P
 
 
 def e4m3_values():
@@ -154,17 +160,18 @@ def attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=False, kv_len=None, H_k
                         continue
                     s = (K[b, hk, lo:hi] @ Q[b, h, i]) * (sqi * float(sk[b, hk, j])) * scale
                     mb = s.max()
-                    if mb > m:                         # raise the reference to the new max
-                        if m > -np.inf:
-                            alpha = np.exp(m - mb)
-                            acc *= alpha
-                            l *= alpha
+                    if m == -np.inf:
+                        m = mb
+                    elif mb > m + SLACK:               # raise the reference to the new max
+                        alpha = np.exp(m - mb)
+                        acc *= alpha
+                        l *= alpha
                         m = mb
                     p = np.exp(s - m)
-                    p8 = e4m3_decode(e4m3_round((p * 256.0).astype(np.float32)))
+                    p8 = e4m3_decode(e4m3_round((p * P_MULT).astype(np.float32)))
                     l += p.sum()
                     acc += V[b, hk, :, lo:hi] @ p8
                 if l > 0:
-                    O[b, h, i] = float(sv[b, hk]) * acc / (256.0 * l)
+                    O[b, h, i] = float(sv[b, hk]) * acc / (P_MULT * l)
                     LSE[b, h, i] = m + np.log(l)
     return O, LSE

@@ -106,3 +106,66 @@ def test_fp8_attention_against_exact_attention_of_dequantised_inputs(causal, kv,
     err = np.abs(o - o_ref)
     assert err.max() <= 2.0 ** -4 * np.abs(vd).max()           # P rounded to E4M3
     assert err.mean() <= 2e-3 * np.abs(vd).max()
+
+
+def _two_block_case(peak):
+    """q = e_0; keys of block 0 score 0, keys of block 1 score `peak` (scale 1,
+    unit Q/K scales); V random, quantised per head."""
+    rng = np.random.default_rng(53)
+    N, d = 256, 32
+    q8 = np.zeros((1, 1, N, d), np.uint8)
+    q8[..., 0] = 0x38                                   # q = e_0 (1.0)
+    k8 = np.zeros((1, 1, N, d), np.uint8)
+    k8[0, 0, 128:, 0] = F.e4m3_round(np.float32(peak))
+    assert F.e4m3_decode(k8[0, 0, 135, 0]) == peak
+    v = rng.standard_normal((1, N, d)).astype(np.float32)
+    v8t, sv = F.quantize_v_transposed(v)
+    return q8, k8, v8t.reshape(1, 1, d, -1), sv.reshape(1, 1)
+
+
+@pytest.mark.parametrize("peak", [2.75, 3.0])
+def test_slack_rule_closed_form(peak):
+    """The recurrence worked by hand for the two-block case.  Block 0: m = 0,
+    p = 1, P8 = E4M3(16) = 16.  Block 1 at peak 2.75 < 4 ln 2: m stays 0,
+    p = e^2.75, P8 = E4M3(16 e^2.75).  At 3.0 > 4 ln 2: m moves to 3, block
+    0's sums scale by e^-3, p = 1, P8 = 16.  O = sv (sum P8 V8) / (16 l)."""
+    q8, k8, v8t, sv = _two_block_case(peak)
+    ones = np.ones((1, 1, 2), np.float32)
+    o, lse = F.attention_fp8(q8, ones, k8, ones, v8t, sv, 1.0, rows=[200])
+    vc = F.e4m3_decode(v8t[0, 0]).T                     # [N, d] decoded codes
+    s0, s1 = vc[:128].sum(0), vc[128:].sum(0)
+    if peak < 4 * np.log(2):
+        w1 = F.e4m3_decode(F.e4m3_round(np.float32(16 * np.exp(peak))))
+        l = 128 + 128 * np.exp(peak)
+        acc, m = 16 * s0 + w1 * s1, 0.0
+    else:
+        a = np.exp(-peak)
+        l = 128 * a + 128
+        acc, m = 16 * a * s0 + 16 * s1, peak
+    np.testing.assert_allclose(o[0, 0, 200], float(sv[0, 0]) * acc / (16 * l), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0, 200], m + np.log(l), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("peak", [2.75, 3.0, 3.5])
+def test_slack_keeps_16p_inside_e4m3(peak):
+    """Block 0 scores 0; every key of block 1 scores `peak`: 2.75 < 4 ln 2
+    (no rescale, so P reaches e^2.75 ~ 15.6 and 16 P ~ 250 must not
+    saturate), 3.0 > 4 ln 2 (the reference moves).  Either way O must match
+    exact attention of the dequantised inputs within E4M3's rounding of P."""
+    N = 256
+    q8, k8, v8t, sv = _two_block_case(peak)
+    sq = np.ones((1, 1, 2), np.float32)
+    sk = np.ones((1, 1, 2), np.float32)
+    rows = [200, 255]                                   # see both blocks
+    o, lse = F.attention_fp8(q8, sq, k8, sk, v8t, sv, 1.0, rows=rows)
+    qd = F.e4m3_decode(q8)
+    kd = F.e4m3_decode(k8)
+    vd = F.e4m3_decode(v8t[..., :N]).transpose(0, 1, 3, 2) * sv[:, :, None, None]
+    o_ref, lse_ref = oracle.attention_fwd(qd, kd, vd, 1.0)
+    np.testing.assert_allclose(lse[0, 0, rows], lse_ref[0, 0, rows], rtol=0, atol=1e-10)
+    # each P is normal here, so rounding it to E4M3 moves it by at most 2^-4
+    # of itself: |dO| <= 2^-4 * sum_j softmax_j |v_j|, element by element
+    s = (kd[0, 0] @ qd[0, 0, rows].T).T                  # exact scores of the rows
+    w = np.exp(s - lse_ref[0, 0, rows][:, None])
+    bound = 2.0 ** -4 * (w @ np.abs(vd[0, 0])) * (1 + 1e-9)
+    assert np.all(np.abs(o[0, 0, rows] - o_ref[0, 0, rows]) <= bound)
