@@ -64,6 +64,12 @@ constexpr int BM = 128;          // query rows per tile = TMEM lanes = MMA M
 constexpr int BN = 128;          // keys per block = MMA N of S
 constexpr int CHUNK = 128 * 128; // bytes of one 128-row x 64-column bf16 chunk (SW128 atom rows)
 constexpr float kRescaleSlack = 8.0f;
+// E4M3: the reference maximum moves when a block exceeds it by more than 4
+// (log2 units), so P <= 2^4 and the E4M3 operand 16 P <= 256 (largest finite
+// E4M3 448); 16 P has the same normal range relative to the row maximum as
+// 256 P would with no slack.
+constexpr float kFp8Slack = 4.0f;
+constexpr float kFp8Shift = 4.0f;   // log2 of the multiplier 16 = 2^(8 - slack)
 constexpr int kThreads = 256;
 
 // FP8 = true: E4M3 Q and K (one byte an element, so a 128-byte swizzle row
@@ -630,16 +636,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               alpha = 0.f;
               m_ref = m_blk;
             }
-          } else if (m_blk > m_ref + (FP8 ? 0.f : kRescaleSlack)) {
-            // (FP8: no slack, so 256 P <= 256 stays inside E4M3's range)
+          } else if (m_blk > m_ref + (FP8 ? kFp8Slack : kRescaleSlack)) {
             alpha = ex2_approx(m_ref - m_blk);
             m_ref = m_blk;
             rescale = true;
           }
-          // FP8 takes 256 p, the E4M3 operand, straight from the exponent
-          // (exp2(x + 8) = 256 exp2(x)); its row sum l is then 256 times the
-          // sum of p, and the epilogue divides the 256 back out.
-          const float base = ((m_ref == -INFINITY) ? 0.f : m_ref) - (FP8 ? 8.f : 0.f);
+          // FP8 takes 16 p, the E4M3 operand, straight from the exponent
+          // (exp2(x + 4) = 16 exp2(x)); its row sum l is then 16 times the
+          // sum of p, and the epilogue divides the 16 back out.
+          const float base = ((m_ref == -INFINITY) ? 0.f : m_ref) - (FP8 ? kFp8Shift : 0.f);
           // p = exp2(S*c - m) two lanes at a time: packed FMA for the argument,
           // packed adds for the row sum, one bf16x2 convert per pair
           const uint64_t c2x2 = f2_make(cb, cb);
@@ -728,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           break;
         }
         tc_fence_after_sync();
-        // FP8: P entered the product as 256 P (and l sums 256 P), V in units
+        // FP8: P entered the product as 16 P (and l sums 16 P), V in units
         // of its head scale
         const float inv_l = l > 0.f ? (FP8 ? __ldg(p.v_scale + t.kvbh) / l : 1.f / l) : 0.f;
 #pragma unroll 1
@@ -765,7 +770,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         if (lane == 0) mbar_arrive(&sm.o_free);
         if (row_valid) {
           const float lse_row =
-              l > 0.f ? (m_ref + (log2f(l) - (FP8 ? 8.f : 0.f))) * 0.69314718055994531f : -INFINITY;
+              l > 0.f ? (m_ref + (log2f(l) - (FP8 ? kFp8Shift : 0.f))) * 0.69314718055994531f
+                      : -INFINITY;
           if constexpr (DEC)
             p.lse_part[row_off] = lse_row;
           else
