@@ -40,7 +40,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd.cu", "sm103_ptx.cuh"],
     "bwd_main_kernel": ["fa_bwd.cu", "fa_api.cu", "sm103_ptx.cuh"],
-    "bwd_dt_kernel": ["fa_bwd_dt.cu", "fa_api.cu", "sm103_ptx.cuh"],
+    "bwd_dt_kernel": ["fa_bwd_dt.cu", "fa_bwd_common.cuh", "fa_api.cu", "sm103_ptx.cuh"],
 }
 
 
