@@ -63,7 +63,11 @@ using namespace ptx;
 constexpr int BM = 128;          // query rows per tile = TMEM lanes = MMA M
 constexpr int BN = 128;          // keys per block = MMA N of S
 constexpr int CHUNK = 128 * 128; // bytes of one 128-row x 64-column bf16 chunk (SW128 atom rows)
-constexpr float kRescaleSlack = 8.0f;
+// bf16: the reference maximum moves only when a block exceeds it by more than
+// 24 (log2 units), so P <= 2^24, l <= N * 2^24 and O~ stay far inside fp32's
+// (and P inside bf16's) range, and most blocks of even large-score rows skip
+// the rescale of O (8 measured 8 % slower at scores of standard deviation 9).
+constexpr float kRescaleSlack = 24.0f;
 // E4M3: the reference maximum moves when a block exceeds it by more than 4
 // (log2 units), so P <= 2^4 and the E4M3 operand 16 P <= 256 (largest finite
 // E4M3 448); 16 P has the same normal range relative to the row maximum as
