@@ -405,8 +405,18 @@ int fa_decode_splits(int B, int H_kv, int Nk) {
   const int sms = (di && di->err == cudaSuccess && di->num_sms > 0) ? di->num_sms : 148;
   const long long heads = static_cast<long long>(B) * H_kv;
   const int nblk = (Nk + 127) / 128;
-  // Chunks of at least 8 key blocks; among those, the count whose units fill
-  // the SMs' waves best (ties: fewer chunks, less merging).
+  // Fewer K/V heads than SMs: the most chunks that still run in one wave (a
+  // unit pays a fixed cost for its Q load, pipeline fill and epilogue, so one
+  // wave of long chunks measured faster than four full waves of short ones:
+  // 4 x 8 heads, 32K keys: 5.2 TB/s with 4 chunks per head, 4.7 with 19),
+  // keeping chunks of at least 8 key blocks.
+  if (heads < sms) {
+    const long long by_sms = sms / heads;
+    const long long by_len = nblk / 8 > 1 ? nblk / 8 : 1;
+    return static_cast<int>(by_sms < by_len ? by_sms : by_len);
+  }
+  // Otherwise chunks of at least 8 key blocks; among those, the count whose
+  // units fill the SMs' waves best (ties: fewer chunks, less merging).
   int best = 1;
   double best_eff = -1.0;
   for (int s = 1; s <= nblk; ++s) {

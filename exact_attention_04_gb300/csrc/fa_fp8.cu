@@ -46,12 +46,12 @@ __device__ __forceinline__ void unpack8(uint4 u, float* f) {
   }
 }
 
-// Largest |x| of each 128-row block of G heads ([G, N, D] bf16): written to
-// out[g * nb + b], or (PER_HEAD) folded into out[g] with an integer max on
-// the bit patterns, which orders non-negative floats correctly.
-template <int D, bool PER_HEAD>
-__global__ void __launch_bounds__(kThreads) amax_kernel(const __nv_bfloat16* x, int N, int nb,
-                                                        float* out) {
+// Largest |x| of each 128-row block of G heads ([G, N, D] bf16), folded into
+// out[g] with an integer max on the bit patterns, which orders non-negative
+// floats correctly (V: one scale per head).
+template <int D>
+__global__ void __launch_bounds__(kThreads) head_amax_kernel(const __nv_bfloat16* x, int N, int nb,
+                                                             float* out) {
   const int blk = blockIdx.x;
   const int g = blk / nb, b = blk % nb;
   const int r0 = b * kRowsPerBlock;
@@ -66,12 +66,7 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const __nv_bfloat16* x, 
     for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
   }
   m = block_max(m);
-  if (threadIdx.x == 0) {
-    if (PER_HEAD)
-      atomicMax(reinterpret_cast<int*>(out + g), __float_as_int(m));
-    else
-      out[blk] = m;
-  }
+  if (threadIdx.x == 0) atomicMax(reinterpret_cast<int*>(out + g), __float_as_int(m));
 }
 
 __device__ __forceinline__ void scale_of(float amax, float& s, float& mul) {
@@ -83,31 +78,51 @@ __device__ __forceinline__ void scale_of(float amax, float& s, float& mul) {
   }
 }
 
-// Rows of each 128-row block to E4M3; io holds the block's amax on entry and
-// its dequantisation scale on exit.
+// One 128-row block of G heads ([G, N, D] bf16) to E4M3 in one pass: the
+// block stays in registers while the CTA reduces its largest |x|, then is
+// scaled and converted; scales[g * nb + b] gets the dequantisation scale.
 template <int D>
 __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const __nv_bfloat16* x, int N,
-                                                              int nb, float* io,
+                                                              int nb, float* scales,
                                                               uint8_t* codes) {
+  constexpr int PER = kRowsPerBlock * (D / 8) / kThreads;   // 16-byte loads per thread
+  __shared__ float s_amax;
   const int blk = blockIdx.x;
   const int g = blk / nb, b = blk % nb;
-  float s, mul;
-  scale_of(io[blk], s, mul);
-  __syncthreads();                       // every thread has read the amax
-  if (threadIdx.x == 0) io[blk] = s;
   const int r0 = b * kRowsPerBlock;
   const int r1 = r0 + kRowsPerBlock < N ? r0 + kRowsPerBlock : N;
   const size_t off = (static_cast<size_t>(g) * N + r0) * D;
   const uint4* src = reinterpret_cast<const uint4*>(x + off);
   uint2* dst = reinterpret_cast<uint2*>(codes + off);
   const int n8 = (r1 - r0) * (D / 8);
-  for (int i = threadIdx.x; i < n8; i += kThreads) {
-    float f[8];
-    unpack8(src[i], f);
+  uint4 v[PER];
+  float m = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] = __fmul_rn(f[e], mul);
-    dst[i] = make_uint2(ptx::pack_e4m3x4(f[0], f[1], f[2], f[3]),
-                        ptx::pack_e4m3x4(f[4], f[5], f[6], f[7]));
+  for (int k = 0; k < PER; ++k) {
+    const int i = threadIdx.x + k * kThreads;
+    v[k] = i < n8 ? src[i] : make_uint4(0, 0, 0, 0);
+    float f[8];
+    unpack8(v[k], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
+  }
+  m = block_max(m);
+  if (threadIdx.x == 0) s_amax = m;
+  __syncthreads();
+  float s, mul;
+  scale_of(s_amax, s, mul);
+  if (threadIdx.x == 0) scales[blk] = s;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int i = threadIdx.x + k * kThreads;
+    if (i < n8) {
+      float f[8];
+      unpack8(v[k], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = __fmul_rn(f[e], mul);
+      dst[i] = make_uint2(ptx::pack_e4m3x4(f[0], f[1], f[2], f[3]),
+                          ptx::pack_e4m3x4(f[4], f[5], f[6], f[7]));
+    }
   }
 }
 
@@ -167,11 +182,9 @@ cudaError_t quantize(const Fp8QuantArgs& a, cudaStream_t st) {
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
   const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
-  amax_kernel<D, false><<<gq * nb, kThreads, 0, st>>>(q, a.N, nb, a.q_scale);
-  amax_kernel<D, false><<<gk * nb, kThreads, 0, st>>>(k, a.N, nb, a.k_scale);
   cudaError_t e = cudaMemsetAsync(a.v_scale, 0, sizeof(float) * gk, st);
   if (e != cudaSuccess) return e;
-  amax_kernel<D, true><<<gk * nb, kThreads, 0, st>>>(v, a.N, nb, a.v_scale);
+  head_amax_kernel<D><<<gk * nb, kThreads, 0, st>>>(v, a.N, nb, a.v_scale);
   quant_rows_kernel<D><<<gq * nb, kThreads, 0, st>>>(q, a.N, nb, a.q_scale,
                                                      static_cast<uint8_t*>(a.q8));
   quant_rows_kernel<D><<<gk * nb, kThreads, 0, st>>>(k, a.N, nb, a.k_scale,

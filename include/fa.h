@@ -183,7 +183,9 @@ fa_status_t fa_bwd_dkdv_v(const void* q, const void* k, const void* v, const voi
  * bytes, 256-byte aligned, for the fp32 partials.  splits >= 1; chunks are
  * whole 128-key blocks, so at most ceil(Nk / 128) chunks are used.
  * fa_decode_splits returns the library's choice for this GPU (0 for invalid
- * sizes).  Other arguments and errors as for fa_fwd_v.
+ * sizes): with fewer K/V heads (B * h_kv) than SMs, the most chunks of at
+ * least 8 key blocks that run as one wave; otherwise the count whose units
+ * fill the SMs' waves best.  Other arguments and errors as for fa_fwd_v.
  */
 int fa_decode_splits(int B, int h_kv, int Nk);
 size_t fa_decode_workspace_bytes(int B, int H, int Nq, int d, int splits);

@@ -166,3 +166,20 @@ def test_fp8_argument_errors(lib):
     assert fwd8(N=0) == fa.FA_ERR_INVALID_ARG
     assert fwd8(scale=0.0) == fa.FA_ERR_INVALID_ARG
     assert fwd8(h_kv=4) == fa.FA_ERR_INVALID_ARG
+
+
+def test_decode_split_choice(lib):
+    """fa_decode_splits: with fewer K/V heads than SMs, the most chunks of at
+    least 8 key blocks that fit one wave; always within [1, key blocks]."""
+    import torch
+    sms = (torch.cuda.get_device_properties(0).multi_processor_count
+           if torch.cuda.is_available() else 148)
+    assert fa.fa_decode_splits(4, 8, 32768) == min(sms // 32, 256 // 8)
+    assert fa.fa_decode_splits(1, 1, 1000) == 1                  # 8 blocks: one chunk
+    assert fa.fa_decode_splits(1, 2, 131072) == min(sms // 2, 1024 // 8)
+    for B, hk, nk in ((64, 8, 4096), (3, 100, 20000), (1, 1, 1), (2, 40, 128 * 64)):
+        s = fa.fa_decode_splits(B, hk, nk)
+        assert 1 <= s <= -(-nk // 128)
+        if B * hk < sms:
+            assert B * hk * s <= sms
+    assert fa.fa_decode_splits(0, 8, 100) == 0
