@@ -74,7 +74,6 @@ constexpr float kRescaleSlack = 24.0f;
 // 256 P would with no slack.
 constexpr float kFp8Slack = 4.0f;
 constexpr float kFp8Shift = 4.0f;   // log2 of the multiplier 16 = 2^(8 - slack)
-constexpr int kThreads = 256;
 
 // FP8 = true: E4M3 Q and K (one byte an element, so a 128-byte swizzle row
 // holds 128 of them) and V transposed per K/V head ([d, keys]: a V block is d
@@ -103,6 +102,12 @@ struct Cfg {
   static constexpr uint32_t TM_O = SEP ? TM_P + PW * NPB : 128 * NSB;
   static constexpr uint32_t TM_COLS = 512;
   static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
+  // NHALF softmax warps per sub-partition, each taking BN / NHALF keys of a
+  // block and D / NHALF columns of O.  At d = 64 the products of a block take
+  // a quarter of the time the softmax of one warp does, so two warps share
+  // each row (agreeing on its maximum once a block); elsewhere one.
+  static constexpr int NHALF = (D == 64 && !FP8) ? 2 : 1;
+  static constexpr int THREADS = NHALF == 2 ? 352 : 256;
 };
 
 template <int D, bool FP8 = false>
@@ -120,6 +125,11 @@ struct FwdSmem {
   uint64_t pv_done[C::NPB];  // O += P V of block g (P buffer g % NPB) has completed
   uint64_t o_free;
   uint64_t mma_done, pv_mma_done;
+  // NHALF = 2: the warp pairs' barriers and exchanged partial maxima / sums;
+  // in its n-th exchange the warp of half h writes slot h ^ (n & 1) of its
+  // row and reads the other, so it only overwrites the value it has just read
+  uint64_t pair_bar[4];
+  float xch[C::NHALF == 2 ? 2 : 1][C::NHALF == 2 ? BM : 1];
   uint32_t tmem_base;
   int abort;
 };
@@ -127,7 +137,7 @@ struct FwdSmem {
 // Wait sites reported in the status word.
 enum Site {
   kSiteProdQ = 1, kSiteProdK, kSiteProdV, kSiteMmaQ, kSiteMmaK, kSiteMmaS, kSiteMmaP, kSiteMmaV,
-  kSiteMmaO, kSiteSmS, kSiteSmP, kSiteSmO, kSiteSmEpi, kSiteDrain
+  kSiteMmaO, kSiteSmS, kSiteSmP, kSiteSmO, kSiteSmEpi, kSiteDrain, kSiteSmPair
 };
 
 __device__ __forceinline__ void record_failure(int* status, volatile int* abort, int site) {
@@ -248,7 +258,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 template <int D, bool DEC, bool FP8>
-__global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
+    fa_fwd_kernel(const __grid_constant__ FwdParams p) {
   static_assert(!(DEC && FP8), "decode runs in bf16");
   using C = Cfg<D, FP8>;
   using Smem = FwdSmem<D, FP8>;
@@ -279,11 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       mbar_init(&sm.s_free[b], 4);
     }
     for (int b = 0; b < C::NPB; ++b) {
-      mbar_init(&sm.p_full[b], 4);
+      mbar_init(&sm.p_full[b], 4 * C::NHALF);
       mbar_init(&sm.pv_done[b], 1);
     }
+    for (int q = 0; q < 4; ++q) mbar_init(&sm.pair_bar[q], 64);
     mbar_init(&sm.pv_mma_done, 1);
-    mbar_init(&sm.o_free, 4);
+    mbar_init(&sm.o_free, 4 * C::NHALF);
     mbar_init(&sm.mma_done, 1);
     fence_mbar_init();
   }
@@ -377,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
       }
     }
     __syncwarp();
-  } else if (warp == 7) {
+  } else if (C::NHALF == 1 && warp == 7) {
     // ------------------------------------------------------------ V producer (SEP)
     if (C::SEP && lane == 0) {
       prefetch_tmap(&p.tv);
@@ -548,12 +560,28 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
   } else {
     // ------------------------------------------------------------ softmax warps
     const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
+    const int hf = (warp - 3) >> 2;                // key half (NHALF = 2)
+    constexpr int NC = BN / C::NHALF;              // S columns (keys) of this warp
+    constexpr int DO = D / C::NHALF;               // O columns of this warp
     const int row_local = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t t_o = t_lane + C::TM_O + DO * hf;
     const float c2 = p.scale_log2;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o);
-    uint32_t kv_it = 0;
+    uint32_t kv_it = 0, hs = 0;
     bool ok = true;
+    // NHALF = 2: one exchange with the partner warp (same rows, other keys)
+    auto exchange = [&](float v, float& other) -> bool {
+      const int flip = static_cast<int>(hs & 1);
+      sm.xch[hf ^ flip][row_local] = v;
+      tc_fence_before_sync();
+      mbar_arrive(&sm.pair_bar[quarter]);
+      if (!warp_wait(&sm.pair_bar[quarter], hs & 1, abort)) return false;
+      tc_fence_after_sync();
+      other = sm.xch[hf ^ 1 ^ flip][row_local];
+      ++hs;
+      return true;
+    };
     for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
       for (int kt = 0; ok && kt < (DEC ? 1 : sched.ntiles(u)); ++kt) {
         Tile t;
@@ -567,15 +595,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         if (nkv == 0) {
           if (row_valid) {
             if constexpr (DEC) {
-              float4* dst = reinterpret_cast<float4*>(p.o_part + row_off * D);
+              float4* dst = reinterpret_cast<float4*>(p.o_part + row_off * D + DO * hf);
 #pragma unroll
-              for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-              p.lse_part[row_off] = -INFINITY;
+              for (int i = 0; i < DO / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (hf == 0) p.lse_part[row_off] = -INFINITY;
             } else {
-              uint4* dst = reinterpret_cast<uint4*>(out + row_off * D);
+              uint4* dst = reinterpret_cast<uint4*>(out + row_off * D + DO * hf);
 #pragma unroll
-              for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-              p.lse[row_off] = -INFINITY;
+              for (int i = 0; i < DO / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+              if (hf == 0) p.lse[row_off] = -INFINITY;
             }
           }
           continue;
@@ -591,48 +619,59 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             break;
           }
           tc_fence_after_sync();
-          uint32_t sr[BN];
+          uint32_t sr[NC];
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) tmem_ld_x32(t_s + 32 * c, sr + 32 * c);
+          for (int c = 0; c < NC / 32; ++c) tmem_ld_x32(t_s + NC * hf + 32 * c, sr + 32 * c);
           tmem_wait_ld();
-          reg_fence<BN>(sr);
+          reg_fence<NC>(sr);
           if constexpr (C::SEP) {
             // S is in registers: the S issuer may reuse the buffer
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.s_free[b]);
           }
-          float s[BN];
+          float s[NC];
 #pragma unroll
-          for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
+          for (int c = 0; c < NC; ++c) s[c] = __uint_as_float(sr[c]);
           // masks: keys past the sequence (tail / padding), right of the
           // window (above the diagonal when causal) and left of the window;
           // skipped when every key of the block is visible to every row
-          const int key0 = (jlo + j) * BN;
-          if (key0 + BN > len || key0 + BN - 1 > t.qlo + p.wr || key0 < t.qhi - p.wl) {
+          const int key0 = (jlo + j) * BN + NC * hf;
+          if (key0 + NC > len || key0 + NC - 1 > t.qlo + p.wr || key0 < t.qhi - p.wl) {
             // visible columns [c_lo, c_hi]: before the sequence end and
             // inside the window [row - wl, row + wr]
             const int c_hi = min(len - key0 - 1, row + p.wr - key0);
             const int c_lo = row - p.wl - key0;
 #pragma unroll
-            for (int c = 0; c < BN; ++c)
+            for (int c = 0; c < NC; ++c)
               if (c > c_hi || c < c_lo) s[c] = -INFINITY;
           }
-          // row maximum: four chains of three-input max over s[0 .. BN)
-          static_assert(BN % 8 == 0, "the max chains take 8 columns a step");
+          // row maximum: four chains of three-input max over s[0 .. NC)
+          static_assert(NC % 8 == 0, "the max chains take 8 columns a step");
           float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-          for (int c = 4; c + 8 <= BN; c += 8) {
+          for (int c = 4; c + 8 <= NC; c += 8) {
             mx0 = fmax3(mx0, s[c], s[c + 1]);
             mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
             mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
             mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
           }
-          mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
-          mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
+          mx0 = fmax3(mx0, s[NC - 4], s[NC - 3]);
+          mx1 = fmax3(mx1, s[NC - 2], s[NC - 1]);
           // this block's multiplier from MMA output to base-2 units of S*scale
           const float cb = FP8 ? c2 * q_sc * __ldg(p.k_scale + t.kvbh * p.nb + jlo + j) : c2;
-          const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cb;
+          float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cb;
+          if constexpr (C::NHALF == 2) {
+            // the partner's half of the block (it loaded its S before arriving,
+            // so its columns may now take this warp's P)
+            float m_other;
+            if (!exchange(m_blk, m_other)) {
+              if (lane == 0) record_failure(p.status, abort, kSiteSmPair);
+              ok = false;
+              break;
+            }
+            m_blk = fmaxf(m_blk, m_other);
+          }
           float alpha = 1.f;
           bool rescale = false;
           if (m_ref == -INFINITY) {
@@ -654,9 +693,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           const uint64_t c2x2 = f2_make(cb, cb);
           const uint64_t nbx2 = f2_make(-base, -base);
           uint64_t rsa = f2_make(0.f, 0.f), rsb = f2_make(0.f, 0.f);
-          uint32_t pk[FP8 ? BN / 4 : BN / 2];
+          uint32_t pk[FP8 ? NC / 4 : NC / 2];
 #pragma unroll
-          for (int c = 0; c < BN / 2; c += 2) {
+          for (int c = 0; c < NC / 2; c += 2) {
             float a0, a1, a2, a3;
             f2_split(f2_fma(f2_make(s[2 * c], s[2 * c + 1]), c2x2, nbx2), a0, a1);
             f2_split(f2_fma(f2_make(s[2 * c + 2], s[2 * c + 3]), c2x2, nbx2), a2, a3);
@@ -686,9 +725,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             break;
           }
           if constexpr (C::SEP) tc_fence_after_sync();
-          const uint32_t t_p = t_lane + C::TM_P + C::P_STRIDE * pb;
+          // (NHALF = 2: this warp's keys from column NC / 2 * hf)
+          constexpr int PCOLS = FP8 ? NC / 4 : NC / 2;
+          const uint32_t t_p = t_lane + C::TM_P + C::P_STRIDE * pb + PCOLS * hf;
           tmem_st_x32(t_p, pk);
-          if constexpr (!FP8) tmem_st_x32(t_p + 32, pk + 32);
+          if constexpr (PCOLS == 64) tmem_st_x32(t_p + 32, pk + 32);
           if (__any_sync(0xffffffffu, rescale && j > 0)) {
             // O must hold every earlier P V before it is scaled: wait for the
             // previous block's P V to complete.
@@ -699,15 +740,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
               break;
             }
             tc_fence_after_sync();
-            // up to 128 columns of O per round trip (S is no longer live),
-            // scaled two at a time
-            constexpr int RC = D < 128 ? D / 32 : 4;
+            // this warp's columns of O, up to 128 per round trip (S is no
+            // longer live), scaled two at a time
+            constexpr int RC = DO < 128 ? DO / 32 : 4;
             const uint64_t a2 = f2_make(alpha, alpha);
 #pragma unroll 1
-            for (int c0 = 0; c0 < D / 32; c0 += RC) {
+            for (int c0 = 0; c0 < DO / 32; c0 += RC) {
               uint32_t orr[RC * 32];
 #pragma unroll
-              for (int c = 0; c < RC; ++c) tmem_ld_x32(t_lane + C::TM_O + 32 * (c0 + c), orr + 32 * c);
+              for (int c = 0; c < RC; ++c) tmem_ld_x32(t_o + 32 * (c0 + c), orr + 32 * c);
               tmem_wait_ld();
               reg_fence<RC * 32>(orr);
 #pragma unroll
@@ -719,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
                 orr[2 * i + 1] = __float_as_uint(hi);
               }
 #pragma unroll
-              for (int c = 0; c < RC; ++c) tmem_st_x32(t_lane + C::TM_O + 32 * (c0 + c), orr + 32 * c);
+              for (int c = 0; c < RC; ++c) tmem_st_x32(t_o + 32 * (c0 + c), orr + 32 * c);
             }
           }
           tmem_wait_st();
@@ -729,6 +770,16 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
           ++kv_it;
         }
         if (!ok) break;
+        if constexpr (C::NHALF == 2) {
+          // the row sum over both halves of the keys
+          float l_other;
+          if (!exchange(l, l_other)) {
+            if (lane == 0) record_failure(p.status, abort, kSiteSmPair);
+            ok = false;
+            break;
+          }
+          l += l_other;
+        }
         // epilogue: wait for the tile's last P V, then O / l and LSE
         const uint32_t last = kv_it - 1;
         if (!warp_wait(&sm.pv_done[last % C::NPB], (last / C::NPB) & 1, abort)) {
@@ -741,14 +792,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         // of its head scale
         const float inv_l = l > 0.f ? (FP8 ? __ldg(p.v_scale + t.kvbh) / l : 1.f / l) : 0.f;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < DO / 32; ++c) {
           uint32_t orr[32];
-          tmem_ld_x32(t_lane + C::TM_O + 32 * c, orr);
+          tmem_ld_x32(t_o + 32 * c, orr);
           tmem_wait_ld();
           reg_fence<32>(orr);
           if constexpr (DEC) {
             if (row_valid) {
-              float4* dst = reinterpret_cast<float4*>(p.o_part + row_off * D + 32 * c);
+              float4* dst = reinterpret_cast<float4*>(p.o_part + row_off * D + DO * hf + 32 * c);
 #pragma unroll
               for (int i = 0; i < 8; ++i)
                 dst[i] = make_float4(__uint_as_float(orr[4 * i]) * inv_l,
@@ -762,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
             for (int i = 0; i < 16; ++i)
               packed[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
                                       __uint_as_float(orr[2 * i + 1]) * inv_l);
-            uint4* dst = reinterpret_cast<uint4*>(out + row_off * D + 32 * c);
+            uint4* dst = reinterpret_cast<uint4*>(out + row_off * D + DO * hf + 32 * c);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
@@ -772,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_fwd_kernel(const __grid_consta
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.o_free);
-        if (row_valid) {
+        if (row_valid && hf == 0) {
           const float lse_row =
               l > 0.f ? (m_ref + (log2f(l) - (FP8 ? kFp8Shift : 0.f))) * 0.69314718055994531f
                       : -INFINITY;
@@ -809,7 +860,7 @@ cudaError_t launch(const FwdParams& p, int num_sms, int max_smem, cudaStream_t s
                      : static_cast<long long>(p.B) * p.H * T;
   }
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  fa_fwd_kernel<D, DEC, FP8><<<grid, kThreads, smem, stream>>>(p);
+  fa_fwd_kernel<D, DEC, FP8><<<grid, Cfg<D, FP8>::THREADS, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
