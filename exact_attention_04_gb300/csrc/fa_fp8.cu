@@ -127,12 +127,19 @@ __global__ void __launch_bounds__(kThreads) quant_rows_kernel(const __nv_bfloat1
 }
 
 // One 128-key block of V to E4M3, transposed: vt[(g*D + c) * npad + key].
+// The codes go to shared memory in V's own layout ([key][D] bytes, rows
+// padded by one word so that rows 16 apart fall in different banks).  The
+// transposed pass gathers 16 keys of a column into one 16-byte store; a warp
+// takes 16 adjacent columns and two adjacent 16-key groups, so each column's
+// two stores fill one 32-byte sector and the shared-memory reads (16 columns
+// = 4 words, two rows 16 apart) hit 8 distinct banks.
 template <int D>
 __global__ void __launch_bounds__(kThreads) quant_vt_kernel(const __nv_bfloat16* v, int N,
                                                             int npad, int nb,
                                                             const float* head_amax,
                                                             uint8_t* vt) {
-  __shared__ __align__(16) uint8_t tile[D][kRowsPerBlock + 16];
+  constexpr int kRow = D + 4;                       // padded row, bytes
+  __shared__ __align__(16) uint8_t tile[kRowsPerBlock * kRow];
   const int blk = blockIdx.x;
   const int g = blk / nb, b = blk % nb;
   float s, mul;
@@ -149,19 +156,26 @@ __global__ void __launch_bounds__(kThreads) quant_vt_kernel(const __nv_bfloat16*
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) f[e] = __fmul_rn(f[e], mul);
-    const uint32_t lo = ptx::pack_e4m3x4(f[0], f[1], f[2], f[3]);
-    const uint32_t hi = ptx::pack_e4m3x4(f[4], f[5], f[6], f[7]);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      tile[c8 * 8 + e][k] = static_cast<uint8_t>(lo >> (8 * e));
-      tile[c8 * 8 + 4 + e][k] = static_cast<uint8_t>(hi >> (8 * e));
-    }
+    uint32_t* row = reinterpret_cast<uint32_t*>(&tile[k * kRow + c8 * 8]);
+    row[0] = ptx::pack_e4m3x4(f[0], f[1], f[2], f[3]);
+    row[1] = ptx::pack_e4m3x4(f[4], f[5], f[6], f[7]);
   }
   __syncthreads();
   for (int it = threadIdx.x; it < D * (kRowsPerBlock / 16); it += kThreads) {
-    const int c = it / (kRowsPerBlock / 16), k16 = it % (kRowsPerBlock / 16);
+    const int rest = it / 32;
+    const int c = (rest % (D / 16)) * 16 + it % 16;
+    const int k16 = (rest / (D / 16)) * 2 + (it / 16) % 2;
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        x |= static_cast<uint32_t>(tile[(16 * k16 + 4 * q + e) * kRow + c]) << (8 * e);
+      w[q] = x;
+    }
     *reinterpret_cast<uint4*>(vt + (static_cast<size_t>(g) * D + c) * npad + b * kRowsPerBlock +
-                              16 * k16) = *reinterpret_cast<const uint4*>(&tile[c][16 * k16]);
+                              16 * k16) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 

@@ -274,6 +274,10 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   volatile int* abort = &sm.abort;
+  // The grid is persistent (every CTA resident from the start), so the merge
+  // kernel that follows a decode launch may be scheduled beside it now; it
+  // waits for this grid's completion before reading the partials.
+  if constexpr (DEC) launch_dependents();
 
   if (threadIdx.x == 0) {
     sm.abort = 0;
@@ -875,6 +879,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
                                                              long long rows) {
   const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
+  grid_dependency_wait();                  // the split kernel's partials are complete
   if (row >= rows) return;
   constexpr int PER = D / 32;
   float m = -INFINITY;
@@ -937,13 +942,24 @@ cudaError_t launch_decode_combine(const FwdParams& p, int d, void* o, float* lse
   const long long rows = static_cast<long long>(p.B) * p.H * p.Nq;
   const unsigned grid = static_cast<unsigned>((rows * 32 + 255) / 256);
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+  // Launched as a programmatic dependent of the split kernel, so its launch
+  // overlaps that kernel's run instead of following its completion.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (d) {
-    case 64: decode_combine_kernel<64><<<grid, 256, 0, stream>>>(p, ob, lse, rows); break;
-    case 128: decode_combine_kernel<128><<<grid, 256, 0, stream>>>(p, ob, lse, rows); break;
-    case 256: decode_combine_kernel<256><<<grid, 256, 0, stream>>>(p, ob, lse, rows); break;
+    case 64: return cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, p, ob, lse, rows);
+    case 128: return cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, p, ob, lse, rows);
+    case 256: return cudaLaunchKernelEx(&cfg, decode_combine_kernel<256>, p, ob, lse, rows);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace fa

@@ -101,6 +101,21 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ dependent launch
+
+// Programmatic dependent launch: once every CTA of this grid has executed
+// launch_dependents (or exited), the next kernel of the stream, if launched
+// with programmatic stream serialisation, may start; it must execute
+// grid_dependency_wait, which returns when this grid has completed and its
+// memory operations are visible, before it reads anything this grid wrote.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
