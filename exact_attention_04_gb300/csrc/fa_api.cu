@@ -1,10 +1,15 @@
 // C-ABI front end: argument validation, TMA tensor maps, the per-device
 // status word, and dispatch to the kernels.  No allocation, no
 // synchronisation (except fa_check), no host copies.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <mutex>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -163,6 +168,64 @@ fa_status_t resolve_variant(const fa_variant_t* var, int H, int causal, Variant*
 }
 
 }  // namespace
+
+namespace fa {
+
+void plan_causal_tail(int BH, int T, int nsplit, int G, bool fwd, long long head_bytes,
+                      TailTable* t) {
+  std::memset(t->item, 0xff, sizeof(t->item));         // every entry -1
+  t->heads = 0;
+  if (BH < 1 || T < 1 || T > 2048 || nsplit < 1 || nsplit > 2 || G < 1 || G > kTailCtas) return;
+  const int P = (T + 1) / 2;
+  const long long fixed = fwd ? 1 : 2;                   // start-up + epilogue, in blocks / steps
+  auto item_cost = [&](int blk) -> long long {
+    return (fwd ? blk + 1 : 2ll * (T - blk)) + fixed;
+  };
+  auto unit_cost = [&](int pp) -> long long {           // the pair (pp, T - 1 - pp)
+    return pp == T - 1 - pp ? item_cost(pp) : item_cost(pp) + item_cost(T - 1 - pp);
+  };
+  std::vector<long long> load(G);
+  std::vector<int> count(G);
+  using Slot = std::pair<long long, int>;                // (work so far, CTA)
+  // about six tail items a CTA on average, at most kTailL2Bytes of streamed
+  // data; fewer heads if a CTA would overflow its row
+  const long long by_l2 = head_bytes > 0 ? std::max(1ll, kTailL2Bytes / head_bytes) : BH;
+  const int first = static_cast<int>(
+      std::max(1ll, std::min({static_cast<long long>(BH), 6ll * G / (T * nsplit), by_l2})));
+  for (int heads = first; heads >= 1; --heads) {
+    std::fill(load.begin(), load.end(), 0ll);
+    std::fill(count.begin(), count.end(), 0);
+    const long long units = static_cast<long long>(BH - heads) * P * nsplit;
+    for (long long u = 0; u < units; ++u)                // round-robin: unit u on CTA u % G
+      load[u % G] += unit_cost(static_cast<int>((u / nsplit) % P));
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> least;
+    for (int c = 0; c < G; ++c) least.push({load[c], c});
+    bool fits = true;
+    for (int r = 0; r < T && fits; ++r) {                // longest first
+      const int blk = fwd ? T - 1 - r : r;
+      for (int h = BH - heads; h < BH && fits; ++h) {
+        for (int s = 0; s < nsplit; ++s) {
+          const Slot top = least.top();
+          least.pop();
+          const int c = top.second;
+          if (count[c] == kTailItems) {
+            fits = false;
+            break;
+          }
+          t->item[c][count[c]++] = tail_code(h, s, blk);
+          least.push({top.first + item_cost(blk), c});
+        }
+      }
+    }
+    if (fits) {
+      t->heads = heads;
+      return;
+    }
+    std::memset(t->item, 0xff, sizeof(t->item));
+  }
+}
+
+}  // namespace fa
 
 extern "C" {
 

@@ -34,6 +34,8 @@
 // D=128 (the next S^T waits until dQ has been drained).  Successive
 // tcgen05.mma issued by one thread execute in order, so an MMA that writes
 // columns an earlier MMA reads as an operand needs no extra wait.
+#include <cstring>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -106,13 +108,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // query heads of kvbh's group and, for each, the query blocks the key block
 // is visible to.  Plain causal: key block n meets query blocks n..T-1, so
 // items n and T-1-n are paired (longest first) and every unit costs T+1
-// steps per query head.  Otherwise: one item per unit, head-major.
+// steps per query head; the last tail.heads heads come as single items from
+// the tail table.  Otherwise: one item per unit, head-major.
+struct BIter {
+  int u, kt, k;
+};
+
 struct BSched {
-  int T, P, units, causal;
-  __device__ BSched(int BH, int N, int causal_) : causal(causal_) {
+  int T, P, units, causal;   // units: the round-robin units
+  __device__ BSched(int BH, int N, int causal_, int tail_heads) : causal(causal_) {
     T = (N + BN - 1) / BN;
     P = (T + 1) / 2;
-    units = causal ? BH * P : BH * T;
+    units = causal ? (BH - tail_heads) * P : BH * T;
   }
   __device__ int nitems(int u) const {
     if (!causal) return 1;
@@ -128,6 +135,26 @@ struct BSched {
       const int p = u % P;
       n = (k == 0) ? p : (T - 1 - p);
     }
+  }
+  // The next item of this CTA; false when it has none left.  Every role walks
+  // the same sequence: the round-robin units, then this CTA's tail row.
+  __device__ bool next(const TailTable& tail, BIter& it, int& bh, int& n) const {
+    while (it.u < units) {
+      if (it.kt < nitems(it.u)) {
+        item(it.u, it.kt, bh, n);
+        ++it.kt;
+        return true;
+      }
+      it.u += gridDim.x;
+      it.kt = 0;
+    }
+    if (!causal || tail.heads == 0 || blockIdx.x >= kTailCtas || it.k >= kTailItems) return false;
+    const int e = tail.item[blockIdx.x][it.k];
+    if (e < 0) return false;
+    ++it.k;
+    bh = tail_head(e);
+    n = tail_block(e);
+    return true;
   }
 };
 
@@ -155,7 +182,8 @@ __device__ __forceinline__ void q_range(const BwdParams& p, int n, int len, int&
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdParams p,
+                                                                   const __grid_constant__ TailTable tail) {
   using C = BCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
@@ -196,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-  const BSched sched(p.B * p.H_kv, p.N, p.causal);
+  const BSched sched(p.B * p.H_kv, p.N, p.causal, tail.heads);
   const int G = p.H / p.H_kv;                     // query heads per K/V head
 
   if (warp == 0) {
@@ -208,10 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       prefetch_tmap(&p.tdo);
       uint32_t w_it = 0, g = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        for (int kt = 0; ok && kt < sched.nitems(u); ++kt) {
-          int kvbh, n, i0, i1;
-          sched.item(u, kt, kvbh, n);
+      BIter it{static_cast<int>(blockIdx.x), 0, 0};
+      for (int kvbh, n; ok && sched.next(tail, it, kvbh, n);) {
+        {
+          int i0, i1;
           q_range(p, n, bwd_len(p, kvbh), i0, i1);
           if (i0 >= i1) continue;
           if (!mbar_wait(&sm.kv_empty, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
@@ -273,10 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
       const uint64_t dDS = sdesc_sw128(smem_u32(sm.ds), CHUNK, 1024);
       uint32_t w_it = 0, g = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        for (int kt = 0; ok && kt < sched.nitems(u); ++kt) {
-          int kvbh, n, i0, i1;
-          sched.item(u, kt, kvbh, n);
+      BIter it{static_cast<int>(blockIdx.x), 0, 0};
+      for (int kvbh, n; ok && sched.next(tail, it, kvbh, n);) {
+        {
+          int i0, i1;
           q_range(p, n, bwd_len(p, kvbh), i0, i1);
           if (i0 >= i1) continue;
           if (!mbar_wait_warp(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
@@ -381,10 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
     __nv_bfloat16* dv_out = static_cast<__nv_bfloat16*>(p.dv);
     uint32_t w_it = 0, g = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-      for (int kt = 0; ok && kt < sched.nitems(u); ++kt) {
-        int kvbh, n, i0, i1;
-        sched.item(u, kt, kvbh, n);
+    BIter it{static_cast<int>(blockIdx.x), 0, 0};
+    for (int kvbh, n; ok && sched.next(tail, it, kvbh, n);) {
+      {
+        int i0, i1;
         const int len = bwd_len(p, kvbh);
         q_range(p, n, len, i0, i1);
         const int key = n * BN + r;
@@ -680,10 +708,23 @@ cudaError_t launch_main(const BwdParams& p, int num_sms, int max_smem, cudaStrea
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int T = (p.N + BN - 1) / BN;
-  const long long units = p.causal ? static_cast<long long>(p.B) * p.H_kv * ((T + 1) / 2)
-                                   : static_cast<long long>(p.B) * p.H_kv * T;
+  const int BH = p.B * p.H_kv;
+  long long units = p.causal ? static_cast<long long>(BH) * ((T + 1) / 2)
+                             : static_cast<long long>(BH) * T;
+  TailTable tail;
+  tail.heads = 0;
+  if (p.causal) {
+    // single key blocks in the tail: up to one CTA per block; the tail's
+    // K/V heads share their group's Q and dO through L2
+    const long long blocks = static_cast<long long>(BH) * T;
+    const int g = static_cast<int>(blocks < num_sms ? blocks : num_sms);
+    const long long qdo_bytes = 2ll * (p.H / p.H_kv) * p.N * D * 2;
+    plan_causal_tail(BH, T, 1, g, false, qdo_bytes, &tail);
+    if (tail.heads > 0) units = g;
+  }
+  if (tail.heads == 0) std::memset(tail.item, 0xff, sizeof(tail.item));
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  bwd_main_kernel<D><<<grid, kThreads, smem, stream>>>(p);
+  bwd_main_kernel<D><<<grid, kThreads, smem, stream>>>(p, tail);
   return cudaGetLastError();
 }
 

@@ -59,13 +59,20 @@ __device__ __forceinline__ void issuer_fail(int* status, volatile int* abort, in
 // query blocks from its diagonal on, so blocks p and T-1-p are paired,
 // longest first.  The halves of one key block are adjacent units so they run
 // at the same time and share K, V, Q, dO in L2.
+// This CTA's place in the schedule: its round-robin units (and the key
+// blocks of a causal pair), then its row of the tail table.
+struct DtIter {
+  int u, kt, k;
+};
+
 struct DtSched {
-  int T, P, per_bh, units, causal, nsplit;
-  __device__ DtSched(int BH, int N, int causal_, int nsplit_) : causal(causal_), nsplit(nsplit_) {
+  int T, P, per_bh, units, causal, nsplit;   // units: the round-robin units
+  __device__ DtSched(int BH, int N, int causal_, int nsplit_, int tail_heads)
+      : causal(causal_), nsplit(nsplit_) {
     T = (N + BK - 1) / BK;
     P = (T + 1) / 2;
     per_bh = causal ? P : T;
-    units = BH * per_bh * nsplit;
+    units = (BH - (causal ? tail_heads : 0)) * per_bh * nsplit;
   }
   __device__ void decode(int u, int& bh, int& pp, int& h) const {
     bh = u / (per_bh * nsplit);
@@ -80,6 +87,29 @@ struct DtSched {
   __device__ int block(int pp, int k) const {
     if (!causal) return pp;
     return (k == 0) ? pp : (T - 1 - pp);
+  }
+  // The next work item of this CTA (K/V head, half of d, key block); false
+  // when it has none left.  Every role walks the same sequence.
+  __device__ bool next(const TailTable& tail, DtIter& it, int& kvbh, int& h, int& n) const {
+    while (it.u < units) {
+      int pp;
+      decode(it.u, kvbh, pp, h);
+      if (it.kt < nitems(pp)) {
+        n = block(pp, it.kt);
+        ++it.kt;
+        return true;
+      }
+      it.u += gridDim.x;
+      it.kt = 0;
+    }
+    if (!causal || tail.heads == 0 || blockIdx.x >= kTailCtas || it.k >= kTailItems) return false;
+    const int e = tail.item[blockIdx.x][it.k];
+    if (e < 0) return false;
+    ++it.k;
+    kvbh = tail_head(e);
+    h = tail_half(e);
+    n = tail_block(e);
+    return true;
   }
 };
 

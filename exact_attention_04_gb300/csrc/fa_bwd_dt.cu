@@ -42,6 +42,8 @@
 // P^T while dQ^T(g) is in flight.  Within one issuer the tensor core keeps
 // issue order, which orders dQ^T(g) after dK(g)'s reads of dS^T(g) in the
 // same columns.
+#include <cstring>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -108,7 +110,8 @@ static_assert(sizeof(DtSmem<128>) <= 232448 && sizeof(DtSmem<256>) <= 232448,
               "shared-memory layout exceeds the per-block limit");
 
 template <int D>
-__global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_constant__ BwdParams p,
+                                                                 const __grid_constant__ TailTable tail) {
   using C = DtCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-  const DtSched sched(p.B * p.H_kv, p.N, p.causal, C::NSPLIT);
+  const DtSched sched(p.B * p.H_kv, p.N, p.causal, C::NSPLIT, tail.heads);
   const int G = p.H / p.H_kv;                     // query heads per K/V head
 
   if (warp == 0) {
@@ -170,11 +173,9 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
       prefetch_tmap(&p.tdo);
       uint32_t w_it = 0, g = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        int kvbh, pp, h;
-        sched.decode(u, kvbh, pp, h);
-        for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
-          const int n = sched.block(pp, kt);
+      DtIter it{static_cast<int>(blockIdx.x), 0, 0};
+      for (int kvbh, h, n; ok && sched.next(tail, it, kvbh, h, n);) {
+        {
           int i0, i1;
           dt_range(p, n, dt_len(p, kvbh), i0, i1);
           if (i0 >= i1) continue;
@@ -237,11 +238,9 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
       const uint64_t dV0 = sdesc_sw128(smem_u32(sm.v), 16, 1024);
       uint32_t w_it = 0, g = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        int kvbh, pp, h;
-        sched.decode(u, kvbh, pp, h);
-        for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
-          const int n = sched.block(pp, kt);
+      DtIter it{static_cast<int>(blockIdx.x), 0, 0};
+      for (int kvbh, h, n; ok && sched.next(tail, it, kvbh, h, n);) {
+        {
           int i0, i1;
           dt_range(p, n, dt_len(p, kvbh), i0, i1);
           if (i0 >= i1) continue;
@@ -333,13 +332,11 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         issuer_fail(p.status, abort, lane, site);
         ok = false;
       };
-      for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-        int kvbh, pp, h;
-        sched.decode(u, kvbh, pp, h);
+      DtIter it{static_cast<int>(blockIdx.x), 0, 0};
+      for (int kvbh, h, n; ok && sched.next(tail, it, kvbh, h, n);) {
         // K[:, h] as the MN-major A operand of dQ^T: 64-column chunks 2h, 2h+1
         const uint64_t dKmn = sdesc_sw128(smem_u32(sm.k) + 2 * h * KCH, KCH, 1024);
-        for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
-          const int n = sched.block(pp, kt);
+        {
           int i0, i1;
           dt_range(p, n, dt_len(p, kvbh), i0, i1);
           if (i0 >= i1) continue;
@@ -414,11 +411,9 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
     __nv_bfloat16* dv_out = static_cast<__nv_bfloat16*>(p.dv);
     uint32_t w_it = 0, g = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-      int kvbh, pp, h;
-      sched.decode(u, kvbh, pp, h);
-      for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
-        const int n = sched.block(pp, kt);
+    DtIter it{static_cast<int>(blockIdx.x), 0, 0};
+    for (int kvbh, h, n; ok && sched.next(tail, it, kvbh, h, n);) {
+      {
         const int len = dt_len(p, kvbh);
         int i0, i1;
         dt_range(p, n, len, i0, i1);
@@ -628,11 +623,9 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
     if (C::DQ_TMA && issuer) prefetch_tmap(&p.tdq);
     uint32_t g = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < sched.units; u += gridDim.x) {
-      int kvbh, pp, h;
-      sched.decode(u, kvbh, pp, h);
-      for (int kt = 0; ok && kt < sched.nitems(pp); ++kt) {
-        const int n = sched.block(pp, kt);
+    DtIter it{static_cast<int>(blockIdx.x), 0, 0};
+    for (int kvbh, h, n; ok && sched.next(tail, it, kvbh, h, n);) {
+      {
         int i0, i1;
         dt_range(p, n, dt_len(p, kvbh), i0, i1);
         StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv));
@@ -729,10 +722,24 @@ cudaError_t launch(const BwdParams& p, int num_sms, int max_smem, cudaStream_t s
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int T = (p.N + BK - 1) / BK;
+  const int BH = p.B * p.H_kv;
+  constexpr int NS = DtCfg<D>::NSPLIT;
   const long long per_bh = p.causal ? (T + 1) / 2 : T;
-  const long long units = static_cast<long long>(p.B) * p.H_kv * per_bh * DtCfg<D>::NSPLIT;
+  long long units = static_cast<long long>(BH) * per_bh * NS;
+  TailTable tail;
+  tail.heads = 0;
+  if (p.causal) {
+    // single key blocks in the tail: up to one CTA per block
+    const long long blocks = static_cast<long long>(BH) * T * NS;
+    const int g = static_cast<int>(blocks < num_sms ? blocks : num_sms);
+    // the tail's K/V heads share their group's Q and dO through L2
+    const long long qdo_bytes = 2ll * (p.H / p.H_kv) * p.N * D * 2;
+    plan_causal_tail(BH, T, NS, g, false, qdo_bytes, &tail);
+    if (tail.heads > 0) units = g;
+  }
+  if (tail.heads == 0) std::memset(tail.item, 0xff, sizeof(tail.item));
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  bwd_dt_kernel<D><<<grid, kThreads, smem, stream>>>(p);
+  bwd_dt_kernel<D><<<grid, kThreads, smem, stream>>>(p, tail);
   return cudaGetLastError();
 }
 

@@ -48,6 +48,8 @@
 // buffers of their own (SEP), so that the S buffer is free as soon as the
 // softmax has read S out of it (s_free); the softmax writes P buffer j % NPB
 // once P_{j-NPB} V has completed.
+#include <cstring>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -151,11 +153,11 @@ __device__ __forceinline__ void record_failure(int* status, volatile int* abort,
 // longest first, so every unit costs T+1 key blocks and the static
 // round-robin assignment is balanced.
 struct Sched {
-  int T, P, units, causal;
-  __device__ Sched(int BH, int N, int causal_) : causal(causal_) {
+  int T, P, units, causal;   // units: the round-robin units (tile pairs when causal)
+  __device__ Sched(int BH, int N, int causal_, int tail_heads) : causal(causal_) {
     T = (N + BM - 1) / BM;
     P = (T + 1) / 2;
-    units = causal ? BH * P : BH * T;
+    units = causal ? (BH - tail_heads) * P : BH * T;
   }
   __device__ int ntiles(int u) const {
     if (!causal) return 1;
@@ -214,11 +216,8 @@ struct Tile {
 };
 
 template <bool DEC>
-__device__ __forceinline__ void make_tile(const FwdParams& p, const Sched& sched, int u, int kt,
-                                          Tile& t) {
+__device__ __forceinline__ void make_tile(const FwdParams& p, int u, int bh, int m, Tile& t) {
   if constexpr (!DEC) {
-    int bh, m;
-    sched.tile(u, kt, bh, m);
     t.qy = m * BM;
     t.qz = bh;
     t.kvbh = kv_head_of(bh, p.H, p.H_kv);
@@ -251,6 +250,43 @@ __device__ __forceinline__ void make_tile(const FwdParams& p, const Sched& sched
   }
 }
 
+// This CTA's place in the schedule: its round-robin units (and the tiles of
+// a causal pair), then its row of the tail table.
+struct TileIter {
+  int u, kt, k;
+};
+
+// The next tile of this CTA into t; false when it has none left.  Every role
+// walks the same sequence.
+template <bool DEC>
+__device__ __forceinline__ bool next_tile(const FwdParams& p, const TailTable& tail,
+                                          const Sched& sched, int nunits, TileIter& it, Tile& t) {
+  if constexpr (DEC) {
+    if (it.u >= nunits) return false;
+    make_tile<true>(p, it.u, 0, 0, t);
+    it.u += gridDim.x;
+    return true;
+  } else {
+    while (it.u < sched.units) {
+      if (it.kt < sched.ntiles(it.u)) {
+        int bh, m;
+        sched.tile(it.u, it.kt, bh, m);
+        ++it.kt;
+        make_tile<false>(p, 0, bh, m, t);
+        return true;
+      }
+      it.u += gridDim.x;
+      it.kt = 0;
+    }
+    if (tail.heads == 0 || blockIdx.x >= kTailCtas || it.k >= kTailItems) return false;
+    const int e = tail.item[blockIdx.x][it.k];
+    if (e < 0) return false;
+    ++it.k;
+    make_tile<false>(p, 0, tail_head(e), tail_block(e), t);
+    return true;
+  }
+}
+
 // All 32 lanes wait; the decision is made uniform across the warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   bool ok = mbar_wait(bar, parity, abort, kWaitTimeoutNs);
@@ -259,7 +295,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 template <int D, bool DEC, bool FP8>
 __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
-    fa_fwd_kernel(const __grid_constant__ FwdParams p) {
+    fa_fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ TailTable tail) {
   static_assert(!(DEC && FP8), "decode runs in bf16");
   using C = Cfg<D, FP8>;
   using Smem = FwdSmem<D, FP8>;
@@ -312,7 +348,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
   const int BH = p.B * p.H;
-  const Sched sched(BH, p.N, p.causal);
+  const Sched sched(BH, p.N, p.causal, DEC ? 0 : tail.heads);
   const int nunits = DEC ? p.B * p.H_kv * p.splits : sched.units;
 
   if (warp == 0) {
@@ -323,10 +359,9 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
       if constexpr (!C::SEP) prefetch_tmap(&p.tv);
       uint32_t q_it = 0, k_it = 0, v_it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-        for (int kt = 0; ok && kt < (DEC ? 1 : sched.ntiles(u)); ++kt) {
-          Tile t;
-          make_tile<DEC>(p, sched, u, kt, t);
+      TileIter it{static_cast<int>(blockIdx.x), 0, 0};
+      for (Tile t; ok && next_tile<DEC>(p, tail, sched, nunits, it, t);) {
+        {
           const int jlo = t.jlo, nkv = t.nkv;
           if (nkv == 0) continue;
           const int kvbh = t.kvbh;
@@ -399,10 +434,9 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
       prefetch_tmap(&p.tv);
       uint32_t v_it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-        for (int kt = 0; ok && kt < (DEC ? 1 : sched.ntiles(u)); ++kt) {
-          Tile t;
-          make_tile<DEC>(p, sched, u, kt, t);
+      TileIter it{static_cast<int>(blockIdx.x), 0, 0};
+      for (Tile t; ok && next_tile<DEC>(p, tail, sched, nunits, it, t);) {
+        {
           const int jlo = t.jlo, nkv = t.nkv;
           const int kvbh = t.kvbh;
           for (int j = 0; j < nkv; ++j) {
@@ -443,10 +477,9 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
       const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q), 16, 1024);
       uint32_t q_it = 0, g = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-        for (int kt = 0; ok && kt < (DEC ? 1 : sched.ntiles(u)); ++kt) {
-          Tile t;
-          make_tile<DEC>(p, sched, u, kt, t);
+      TileIter it{static_cast<int>(blockIdx.x), 0, 0};
+      for (Tile t; ok && next_tile<DEC>(p, tail, sched, nunits, it, t);) {
+        {
           const int nkv = t.nkv;
           if (nkv == 0) continue;
           if (!mbar_wait_warp(&sm.q_full, q_it & 1, abort, kWaitTimeoutNs)) {
@@ -503,10 +536,9 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
       constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3_f32(BM, D, 0, 0) : idesc_bf16_f32(BM, D, 0, 1);
       uint32_t g = 0, t_it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-        for (int kt = 0; ok && kt < (DEC ? 1 : sched.ntiles(u)); ++kt) {
-          Tile t;
-          make_tile<DEC>(p, sched, u, kt, t);
+      TileIter it{static_cast<int>(blockIdx.x), 0, 0};
+      for (Tile t; ok && next_tile<DEC>(p, tail, sched, nunits, it, t);) {
+        {
           const int nkv = t.nkv;
           if (nkv == 0) continue;
           for (int j = 0; j < nkv; ++j, ++g) {
@@ -586,10 +618,9 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
       ++hs;
       return true;
     };
-    for (int u = blockIdx.x; ok && u < nunits; u += gridDim.x) {
-      for (int kt = 0; ok && kt < (DEC ? 1 : sched.ntiles(u)); ++kt) {
-        Tile t;
-        make_tile<DEC>(p, sched, u, kt, t);
+    TileIter it{static_cast<int>(blockIdx.x), 0, 0};
+    for (Tile t; ok && next_tile<DEC>(p, tail, sched, nunits, it, t);) {
+      {
         const int len = t.len, jlo = t.jlo, nkv = t.nkv;
         const int row = DEC ? t.qlo + row_local % p.Nq : t.qlo + row_local;   // query position
         // FP8: scores come out of the MMA in units of sq * sk
@@ -855,16 +886,28 @@ cudaError_t launch(const FwdParams& p, int num_sms, int max_smem, cudaStream_t s
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  TailTable tail;
+  tail.heads = 0;
   long long units;
   if (DEC) {
     units = static_cast<long long>(p.B) * p.H_kv * p.splits;
   } else {
     const int T = (p.N + BM - 1) / BM;
-    units = p.causal ? static_cast<long long>(p.B) * p.H * ((T + 1) / 2)
-                     : static_cast<long long>(p.B) * p.H * T;
+    const int BH = p.B * p.H;
+    units = p.causal ? static_cast<long long>(BH) * ((T + 1) / 2) : static_cast<long long>(BH) * T;
+    if (p.causal) {
+      // single tiles in the tail: up to one CTA per tile
+      const long long tiles = static_cast<long long>(BH) * T;
+      const int g = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+      // the tail's heads share their K and V through L2
+      const long long kv_bytes = 2ll * p.N * D * (FP8 ? 1 : 2);
+      plan_causal_tail(BH, T, 1, g, true, kv_bytes, &tail);
+      if (tail.heads > 0) units = g;
+    }
   }
+  if (tail.heads == 0) std::memset(tail.item, 0xff, sizeof(tail.item));
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  fa_fwd_kernel<D, DEC, FP8><<<grid, Cfg<D, FP8>::THREADS, smem, stream>>>(p);
+  fa_fwd_kernel<D, DEC, FP8><<<grid, Cfg<D, FP8>::THREADS, smem, stream>>>(p, tail);
   return cudaGetLastError();
 }
 

@@ -64,6 +64,40 @@ struct BwdParams {
   int* status;
 };
 
+// Causal schedules.  A causal work item (a query tile of the forward, a key
+// block of the backward) costs in proportion to its distance from one end of
+// the sequence, so items are paired (longest with shortest) into units of
+// equal cost and the units go round-robin over the CTAs.  Whole rounds of
+// equal units leave the last round part-empty; so the units of the last
+// `heads` heads are not paired: their single items, longest first, each go to
+// the CTA that has the least work so far (planned on the host).  Row c of
+// `item` lists CTA c's items in the order it runs them, after its paired units.
+constexpr int kTailCtas = 160;               // grids above this take no tail
+constexpr int kTailItems = 8;                // items a CTA may take from the tail
+struct TailTable {
+  int heads;                                 // 0: no tail, every unit round-robin
+  int item[kTailCtas][kTailItems];           // tail_code(head, half, block), -1 ends a row
+};
+__host__ __device__ constexpr int tail_code(int head, int half, int blk) {
+  return (head << 12) | (half << 11) | blk;
+}
+__host__ __device__ constexpr int tail_head(int code) { return code >> 12; }
+__host__ __device__ constexpr int tail_half(int code) { return (code >> 11) & 1; }
+__host__ __device__ constexpr int tail_block(int code) { return code & 2047; }
+
+// Plans the tail of a causal schedule over BH heads of T blocks (times
+// nsplit halves of the head dimension) on G CTAs.  fwd: query tile m costs
+// m + 1 key blocks; backward: key block n costs 2 (T - n) query steps; each
+// item also costs a fixed start-up and epilogue.  head_bytes: what the items
+// of one head stream and share through L2 (K and V for the forward, the
+// group's Q and dO for the backward).  The tail runs all its heads at once,
+// so it takes at most kTailL2Bytes of them.  Sets t->heads = 0 (no tail)
+// when the table cannot describe it (G > kTailCtas, T > 2048, or a CTA would
+// take more than kTailItems items).
+constexpr long long kTailL2Bytes = 64ll << 20;
+void plan_causal_tail(int BH, int T, int nsplit, int G, bool fwd, long long head_bytes,
+                      TailTable* t);
+
 // Wait site recorded when the dynamic shared memory cannot hold the kernel's
 // layout at a 1024-byte aligned base.
 constexpr int kSiteSmemLayout = 99;

@@ -1,0 +1,148 @@
+"""Host-side checks of the causal schedule planner (no GPU needed).
+
+A causal work item costs in proportion to its distance from one end of the
+sequence: query tile m of the forward sees m + 1 key blocks, key block n of
+the backward is seen by 2 (T - n) query steps.  The kernels pair items into
+equal units that go round-robin over the CTAs (unit u on CTA u % G), except
+for the last `heads` heads, whose single items the host places, longest
+first, on the least-loaded CTA.  The kernels walk each CTA's round-robin
+units, then its row of the table.
+
+These tests call the planner in the built library and check the plan it
+returns:
+- the paired units and the table together hold every (head, half, block)
+  exactly once;
+- rows are -1-terminated and within their capacity;
+- each CTA's items run longest first;
+- the plan beats plain round-robin of pairs.
+"""
+import ctypes
+
+import pytest
+
+from exact_attention_04_gb300 import build as fabuild
+from exact_attention_04_gb300 import fa
+
+TAIL_CTAS, TAIL_ITEMS = 160, 8
+PLAN = "_ZN2fa16plan_causal_tailEiiiibxPNS_9TailTableE"  # fa::plan_causal_tail, Itanium ABI
+
+
+class TailTable(ctypes.Structure):
+    _fields_ = [("heads", ctypes.c_int), ("item", (ctypes.c_int * TAIL_ITEMS) * TAIL_CTAS)]
+
+
+@pytest.fixture(scope="module")
+def plan():
+    fabuild.build()
+    lib = fa.load()
+    f = getattr(lib, PLAN)
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_bool,
+                  ctypes.c_longlong, ctypes.POINTER(TailTable)]
+    f.restype = None
+
+    def run(BH, T, nsplit, G, fwd, head_bytes=0):
+        t = TailTable()
+        f(BH, T, nsplit, G, fwd, head_bytes, ctypes.byref(t))
+        return t
+    return run
+
+
+def cost(T, fwd, blk):
+    return (blk + 1 if fwd else 2 * (T - blk)) + (1 if fwd else 2)
+
+
+def items_of_pair(T, pp):
+    return [pp] if pp == T - 1 - pp else [pp, T - 1 - pp]
+
+
+def walk(t, BH, T, nsplit, G, fwd):
+    """Each CTA's items as the kernels walk them: (head, half, block) lists."""
+    P = (T + 1) // 2
+    units = (BH - t.heads) * P * nsplit
+    per_cta = [[] for _ in range(G)]
+    for u in range(units):
+        bh, rem = divmod(u, P * nsplit)
+        pp, h = divmod(rem, nsplit)
+        for n in items_of_pair(T, pp):
+            per_cta[u % G].append((bh, h, n))
+    for c in range(G):
+        row = list(t.item[c]) if c < TAIL_CTAS else []
+        seen_end = False
+        for e in row:
+            if e < 0:
+                seen_end = True
+                continue
+            assert not seen_end, f"CTA {c}: an entry after the end of its row"
+            per_cta[c].append((e >> 12, (e >> 11) & 1, e & 2047))
+    return per_cta
+
+
+SHAPES = [
+    # BH, T, nsplit, G, fwd
+    (32, 64, 1, 152, True),      # B=2, H=16, N=8192 forward
+    (32, 64, 1, 152, False),     # its backward, d = 128
+    (32, 64, 2, 152, False),     # d = 256: two halves of the head dimension
+    (64, 64, 1, 152, True),      # B=2, H=32
+    (16, 64, 1, 152, False),     # GQA: B=2, H_kv=8
+    (96, 8, 1, 152, True),       # B=8, H=12, N=1024
+    (1, 2, 1, 2, True),          # B=1, H=1, N=256: two tiles, two CTAs
+    (4, 5, 1, 20, False),        # odd T: the middle pair is a single item
+    (2, 3, 2, 12, False),
+    (8, 256, 1, 152, True),      # long sequence, few heads
+]
+
+
+@pytest.mark.parametrize("BH,T,nsplit,G,fwd", SHAPES)
+def test_plan_covers_every_item_once(plan, BH, T, nsplit, G, fwd):
+    t = plan(BH, T, nsplit, G, fwd)
+    assert 0 <= t.heads <= BH
+    got = sorted(x for c in walk(t, BH, T, nsplit, G, fwd) for x in c)
+    want = sorted((bh, h, n) for bh in range(BH) for h in range(nsplit) for n in range(T))
+    assert got == want
+    for c in range(TAIL_CTAS):
+        for e in t.item[c]:
+            if e >= 0:
+                assert e >> 12 >= BH - t.heads, "a tail item outside the tail heads"
+
+
+@pytest.mark.parametrize("BH,T,nsplit,G,fwd", SHAPES)
+def test_tail_items_run_longest_first(plan, BH, T, nsplit, G, fwd):
+    t = plan(BH, T, nsplit, G, fwd)
+    for c in range(min(G, TAIL_CTAS)):
+        costs = [cost(T, fwd, e & 2047) for e in t.item[c] if e >= 0]
+        assert costs == sorted(costs, reverse=True)
+
+
+@pytest.mark.parametrize("BH,T,nsplit,G,fwd,bound", [
+    (32, 64, 1, 152, True, 0.015), (32, 64, 1, 152, False, 0.015),
+    (64, 64, 1, 152, True, 0.015), (96, 8, 1, 152, True, 0.05)])
+def test_plan_balances_the_causal_step(plan, BH, T, nsplit, G, fwd, bound):
+    """The busiest CTA's work within `bound` of the mean, where plain
+    round-robin of equal pairs leaves the last round part-empty (3.9 % above
+    the mean at B=2, H=16, N=8192 and 18.75 % at B=8, H=12, N=1024)."""
+    t = plan(BH, T, nsplit, G, fwd)
+    assert t.heads > 0
+    loads = [sum(cost(T, fwd, n) for _, _, n in c) for c in walk(t, BH, T, nsplit, G, fwd)]
+    mean = sum(loads) / G
+    assert max(loads) <= mean * (1 + bound)
+    P = (T + 1) // 2
+    rr = [0] * G
+    for u in range(BH * P * nsplit):
+        rr[u % G] += sum(cost(T, fwd, n) for n in items_of_pair(T, (u // nsplit) % P))
+    assert max(loads) < max(rr)
+
+
+def test_tail_heads_fit_their_l2_share(plan):
+    """The tail runs its heads at once: at most 64 MB of what they share."""
+    mb = 1 << 20
+    assert plan(32, 64, 1, 152, True, 4 * mb).heads == 14      # K+V of N=8192, d=128: 56 MB
+    assert plan(32, 64, 1, 152, True, 8 * mb).heads == 8       # d = 256
+    assert plan(32, 64, 1, 152, True, 100 * mb).heads == 1
+    assert plan(32, 64, 1, 152, True, 0).heads == 14           # no limit: six items a CTA
+
+
+def test_plan_declines_what_the_table_cannot_hold(plan):
+    assert plan(32, 64, 1, TAIL_CTAS + 1, True).heads == 0     # too many CTAs
+    assert plan(1, 4096, 1, 152, True).heads == 0              # blocks past 2047
+    t = plan(32, 64, 1, 152, True)
+    assert all(t.item[c][k] == -1 for c in range(152, TAIL_CTAS) for k in range(TAIL_ITEMS))
