@@ -618,6 +618,95 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
       ++hs;
       return true;
     };
+    // The epilogue of a tile (O / l into bf16 O, and LSE): run once the next
+    // tile's first block of P is written, so that the softmax warps spend the
+    // wait for this tile's last P V on that block instead of idling; the next
+    // tile's first P V waits for o_free, so O is read before it is replaced.
+    auto epilogue = [&](uint32_t last, float l, float m_ref, size_t row_off, bool row_valid,
+                        int kvbh) -> bool {
+      // wait for the tile's last P V, then O / l and LSE
+      if (!warp_wait(&sm.pv_done[last % C::NPB], (last / C::NPB) & 1, abort)) {
+        if (lane == 0) record_failure(p.status, abort, kSiteSmEpi);
+        return false;
+      }
+      tc_fence_after_sync();
+      // FP8: P entered the product as 16 P (and l sums 16 P), V in units
+      // of its head scale
+      const float inv_l = l > 0.f ? (FP8 ? __ldg(p.v_scale + kvbh) / l : 1.f / l) : 0.f;
+      // O leaves tensor memory up to 128 columns a batch, each batch on one
+      // wait; after the last batch the P V issuer may start the next tile
+      // while the rows are scaled and stored.  Each thread stores its own
+      // row, 32 bytes a store (16 when O is only 16-byte aligned), so a warp
+      // store touches half as many lines as with 16-byte stores.
+      constexpr int OB = DO < 128 ? DO / 32 : 4;          // 32-column chunks a batch
+      const bool st32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+#pragma unroll 1
+      for (int c0 = 0; c0 < DO / 32; c0 += OB) {
+        uint32_t orr[OB * 32];
+#pragma unroll
+        for (int c = 0; c < OB; ++c) tmem_ld_x32(t_o + 32 * (c0 + c), orr + 32 * c);
+        tmem_wait_ld();
+        reg_fence<OB * 32>(orr);
+        if (c0 + OB == DO / 32) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.o_free);
+        }
+        if constexpr (DEC) {
+          if (row_valid) {
+            // the workspace is 256-byte aligned and a row is D floats
+            float* dst = p.o_part + row_off * D + DO * hf + 32 * c0;
+#pragma unroll
+            for (int i = 0; i < OB * 4; ++i) {
+              uint32_t r8[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) r8[e] = __float_as_uint(__uint_as_float(orr[8 * i + e]) * inv_l);
+              st_global_v8(dst + 8 * i, r8);
+            }
+          }
+        } else if (row_valid) {
+          __nv_bfloat16* dst = out + row_off * D + DO * hf + 32 * c0;
+#pragma unroll
+          for (int i = 0; i < OB * 2; ++i) {                // 16 columns a step
+            uint32_t pk8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              pk8[e] = pack_bf16x2(__uint_as_float(orr[16 * i + 2 * e]) * inv_l,
+                                   __uint_as_float(orr[16 * i + 2 * e + 1]) * inv_l);
+            if (st32) {
+              st_global_v8(dst + 16 * i, pk8);
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * i);
+              d4[0] = make_uint4(pk8[0], pk8[1], pk8[2], pk8[3]);
+              d4[1] = make_uint4(pk8[4], pk8[5], pk8[6], pk8[7]);
+            }
+          }
+        }
+      }
+      if (row_valid && hf == 0) {
+        const float lse_row =
+            l > 0.f ? (m_ref + (log2f(l) - (FP8 ? kFp8Shift : 0.f))) * 0.69314718055994531f
+                    : -INFINITY;
+        if constexpr (DEC)
+          p.lse_part[row_off] = lse_row;
+        else
+          p.lse[row_off] = lse_row;
+      }
+      return true;
+    };
+    struct Pending {
+      bool on;
+      uint32_t last;
+      float l, m_ref;
+      size_t row_off;
+      bool row_valid;
+      int kvbh;
+    } pend{false, 0u, 0.f, 0.f, 0, false, 0};
+    auto finish = [&]() -> bool {
+      if (!pend.on) return true;
+      pend.on = false;
+      return epilogue(pend.last, pend.l, pend.m_ref, pend.row_off, pend.row_valid, pend.kvbh);
+    };
     TileIter it{static_cast<int>(blockIdx.x), 0, 0};
     for (Tile t; ok && next_tile<DEC>(p, tail, sched, nunits, it, t);) {
       {
@@ -628,6 +717,10 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
         const bool row_valid = row_local < t.rows;
         const size_t row_off = static_cast<size_t>(t.out0 + row_local);
         if (nkv == 0) {
+          if (!finish()) {
+            ok = false;
+            break;
+          }
           if (row_valid) {
             if constexpr (DEC) {
               float4* dst = reinterpret_cast<float4*>(p.o_part + row_off * D + DO * hf);
@@ -803,6 +896,11 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.p_full[pb]);
           ++kv_it;
+          // the previous tile's epilogue, now that this tile's first P is out
+          if (j == 0 && !finish()) {
+            ok = false;
+            break;
+          }
         }
         if (!ok) break;
         if constexpr (C::NHALF == 2) {
@@ -815,60 +913,10 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           }
           l += l_other;
         }
-        // epilogue: wait for the tile's last P V, then O / l and LSE
-        const uint32_t last = kv_it - 1;
-        if (!warp_wait(&sm.pv_done[last % C::NPB], (last / C::NPB) & 1, abort)) {
-          if (lane == 0) record_failure(p.status, abort, kSiteSmEpi);
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        // FP8: P entered the product as 16 P (and l sums 16 P), V in units
-        // of its head scale
-        const float inv_l = l > 0.f ? (FP8 ? __ldg(p.v_scale + t.kvbh) / l : 1.f / l) : 0.f;
-#pragma unroll 1
-        for (int c = 0; c < DO / 32; ++c) {
-          uint32_t orr[32];
-          tmem_ld_x32(t_o + 32 * c, orr);
-          tmem_wait_ld();
-          reg_fence<32>(orr);
-          if constexpr (DEC) {
-            if (row_valid) {
-              float4* dst = reinterpret_cast<float4*>(p.o_part + row_off * D + DO * hf + 32 * c);
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(__uint_as_float(orr[4 * i]) * inv_l,
-                                     __uint_as_float(orr[4 * i + 1]) * inv_l,
-                                     __uint_as_float(orr[4 * i + 2]) * inv_l,
-                                     __uint_as_float(orr[4 * i + 3]) * inv_l);
-            }
-          } else if (row_valid) {
-            uint32_t packed[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              packed[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
-                                      __uint_as_float(orr[2 * i + 1]) * inv_l);
-            uint4* dst = reinterpret_cast<uint4*>(out + row_off * D + DO * hf + 32 * c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                  packed[4 * i + 3]);
-          }
-        }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.o_free);
-        if (row_valid && hf == 0) {
-          const float lse_row =
-              l > 0.f ? (m_ref + (log2f(l) - (FP8 ? kFp8Shift : 0.f))) * 0.69314718055994531f
-                      : -INFINITY;
-          if constexpr (DEC)
-            p.lse_part[row_off] = lse_row;
-          else
-            p.lse[row_off] = lse_row;
-        }
+        pend = {true, kv_it - 1, l, m_ref, row_off, row_valid, t.kvbh};
       }
     }
+    if (ok && !finish()) ok = false;
   }
 
   tc_fence_before_sync();
