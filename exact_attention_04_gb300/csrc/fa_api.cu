@@ -177,7 +177,10 @@ void plan_causal_tail(int BH, int T, int nsplit, int G, bool fwd, long long head
   t->heads = 0;
   if (BH < 1 || T < 1 || T > 2048 || nsplit < 1 || nsplit > 2 || G < 1 || G > kTailCtas) return;
   const int P = (T + 1) / 2;
-  const long long fixed = fwd ? 1 : 2;                   // start-up + epilogue, in blocks / steps
+  // start-up and epilogue of an item, in blocks / steps: a clock64 trace of
+  // one CTA puts a forward tile boundary near 3 key blocks' time and a
+  // backward key-block boundary near 4 query steps'
+  const long long fixed = fwd ? 3 : 4;
   auto item_cost = [&](int blk) -> long long {
     return (fwd ? blk + 1 : 2ll * (T - blk)) + fixed;
   };

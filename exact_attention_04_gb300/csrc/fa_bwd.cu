@@ -668,8 +668,9 @@ __global__ void __launch_bounds__(256) bwd_post_kernel(const __grid_constant__ B
 }
 
 // dQ = bf16(scale * dQ_acc^T) from the [BH, D, Npad] accumulator.  Thread
-// (bh, column group c8, query q): lanes run over q, so each of its 8 column
-// reads is a coalesced 128-byte row segment; it writes 8 bf16 of query q.
+// (bh, column group c16, query q): lanes run over q, so each of its 16 column
+// reads is a coalesced 128-byte row segment; it writes 16 bf16 of query q in
+// one 32-byte store (two 16-byte stores when dQ is only 16-byte aligned).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_post_t_kernel(const __grid_constant__ BwdParams p,
                                                          long long total) {
@@ -677,19 +678,24 @@ __global__ void __launch_bounds__(256) bwd_post_t_kernel(const __grid_constant__
   if (t >= total) return;
   const int q = static_cast<int>(t % p.Npad);
   const long long rest = t / p.Npad;
-  const int c8 = static_cast<int>(rest % (D / 8));
-  const long long bh = rest / (D / 8);
+  const int c16 = static_cast<int>(rest % (D / 16));
+  const long long bh = rest / (D / 16);
   if (q >= p.N) return;
-  const float* src = p.dq_acc + (bh * D + c8 * 8) * p.Npad + q;
-  float a[8];
+  const float* src = p.dq_acc + (bh * D + c16 * 16) * p.Npad + q;
+  float a[16];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) a[j] = src[static_cast<size_t>(j) * p.Npad] * p.scale;
-  uint4 out;
-  out.x = pack_bf16x2(a[0], a[1]);
-  out.y = pack_bf16x2(a[2], a[3]);
-  out.z = pack_bf16x2(a[4], a[5]);
-  out.w = pack_bf16x2(a[6], a[7]);
-  reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.dq) + (bh * p.N + q) * D)[c8] = out;
+  for (int j = 0; j < 16; ++j) a[j] = src[static_cast<size_t>(j) * p.Npad] * p.scale;
+  uint32_t pk[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) pk[j] = pack_bf16x2(a[2 * j], a[2 * j + 1]);
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.dq) + (bh * p.N + q) * D + c16 * 16;
+  if ((reinterpret_cast<uintptr_t>(p.dq) & 31u) == 0) {
+    st_global_v8(dst, pk);
+  } else {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  }
 }
 
 template <int D>
@@ -753,7 +759,7 @@ cudaError_t launch_bwd_post(const BwdParams& p, int d, cudaStream_t stream) {
     bwd_post_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(p, n8);
     return cudaGetLastError();
   }
-  const long long total = static_cast<long long>(p.B) * p.H * (d / 8) * p.Npad;
+  const long long total = static_cast<long long>(p.B) * p.H * (d / 16) * p.Npad;
   const unsigned grid = static_cast<unsigned>((total + 255) / 256);
   switch (d) {
     case 128: bwd_post_t_kernel<128><<<grid, 256, 0, stream>>>(p, total); break;

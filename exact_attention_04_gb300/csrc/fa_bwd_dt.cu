@@ -409,6 +409,11 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
     const float c2 = p.scale_log2;
     __nv_bfloat16* dk_out = static_cast<__nv_bfloat16*>(p.dk);
     __nv_bfloat16* dv_out = static_cast<__nv_bfloat16*>(p.dv);
+    // Each thread stores its own key row; 32-byte stores (when both outputs
+    // are 32-byte aligned) halve the lines a warp store touches, which is
+    // what the dK/dV epilogue at the end of a key block waits on.
+    const bool st32 = ((reinterpret_cast<uintptr_t>(dk_out) | reinterpret_cast<uintptr_t>(dv_out)) &
+                       31u) == 0;
     uint32_t w_it = 0, g = 0;
     bool ok = true;
     DtIter it{static_cast<int>(blockIdx.x), 0, 0};
@@ -599,12 +604,20 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
               pkk[t] = pack_bf16x2(__uint_as_float(bb[2 * t]) * p.scale,
                                    __uint_as_float(bb[2 * t + 1]) * p.scale);
             }
-            uint4* dvp = reinterpret_cast<uint4*>(dv_out + out_off + 32 * c4);
-            uint4* dkp = reinterpret_cast<uint4*>(dk_out + out_off + 32 * c4);
+            if (st32) {
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              dvp[t] = make_uint4(pv[4 * t], pv[4 * t + 1], pv[4 * t + 2], pv[4 * t + 3]);
-              dkp[t] = make_uint4(pkk[4 * t], pkk[4 * t + 1], pkk[4 * t + 2], pkk[4 * t + 3]);
+              for (int t = 0; t < 2; ++t) {
+                st_global_v8(dv_out + out_off + 32 * c4 + 16 * t, pv + 8 * t);
+                st_global_v8(dk_out + out_off + 32 * c4 + 16 * t, pkk + 8 * t);
+              }
+            } else {
+              uint4* dvp = reinterpret_cast<uint4*>(dv_out + out_off + 32 * c4);
+              uint4* dkp = reinterpret_cast<uint4*>(dk_out + out_off + 32 * c4);
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                dvp[t] = make_uint4(pv[4 * t], pv[4 * t + 1], pv[4 * t + 2], pv[4 * t + 3]);
+                dkp[t] = make_uint4(pkk[4 * t], pkk[4 * t + 1], pkk[4 * t + 2], pkk[4 * t + 3]);
+              }
             }
           }
         }

@@ -48,7 +48,7 @@ def plan():
 
 
 def cost(T, fwd, blk):
-    return (blk + 1 if fwd else 2 * (T - blk)) + (1 if fwd else 2)
+    return (blk + 1 if fwd else 2 * (T - blk)) + (3 if fwd else 4)
 
 
 def items_of_pair(T, pp):
@@ -115,11 +115,12 @@ def test_tail_items_run_longest_first(plan, BH, T, nsplit, G, fwd):
 
 @pytest.mark.parametrize("BH,T,nsplit,G,fwd,bound", [
     (32, 64, 1, 152, True, 0.015), (32, 64, 1, 152, False, 0.015),
-    (64, 64, 1, 152, True, 0.015), (96, 8, 1, 152, True, 0.05)])
+    (64, 64, 1, 152, True, 0.015), (96, 8, 1, 152, True, 0.1)])
 def test_plan_balances_the_causal_step(plan, BH, T, nsplit, G, fwd, bound):
     """The busiest CTA's work within `bound` of the mean, where plain
-    round-robin of equal pairs leaves the last round part-empty (3.9 % above
-    the mean at B=2, H=16, N=8192 and 18.75 % at B=8, H=12, N=1024)."""
+    round-robin of equal pairs leaves the last round part-empty (about 4 %
+    above the mean at B=2, H=16, N=8192 and 19 % at B=8, H=12, N=1024, where
+    an item costs 4 to 11 against a mean of 38 a CTA)."""
     t = plan(BH, T, nsplit, G, fwd)
     assert t.heads > 0
     loads = [sum(cost(T, fwd, n) for _, _, n in c) for c in walk(t, BH, T, nsplit, G, fwd)]
