@@ -561,34 +561,50 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           break;
         }
         tc_fence_after_sync();
-#pragma unroll 1
+        // dV and dK rows leave tensor memory on one wait; the accumulators are
+        // then free for the next key block while the rows are converted and
+        // stored, 32 bytes a store when both outputs are 32-byte aligned
+        static_assert(D == 64, "this kernel serves d = 64");
+        uint32_t a[D], b[D];
+#pragma unroll
         for (int c4 = 0; c4 < D / 32; ++c4) {
-          uint32_t a[32], b[32];
-          tmem_ld_x32(t_lane + C::TM_DV + 32 * c4, a);
-          tmem_ld_x32(t_lane + C::TM_DK + 32 * c4, b);
-          tmem_wait_ld();
-          reg_fence<32>(a);
-          reg_fence<32>(b);
-          if (key < p.N) {
-            uint32_t pv[16], pk[16];
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-              pv[t] = pack_bf16x2(__uint_as_float(a[2 * t]), __uint_as_float(a[2 * t + 1]));
-              pk[t] = pack_bf16x2(__uint_as_float(b[2 * t]) * p.scale,
-                                  __uint_as_float(b[2 * t + 1]) * p.scale);
-            }
-            uint4* dvp = reinterpret_cast<uint4*>(dv_out + key_off * D + 32 * c4);
-            uint4* dkp = reinterpret_cast<uint4*>(dk_out + key_off * D + 32 * c4);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              dvp[t] = make_uint4(pv[4 * t], pv[4 * t + 1], pv[4 * t + 2], pv[4 * t + 3]);
-              dkp[t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
-            }
-          }
+          tmem_ld_x32(t_lane + C::TM_DV + 32 * c4, a + 32 * c4);
+          tmem_ld_x32(t_lane + C::TM_DK + 32 * c4, b + 32 * c4);
         }
+        tmem_wait_ld();
+        reg_fence<D>(a);
+        reg_fence<D>(b);
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.acc_free);
+        if (key < p.N) {
+          const bool st32 = ((reinterpret_cast<uintptr_t>(dk_out) |
+                              reinterpret_cast<uintptr_t>(dv_out)) & 31u) == 0;
+#pragma unroll
+          for (int c16 = 0; c16 < D / 16; ++c16) {          // 16 columns a step
+            uint32_t pv[8], pk[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              pv[t] = pack_bf16x2(__uint_as_float(a[16 * c16 + 2 * t]),
+                                  __uint_as_float(a[16 * c16 + 2 * t + 1]));
+              pk[t] = pack_bf16x2(__uint_as_float(b[16 * c16 + 2 * t]) * p.scale,
+                                  __uint_as_float(b[16 * c16 + 2 * t + 1]) * p.scale);
+            }
+            __nv_bfloat16* dvp = dv_out + key_off * D + 16 * c16;
+            __nv_bfloat16* dkp = dk_out + key_off * D + 16 * c16;
+            if (st32) {
+              st_global_v8(dvp, pv);
+              st_global_v8(dkp, pk);
+            } else {
+              uint4* v4 = reinterpret_cast<uint4*>(dvp);
+              uint4* k4 = reinterpret_cast<uint4*>(dkp);
+              v4[0] = make_uint4(pv[0], pv[1], pv[2], pv[3]);
+              v4[1] = make_uint4(pv[4], pv[5], pv[6], pv[7]);
+              k4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              k4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+          }
+        }
         ++w_it;
       }
     }
