@@ -25,7 +25,9 @@
 //               l, writes P = exp2(S*c - m) as bf16 into one of NPB P
 //               buffers in tensor memory,
 //               rescales its row of O when m moved, and runs the epilogue
-//               O / l, LSE = (m + log2 l) * ln 2.
+//               O / l, LSE = (m + log2 l) * ln 2 (bf16: after the next
+//               tile's first block, so that the wait for the tile's last
+//               P V is spent on that block).
 //
 // The recurrence is the online softmax of "注意力为什么受限于显存带宽：用算术
 // 强度与分块把 FlashAttention 推导清楚" (section 六) and "4. FlashAttention 深度
@@ -150,8 +152,10 @@ __device__ __forceinline__ void record_failure(int* status, volatile int* abort,
 // Static persistent schedule.  Non-causal: one unit per (bh, q-tile), bh-major
 // so CTAs running at the same time share K/V in L2.  Causal: a unit pairs
 // q-tile T-1-p (longest: T-p key blocks) with q-tile p (p+1 key blocks), the
-// longest first, so every unit costs T+1 key blocks and the static
-// round-robin assignment is balanced.
+// longest first, so every unit costs T+1 key blocks; the units go
+// round-robin, except those of the last tail_heads heads, whose single tiles
+// come from the host-planned tail table (longest first on the least-loaded
+// CTA), so that the last round of equal units does not leave CTAs idle.
 struct Sched {
   int T, P, units, causal;   // units: the round-robin units (tile pairs when causal)
   __device__ Sched(int BH, int N, int causal_, int tail_heads) : causal(causal_) {
