@@ -171,8 +171,11 @@ fa_status_t resolve_variant(const fa_variant_t* var, int H, int causal, Variant*
 
 namespace fa {
 
-void plan_causal_tail(int BH, int T, int nsplit, int G, bool fwd, long long head_bytes,
-                      TailTable* t) {
+namespace {
+
+// The plan itself (see plan_causal_tail).
+void plan_tail_uncached(int BH, int T, int nsplit, int G, bool fwd, long long head_bytes,
+                        TailTable* t) {
   std::memset(t->item, 0xff, sizeof(t->item));         // every entry -1
   t->heads = 0;
   if (BH < 1 || T < 1 || T > 2048 || nsplit < 1 || nsplit > 2 || G < 1 || G > kTailCtas) return;
@@ -184,39 +187,50 @@ void plan_causal_tail(int BH, int T, int nsplit, int G, bool fwd, long long head
   auto item_cost = [&](int blk) -> long long {
     return (fwd ? blk + 1 : 2ll * (T - blk)) + fixed;
   };
-  auto unit_cost = [&](int pp) -> long long {           // the pair (pp, T - 1 - pp)
-    return pp == T - 1 - pp ? item_cost(pp) : item_cost(pp) + item_cost(T - 1 - pp);
-  };
-  std::vector<long long> load(G);
-  std::vector<int> count(G);
-  using Slot = std::pair<long long, int>;                // (work so far, CTA)
+  std::vector<long long> unit_cost(P);                   // the pair (pp, T - 1 - pp)
+  for (int pp = 0; pp < P; ++pp)
+    unit_cost[pp] = pp == T - 1 - pp ? item_cost(pp) : item_cost(pp) + item_cost(T - 1 - pp);
   // about six tail items a CTA on average, at most kTailL2Bytes of streamed
   // data; fewer heads if a CTA would overflow its row
   const long long by_l2 = head_bytes > 0 ? std::max(1ll, kTailL2Bytes / head_bytes) : BH;
   const int first = static_cast<int>(
       std::max(1ll, std::min({static_cast<long long>(BH), 6ll * G / (T * nsplit), by_l2})));
+  // with this many rounds of equal units the last one does not matter
+  if (static_cast<long long>(BH - first) * P * nsplit > (1ll << 18)) return;
+  std::vector<long long> load(G);
+  std::vector<int> count(G);
+  using Slot = std::pair<long long, int>;                // (work so far, CTA)
   for (int heads = first; heads >= 1; --heads) {
     std::fill(load.begin(), load.end(), 0ll);
     std::fill(count.begin(), count.end(), 0);
+    // round-robin: unit u (pair (u / nsplit) % P of its head) on CTA u % G
     const long long units = static_cast<long long>(BH - heads) * P * nsplit;
-    for (long long u = 0; u < units; ++u)                // round-robin: unit u on CTA u % G
-      load[u % G] += unit_cost(static_cast<int>((u / nsplit) % P));
+    int c = 0, half = 0, pp = 0;
+    for (long long u = 0; u < units; ++u) {
+      load[c] += unit_cost[pp];
+      if (++c == G) c = 0;
+      if (++half == nsplit) {
+        half = 0;
+        if (++pp == P) pp = 0;
+      }
+    }
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> least;
-    for (int c = 0; c < G; ++c) least.push({load[c], c});
+    for (int k = 0; k < G; ++k) least.push({load[k], k});
     bool fits = true;
     for (int r = 0; r < T && fits; ++r) {                // longest first
       const int blk = fwd ? T - 1 - r : r;
+      const long long cost = item_cost(blk);
       for (int h = BH - heads; h < BH && fits; ++h) {
         for (int s = 0; s < nsplit; ++s) {
           const Slot top = least.top();
           least.pop();
-          const int c = top.second;
-          if (count[c] == kTailItems) {
+          const int k = top.second;
+          if (count[k] == kTailItems) {
             fits = false;
             break;
           }
-          t->item[c][count[c]++] = tail_code(h, s, blk);
-          least.push({top.first + item_cost(blk), c});
+          t->item[k][count[k]++] = tail_code(h, s, blk);
+          least.push({top.first + cost, k});
         }
       }
     }
@@ -226,6 +240,55 @@ void plan_causal_tail(int BH, int T, int nsplit, int G, bool fwd, long long head
     }
     std::memset(t->item, 0xff, sizeof(t->item));
   }
+}
+
+// The last few plans: a training loop asks for the same few shapes on every
+// step, and a plan is a pure function of its arguments.
+struct TailPlanCache {
+  struct Entry {
+    bool used;
+    int BH, T, nsplit, G;
+    bool fwd;
+    long long head_bytes;
+    TailTable table;
+  };
+  static constexpr int kEntries = 8;
+  std::mutex mu;
+  Entry e[kEntries] = {};
+  int next = 0;
+};
+
+TailPlanCache& tail_plan_cache() {
+  static TailPlanCache cache;
+  return cache;
+}
+
+}  // namespace
+
+void plan_causal_tail(int BH, int T, int nsplit, int G, bool fwd, long long head_bytes,
+                      TailTable* t) {
+  TailPlanCache& cache = tail_plan_cache();
+  {
+    std::lock_guard<std::mutex> lock(cache.mu);
+    for (const auto& en : cache.e)
+      if (en.used && en.BH == BH && en.T == T && en.nsplit == nsplit && en.G == G &&
+          en.fwd == fwd && en.head_bytes == head_bytes) {
+        *t = en.table;
+        return;
+      }
+  }
+  plan_tail_uncached(BH, T, nsplit, G, fwd, head_bytes, t);
+  std::lock_guard<std::mutex> lock(cache.mu);
+  TailPlanCache::Entry& en = cache.e[cache.next];
+  cache.next = (cache.next + 1) % TailPlanCache::kEntries;
+  en.used = true;
+  en.BH = BH;
+  en.T = T;
+  en.nsplit = nsplit;
+  en.G = G;
+  en.fwd = fwd;
+  en.head_bytes = head_bytes;
+  en.table = *t;
 }
 
 }  // namespace fa

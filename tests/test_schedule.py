@@ -147,3 +147,17 @@ def test_plan_declines_what_the_table_cannot_hold(plan):
     assert plan(1, 4096, 1, 152, True).heads == 0              # blocks past 2047
     t = plan(32, 64, 1, 152, True)
     assert all(t.item[c][k] == -1 for c in range(152, TAIL_CTAS) for k in range(TAIL_ITEMS))
+
+
+def test_plan_is_repeatable_across_interleaved_calls(plan):
+    """Plans are memoised per argument set; interleaved calls with other
+    arguments must not hand back another shape's table."""
+    shapes = [(32, 64, 1, 152, True, 4 << 20), (32, 64, 1, 152, False, 4 << 20),
+              (96, 8, 1, 152, True, 1 << 20), (32, 64, 2, 152, False, 8 << 20),
+              (16, 64, 1, 152, False, 16 << 20)]
+    first = [plan(*s) for s in shapes]
+    for _ in range(3):                      # more calls than the memo holds between repeats
+        for s, t0 in zip(shapes[::-1], first[::-1]):
+            t = plan(*s)
+            assert t.heads == t0.heads
+            assert all(list(t.item[c]) == list(t0.item[c]) for c in range(TAIL_CTAS))
