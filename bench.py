@@ -473,6 +473,13 @@ def run_e2e(rs, w, fa, steps, flops_step, dist):
                         "their own streams while step s computes (two device buffer sets)"}
 
 
+def visible_pairs(L, N, causal):
+    """(query, key) pairs of one head that a key-padding length L leaves
+    visible: every query sees keys j < L (and j <= i when causal)."""
+    L = max(0, min(L, N))
+    return L * (L + 1) // 2 + (N - L) * L if causal else N * L
+
+
 def run_sweep(fa, peaks, only=None):
     """Every other workload, timed briefly: TFLOP/s, fraction of peak, GB/s of
     algorithmic traffic (inputs read + outputs written once).  only: keep the
@@ -526,6 +533,14 @@ def run_sweep(fa, peaks, only=None):
                           "bwd_gbs": round(bwd_bytes / (bwd_ms * 1e-3) / 1e9, 1)})
         if w.backward and not r.backward:
             entry["bwd"] = "not built for this head dimension"
+        if inp["kv_len"] is not None and w.window is None:
+            # key padding: the headline convention counts every (query, key)
+            # pair; this second figure counts only the pairs a query can see
+            uf = 4.0 * w.H * w.d * sum(visible_pairs(int(L), w.N, w.causal)
+                                       for L in inp["kv_len"].tolist())
+            entry["useful_fwd_tflops"] = round(uf / (fwd_ms * 1e-3) / 1e12, 2)
+            if r.backward:
+                entry["useful_bwd_tflops"] = round(2.5 * uf / (bwd_ms * 1e-3) / 1e12, 2)
         del r
         torch.cuda.empty_cache()
         if w.d in (128, 256):
