@@ -285,12 +285,13 @@ class Fp8Runner:
             f()
 
 
-def time_steps(runner, steps, flush=None):
-    """Per-phase and per-step device times (ms) over `steps` timed steps."""
+def time_steps(runner, steps, flush=None, median=False):
+    """Per-phase and per-step device times (ms) over `steps` timed steps.
+    Per phase: the mean launch time, or with median=True the median."""
     phases = runner.phases()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
           for _ in range(steps)]
-    per_phase = {name: 0.0 for name, _ in phases}
+    per_phase = {name: [] for name, _ in phases}
     step_ms = []
     for s in range(steps):
         if flush is not None:
@@ -302,9 +303,10 @@ def time_steps(runner, steps, flush=None):
     torch.cuda.synchronize()
     for s in range(steps):
         for i, (name, _) in enumerate(phases):
-            per_phase[name] += ev[s][i].elapsed_time(ev[s][i + 1])
+            per_phase[name].append(ev[s][i].elapsed_time(ev[s][i + 1]))
         step_ms.append(ev[s][0].elapsed_time(ev[s][-1]))
-    return {k: v / steps for k, v in per_phase.items()}, step_ms
+    pick = statistics.median if median else (lambda v: sum(v) / len(v))
+    return {k: pick(v) for k, v in per_phase.items()}, step_ms
 
 
 def bytes_of(*ts):
@@ -509,8 +511,8 @@ def run_sweep(fa, peaks, only=None):
         for _ in range(3):
             r.step()
         torch.cuda.synchronize()
-        steps = 10
-        per_phase, _ = time_steps(r, steps, flush=lambda: flush_l2(flush_buf))
+        steps = 20
+        per_phase, _ = time_steps(r, steps, flush=lambda: flush_l2(flush_buf), median=True)
         fa.fa_check()
         fwd_ms = per_phase["fa_fwd_kernel"]
         rowb = w.B * w.H * w.N               # query rows
@@ -522,7 +524,8 @@ def run_sweep(fa, peaks, only=None):
                  "fwd_tflops": round(w.fwd_flops() / (fwd_ms * 1e-3) / 1e12, 2),
                  "fwd_frac_of_peak": round(w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
                                            / peaks["bf16_tflops"], 4),
-                 "fwd_gbs": round(fwd_bytes / (fwd_ms * 1e-3) / 1e9, 1)}
+                 "fwd_gbs": round(fwd_bytes / (fwd_ms * 1e-3) / 1e9, 1),
+                 "timing": "median of 20 steps, L2 flushed before each"}
         if r.backward:
             bwd_ms = sum(v for k, v in per_phase.items() if k != "fa_fwd_kernel")
             bwd_bytes = 8 * rowb * w.d + 8 * kvrowb * w.d + 12 * rowb   # Q,O,dO,dQ; K,V,dK,dV
@@ -558,7 +561,7 @@ def sweep_fp8(w, inp, fa, peaks, flush_buf):
     for _ in range(3):
         r.step()
     torch.cuda.synchronize()
-    per_phase, _ = time_steps(r, 10, flush=lambda: flush_l2(flush_buf))
+    per_phase, _ = time_steps(r, 20, flush=lambda: flush_l2(flush_buf), median=True)
     fa.fa_check()
     qb = w.B * w.H * w.N * w.d
     kb = w.B * w.kv_heads * w.N * w.d
@@ -588,9 +591,9 @@ def sweep_decode(w, inp, fa, peaks, flush_buf):
     qrows = w.B * w.H * w.queries
     kv_bytes = 4 * w.B * w.kv_heads * w.N * w.d           # K and V, bf16, read once
     nbytes = kv_bytes + 4 * qrows * w.d + 4 * qrows       # + Q, O (bf16) and LSE
-    per_phase, _ = time_steps(r, 20, flush=lambda: flush_l2(flush_buf))
+    per_phase, _ = time_steps(r, 20, flush=lambda: flush_l2(flush_buf), median=True)
     ms_flush = per_phase["fa_decode"]
-    per_phase, _ = time_steps(r, 20)
+    per_phase, _ = time_steps(r, 20, median=True)
     ms = per_phase["fa_decode"]
     fa.fa_check()
     l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 129 * 10 ** 6)
@@ -607,7 +610,8 @@ def sweep_decode(w, inp, fa, peaks, flush_buf):
                 round(nbytes / (ms_flush * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "bytes": nbytes,
             "l2": ("K and V larger than L2, back to back" if large else
-                   "flushed between steps")}
+                   "flushed between steps"),
+            "timing": "median of 20 steps each way"}
 
 
 # ------------------------------------------------------------------ the oracle as baseline
