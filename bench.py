@@ -639,13 +639,41 @@ def oracle_sample(w, inp):
     return run, flops, threads, desc
 
 
+# the small configurations the fp64 oracle runs whole, every head
+ORACLE_WHOLE = ("single_head_b1_h1_n256_d64", "bert_large_b16_h16_n512_d64_pad",
+                "gpt2_small_b8_h12_n1024_d64_causal")
+
+
+def oracle_whole(name):
+    """Seconds and TFLOP/s of the fp64 oracle on a whole small workload
+    (forward, and backward where the workload has one) on every host core."""
+    import oracle
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    f64 = {n: inp[n].float().double().numpy() for n in ("q", "k", "v")}
+    kv = None if inp["kv_len"] is None else [int(x) for x in inp["kv_len"].tolist()]
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.attention_fwd(f64["q"], f64["k"], f64["v"], w.scale, causal=w.causal, kv_len=kv,
+                         threads=threads)
+    if w.backward:
+        do = inp["do"].float().double().numpy()
+        oracle.attention_bwd(f64["q"], f64["k"], f64["v"], do, w.scale, causal=w.causal,
+                             kv_len=kv, threads=threads)
+    sec = time.perf_counter() - t0
+    flops = w.fwd_flops() + (w.bwd_flops() if w.backward else 0.0)
+    return {"workload": name, "pass": "fwd+bwd" if w.backward else "fwd",
+            "seconds": round(sec, 3), "tflops": round(flops / sec / 1e12, 6)}
+
+
 def cpu_baseline(w, inp):
     run, flops, threads, desc = oracle_sample(w, inp)
     t0 = time.perf_counter()
     run()
     sec = time.perf_counter() - t0
     return {"value": round(flops / sec / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
-            "kind": "oracle", "sample": desc, "seconds": round(sec, 3)}
+            "kind": "oracle", "sample": desc, "seconds": round(sec, 3),
+            "whole_small_configs": [oracle_whole(n) for n in ORACLE_WHOLE]}
 
 
 def run_reference(args, dist):
