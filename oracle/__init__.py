@@ -38,6 +38,14 @@ def _load():
         lib.fa_oracle_forward_v.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_int,
                                             c_double, c_int, ip, c_int, c_int, c_int]
         lib.fa_oracle_forward_v.restype = c_int
+        u8p = ctypes.POINTER(ctypes.c_ubyte)
+        lib.fa_oracle_forward_m.argtypes = [dp, dp, dp, dp, dp, c_int, c_int, c_int, c_int, c_int,
+                                            c_double, c_int, ip, c_int, c_int, u8p, c_int, c_int]
+        lib.fa_oracle_forward_m.restype = c_int
+        lib.fa_oracle_backward_m.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, c_int, c_int, c_int,
+                                             c_int, c_int, c_double, c_int, ip, c_int, c_int,
+                                             u8p, c_int, c_int]
+        lib.fa_oracle_backward_m.restype = c_int
         lib.fa_oracle_forward_rows_v.argtypes = [dp, dp, dp, c_int, c_int, c_double, c_int, c_int,
                                                  c_int, c_int, ip, c_int, dp, dp, c_int]
         lib.fa_oracle_forward_rows_v.restype = c_int
@@ -86,6 +94,20 @@ def _window(window):
     return wl, wr
 
 
+def _block_mask(block_mask, N, block):
+    """(array, pointer) of a block mask: a [ceil(N/block), ceil(N/block)]
+    array, nonzero where a (query block, key block) pair is computed."""
+    if block_mask is None:
+        return None, None
+    if block < 1:
+        raise ValueError("block size must be positive")
+    t = -(-N // block)
+    bm = np.ascontiguousarray((np.asarray(block_mask) != 0).astype(np.uint8))
+    if bm.shape != (t, t):
+        raise ValueError(f"block mask must be [{t}, {t}] for N={N}, block {block}")
+    return bm, _ptr(bm, ctypes.c_ubyte)
+
+
 def _heads(q, k):
     B, H, N, d = q.shape
     Hkv = k.shape[1]
@@ -94,21 +116,25 @@ def _heads(q, k):
     return B, H, Hkv, N, d
 
 
-def attention_fwd(q, k, v, scale, causal=False, kv_len=None, threads=None, window=None):
+def attention_fwd(q, k, v, scale, causal=False, kv_len=None, threads=None, window=None,
+                  block_mask=None, block=128):
     """O [B,H,N,d] and LSE [B,H,N] of exact attention (float64 numpy arrays).
 
     k, v are [B,H_kv,N,d] with H_kv dividing H (query head h reads K/V head
-    h // (H // H_kv)); window is flash-attn's (left, right), -1 = unbounded."""
+    h // (H // H_kv)); window is flash-attn's (left, right), -1 = unbounded;
+    block_mask, [ceil(N/block)]^2, hides the keys of every (query block, key
+    block) pair where it is zero, for every head."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, Hkv, N, d = _heads(q, k)
     assert v.shape == k.shape
     wl, wr = _window(window)
+    bm, bmp = _block_mask(block_mask, N, block)
     o = np.empty_like(q)
     lse = np.empty((B, H, N), dtype=np.float64)
     kv, kvp = _kv(kv_len, B)
-    rc = _load().fa_oracle_forward_v(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv,
-                                     N, d, float(scale), int(bool(causal)), kvp, wl, wr,
-                                     threads or default_threads())
+    rc = _load().fa_oracle_forward_m(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Hkv,
+                                     N, d, float(scale), int(bool(causal)), kvp, wl, wr, bmp,
+                                     int(block), threads or default_threads())
     if rc:
         raise RuntimeError(f"oracle forward failed ({rc})")
     return o, lse
@@ -133,20 +159,22 @@ def attention_fwd_rows(q, k, v, rows, scale, causal=False, kv_len=None, threads=
     return o, lse
 
 
-def attention_bwd(q, k, v, do, scale, causal=False, kv_len=None, threads=None, window=None):
+def attention_bwd(q, k, v, do, scale, causal=False, kv_len=None, threads=None, window=None,
+                  block_mask=None, block=128):
     """dQ [B,H,N,d], dK and dV [B,H_kv,N,d] (summed over each group's query
-    heads) and D [B,H,N] (D_i = sum_j P_ij dP_ij)."""
+    heads) and D [B,H,N] (D_i = sum_j P_ij dP_ij); masks as in attention_fwd."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     B, H, Hkv, N, d = _heads(q, k)
     assert v.shape == k.shape and do.shape == q.shape
     wl, wr = _window(window)
+    bm, bmp = _block_mask(block_mask, N, block)
     dq = np.empty_like(q)
     dk, dv = np.empty_like(k), np.empty_like(k)
     D = np.empty((B, H, N), dtype=np.float64)
     kv, kvp = _kv(kv_len, B)
-    rc = _load().fa_oracle_backward_v(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
+    rc = _load().fa_oracle_backward_m(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq), _ptr(dk),
                                       _ptr(dv), _ptr(D), B, H, Hkv, N, d, float(scale),
-                                      int(bool(causal)), kvp, wl, wr,
+                                      int(bool(causal)), kvp, wl, wr, bmp, int(block),
                                       threads or default_threads())
     if rc:
         raise RuntimeError(f"oracle backward failed ({rc})")

@@ -42,8 +42,12 @@
  * indices).  The window is the (left, right) pair of flash-attn's
  * window_size argument, (-1, -1) meaning no window ("炉案与百步之外的仓库：
  * Flash Attention 与注意力计算的工艺极限" section 六; "4. FlashAttention 深度
- * 剖析" 4.8.1, sliding window).  A row with no visible key gets O = 0 and
- * LSE = -inf.
+ * 剖析" 4.8.1, sliding window).  A block mask (the coarse block-level mask
+ * matrix of "炉案与百步之外的仓库…" 第八部分, Block-Sparse FlashAttention)
+ * hides further keys: with blocks of bs rows and bs columns, key j is
+ * visible to query i only if entry (i / bs, j / bs) of the row-major
+ * [ceil(N/bs), ceil(N/bs)] byte matrix is nonzero.  A row with no visible key
+ * gets O = 0 and LSE = -inf.
  *
  * Grouped K/V heads (GQA / MQA, the same section 六 and the FlashAttention-2
  * summary in "注意力为什么受限于显存带宽…" section 九): K and V have
@@ -73,6 +77,8 @@ typedef struct {
     int causal;
     long len;          /* kv_len of the batch entry */
     long wl, wr;       /* window: -1 = unbounded on that side */
+    const unsigned char *bm;   /* block mask or NULL */
+    long bs, tk;       /* its block size and row length (blocks of keys) */
 } mask_t;
 
 static int key_visible(long i, long j, const mask_t *m)
@@ -81,6 +87,7 @@ static int key_visible(long i, long j, const mask_t *m)
     if (m->causal && j > i) return 0;
     if (m->wl >= 0 && j < i - m->wl) return 0;
     if (m->wr >= 0 && j > i + m->wr) return 0;
+    if (m->bm && !m->bm[(i / m->bs) * m->tk + j / m->bs]) return 0;
     return 1;
 }
 
@@ -142,14 +149,18 @@ int fa_oracle_num_threads(void)
 }
 
 /* Forward over every (b, h) and every row; K/V head of query head h is
- * h / (H / H_kv), window (wl, wr) as in the header. */
-int fa_oracle_forward_v(const double *q, const double *k, const double *v,
+ * h / (H / H_kv), window (wl, wr) and block mask (bm, bs) as in the header
+ * (bm NULL: none). */
+int fa_oracle_forward_m(const double *q, const double *k, const double *v,
                         double *o, double *lse,
                         int B, int H, int H_kv, int N, int d, double scale, int causal,
-                        const int *kv_len, int wl, int wr, int nthreads)
+                        const int *kv_len, int wl, int wr, const unsigned char *bm, int bs,
+                        int nthreads)
 {
-    if (!check_args(q, k, v, B, H, N, d) || !o || !lse || !check_heads(H, H_kv))
+    if (!check_args(q, k, v, B, H, N, d) || !o || !lse || !check_heads(H, H_kv) ||
+        (bm && bs < 1))
         return ORACLE_EINVAL;
+    const long tk = bm ? ((long)N + bs - 1) / bs : 0;
     if (nthreads < 1) nthreads = 1;
     const long hd = (long)N * d;
     const int group = H / H_kv;
@@ -157,7 +168,7 @@ int fa_oracle_forward_v(const double *q, const double *k, const double *v,
     for (long bh = 0; bh < (long)B * H; ++bh) {
         const long b = bh / H;
         const long kvh = b * H_kv + (bh % H) / group;
-        const mask_t mk = {causal, kv_len ? kv_len[b] : N, wl, wr};
+        const mask_t mk = {causal, kv_len ? kv_len[b] : N, wl, wr, bm, bm ? bs : 1, tk};
         const double *Q = q + bh * hd, *K = k + kvh * hd, *V = v + kvh * hd;
         double *O = o + bh * hd, *L = lse + bh * (long)N;
 #pragma omp parallel num_threads(nthreads)
@@ -189,6 +200,15 @@ int fa_oracle_forward_v(const double *q, const double *k, const double *v,
     return ORACLE_OK;
 }
 
+int fa_oracle_forward_v(const double *q, const double *k, const double *v,
+                        double *o, double *lse,
+                        int B, int H, int H_kv, int N, int d, double scale, int causal,
+                        const int *kv_len, int wl, int wr, int nthreads)
+{
+    return fa_oracle_forward_m(q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, kv_len, wl, wr,
+                               NULL, 1, nthreads);
+}
+
 int fa_oracle_forward(const double *q, const double *k, const double *v,
                       double *o, double *lse,
                       int B, int H, int N, int d, double scale, int causal,
@@ -205,7 +225,7 @@ int fa_oracle_forward_rows_v(const double *q, const double *k, const double *v,
                              const int *rows, int nrows,
                              double *o_rows, double *lse_rows, int nthreads)
 {
-    const mask_t mk = {causal, len, wl, wr};
+    const mask_t mk = {causal, len, wl, wr, NULL, 1, 0};
     if (!check_args(q, k, v, 1, 1, N, d) || !rows || !o_rows || !lse_rows || nrows < 0)
         return ORACLE_EINVAL;
     for (int r = 0; r < nrows; ++r)
@@ -252,15 +272,17 @@ int fa_oracle_forward_rows(const double *q, const double *k, const double *v,
  * (sums over the query heads of each group); D is [B,H,N]
  * (D_i = sum_j P_ij dP_ij).  P is rebuilt from its definition, not from a
  * stored LSE, so the oracle does not depend on the forward's outputs. */
-int fa_oracle_backward_v(const double *q, const double *k, const double *v,
+int fa_oracle_backward_m(const double *q, const double *k, const double *v,
                          const double *dout,
                          double *dq, double *dk, double *dv, double *D,
                          int B, int H, int H_kv, int N, int d, double scale, int causal,
-                         const int *kv_len, int wl, int wr, int nthreads)
+                         const int *kv_len, int wl, int wr, const unsigned char *bm, int bs,
+                         int nthreads)
 {
     if (!check_args(q, k, v, B, H, N, d) || !dout || !dq || !dk || !dv || !D ||
-        !check_heads(H, H_kv))
+        !check_heads(H, H_kv) || (bm && bs < 1))
         return ORACLE_EINVAL;
+    const long tk = bm ? ((long)N + bs - 1) / bs : 0;
     if (nthreads < 1) nthreads = 1;
     const long hd = (long)N * d;
     const int group = H / H_kv;
@@ -270,7 +292,7 @@ int fa_oracle_backward_v(const double *q, const double *k, const double *v,
     for (long bh = 0; bh < (long)B * H; ++bh) {
         const long b = bh / H;
         const long kvh = b * H_kv + (bh % H) / group;
-        const mask_t mk = {causal, kv_len ? kv_len[b] : N, wl, wr};
+        const mask_t mk = {causal, kv_len ? kv_len[b] : N, wl, wr, bm, bm ? bs : 1, tk};
         const double *Q = q + bh * hd, *K = k + kvh * hd, *V = v + kvh * hd;
         const double *dO = dout + bh * hd;
         double *dQ = dq + bh * hd, *dK = dk + kvh * hd, *dV = dv + kvh * hd;
@@ -332,6 +354,16 @@ int fa_oracle_backward_v(const double *q, const double *k, const double *v,
     return ORACLE_OK;
 }
 
+int fa_oracle_backward_v(const double *q, const double *k, const double *v,
+                         const double *dout,
+                         double *dq, double *dk, double *dv, double *D,
+                         int B, int H, int H_kv, int N, int d, double scale, int causal,
+                         const int *kv_len, int wl, int wr, int nthreads)
+{
+    return fa_oracle_backward_m(q, k, v, dout, dq, dk, dv, D, B, H, H_kv, N, d, scale, causal,
+                                kv_len, wl, wr, NULL, 1, nthreads);
+}
+
 int fa_oracle_backward(const double *q, const double *k, const double *v,
                        const double *dout,
                        double *dq, double *dk, double *dv, double *D,
@@ -366,7 +398,7 @@ int fa_oracle_decode(const double *q, const double *k, const double *v,
         const long kvh = b * H_kv + (bh % H) / group;
         long len = kv_len ? kv_len[b] : Nk;
         if (len > Nk) len = Nk;
-        const mask_t mk = {causal, len, wl, wr};
+        const mask_t mk = {causal, len, wl, wr, NULL, 1, 0};
         const double *Q = q + bh * qd, *K = k + kvh * kd, *V = v + kvh * kd;
         double *O = o + bh * qd, *L = lse + bh * (long)Nq;
 #pragma omp parallel num_threads(nthreads)
