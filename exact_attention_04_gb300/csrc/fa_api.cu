@@ -147,10 +147,12 @@ size_t round_up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // The variant as the kernels see it: K/V heads, and the window folded with
 // causal into the bounds wl, wr (key j visible to query i iff
 // i - wl <= j <= i + wr), unbounded sides as fa::kUnbounded.  `pair` is true
-// for plain causal attention, where the schedule pairs long and short tiles.
+// for plain causal attention (no block mask), where the schedule pairs long
+// and short tiles.  bm: the block mask or nullptr.
 struct Variant {
   int H_kv, wl, wr;
   bool pair;
+  const uint8_t* bm;
 };
 
 fa_status_t resolve_variant(const fa_variant_t* var, int H, int causal, Variant* out) {
@@ -163,7 +165,8 @@ fa_status_t resolve_variant(const fa_variant_t* var, int H, int causal, Variant*
   out->wl = left < 0 ? fa::kUnbounded : left;
   out->wr = right < 0 ? fa::kUnbounded : right;
   if (causal && out->wr > 0) out->wr = 0;
-  out->pair = causal && left < 0;
+  out->bm = var ? var->block_mask : nullptr;
+  out->pair = causal && left < 0 && !out->bm;
   return FA_OK;
 }
 
@@ -346,6 +349,8 @@ fa_status_t fa_fwd_v(const void* q, const void* k, const void* v, void* o, float
   p.wl = var.wl;
   p.wr = var.wr;
   p.causal = var.pair ? 1 : 0;
+  p.block_mask = var.bm;
+  p.bm_t = (N + 127) / 128;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.status = di->status;
   if (fa::launch_fwd(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -380,6 +385,7 @@ fa_status_t bwd_setup(fa::BwdParams* p, DeviceInfo** di, int B, int H, int N, in
   Variant var;
   const fa_status_t vs = resolve_variant(variant, H, causal, &var);
   if (vs != FA_OK) return vs;
+  if (var.bm) return FA_ERR_UNSUPPORTED;
   if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
   *di = device_info(nullptr);
   if (!*di || (*di)->err != cudaSuccess) return FA_ERR_CUDA;
@@ -585,6 +591,7 @@ fa_status_t fa_decode(const void* q, const void* k, const void* v, void* o, floa
   Variant var;
   const fa_status_t vs = resolve_variant(variant, H, causal, &var);
   if (vs != FA_OK) return vs;
+  if (var.bm) return FA_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H * Nq * d >= (1ll << 31) ||
       static_cast<long long>(B) * var.H_kv * Nk * d >= (1ll << 31))
     return FA_ERR_INVALID_ARG;
@@ -691,6 +698,8 @@ fa_status_t fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8,
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.nb = nb;
+  p.block_mask = var.bm;
+  p.bm_t = nb;
   return fa::launch_fwd_fp8(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? FA_OK

@@ -213,7 +213,9 @@ struct Tile {
   int kvbh;            // K/V head
   int len;             // keys of the batch entry (kv_len)
   int qlo, qhi;        // query positions of the tile's first and last row
-  int jlo, nkv;        // key blocks [jlo, jlo + nkv)
+  int jlo, nkv;        // key blocks [jlo, jend), nkv of them not masked out
+  int jend;
+  const uint8_t* bmrow;  // block-mask row of the tile's query block, or nullptr
   long long out0;      // output row of tile row 0
   int rows;            // rows of the tile that are real queries
   int qs;              // index of the tile's Q scale (FP8)
@@ -229,6 +231,13 @@ __device__ __forceinline__ void make_tile(const FwdParams& p, int u, int bh, int
     t.qlo = m * BM;
     t.qhi = m * BM + BM - 1;
     t.nkv = tile_blocks(p, m, t.len, t.jlo);
+    t.jend = t.jlo + t.nkv;
+    t.bmrow = p.block_mask ? p.block_mask + static_cast<size_t>(m) * p.bm_t : nullptr;
+    if (t.bmrow) {
+      int n = 0;
+      for (int jb = t.jlo; jb < t.jend; ++jb) n += __ldg(t.bmrow + jb) != 0;
+      t.nkv = n;
+    }
     t.out0 = static_cast<long long>(bh) * p.N + m * BM;
     t.rows = p.N - m * BM < BM ? p.N - m * BM : BM;
     t.qs = bh * p.nb + m;
@@ -248,10 +257,21 @@ __device__ __forceinline__ void make_tile(const FwdParams& p, int u, int bh, int
     if (k_hi > c0 + p.chunk_blocks * BN) k_hi = c0 + p.chunk_blocks * BN;
     t.jlo = k_lo / BN;
     t.nkv = k_hi > k_lo ? (k_hi + BN - 1) / BN - t.jlo : 0;
+    t.jend = t.jlo + t.nkv;
+    t.bmrow = nullptr;
     t.out0 = static_cast<long long>(split) * p.B * p.H * p.Nq + row0;
     t.rows = (p.H / p.H_kv) * p.Nq;
     t.qs = 0;
   }
+}
+
+// The first key block at or after jb that the tile computes: every block of
+// [jlo, jend) without a block mask, else those whose mask byte is nonzero
+// (every role walks the same sequence).
+__device__ __forceinline__ int next_block(const Tile& t, int jb) {
+  if (t.bmrow)
+    while (jb < t.jend && __ldg(t.bmrow + jb) == 0) ++jb;
+  return jb;
 }
 
 // This CTA's place in the schedule: its round-robin units (and the tiles of
@@ -379,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d(sm.q + c * CHUNK, &p.tq, &sm.q_full, C::BOX_COLS * c, t.qy, t.qz);
           ++q_it;
-          for (int j = 0; j < nkv; ++j) {
+          for (int j = 0, jb = next_block(t, t.jlo); j < nkv; ++j, jb = next_block(t, jb + 1)) {
             const int st = k_it % C::STAGES;
             const uint32_t ph = (k_it / C::STAGES) & 1;
             if (!mbar_wait(&sm.k_empty[st], ph ^ 1, abort, kWaitTimeoutNs)) {
@@ -390,7 +410,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
             mbar_arrive_expect_tx(&sm.k_full[st], C::TILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c)
-              tma_load_3d(sm.k[st] + c * CHUNK, &p.tk, &sm.k_full[st], C::BOX_COLS * c, (jlo + j) * BN,
+              tma_load_3d(sm.k[st] + c * CHUNK, &p.tk, &sm.k_full[st], C::BOX_COLS * c, jb * BN,
                           kvbh);
             ++k_it;
             if constexpr (!C::SEP) {
@@ -401,11 +421,11 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
               }
               mbar_arrive_expect_tx(&sm.v_full[st], C::V_BYTES);
               if constexpr (FP8) {
-                tma_load_3d(sm.v[st], &p.tv, &sm.v_full[st], (jlo + j) * BN, 0, kvbh);
+                tma_load_3d(sm.v[st], &p.tv, &sm.v_full[st], jb * BN, 0, kvbh);
               } else {
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c)
-                  tma_load_3d(sm.v[st] + c * CHUNK, &p.tv, &sm.v_full[st], 64 * c, (jlo + j) * BN,
+                  tma_load_3d(sm.v[st] + c * CHUNK, &p.tv, &sm.v_full[st], 64 * c, jb * BN,
                               kvbh);
               }
               ++v_it;
@@ -443,7 +463,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
         {
           const int jlo = t.jlo, nkv = t.nkv;
           const int kvbh = t.kvbh;
-          for (int j = 0; j < nkv; ++j) {
+          for (int j = 0, jb = next_block(t, t.jlo); j < nkv; ++j, jb = next_block(t, jb + 1)) {
             const int st = v_it % C::STAGES;
             const uint32_t ph = (v_it / C::STAGES) & 1;
             if (!mbar_wait(&sm.v_empty[st], ph ^ 1, abort, kWaitTimeoutNs)) {
@@ -454,11 +474,11 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
             mbar_arrive_expect_tx(&sm.v_full[st], C::V_BYTES);
             if constexpr (FP8) {
               // transposed V: one box of D rows x 128 keys
-              tma_load_3d(sm.v[st], &p.tv, &sm.v_full[st], (jlo + j) * BN, 0, kvbh);
+              tma_load_3d(sm.v[st], &p.tv, &sm.v_full[st], jb * BN, 0, kvbh);
             } else {
 #pragma unroll
               for (int c = 0; c < C::NCH; ++c)
-                tma_load_3d(sm.v[st] + c * CHUNK, &p.tv, &sm.v_full[st], 64 * c, (jlo + j) * BN, kvbh);
+                tma_load_3d(sm.v[st] + c * CHUNK, &p.tv, &sm.v_full[st], 64 * c, jb * BN, kvbh);
             }
             ++v_it;
           }
@@ -742,7 +762,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
         }
         float m_ref = -INFINITY;    // reference maximum, base-2 units of S*scale
         float l = 0.f;
-        for (int j = 0; j < nkv; ++j) {
+        for (int j = 0, jb = next_block(t, t.jlo); j < nkv; ++j, jb = next_block(t, jb + 1)) {
           const uint32_t b = kv_it % C::NSB;
           const uint32_t t_s = t_lane + C::TM_S + 128 * b;      // this block's S buffer
           if (!warp_wait(&sm.s_full[b], (kv_it / C::NSB) & 1, abort)) {
@@ -768,7 +788,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           // masks: keys past the sequence (tail / padding), right of the
           // window (above the diagonal when causal) and left of the window;
           // skipped when every key of the block is visible to every row
-          const int key0 = (jlo + j) * BN + NC * hf;
+          const int key0 = jb * BN + NC * hf;
           if (key0 + NC > len || key0 + NC - 1 > t.qlo + p.wr || key0 < t.qhi - p.wl) {
             // visible columns [c_lo, c_hi]: before the sequence end and
             // inside the window [row - wl, row + wr]
@@ -791,7 +811,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           mx0 = fmax3(mx0, s[NC - 4], s[NC - 3]);
           mx1 = fmax3(mx1, s[NC - 2], s[NC - 1]);
           // this block's multiplier from MMA output to base-2 units of S*scale
-          const float cb = FP8 ? c2 * q_sc * __ldg(p.k_scale + t.kvbh * p.nb + jlo + j) : c2;
+          const float cb = FP8 ? c2 * q_sc * __ldg(p.k_scale + t.kvbh * p.nb + jb) : c2;
           float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cb;
           if constexpr (C::NHALF == 2) {
             // the partner's half of the block (it loaded its S before arriving,

@@ -38,6 +38,10 @@ struct FwdParams {
   const float* k_scale;        // [B*H_kv, nb], one per 128-key block
   const float* v_scale;        // [B*H_kv]
   int nb;                      // ceil(N / 128)
+  // block-sparse: [bm_t, bm_t] bytes, nonzero where (query block, key block)
+  // is computed (blocks of 128), or nullptr
+  const uint8_t* block_mask;
+  int bm_t;
 };
 
 struct BwdParams {

@@ -24,9 +24,10 @@ _lib = None
 
 
 class FaVariant(ctypes.Structure):
-    """fa_variant_t: K/V heads and flash-attn's (left, right) window, -1 = unbounded."""
+    """fa_variant_t: K/V heads, flash-attn's (left, right) window (-1 =
+    unbounded) and a block mask (device pointer or None)."""
     _fields_ = [("h_kv", ctypes.c_int), ("window_left", ctypes.c_int),
-                ("window_right", ctypes.c_int)]
+                ("window_right", ctypes.c_int), ("block_mask", ctypes.c_void_p)]
 
 
 class FAError(RuntimeError):
@@ -235,22 +236,37 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, kv_len=
            "fa_bwd_noalloc")
 
 
-def _variant(q, k, window):
-    """fa_variant_t for K/V of k's head count and the (left, right) window."""
+def _check_block_mask(bm, N):
+    """A block mask: a contiguous uint8 CUDA tensor [T, T], T = ceil(N/128)."""
+    if bm is None:
+        return None
+    t = -(-N // 128)
+    if bm.dtype != torch.uint8 or not bm.is_cuda or tuple(bm.shape) != (t, t) \
+            or not bm.is_contiguous():
+        raise ValueError(f"block_mask: expected a contiguous uint8 CUDA tensor [{t}, {t}]")
+    return bm
+
+
+def _variant(q, k, window, block_mask=None):
+    """fa_variant_t for K/V of k's head count, the (left, right) window and a
+    block mask."""
     B, H, N, d = q.shape
     if k.dim() != 4 or (k.shape[0], k.shape[2], k.shape[3]) != (B, N, d) or k.shape[1] < 1 \
             or H % k.shape[1]:
         raise ValueError(f"k: shape {tuple(k.shape)} does not group the {H} query heads")
     wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
-    return FaVariant(int(k.shape[1]), wl, wr)
+    bm = _check_block_mask(block_mask, N)
+    return FaVariant(int(k.shape[1]), wl, wr, None if bm is None else bm.data_ptr())
 
 
-def fa_fwd_v(q, k, v, o, lse, scale, causal=False, kv_len=None, window=None, stream=None):
+def fa_fwd_v(q, k, v, o, lse, scale, causal=False, kv_len=None, window=None, stream=None,
+             block_mask=None):
     """Calls fa_fwd_v: k, v are [B,H_kv,N,d] (H_kv divides H); window is
-    flash-attn's (left, right), -1 = unbounded."""
+    flash-attn's (left, right), -1 = unbounded; block_mask a uint8 CUDA
+    tensor [ceil(N/128)]^2, zero where a (query block, key block) is skipped."""
     _check_qkv("q", q)
     B, H, N, d = q.shape
-    var = _variant(q, k, window)
+    var = _variant(q, k, window, block_mask)
     _check_qkv("k", k, k.shape)
     _check_qkv("v", v, k.shape)
     _check_qkv("o", o, q.shape)
@@ -264,11 +280,11 @@ def fa_fwd_v(q, k, v, o, lse, scale, causal=False, kv_len=None, window=None, str
 
 
 def fa_bwd_v(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, kv_len=None, window=None,
-             workspace=None, stream=None):
+             workspace=None, stream=None, block_mask=None):
     """Calls fa_bwd_v: k, v, dk, dv are [B,H_kv,N,d]; dk, dv sum over each group."""
     _check_qkv("q", q)
     B, H, N, d = q.shape
-    var = _variant(q, k, window)
+    var = _variant(q, k, window, block_mask)
     for name, t in (("o", o), ("do", do), ("dq", dq)):
         _check_qkv(name, t, q.shape)
     for name, t in (("k", k), ("v", v), ("dk", dk), ("dv", dv)):
@@ -284,11 +300,11 @@ def fa_bwd_v(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, kv_len=None, 
 
 
 def fa_bwd_dkdv_v(q, k, v, do, dk, dv, scale, causal=False, kv_len=None, window=None,
-                  workspace=None, stream=None):
+                  workspace=None, stream=None, block_mask=None):
     """Second backward phase for a variant: k, v, dk, dv are [B,H_kv,N,d]."""
     _check_qkv("q", q)
     B, H, N, d = q.shape
-    var = _variant(q, k, window)
+    var = _variant(q, k, window, block_mask)
     _check_qkv("do", do, q.shape)
     for name, t in (("k", k), ("v", v), ("dk", dk), ("dv", dv)):
         _check_qkv(name, t, k.shape)
@@ -371,7 +387,8 @@ def fa_fp8_quantize(q, k, v, buf, stream=None):
                                   _stream_ptr(stream)), "fa_fp8_quantize")
 
 
-def fa_fwd_fp8(buf, o, lse, scale, causal=False, kv_len=None, window=None, stream=None):
+def fa_fwd_fp8(buf, o, lse, scale, causal=False, kv_len=None, window=None, stream=None,
+               block_mask=None):
     """Calls fa_fwd_fp8 on E4M3 buffers (from fp8_buffers / fa_fp8_quantize)."""
     B, H, N, d = buf["q8"].shape
     Hkv = buf["k8"].shape[1]
@@ -380,14 +397,16 @@ def fa_fwd_fp8(buf, o, lse, scale, causal=False, kv_len=None, window=None, strea
         raise ValueError("lse: expected fp32 CUDA tensor [B,H,N]")
     kv_len = _check_kv_len(kv_len, B)
     wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
-    var = FaVariant(int(Hkv), wl, wr)
+    bm = _check_block_mask(block_mask, N)
+    var = FaVariant(int(Hkv), wl, wr, None if bm is None else bm.data_ptr())
     _raise(load().fa_fwd_fp8(_ptr(buf["q8"]), _ptr(buf["q_scale"]), _ptr(buf["k8"]),
                              _ptr(buf["k_scale"]), _ptr(buf["v8t"]), _ptr(buf["v_scale"]),
                              _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),
                              _ptr(kv_len), ctypes.byref(var), _stream_ptr(stream)), "fa_fwd_fp8")
 
 
-def forward_fp8(q, k, v, scale=None, causal=False, kv_len=None, window=None, stream=None):
+def forward_fp8(q, k, v, scale=None, causal=False, kv_len=None, window=None, stream=None,
+                block_mask=None):
     """(O, LSE, E4M3 buffers): quantise bf16 Q, K, V and run the FP8 forward."""
     B, H, N, d = q.shape
     buf = fp8_buffers(B, H, k.shape[1], N, d, q.device)
@@ -395,7 +414,7 @@ def forward_fp8(q, k, v, scale=None, causal=False, kv_len=None, window=None, str
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     fa_fwd_fp8(buf, o, lse, default_scale(d) if scale is None else scale, causal, kv_len, window,
-               stream)
+               stream, block_mask)
     return o, lse, buf
 
 
@@ -415,17 +434,18 @@ def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 
 
-def forward(q, k, v, scale=None, causal=False, kv_len=None, window=None, stream=None):
+def forward(q, k, v, scale=None, causal=False, kv_len=None, window=None, stream=None,
+            block_mask=None):
     """(O, LSE) with outputs allocated by torch on q's device.  K/V with fewer
-    heads than Q, or a window, go through fa_fwd_v."""
+    heads than Q, a window or a block mask go through fa_fwd_v."""
     B, H, N, d = q.shape
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     sc = default_scale(d) if scale is None else scale
-    if window is None and k.shape == q.shape:
+    if window is None and block_mask is None and k.shape == q.shape:
         fa_fwd(q, k, v, o, lse, sc, causal, kv_len, stream)
     else:
-        fa_fwd_v(q, k, v, o, lse, sc, causal, kv_len, window, stream)
+        fa_fwd_v(q, k, v, o, lse, sc, causal, kv_len, window, stream, block_mask)
     return o, lse
 
 
@@ -434,7 +454,7 @@ def workspace(B, H, N, d, device):
 
 
 def backward(q, k, v, o, lse, do, scale=None, causal=False, kv_len=None, ws=None, window=None,
-             stream=None):
+             stream=None, block_mask=None):
     """(dQ, dK, dV) with outputs (and, if not given, the workspace) allocated by
     torch; dK, dV are shaped like k."""
     B, H, N, d = q.shape
@@ -442,8 +462,9 @@ def backward(q, k, v, o, lse, do, scale=None, causal=False, kv_len=None, ws=None
     if ws is None:
         ws = workspace(B, H, N, d, q.device)
     sc = default_scale(d) if scale is None else scale
-    if window is None and k.shape == q.shape:
+    if window is None and block_mask is None and k.shape == q.shape:
         fa_bwd(q, k, v, o, do, lse, dq, dk, dv, sc, causal, kv_len, ws, stream)
     else:
-        fa_bwd_v(q, k, v, o, do, lse, dq, dk, dv, sc, causal, kv_len, window, ws, stream)
+        fa_bwd_v(q, k, v, o, do, lse, dq, dk, dv, sc, causal, kv_len, window, ws, stream,
+                 block_mask)
     return dq, dk, dv

@@ -133,12 +133,24 @@ fa_status_t fa_bwd_dq(void* dq, int B, int H, int N, int d, float scale, void* w
  *   Key blocks outside every row's window are skipped, not masked
  *   ("深入浅出 FlashAttention：快如闪电的精确注意力机制与 IO 感知计算"
  *   第八部分).
- * A NULL variant pointer means {H, -1, -1}.
+ * block_mask: NULL, or device memory holding a row-major [T, T] byte matrix
+ *   with T = ceil(N / 128), shared by every batch entry and head.  Entry
+ *   (a, b) zero hides keys 128b .. 128b+127 from queries 128a .. 128a+127:
+ *   the coarse block-level mask of Block-Sparse FlashAttention
+ *   ("深入浅出 FlashAttention…" 第八部分).  The kernels skip such blocks
+ *   (neither load nor compute them).  It combines with causal, the window
+ *   and kv_len; a row may then see no key (O = 0, LSE = -inf).  With a block
+ *   mask, tiles are scheduled one per unit instead of in causal pairs.  The
+ *   caller keeps the mask unchanged until the call's work has run.  fa_decode
+ *   rejects a block mask (FA_ERR_UNSUPPORTED).
+ * A NULL variant pointer means {H, -1, -1, NULL}; an aggregate initialiser
+ * that stops after window_right leaves block_mask NULL.
  */
 typedef struct fa_variant {
   int h_kv;
   int window_left;
   int window_right;
+  const unsigned char* block_mask;
 } fa_variant_t;
 
 /*

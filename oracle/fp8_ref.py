@@ -123,14 +123,17 @@ def quantize_v_transposed(v):
 
 
 def attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=False, kv_len=None, H_kv=None,
-                  rows=None, window=None):
+                  rows=None, window=None, block_mask=None):
     """O [B,H,N,d] and LSE [B,H,N] of the FP8 forward, step by step.
 
     q8 [B,H,N,d] codes with sq [B,H,ceil(N/128)]; k8 [B,H_kv,N,d] with
     sk [B,H_kv,ceil(N/128)]; v8t [B,H_kv,d,Npad] with sv [B,H_kv].  rows: a
     list of query rows to compute (the others are left 0 / -inf).  window:
     (left, right), query i sees keys i-left..i+right (-1: unbounded side),
-    the same visibility rule as the bf16 oracle; causal caps right at 0."""
+    the same visibility rule as the bf16 oracle; causal caps right at 0.
+    block_mask: [nb, nb] (or None), zero where key block j is skipped for
+    the rows of query block i // 128 (Block-Sparse FlashAttention, "炉案与百步
+    之外的仓库…" 第八部分): the recurrence passes over that block."""
     wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
     if causal:
         wr = 0
@@ -153,6 +156,8 @@ def attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=False, kv_len=None, H_k
                 acc = np.zeros(d)
                 sqi = float(sq[b, h, i // BLOCK])
                 for j in range(nb):
+                    if block_mask is not None and not block_mask[i // BLOCK][j]:
+                        continue
                     k0, k1 = j * BLOCK, min((j + 1) * BLOCK, N)
                     lo = k0 if wl < 0 else max(k0, i - wl)
                     hi = min(k1, ln, k1 if wr < 0 else i + wr + 1)

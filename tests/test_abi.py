@@ -168,6 +168,16 @@ def test_fp8_argument_errors(lib):
     assert fwd8(h_kv=4) == fa.FA_ERR_INVALID_ARG
 
 
+def test_decode_refuses_a_block_mask(lib):
+    """fa_decode has no block-sparse schedule: a variant with a block mask is
+    refused before the device (the mask pointer is never read)."""
+    ok = 0x1000
+    var = fa.FaVariant(2, -1, -1, 0x2000)
+    st = lib.fa_decode(P(ok), P(ok), P(ok), P(ok), P(ok), 1, 2, 1, 256, 128, 0.1, 1, None,
+                       ctypes.byref(var), 1, P(0x100000), 1 << 20, None)
+    assert st == fa.FA_ERR_UNSUPPORTED
+
+
 def test_decode_split_choice(lib):
     """fa_decode_splits: with fewer K/V heads than SMs, the most chunks of at
     least 8 key blocks that fit one wave; always within [1, key blocks]."""

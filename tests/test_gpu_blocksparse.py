@@ -1,0 +1,99 @@
+"""Block-sparse attention on the GPU: a [ceil(N/128)]^2 block mask whose zero
+entries the kernels skip (Block-Sparse FlashAttention, "炉案与百步之外的仓库…"
+第八部分), against the oracle with the same mask, element by element, with
+the parity tolerances of parity.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import fp8_ref as F
+from exact_attention_04_gb300 import build as fabuild
+from exact_attention_04_gb300 import fa
+from exact_attention_04_gb300.workloads import make_inputs, random_case
+
+import parity as P
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fabuild.build()
+    fa.load()
+
+
+def random_mask(T, density, seed, empty_row=None):
+    rng = np.random.default_rng(seed)
+    bm = (rng.random((T, T)) < density).astype(np.uint8)
+    if empty_row is not None:
+        bm[empty_row] = 0                     # a query block that sees no key at all
+    return bm
+
+
+CASES = [
+    # B, H, H_kv, N, d, causal, kv_len range, density, empty row
+    (2, 2, 2, 700, 128, False, None, 0.5, None),
+    (1, 4, 2, 1000, 128, True, None, 0.6, 2),
+    (2, 2, 1, 520, 64, False, (300, 520), 0.5, None),
+    (1, 2, 2, 640, 256, True, None, 0.7, None),
+    (2, 3, 3, 383, 64, True, (100, 383), 0.4, 1),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal,kv,density,empty", CASES)
+def test_forward_block_mask_against_oracle(B, H, Hkv, N, d, causal, kv, density, empty):
+    w = random_case(B, H, N, d, seed=N + d, causal=causal, kv_len_range=kv, h_kv=Hkv,
+                    backward=False)
+    inp = make_inputs(w, with_grad_out=False)
+    T = -(-N // 128)
+    bm = random_mask(T, density, seed=N, empty_row=empty)
+    g = P.to_gpu(inp)
+    o, lse = fa.forward(g["q"], g["k"], g["v"], scale=w.scale, causal=causal, kv_len=g["kv_len"],
+                        block_mask=torch.from_numpy(bm).cuda())
+    fa.fa_check()
+    kvn = None if inp["kv_len"] is None else inp["kv_len"].numpy()
+    o_ref, lse_ref = oracle.attention_fwd(P.f64(inp["q"]), P.f64(inp["k"]), P.f64(inp["v"]),
+                                          w.scale, causal=causal, kv_len=kvn, block_mask=bm)
+    P.check_o(P.f64(o), o_ref, w.name + " O (block mask)")
+    P.check_lse(P.f64(lse), lse_ref, w.name + " LSE (block mask)")
+    if empty is not None:
+        rows = slice(empty * 128, min((empty + 1) * 128, N))
+        assert torch.all(o[:, :, rows] == 0)
+        assert torch.all(torch.isinf(lse[:, :, rows]) & (lse[:, :, rows] < 0))
+
+
+def test_full_mask_equals_no_mask_bit_for_bit():
+    w = random_case(2, 2, 900, 128, seed=5, causal=True, backward=False)
+    g = P.to_gpu(make_inputs(w, with_grad_out=False))
+    T = -(-900 // 128)
+    o1, l1 = fa.forward(g["q"], g["k"], g["v"], scale=w.scale, causal=False, window=(-1, 0))
+    o2, l2 = fa.forward(g["q"], g["k"], g["v"], scale=w.scale, causal=True,
+                        block_mask=torch.ones(T, T, dtype=torch.uint8, device="cuda"))
+    fa.fa_check()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("N,d,causal", [(600, 128, False), (520, 256, True)])
+def test_fp8_forward_block_mask_against_oracle(N, d, causal):
+    w = random_case(1, 2, N, d, seed=3 * N, causal=causal, backward=False)
+    inp = make_inputs(w, with_grad_out=False)
+    T = -(-N // 128)
+    bm = random_mask(T, 0.6, seed=N + 1)
+    g = P.to_gpu(inp)
+    o, lse, _ = fa.forward_fp8(g["q"], g["k"], g["v"], scale=w.scale, causal=causal,
+                               block_mask=torch.from_numpy(bm).cuda())
+    fa.fa_check()
+    q, k, v = (P.f64(inp[n]).astype(np.float32) for n in ("q", "k", "v"))
+    q8, sq = F.quantize_rows(q.reshape(2, N, d))
+    k8, sk = F.quantize_rows(k.reshape(2, N, d))
+    v8t, sv = F.quantize_v_transposed(v.reshape(2, N, d))
+    o_ref, lse_ref = F.attention_fp8(q8.reshape(1, 2, N, d), sq.reshape(1, 2, -1),
+                                     k8.reshape(1, 2, N, d), sk.reshape(1, 2, -1),
+                                     v8t.reshape(1, 2, d, -1), sv.reshape(1, 2), w.scale,
+                                     causal=causal, block_mask=bm)
+    P.check_o(P.f64(o), o_ref, w.name + " O (fp8, block mask)")
+    P.check_lse(P.f64(lse), lse_ref, w.name + " LSE (fp8, block mask)")
+
+
