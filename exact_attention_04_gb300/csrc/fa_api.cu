@@ -385,7 +385,6 @@ fa_status_t bwd_setup(fa::BwdParams* p, DeviceInfo** di, int B, int H, int N, in
   Variant var;
   const fa_status_t vs = resolve_variant(variant, H, causal, &var);
   if (vs != FA_OK) return vs;
-  if (var.bm) return FA_ERR_UNSUPPORTED;
   if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
   *di = device_info(nullptr);
   if (!*di || (*di)->err != cudaSuccess) return FA_ERR_CUDA;
@@ -406,6 +405,8 @@ fa_status_t bwd_setup(fa::BwdParams* p, DeviceInfo** di, int B, int H, int N, in
   p->wl = var.wl;
   p->wr = var.wr;
   p->causal = var.pair ? 1 : 0;
+  p->block_mask = var.bm;
+  p->bm_t = (N + 127) / 128;
   p->scale = scale;
   p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p->status = (*di)->status;

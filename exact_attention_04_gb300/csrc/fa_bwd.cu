@@ -241,6 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         {
           int i0, i1;
           q_range(p, n, bwd_len(p, kvbh), i0, i1);
+          const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, 128 / BM};
+          const int nst = count_steps(sk, i0, i1);
+          if (nst == 0) i1 = i0;
           if (i0 >= i1) continue;
           if (!mbar_wait(&sm.kv_empty, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
             record_failure(p.status, abort, kSiteProdKV);
@@ -254,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
             tma_load_3d(sm.v + c * CHUNK, &p.tv, &sm.kv_full, 64 * c, n * BN, kvbh);
           }
           ++w_it;
-          StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv));
-          for (int s = 0; s < (i1 - i0) * G; ++s, wk.next()) {
+          StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv), sk);
+          for (int s = 0; s < nst * G; ++s, wk.next()) {
             const int i = wk.i;
             const int bh = wk.bh;
             const int st = g % kStages;
@@ -306,13 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         {
           int i0, i1;
           q_range(p, n, bwd_len(p, kvbh), i0, i1);
+          const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, 128 / BM};
+          const int nst = count_steps(sk, i0, i1);
+          if (nst == 0) i1 = i0;
           if (i0 >= i1) continue;
           if (!mbar_wait_warp(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
             issuer_fail(p.status, abort, lane, kSiteMmaKV);
             ok = false;
             break;
           }
-          const int nsteps = (i1 - i0) * G;
+          const int nsteps = nst * G;
           for (int s = 0; s < nsteps; ++s) {
             const int st = g % kStages;
             const bool first = (s == 0);
@@ -415,6 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         int i0, i1;
         const int len = bwd_len(p, kvbh);
         q_range(p, n, len, i0, i1);
+        const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, 128 / BM};
+        const int nst = count_steps(sk, i0, i1);
+        if (nst == 0) i1 = i0;
         const int key = n * BN + r;
         const size_t key_off = static_cast<size_t>(kvbh) * p.N + key;
         if (i0 >= i1) {
@@ -430,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
           }
           continue;
         }
-        StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv));
-        for (int s = 0; s < (i1 - i0) * G; ++s, wk.next()) {
+        StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv), sk);
+        for (int s = 0; s < nst * G; ++s, wk.next()) {
           const int i = wk.i;
           const int bh = wk.bh;
           const int st = g % kStages;

@@ -178,6 +178,9 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         {
           int i0, i1;
           dt_range(p, n, dt_len(p, kvbh), i0, i1);
+          const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
+          const int nst = count_steps(sk, i0, i1);
+          if (nst == 0) i1 = i0;
           if (i0 >= i1) continue;
           if (!mbar_wait(&sm.kv_empty, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
             record_failure(p.status, abort, kSiteProdKV);
@@ -192,8 +195,8 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
               tma_load_3d(sm.v + c * KCH, &p.tv, &sm.kv_full, 64 * c, n * BK, kvbh);
           }
           ++w_it;
-          StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv));
-          for (int s = 0; s < (i1 - i0) * G; ++s, wk.next()) {
+          StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv), sk);
+          for (int s = 0; s < nst * G; ++s, wk.next()) {
             const int i = wk.i;
             const int bh = wk.bh;
             const int st = g % C::STAGES;
@@ -243,8 +246,11 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         {
           int i0, i1;
           dt_range(p, n, dt_len(p, kvbh), i0, i1);
+          const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
+          const int nst = count_steps(sk, i0, i1);
+          if (nst == 0) i1 = i0;
           if (i0 >= i1) continue;
-          const int nsteps = (i1 - i0) * G;
+          const int nsteps = nst * G;
           if (!mbar_wait_warp(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
             issuer_fail(p.status, abort, lane, kSiteMmaKV);
             ok = false;
@@ -339,8 +345,11 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         {
           int i0, i1;
           dt_range(p, n, dt_len(p, kvbh), i0, i1);
+          const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
+          const int nst = count_steps(sk, i0, i1);
+          if (nst == 0) i1 = i0;
           if (i0 >= i1) continue;
-          const int nsteps = (i1 - i0) * G;
+          const int nsteps = nst * G;
           for (int s = 0; s < nsteps; ++s, ++g) {
             const int st = g % C::STAGES;
             const uint32_t b = g % C::NSB;          // tensor-memory S / dP buffer
@@ -422,6 +431,9 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         const int len = dt_len(p, kvbh);
         int i0, i1;
         dt_range(p, n, len, i0, i1);
+        const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
+        const int nst = count_steps(sk, i0, i1);
+        if (nst == 0) i1 = i0;
         const int key = n * BK + r;
         const size_t out_off = (static_cast<size_t>(kvbh) * p.N + key) * D + h * DH + 64 * hh;
         if (i0 >= i1) {
@@ -468,8 +480,8 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.v_full);
         }
-        StepWalk wk(i0, i1, 0);
-        for (int s = 0; s < (i1 - i0) * G; ++s, ++g, wk.next()) {
+        StepWalk wk(i0, i1, 0, sk);
+        for (int s = 0; s < nst * G; ++s, ++g, wk.next()) {
           const int i = wk.i;
           const int st = g % C::STAGES;
           const int q0 = i * BQ;
@@ -641,8 +653,11 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
       {
         int i0, i1;
         dt_range(p, n, dt_len(p, kvbh), i0, i1);
-        StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv));
-        for (int s = 0; s < (i1 - i0) * G; ++s, ++g, wk.next()) {
+        const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
+        const int nst = count_steps(sk, i0, i1);
+        if (nst == 0) i1 = i0;
+        StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv), sk);
+        for (int s = 0; s < nst * G; ++s, ++g, wk.next()) {
           const int i = wk.i;
           const int bh = wk.bh;
           const uint32_t tb = g % C::NSB;

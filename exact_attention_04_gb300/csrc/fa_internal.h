@@ -66,6 +66,10 @@ struct BwdParams {
   float scale;
   float scale_log2;
   int* status;
+  // block-sparse: [bm_t, bm_t] bytes, nonzero where (query block, key block)
+  // is computed (blocks of 128), or nullptr
+  const uint8_t* block_mask;
+  int bm_t;
 };
 
 // Causal schedules.  A causal work item (a query tile of the forward, a key

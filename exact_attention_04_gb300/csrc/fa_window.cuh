@@ -9,6 +9,7 @@
 // skipped, not masked ("深入浅出 FlashAttention：快如闪电的精确注意力机制与
 // IO 感知计算" 第八部分, block-sparse skipping).
 #pragma once
+#include <cstdint>
 
 namespace fa {
 
@@ -56,13 +57,41 @@ __device__ __forceinline__ int q_head_of(int kvbh, int gi, int H, int H_kv) {
 // The steps of a backward work item in order: query blocks [i0, i1) of the
 // group's first query head, then of the next, ...  Kept as counters so that a
 // step costs no integer division.
+// Block-sparse attention: column n of the row-major [T, T] block mask
+// (col = mask + n, stride T), read for query steps that are spb to a 128-row
+// query block; a null column computes every step.
+struct StepMask {
+  const uint8_t* col;
+  int stride, spb;
+  __device__ __forceinline__ bool on(int s) const {
+    return !col || __ldg(col + static_cast<size_t>(s / spb) * stride) != 0;
+  }
+};
+
+// Steps of [i0, i1) the mask computes.
+__device__ __forceinline__ int count_steps(const StepMask& m, int i0, int i1) {
+  if (!m.col) return i1 > i0 ? i1 - i0 : 0;
+  int c = 0;
+  for (int s = i0; s < i1; ++s) c += m.on(s);
+  return c;
+}
+
 struct StepWalk {
   int i, bh, i0, i1;
-  __device__ __forceinline__ StepWalk(int i0_, int i1_, int bh0)
-      : i(i0_), bh(bh0), i0(i0_), i1(i1_) {}
+  StepMask m;
+  __device__ __forceinline__ StepWalk(int i0_, int i1_, int bh0,
+                                      const StepMask& m_ = StepMask{nullptr, 0, 1})
+      : i(i0_), bh(bh0), i0(i0_), i1(i1_), m(m_) {
+    i = skip(i0);
+  }
+  __device__ __forceinline__ int skip(int s) const {
+    while (s < i1 && !m.on(s)) ++s;
+    return s;
+  }
   __device__ __forceinline__ void next() {
-    if (++i == i1) {
-      i = i0;
+    i = skip(i + 1);
+    if (i >= i1) {
+      i = skip(i0);
       ++bh;
     }
   }

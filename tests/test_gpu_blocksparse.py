@@ -97,3 +97,53 @@ def test_fp8_forward_block_mask_against_oracle(N, d, causal):
     P.check_lse(P.f64(lse), lse_ref, w.name + " LSE (fp8, block mask)")
 
 
+
+
+BWD_CASES = [
+    # B, H, H_kv, N, d, causal, kv_len range, density, empty row
+    (2, 2, 2, 520, 128, False, None, 0.5, None),
+    (1, 4, 2, 700, 128, True, None, 0.6, 1),
+    (2, 2, 1, 383, 64, True, (100, 383), 0.5, None),
+    (1, 2, 2, 640, 64, False, None, 0.4, 2),
+    (1, 2, 1, 520, 256, True, None, 0.7, None),
+    (2, 1, 1, 300, 256, False, (150, 300), 0.5, 0),
+]
+
+
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal,kv,density,empty", BWD_CASES)
+def test_backward_block_mask_against_oracle(B, H, Hkv, N, d, causal, kv, density, empty):
+    w = random_case(B, H, N, d, seed=2 * N + d, causal=causal, kv_len_range=kv, h_kv=Hkv)
+    inp = make_inputs(w)
+    T = -(-N // 128)
+    bm = random_mask(T, density, seed=N + 7, empty_row=empty)
+    bm_gpu = torch.from_numpy(bm).cuda()
+    g = P.to_gpu(inp)
+    o, lse = fa.forward(g["q"], g["k"], g["v"], scale=w.scale, causal=causal, kv_len=g["kv_len"],
+                        block_mask=bm_gpu)
+    dq, dk, dv = fa.backward(g["q"], g["k"], g["v"], o, lse, g["do"], scale=w.scale,
+                             causal=causal, kv_len=g["kv_len"], block_mask=bm_gpu)
+    fa.fa_check()
+    kvn = None if inp["kv_len"] is None else inp["kv_len"].numpy()
+    dq_r, dk_r, dv_r, _ = oracle.attention_bwd(P.f64(inp["q"]), P.f64(inp["k"]), P.f64(inp["v"]),
+                                               P.f64(inp["do"]), w.scale, causal=causal,
+                                               kv_len=kvn, block_mask=bm)
+    P.check_grad(P.f64(dq), dq_r, w.name + " dQ (block mask)")
+    P.check_grad(P.f64(dk), dk_r, w.name + " dK (block mask)")
+    P.check_grad(P.f64(dv), dv_r, w.name + " dV (block mask)")
+
+
+def test_backward_key_block_with_no_query_has_zero_gradient():
+    """A key block whose column of the mask is all zero meets no query: its dK
+    and dV must be exactly zero (the kernels write them without a step)."""
+    w = random_case(1, 2, 512, 128, seed=77, causal=False)
+    inp = make_inputs(w)
+    bm = np.ones((4, 4), dtype=np.uint8)
+    bm[:, 2] = 0
+    bm_gpu = torch.from_numpy(bm).cuda()
+    g = P.to_gpu(inp)
+    o, lse = fa.forward(g["q"], g["k"], g["v"], scale=w.scale, block_mask=bm_gpu)
+    dq, dk, dv = fa.backward(g["q"], g["k"], g["v"], o, lse, g["do"], scale=w.scale,
+                             block_mask=bm_gpu)
+    fa.fa_check()
+    assert torch.all(dk[:, :, 256:384] == 0) and torch.all(dv[:, :, 256:384] == 0)
+    assert dk[:, :, :256].abs().max() > 0
