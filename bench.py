@@ -32,7 +32,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from exact_attention_04_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+from exact_attention_04_gb300.workloads import (WORKLOADS, block_sparse_mask,  # noqa: E402
+                                                make_inputs, random_case)
 
 METRIC = "attention fwd/bwd TFLOP/s on 1 GB300 and % of dense-BF16 roofline vs N"
 HEADLINE = "large_head_b2_h16_n8192_d128_causal"
@@ -475,6 +476,75 @@ def run_e2e(rs, w, fa, steps, flops_step, dist):
                         "their own streams while step s computes (two device buffer sets)"}
 
 
+BLOCK_SPARSE = dict(B=2, H=16, N=8192, d=128, seed=12)
+BLOCK_SPARSE_NAME = "blocksparse_b2_h16_n8192_d128_local_global_random"
+
+
+class BlockSparseRunner:
+    """Forward (fa_fwd_v) and backward (fa_bwd_v) of block-sparse attention:
+    the local + global + random block pattern of block_sparse_mask."""
+
+    def __init__(self, fa):
+        c = BLOCK_SPARSE
+        self.w = random_case(c["B"], c["H"], c["N"], c["d"], seed=c["seed"], causal=False)
+        inp = make_inputs(self.w)
+        dev = torch.device("cuda")
+        self.q, self.k, self.v, self.do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+        T = -(-c["N"] // 128)
+        self.mask_np = block_sparse_mask(T, seed=c["seed"])
+        self.mask = torch.from_numpy(self.mask_np).to(dev)
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.ws = fa.workspace(c["B"], c["H"], c["N"], c["d"], dev)
+        self.fa = fa
+
+    def fwd(self):
+        self.fa.fa_fwd_v(self.q, self.k, self.v, self.o, self.lse, self.w.scale,
+                         block_mask=self.mask)
+
+    def bwd(self):
+        self.fa.fa_bwd_v(self.q, self.k, self.v, self.o, self.do, self.lse, self.dq, self.dk,
+                         self.dv, self.w.scale, workspace=self.ws, block_mask=self.mask)
+
+    def phases(self):
+        return [("fwd", self.fwd), ("bwd", self.bwd)]
+
+    def step(self):
+        self.fwd()
+        self.bwd()
+
+    def computed_pairs(self):
+        """(query, key) pairs the mask computes, per head (N a multiple of 128)."""
+        return int(self.mask_np.sum()) * 128 * 128
+
+
+def sweep_blocksparse(fa, peaks, flush_buf):
+    r = BlockSparseRunner(fa)
+    for _ in range(3):
+        r.step()
+    torch.cuda.synchronize()
+    per_phase, _ = time_steps(r, 20, flush=lambda: flush_l2(flush_buf), median=True)
+    fa.fa_check()
+    c = BLOCK_SPARSE
+    fwd_flops = 4.0 * c["B"] * c["H"] * c["d"] * r.computed_pairs()
+    dense = 4.0 * c["B"] * c["H"] * c["d"] * c["N"] * c["N"]
+    fwd_ms, bwd_ms = per_phase["fwd"], per_phase["bwd"]
+    return {"workload": BLOCK_SPARSE_NAME,
+            "N": c["N"], "d": c["d"], "causal": False,
+            "block_density": round(float(r.mask_np.mean()), 4),
+            "fwd_ms": round(fwd_ms, 4),
+            "fwd_tflops": round(fwd_flops / (fwd_ms * 1e-3) / 1e12, 2),
+            "fwd_frac_of_peak": round(fwd_flops / (fwd_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "bwd_ms": round(bwd_ms, 4),
+            "bwd_tflops": round(2.5 * fwd_flops / (bwd_ms * 1e-3) / 1e12, 2),
+            "bwd_frac_of_peak": round(2.5 * fwd_flops / (bwd_ms * 1e-3) / 1e12
+                                      / peaks["bf16_tflops"], 4),
+            "dense_equivalent_tflops": round(dense / (fwd_ms * 1e-3) / 1e12, 2),
+            "flops": "computed (query, key) pairs only: 4 d per pair forward, 2.5x backward",
+            "timing": "median of 20 steps, L2 flushed before each"}
+
+
 def visible_pairs(L, N, causal):
     """(query, key) pairs of one head that a key-padding length L leaves
     visible: every query sees keys j < L (and j <= i when causal)."""
@@ -549,6 +619,10 @@ def run_sweep(fa, peaks, only=None):
         if w.d in (128, 256):
             entry["fp8"] = sweep_fp8(w, inp, fa, peaks, flush_buf)
         out.append(entry)
+    if only is None or only in BLOCK_SPARSE_NAME:
+        cache.clear()
+        torch.cuda.empty_cache()
+        out.append(sweep_blocksparse(fa, peaks, flush_buf))
     return out
 
 

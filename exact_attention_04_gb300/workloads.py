@@ -166,3 +166,20 @@ def decode_case(B, H, h_kv, Nq, Nk, d, seed, causal=True, kv_len_range=None, win
 def make_decode_inputs(w: Workload):
     """q [B,H,Nq,d], k and v [B,H_kv,Nk,d], kv_len: make_inputs for a decode workload."""
     return make_inputs(w, with_grad_out=False)
+
+
+def block_sparse_mask(T: int, seed: int = 0, band: int = 4, n_global: int = 2, n_random: int = 5):
+    """A seeded [T, T] block mask (1 = computed) in the local + global + random
+    pattern of long-context block-sparse attention: each 128-row query block
+    sees the key blocks within `band` of its own, the first `n_global` key
+    blocks and `n_random` others drawn at random; the first `n_global` query
+    blocks see every key block.  About 25 % of the blocks at T = 64."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    bm = np.zeros((T, T), dtype=np.uint8)
+    for a in range(T):
+        bm[a, max(0, a - band): a + band + 1] = 1
+        bm[a, :n_global] = 1
+        bm[a, rng.choice(T, size=min(n_random, T), replace=False)] = 1
+    bm[:n_global, :] = 1
+    return bm

@@ -147,3 +147,31 @@ def test_backward_key_block_with_no_query_has_zero_gradient():
     fa.fa_check()
     assert torch.all(dk[:, :, 256:384] == 0) and torch.all(dv[:, :, 256:384] == 0)
     assert dk[:, :, :256].abs().max() > 0
+
+
+def test_blocksparse_bench_workload_sampled_heads():
+    """The bench's block-sparse workload (B=2, H=16, N=8192, d=128, the local +
+    global + random pattern at about 25 % density), two heads against the
+    oracle, forward and backward, in the launch configuration the bench times."""
+    from exact_attention_04_gb300.workloads import block_sparse_mask
+    w = random_case(2, 16, 8192, 128, seed=12, causal=False)
+    inp = make_inputs(w)
+    bm = block_sparse_mask(64, seed=12)
+    bm_gpu = torch.from_numpy(bm).cuda()
+    g = P.to_gpu(inp)
+    o, lse = fa.forward(g["q"], g["k"], g["v"], scale=w.scale, block_mask=bm_gpu)
+    dq, dk, dv = fa.backward(g["q"], g["k"], g["v"], o, lse, g["do"], scale=w.scale,
+                             block_mask=bm_gpu)
+    fa.fa_check()
+    for b, h in ((0, 0), (1, 15)):
+        one = {n: inp[n][b:b + 1, h:h + 1] for n in ("q", "k", "v", "do")}
+        o_r, l_r = oracle.attention_fwd(P.f64(one["q"]), P.f64(one["k"]), P.f64(one["v"]),
+                                        w.scale, block_mask=bm)
+        P.check_o(P.f64(o[b:b + 1, h:h + 1]), o_r, f"block-sparse O ({b},{h})")
+        P.check_lse(P.f64(lse[b:b + 1, h:h + 1]), l_r, f"block-sparse LSE ({b},{h})")
+        dq_r, dk_r, dv_r, _ = oracle.attention_bwd(P.f64(one["q"]), P.f64(one["k"]),
+                                                   P.f64(one["v"]), P.f64(one["do"]), w.scale,
+                                                   block_mask=bm)
+        P.check_grad(P.f64(dq[b:b + 1, h:h + 1]), dq_r, f"block-sparse dQ ({b},{h})")
+        P.check_grad(P.f64(dk[b:b + 1, h:h + 1]), dk_r, f"block-sparse dK ({b},{h})")
+        P.check_grad(P.f64(dv[b:b + 1, h:h + 1]), dv_r, f"block-sparse dV ({b},{h})")
