@@ -181,7 +181,8 @@ __device__ __forceinline__ void q_range(const BwdParams& p, int n, int len, int&
   i1 = (q_hi + BM - 1) / BM;
 }
 
-template <int D>
+// BS: the launch carries a block mask (its own instantiation).
+template <int D, bool BS>
 __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_constant__ BwdParams p,
                                                                    const __grid_constant__ TailTable tail) {
   using C = BCfg<D>;
@@ -241,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         {
           int i0, i1;
           q_range(p, n, bwd_len(p, kvbh), i0, i1);
-          const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, 128 / BM};
+          const StepMask sk{BS ? p.block_mask + n : nullptr, p.bm_t, 128 / BM};
           const int nst = count_steps(sk, i0, i1);
           if (nst == 0) i1 = i0;
           if (i0 >= i1) continue;
@@ -309,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         {
           int i0, i1;
           q_range(p, n, bwd_len(p, kvbh), i0, i1);
-          const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, 128 / BM};
+          const StepMask sk{BS ? p.block_mask + n : nullptr, p.bm_t, 128 / BM};
           const int nst = count_steps(sk, i0, i1);
           if (nst == 0) i1 = i0;
           if (i0 >= i1) continue;
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_main_kernel(const __grid_cons
         int i0, i1;
         const int len = bwd_len(p, kvbh);
         q_range(p, n, len, i0, i1);
-        const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, 128 / BM};
+        const StepMask sk{BS ? p.block_mask + n : nullptr, p.bm_t, 128 / BM};
         const int nst = count_steps(sk, i0, i1);
         if (nst == 0) i1 = i0;
         const int key = n * BN + r;
@@ -731,10 +732,10 @@ cudaError_t launch_prep(const BwdParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool BS>
 cudaError_t launch_main(const BwdParams& p, int num_sms, int max_smem, cudaStream_t stream) {
   const size_t smem = smem_request(sizeof(BwdSmem<D>), max_smem);
-  cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D, BS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -755,7 +756,7 @@ cudaError_t launch_main(const BwdParams& p, int num_sms, int max_smem, cudaStrea
   }
   if (tail.heads == 0) std::memset(tail.item, 0xff, sizeof(tail.item));
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  bwd_main_kernel<D><<<grid, kThreads, smem, stream>>>(p, tail);
+  bwd_main_kernel<D, BS><<<grid, kThreads, smem, stream>>>(p, tail);
   return cudaGetLastError();
 }
 
@@ -773,7 +774,9 @@ cudaError_t launch_bwd_prep(const BwdParams& p, int d, cudaStream_t stream) {
 cudaError_t launch_bwd_main(const BwdParams& p, int d, int num_sms, int max_smem,
                             cudaStream_t stream) {
   switch (d) {
-    case 64: return launch_main<64>(p, num_sms, max_smem, stream);
+    case 64:
+      return p.block_mask ? launch_main<64, true>(p, num_sms, max_smem, stream)
+                          : launch_main<64, false>(p, num_sms, max_smem, stream);
     default: return cudaErrorNotSupported;
   }
 }

@@ -109,7 +109,9 @@ struct DtSmem {
 static_assert(sizeof(DtSmem<128>) <= 232448 && sizeof(DtSmem<256>) <= 232448,
               "shared-memory layout exceeds the per-block limit");
 
-template <int D>
+// BS: the launch carries a block mask (its own instantiation, so that the
+// kernel without one keeps the plain step walk).
+template <int D, bool BS>
 __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_constant__ BwdParams p,
                                                                  const __grid_constant__ TailTable tail) {
   using C = DtCfg<D>;
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         {
           int i0, i1;
           dt_range(p, n, dt_len(p, kvbh), i0, i1);
-          const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
+          const StepMask sk{BS ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
           const int nst = count_steps(sk, i0, i1);
           if (nst == 0) i1 = i0;
           if (i0 >= i1) continue;
@@ -246,7 +248,7 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         {
           int i0, i1;
           dt_range(p, n, dt_len(p, kvbh), i0, i1);
-          const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
+          const StepMask sk{BS ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
           const int nst = count_steps(sk, i0, i1);
           if (nst == 0) i1 = i0;
           if (i0 >= i1) continue;
@@ -345,7 +347,7 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         {
           int i0, i1;
           dt_range(p, n, dt_len(p, kvbh), i0, i1);
-          const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
+          const StepMask sk{BS ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
           const int nst = count_steps(sk, i0, i1);
           if (nst == 0) i1 = i0;
           if (i0 >= i1) continue;
@@ -431,7 +433,7 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         const int len = dt_len(p, kvbh);
         int i0, i1;
         dt_range(p, n, len, i0, i1);
-        const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
+        const StepMask sk{BS ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
         const int nst = count_steps(sk, i0, i1);
         if (nst == 0) i1 = i0;
         const int key = n * BK + r;
@@ -653,7 +655,7 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
       {
         int i0, i1;
         dt_range(p, n, dt_len(p, kvbh), i0, i1);
-        const StepMask sk{p.block_mask ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
+        const StepMask sk{BS ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
         const int nst = count_steps(sk, i0, i1);
         if (nst == 0) i1 = i0;
         StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv), sk);
@@ -743,10 +745,10 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
   }
 }
 
-template <int D>
+template <int D, bool BS>
 cudaError_t launch(const BwdParams& p, int num_sms, int max_smem, cudaStream_t stream) {
   const size_t smem = smem_request(sizeof(DtSmem<D>), max_smem);
-  cudaError_t e = cudaFuncSetAttribute(bwd_dt_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(bwd_dt_kernel<D, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int T = (p.N + BK - 1) / BK;
@@ -767,7 +769,7 @@ cudaError_t launch(const BwdParams& p, int num_sms, int max_smem, cudaStream_t s
   }
   if (tail.heads == 0) std::memset(tail.item, 0xff, sizeof(tail.item));
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  bwd_dt_kernel<D><<<grid, kThreads, smem, stream>>>(p, tail);
+  bwd_dt_kernel<D, BS><<<grid, kThreads, smem, stream>>>(p, tail);
   return cudaGetLastError();
 }
 
@@ -776,8 +778,12 @@ cudaError_t launch(const BwdParams& p, int num_sms, int max_smem, cudaStream_t s
 cudaError_t launch_bwd_main_dt(const BwdParams& p, int d, int num_sms, int max_smem,
                                cudaStream_t stream) {
   switch (d) {
-    case 128: return launch<128>(p, num_sms, max_smem, stream);
-    case 256: return launch<256>(p, num_sms, max_smem, stream);
+    case 128:
+      return p.block_mask ? launch<128, true>(p, num_sms, max_smem, stream)
+                          : launch<128, false>(p, num_sms, max_smem, stream);
+    case 256:
+      return p.block_mask ? launch<256, true>(p, num_sms, max_smem, stream)
+                          : launch<256, false>(p, num_sms, max_smem, stream);
     default: return cudaErrorNotSupported;
   }
 }

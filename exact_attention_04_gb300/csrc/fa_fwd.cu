@@ -221,7 +221,9 @@ struct Tile {
   int qs;              // index of the tile's Q scale (FP8)
 };
 
-template <bool DEC>
+// BS: the launch carries a block mask (a separate instantiation, so that the
+// kernels without one keep the plain block walk).
+template <bool DEC, bool BS = false>
 __device__ __forceinline__ void make_tile(const FwdParams& p, int u, int bh, int m, Tile& t) {
   if constexpr (!DEC) {
     t.qy = m * BM;
@@ -232,8 +234,9 @@ __device__ __forceinline__ void make_tile(const FwdParams& p, int u, int bh, int
     t.qhi = m * BM + BM - 1;
     t.nkv = tile_blocks(p, m, t.len, t.jlo);
     t.jend = t.jlo + t.nkv;
-    t.bmrow = p.block_mask ? p.block_mask + static_cast<size_t>(m) * p.bm_t : nullptr;
-    if (t.bmrow) {
+    t.bmrow = nullptr;
+    if constexpr (BS) {
+      t.bmrow = p.block_mask + static_cast<size_t>(m) * p.bm_t;
       int n = 0;
       for (int jb = t.jlo; jb < t.jend; ++jb) n += __ldg(t.bmrow + jb) != 0;
       t.nkv = n;
@@ -268,8 +271,9 @@ __device__ __forceinline__ void make_tile(const FwdParams& p, int u, int bh, int
 // The first key block at or after jb that the tile computes: every block of
 // [jlo, jend) without a block mask, else those whose mask byte is nonzero
 // (every role walks the same sequence).
+template <bool BS>
 __device__ __forceinline__ int next_block(const Tile& t, int jb) {
-  if (t.bmrow)
+  if constexpr (BS)
     while (jb < t.jend && __ldg(t.bmrow + jb) == 0) ++jb;
   return jb;
 }
@@ -282,7 +286,7 @@ struct TileIter {
 
 // The next tile of this CTA into t; false when it has none left.  Every role
 // walks the same sequence.
-template <bool DEC>
+template <bool DEC, bool BS>
 __device__ __forceinline__ bool next_tile(const FwdParams& p, const TailTable& tail,
                                           const Sched& sched, int nunits, TileIter& it, Tile& t) {
   if constexpr (DEC) {
@@ -296,7 +300,7 @@ __device__ __forceinline__ bool next_tile(const FwdParams& p, const TailTable& t
         int bh, m;
         sched.tile(it.u, it.kt, bh, m);
         ++it.kt;
-        make_tile<false>(p, 0, bh, m, t);
+        make_tile<false, BS>(p, 0, bh, m, t);
         return true;
       }
       it.u += gridDim.x;
@@ -306,7 +310,7 @@ __device__ __forceinline__ bool next_tile(const FwdParams& p, const TailTable& t
     const int e = tail.item[blockIdx.x][it.k];
     if (e < 0) return false;
     ++it.k;
-    make_tile<false>(p, 0, tail_head(e), tail_block(e), t);
+    make_tile<false, BS>(p, 0, tail_head(e), tail_block(e), t);
     return true;
   }
 }
@@ -317,7 +321,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, bool DEC, bool FP8>
+template <int D, bool DEC, bool FP8, bool BS>
 __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ TailTable tail) {
   static_assert(!(DEC && FP8), "decode runs in bf16");
@@ -384,7 +388,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
       uint32_t q_it = 0, k_it = 0, v_it = 0;
       bool ok = true;
       TileIter it{static_cast<int>(blockIdx.x), 0, 0};
-      for (Tile t; ok && next_tile<DEC>(p, tail, sched, nunits, it, t);) {
+      for (Tile t; ok && next_tile<DEC, BS>(p, tail, sched, nunits, it, t);) {
         {
           const int jlo = t.jlo, nkv = t.nkv;
           if (nkv == 0) continue;
@@ -399,7 +403,9 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d(sm.q + c * CHUNK, &p.tq, &sm.q_full, C::BOX_COLS * c, t.qy, t.qz);
           ++q_it;
-          for (int j = 0, jb = next_block(t, t.jlo); j < nkv; ++j, jb = next_block(t, jb + 1)) {
+          for (int j = 0, jbs = next_block<BS>(t, t.jlo); j < nkv;
+               ++j, jbs = BS ? next_block<BS>(t, jbs + 1) : jbs) {
+            const int jb = BS ? jbs : t.jlo + j;        // key block
             const int st = k_it % C::STAGES;
             const uint32_t ph = (k_it / C::STAGES) & 1;
             if (!mbar_wait(&sm.k_empty[st], ph ^ 1, abort, kWaitTimeoutNs)) {
@@ -459,11 +465,13 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
       uint32_t v_it = 0;
       bool ok = true;
       TileIter it{static_cast<int>(blockIdx.x), 0, 0};
-      for (Tile t; ok && next_tile<DEC>(p, tail, sched, nunits, it, t);) {
+      for (Tile t; ok && next_tile<DEC, BS>(p, tail, sched, nunits, it, t);) {
         {
           const int jlo = t.jlo, nkv = t.nkv;
           const int kvbh = t.kvbh;
-          for (int j = 0, jb = next_block(t, t.jlo); j < nkv; ++j, jb = next_block(t, jb + 1)) {
+          for (int j = 0, jbs = next_block<BS>(t, t.jlo); j < nkv;
+               ++j, jbs = BS ? next_block<BS>(t, jbs + 1) : jbs) {
+            const int jb = BS ? jbs : t.jlo + j;        // key block
             const int st = v_it % C::STAGES;
             const uint32_t ph = (v_it / C::STAGES) & 1;
             if (!mbar_wait(&sm.v_empty[st], ph ^ 1, abort, kWaitTimeoutNs)) {
@@ -502,7 +510,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
       uint32_t q_it = 0, g = 0;
       bool ok = true;
       TileIter it{static_cast<int>(blockIdx.x), 0, 0};
-      for (Tile t; ok && next_tile<DEC>(p, tail, sched, nunits, it, t);) {
+      for (Tile t; ok && next_tile<DEC, BS>(p, tail, sched, nunits, it, t);) {
         {
           const int nkv = t.nkv;
           if (nkv == 0) continue;
@@ -561,7 +569,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
       uint32_t g = 0, t_it = 0;
       bool ok = true;
       TileIter it{static_cast<int>(blockIdx.x), 0, 0};
-      for (Tile t; ok && next_tile<DEC>(p, tail, sched, nunits, it, t);) {
+      for (Tile t; ok && next_tile<DEC, BS>(p, tail, sched, nunits, it, t);) {
         {
           const int nkv = t.nkv;
           if (nkv == 0) continue;
@@ -732,7 +740,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
       return epilogue(pend.last, pend.l, pend.m_ref, pend.row_off, pend.row_valid, pend.kvbh);
     };
     TileIter it{static_cast<int>(blockIdx.x), 0, 0};
-    for (Tile t; ok && next_tile<DEC>(p, tail, sched, nunits, it, t);) {
+    for (Tile t; ok && next_tile<DEC, BS>(p, tail, sched, nunits, it, t);) {
       {
         const int len = t.len, jlo = t.jlo, nkv = t.nkv;
         const int row = DEC ? t.qlo + row_local % p.Nq : t.qlo + row_local;   // query position
@@ -762,7 +770,9 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
         }
         float m_ref = -INFINITY;    // reference maximum, base-2 units of S*scale
         float l = 0.f;
-        for (int j = 0, jb = next_block(t, t.jlo); j < nkv; ++j, jb = next_block(t, jb + 1)) {
+        for (int j = 0, jbs = next_block<BS>(t, t.jlo); j < nkv;
+             ++j, jbs = BS ? next_block<BS>(t, jbs + 1) : jbs) {
+          const int jb = BS ? jbs : t.jlo + j;        // key block
           const uint32_t b = kv_it % C::NSB;
           const uint32_t t_s = t_lane + C::TM_S + 128 * b;      // this block's S buffer
           if (!warp_wait(&sm.s_full[b], (kv_it / C::NSB) & 1, abort)) {
@@ -961,10 +971,10 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
   }
 }
 
-template <int D, bool DEC, bool FP8 = false>
+template <int D, bool DEC, bool FP8 = false, bool BS = false>
 cudaError_t launch(const FwdParams& p, int num_sms, int max_smem, cudaStream_t stream) {
   const size_t smem = smem_request(sizeof(FwdSmem<D, FP8>), max_smem);
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, DEC, FP8>,
+  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D, DEC, FP8, BS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -989,7 +999,7 @@ cudaError_t launch(const FwdParams& p, int num_sms, int max_smem, cudaStream_t s
   }
   if (tail.heads == 0) std::memset(tail.item, 0xff, sizeof(tail.item));
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  fa_fwd_kernel<D, DEC, FP8><<<grid, Cfg<D, FP8>::THREADS, smem, stream>>>(p, tail);
+  fa_fwd_kernel<D, DEC, FP8, BS><<<grid, Cfg<D, FP8>::THREADS, smem, stream>>>(p, tail);
   return cudaGetLastError();
 }
 
@@ -1036,9 +1046,15 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const __grid_consta
 
 cudaError_t launch_fwd(const FwdParams& p, int d, int num_sms, int max_smem, cudaStream_t stream) {
   switch (d) {
-    case 64: return launch<64, false>(p, num_sms, max_smem, stream);
-    case 128: return launch<128, false>(p, num_sms, max_smem, stream);
-    case 256: return launch<256, false>(p, num_sms, max_smem, stream);
+    case 64:
+      return p.block_mask ? launch<64, false, false, true>(p, num_sms, max_smem, stream)
+                          : launch<64, false>(p, num_sms, max_smem, stream);
+    case 128:
+      return p.block_mask ? launch<128, false, false, true>(p, num_sms, max_smem, stream)
+                          : launch<128, false>(p, num_sms, max_smem, stream);
+    case 256:
+      return p.block_mask ? launch<256, false, false, true>(p, num_sms, max_smem, stream)
+                          : launch<256, false>(p, num_sms, max_smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1046,8 +1062,12 @@ cudaError_t launch_fwd(const FwdParams& p, int d, int num_sms, int max_smem, cud
 cudaError_t launch_fwd_fp8(const FwdParams& p, int d, int num_sms, int max_smem,
                            cudaStream_t stream) {
   switch (d) {
-    case 128: return launch<128, false, true>(p, num_sms, max_smem, stream);
-    case 256: return launch<256, false, true>(p, num_sms, max_smem, stream);
+    case 128:
+      return p.block_mask ? launch<128, false, true, true>(p, num_sms, max_smem, stream)
+                          : launch<128, false, true>(p, num_sms, max_smem, stream);
+    case 256:
+      return p.block_mask ? launch<256, false, true, true>(p, num_sms, max_smem, stream)
+                          : launch<256, false, true>(p, num_sms, max_smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }
