@@ -298,7 +298,7 @@ void plan_causal_tail(int BH, int T, int nsplit, int G, bool fwd, long long head
 
 extern "C" {
 
-int fa_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+int fa_version(void) { return 1 * 10000 + 1 * 100 + 0; }
 
 const char* fa_status_string(fa_status_t s) {
   switch (s) {

@@ -285,7 +285,9 @@ fa_status_t fa_check(void* stream);
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status_t status);
 
-/* Library version as major*10000 + minor*100 + patch. */
+/* Library version as major*10000 + minor*100 + patch.  1.1: fa_variant_t
+ * gained block_mask (a trailing member, NULL in aggregate initialisers that
+ * stop before it). */
 int fa_version(void);
 
 #ifdef __cplusplus
