@@ -175,3 +175,30 @@ def test_blocksparse_bench_workload_sampled_heads():
         P.check_grad(P.f64(dq[b:b + 1, h:h + 1]), dq_r, f"block-sparse dQ ({b},{h})")
         P.check_grad(P.f64(dk[b:b + 1, h:h + 1]), dk_r, f"block-sparse dK ({b},{h})")
         P.check_grad(P.f64(dv[b:b + 1, h:h + 1]), dv_r, f"block-sparse dV ({b},{h})")
+
+
+@pytest.mark.parametrize("d,causal,window", [(128, False, (200, 50)), (64, True, (300, 0))])
+def test_block_mask_with_window_forward_and_backward(d, causal, window):
+    """The window bounds each tile's block range and the block mask then drops
+    blocks inside it; both together against the oracle with both masks."""
+    N = 900
+    w = random_case(2, 2, N, d, seed=N + d, causal=causal, window=window)
+    inp = make_inputs(w)
+    T = -(-N // 128)
+    bm = random_mask(T, 0.6, seed=d)
+    bm_gpu = torch.from_numpy(bm).cuda()
+    g = P.to_gpu(inp)
+    o, lse = fa.forward(g["q"], g["k"], g["v"], scale=w.scale, causal=causal, window=window,
+                        block_mask=bm_gpu)
+    dq, dk, dv = fa.backward(g["q"], g["k"], g["v"], o, lse, g["do"], scale=w.scale,
+                             causal=causal, window=window, block_mask=bm_gpu)
+    fa.fa_check()
+    args = [P.f64(inp[n]) for n in ("q", "k", "v")]
+    o_r, l_r = oracle.attention_fwd(*args, w.scale, causal=causal, window=window, block_mask=bm)
+    P.check_o(P.f64(o), o_r, "O (window + block mask)")
+    P.check_lse(P.f64(lse), l_r, "LSE (window + block mask)")
+    dq_r, dk_r, dv_r, _ = oracle.attention_bwd(*args, P.f64(inp["do"]), w.scale, causal=causal,
+                                               window=window, block_mask=bm)
+    P.check_grad(P.f64(dq), dq_r, "dQ (window + block mask)")
+    P.check_grad(P.f64(dk), dk_r, "dK (window + block mask)")
+    P.check_grad(P.f64(dv), dv_r, "dV (window + block mask)")
