@@ -482,9 +482,11 @@ BLOCK_SPARSE_NAME = "blocksparse_b2_h16_n8192_d128_local_global_random"
 
 class BlockSparseRunner:
     """Forward (fa_fwd_v) and backward (fa_bwd_v) of block-sparse attention:
-    the local + global + random block pattern of block_sparse_mask."""
+    the local + global + random block pattern of block_sparse_mask.  balanced:
+    pass the mask with its host copy (fa.BlockMask), so the launches plan a
+    balanced schedule; else the device mask alone (round-robin)."""
 
-    def __init__(self, fa):
+    def __init__(self, fa, balanced=True):
         c = BLOCK_SPARSE
         self.w = random_case(c["B"], c["H"], c["N"], c["d"], seed=c["seed"], causal=False)
         inp = make_inputs(self.w)
@@ -492,7 +494,8 @@ class BlockSparseRunner:
         self.q, self.k, self.v, self.do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
         T = -(-c["N"] // 128)
         self.mask_np = block_sparse_mask(T, seed=c["seed"])
-        self.mask = torch.from_numpy(self.mask_np).to(dev)
+        self.mask = (fa.BlockMask(self.mask_np, dev) if balanced
+                     else torch.from_numpy(self.mask_np).to(dev))
         self.o = torch.empty_like(self.q)
         self.lse = torch.empty(self.q.shape[:3], dtype=torch.float32, device=dev)
         self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
@@ -520,12 +523,15 @@ class BlockSparseRunner:
 
 
 def sweep_blocksparse(fa, peaks, flush_buf):
-    r = BlockSparseRunner(fa)
-    for _ in range(3):
-        r.step()
-    torch.cuda.synchronize()
-    per_phase, _ = time_steps(r, 20, flush=lambda: flush_l2(flush_buf), median=True)
-    fa.fa_check()
+    timed = []
+    for balanced in (True, False):
+        r = BlockSparseRunner(fa, balanced)
+        for _ in range(3):
+            r.step()
+        torch.cuda.synchronize()
+        timed.append(time_steps(r, 20, flush=lambda: flush_l2(flush_buf), median=True)[0])
+        fa.fa_check()
+    per_phase, rr = timed
     c = BLOCK_SPARSE
     fwd_flops = 4.0 * c["B"] * c["H"] * c["d"] * r.computed_pairs()
     dense = 4.0 * c["B"] * c["H"] * c["d"] * c["N"] * c["N"]
@@ -541,6 +547,8 @@ def sweep_blocksparse(fa, peaks, flush_buf):
             "bwd_frac_of_peak": round(2.5 * fwd_flops / (bwd_ms * 1e-3) / 1e12
                                       / peaks["bf16_tflops"], 4),
             "dense_equivalent_tflops": round(dense / (fwd_ms * 1e-3) / 1e12, 2),
+            "round_robin": {"fwd_ms": round(rr["fwd"], 4), "bwd_ms": round(rr["bwd"], 4),
+                            "note": "the device mask alone: no host copy, no balanced tail"},
             "flops": "computed (query, key) pairs only: 4 d per pair forward, 2.5x backward",
             "timing": "median of 20 steps, L2 flushed before each"}
 

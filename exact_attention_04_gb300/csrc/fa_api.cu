@@ -153,6 +153,7 @@ struct Variant {
   int H_kv, wl, wr;
   bool pair;
   const uint8_t* bm;
+  const uint8_t* bmh;    // host copy of bm, or nullptr
 };
 
 fa_status_t resolve_variant(const fa_variant_t* var, int H, int causal, Variant* out) {
@@ -166,6 +167,7 @@ fa_status_t resolve_variant(const fa_variant_t* var, int H, int causal, Variant*
   out->wr = right < 0 ? fa::kUnbounded : right;
   if (causal && out->wr > 0) out->wr = 0;
   out->bm = var ? var->block_mask : nullptr;
+  out->bmh = out->bm ? var->block_mask_host : nullptr;
   out->pair = causal && left < 0 && !out->bm;
   return FA_OK;
 }
@@ -176,53 +178,51 @@ namespace fa {
 
 namespace {
 
-// The plan itself (see plan_causal_tail).
-void plan_tail_uncached(int BH, int T, int nsplit, int G, bool fwd, long long head_bytes,
-                        TailTable* t) {
+// The plan itself (see plan_causal_tail and plan_mask_tail).  cost[blk]: one
+// item of block blk, the same in every head and half; pair: the round-robin
+// units pair blocks pp and T - 1 - pp (causal), else each is one item.
+void plan_tail_uncached(int BH, int T, int nsplit, int G, bool pair,
+                        const std::vector<long long>& cost, long long head_bytes, TailTable* t) {
   std::memset(t->item, 0xff, sizeof(t->item));         // every entry -1
   t->heads = 0;
   if (BH < 1 || T < 1 || T > 2048 || nsplit < 1 || nsplit > 2 || G < 1 || G > kTailCtas) return;
-  const int P = (T + 1) / 2;
-  // start-up and epilogue of an item, in blocks / steps: a clock64 trace of
-  // one CTA puts a forward tile boundary near 3 key blocks' time and a
-  // backward key-block boundary near 4 query steps'
-  const long long fixed = fwd ? 3 : 4;
-  auto item_cost = [&](int blk) -> long long {
-    return (fwd ? blk + 1 : 2ll * (T - blk)) + fixed;
-  };
-  std::vector<long long> unit_cost(P);                   // the pair (pp, T - 1 - pp)
-  for (int pp = 0; pp < P; ++pp)
-    unit_cost[pp] = pp == T - 1 - pp ? item_cost(pp) : item_cost(pp) + item_cost(T - 1 - pp);
+  const int per = pair ? (T + 1) / 2 : T;                // round-robin units of one head
+  std::vector<long long> unit_cost(per);
+  for (int pp = 0; pp < per; ++pp)
+    unit_cost[pp] = !pair || pp == T - 1 - pp ? cost[pp] : cost[pp] + cost[T - 1 - pp];
+  // the tail's items longest first (ties in block order)
+  std::vector<int> order(T);
+  for (int b = 0; b < T; ++b) order[b] = b;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cost[a] > cost[b]; });
   // about six tail items a CTA on average, at most kTailL2Bytes of streamed
   // data; fewer heads if a CTA would overflow its row
   const long long by_l2 = head_bytes > 0 ? std::max(1ll, kTailL2Bytes / head_bytes) : BH;
   const int first = static_cast<int>(
       std::max(1ll, std::min({static_cast<long long>(BH), 6ll * G / (T * nsplit), by_l2})));
-  // with this many rounds of equal units the last one does not matter
-  if (static_cast<long long>(BH - first) * P * nsplit > (1ll << 18)) return;
+  // with this many rounds of units the last one does not matter
+  if (static_cast<long long>(BH - first) * per * nsplit > (1ll << 18)) return;
   std::vector<long long> load(G);
   std::vector<int> count(G);
   using Slot = std::pair<long long, int>;                // (work so far, CTA)
   for (int heads = first; heads >= 1; --heads) {
     std::fill(load.begin(), load.end(), 0ll);
     std::fill(count.begin(), count.end(), 0);
-    // round-robin: unit u (pair (u / nsplit) % P of its head) on CTA u % G
-    const long long units = static_cast<long long>(BH - heads) * P * nsplit;
+    // round-robin: unit u (unit (u / nsplit) % per of its head) on CTA u % G
+    const long long units = static_cast<long long>(BH - heads) * per * nsplit;
     int c = 0, half = 0, pp = 0;
     for (long long u = 0; u < units; ++u) {
       load[c] += unit_cost[pp];
       if (++c == G) c = 0;
       if (++half == nsplit) {
         half = 0;
-        if (++pp == P) pp = 0;
+        if (++pp == per) pp = 0;
       }
     }
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> least;
     for (int k = 0; k < G; ++k) least.push({load[k], k});
     bool fits = true;
-    for (int r = 0; r < T && fits; ++r) {                // longest first
-      const int blk = fwd ? T - 1 - r : r;
-      const long long cost = item_cost(blk);
+    for (int r = 0; r < T && fits; ++r) {
+      const int blk = order[r];
       for (int h = BH - heads; h < BH && fits; ++h) {
         for (int s = 0; s < nsplit; ++s) {
           const Slot top = least.top();
@@ -233,7 +233,7 @@ void plan_tail_uncached(int BH, int T, int nsplit, int G, bool fwd, long long he
             break;
           }
           t->item[k][count[k]++] = tail_code(h, s, blk);
-          least.push({top.first + cost, k});
+          least.push({top.first + cost[blk], k});
         }
       }
     }
@@ -245,14 +245,18 @@ void plan_tail_uncached(int BH, int T, int nsplit, int G, bool fwd, long long he
   }
 }
 
-// The last few plans: a training loop asks for the same few shapes on every
-// step, and a plan is a pure function of its arguments.
+// The last few plans: a training loop asks for the same few shapes (and
+// masks) on every step, and a plan is a pure function of its arguments.  A
+// plan is keyed by a hash of its costs: two cost vectors that collide would
+// share a plan that balances one of them less well, but any plan for the same
+// (BH, T, nsplit, G) runs every item exactly once.
 struct TailPlanCache {
   struct Entry {
     bool used;
     int BH, T, nsplit, G;
-    bool fwd;
+    bool pair;
     long long head_bytes;
+    uint64_t cost_hash;
     TailTable table;
   };
   static constexpr int kEntries = 8;
@@ -266,21 +270,29 @@ TailPlanCache& tail_plan_cache() {
   return cache;
 }
 
-}  // namespace
+uint64_t hash_costs(const std::vector<long long>& cost) {
+  uint64_t h = 1469598103934665603ull;                  // FNV-1a over the 8-byte values
+  for (long long c : cost) {
+    uint64_t v = static_cast<uint64_t>(c);
+    for (int i = 0; i < 8; ++i, v >>= 8) h = (h ^ (v & 0xff)) * 1099511628211ull;
+  }
+  return h;
+}
 
-void plan_causal_tail(int BH, int T, int nsplit, int G, bool fwd, long long head_bytes,
-                      TailTable* t) {
+void plan_tail(int BH, int T, int nsplit, int G, bool pair, const std::vector<long long>& cost,
+               long long head_bytes, TailTable* t) {
+  const uint64_t hc = hash_costs(cost);
   TailPlanCache& cache = tail_plan_cache();
   {
     std::lock_guard<std::mutex> lock(cache.mu);
     for (const auto& en : cache.e)
       if (en.used && en.BH == BH && en.T == T && en.nsplit == nsplit && en.G == G &&
-          en.fwd == fwd && en.head_bytes == head_bytes) {
+          en.pair == pair && en.head_bytes == head_bytes && en.cost_hash == hc) {
         *t = en.table;
         return;
       }
   }
-  plan_tail_uncached(BH, T, nsplit, G, fwd, head_bytes, t);
+  plan_tail_uncached(BH, T, nsplit, G, pair, cost, head_bytes, t);
   std::lock_guard<std::mutex> lock(cache.mu);
   TailPlanCache::Entry& en = cache.e[cache.next];
   cache.next = (cache.next + 1) % TailPlanCache::kEntries;
@@ -289,16 +301,65 @@ void plan_causal_tail(int BH, int T, int nsplit, int G, bool fwd, long long head
   en.T = T;
   en.nsplit = nsplit;
   en.G = G;
-  en.fwd = fwd;
+  en.pair = pair;
   en.head_bytes = head_bytes;
+  en.cost_hash = hc;
   en.table = *t;
+}
+
+// Start-up and epilogue of an item, in blocks / steps: a clock64 trace of one
+// CTA puts a forward tile boundary near 3 key blocks' time and a backward
+// key-block boundary near 4 query steps'.
+long long item_fixed_cost(bool fwd) { return fwd ? 3 : 4; }
+
+}  // namespace
+
+void plan_causal_tail(int BH, int T, int nsplit, int G, bool fwd, long long head_bytes,
+                      TailTable* t) {
+  if (T < 1 || T > 2048) {
+    std::memset(t->item, 0xff, sizeof(t->item));
+    t->heads = 0;
+    return;
+  }
+  std::vector<long long> cost(T);
+  for (int b = 0; b < T; ++b) cost[b] = (fwd ? b + 1 : 2ll * (T - b)) + item_fixed_cost(fwd);
+  plan_tail(BH, T, nsplit, G, true, cost, head_bytes, t);
+}
+
+void plan_mask_tail(const uint8_t* bm_host, int BH, int T, int nsplit, int G, bool fwd, int N,
+                    int wl, int wr, long long head_bytes, TailTable* t) {
+  if (!bm_host || T < 1 || T > 2048) {
+    std::memset(t->item, 0xff, sizeof(t->item));
+    t->heads = 0;
+    return;
+  }
+  // the window in 64-bit: an unbounded side is 2^30
+  std::vector<long long> cost(T);
+  for (int b = 0; b < T; ++b) {
+    const long long lo0 = 128ll * b, hi0 = std::min<long long>(128ll * b + 128, N);   // [lo0, hi0)
+    long long lo, hi;                    // the other side's visible positions [lo, hi)
+    if (fwd) {                           // keys seen by query rows [lo0, hi0)
+      lo = std::max(0ll, lo0 - wl);
+      hi = std::min<long long>(N, hi0 - 1 + wr + 1);
+    } else {                             // queries that see keys [lo0, hi0)
+      lo = std::max(0ll, lo0 - wr);
+      hi = std::min<long long>(N, hi0 - 1 + wl + 1);
+    }
+    long long n = 0;
+    if (hi > lo)
+      for (long long o = lo / 128; o < (hi + 127) / 128; ++o)
+        n += (fwd ? bm_host[static_cast<size_t>(b) * T + o]
+                  : bm_host[static_cast<size_t>(o) * T + b]) != 0;
+    cost[b] = (fwd ? n : 2 * n) + item_fixed_cost(fwd);
+  }
+  plan_tail(BH, T, nsplit, G, false, cost, head_bytes, t);
 }
 
 }  // namespace fa
 
 extern "C" {
 
-int fa_version(void) { return 1 * 10000 + 1 * 100 + 0; }
+int fa_version(void) { return 1 * 10000 + 2 * 100 + 0; }
 
 const char* fa_status_string(fa_status_t s) {
   switch (s) {
@@ -351,6 +412,7 @@ fa_status_t fa_fwd_v(const void* q, const void* k, const void* v, void* o, float
   p.causal = var.pair ? 1 : 0;
   p.block_mask = var.bm;
   p.bm_t = (N + 127) / 128;
+  p.block_mask_host = var.bmh;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.status = di->status;
   if (fa::launch_fwd(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -407,6 +469,7 @@ fa_status_t bwd_setup(fa::BwdParams* p, DeviceInfo** di, int B, int H, int N, in
   p->causal = var.pair ? 1 : 0;
   p->block_mask = var.bm;
   p->bm_t = (N + 127) / 128;
+  p->block_mask_host = var.bmh;
   p->scale = scale;
   p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p->status = (*di)->status;
@@ -701,6 +764,7 @@ fa_status_t fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8,
   p.nb = nb;
   p.block_mask = var.bm;
   p.bm_t = nb;
+  p.block_mask_host = var.bmh;
   return fa::launch_fwd_fp8(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? FA_OK

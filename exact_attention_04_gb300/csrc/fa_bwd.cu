@@ -119,7 +119,7 @@ struct BSched {
   __device__ BSched(int BH, int N, int causal_, int tail_heads) : causal(causal_) {
     T = (N + BN - 1) / BN;
     P = (T + 1) / 2;
-    units = causal ? (BH - tail_heads) * P : BH * T;
+    units = (BH - tail_heads) * (causal ? P : T);
   }
   __device__ int nitems(int u) const {
     if (!causal) return 1;
@@ -148,7 +148,7 @@ struct BSched {
       it.u += gridDim.x;
       it.kt = 0;
     }
-    if (!causal || tail.heads == 0 || blockIdx.x >= kTailCtas || it.k >= kTailItems) return false;
+    if (tail.heads == 0 || blockIdx.x >= kTailCtas || it.k >= kTailItems) return false;
     const int e = tail.item[blockIdx.x][it.k];
     if (e < 0) return false;
     ++it.k;
@@ -745,13 +745,16 @@ cudaError_t launch_main(const BwdParams& p, int num_sms, int max_smem, cudaStrea
                              : static_cast<long long>(BH) * T;
   TailTable tail;
   tail.heads = 0;
-  if (p.causal) {
+  if (p.causal || (BS && p.block_mask_host)) {
     // single key blocks in the tail: up to one CTA per block; the tail's
     // K/V heads share their group's Q and dO through L2
     const long long blocks = static_cast<long long>(BH) * T;
     const int g = static_cast<int>(blocks < num_sms ? blocks : num_sms);
     const long long qdo_bytes = 2ll * (p.H / p.H_kv) * p.N * D * 2;
-    plan_causal_tail(BH, T, 1, g, false, qdo_bytes, &tail);
+    if (p.causal)
+      plan_causal_tail(BH, T, 1, g, false, qdo_bytes, &tail);
+    else                       // key blocks cost their computed query steps
+      plan_mask_tail(p.block_mask_host, BH, T, 1, g, false, p.N, p.wl, p.wr, qdo_bytes, &tail);
     if (tail.heads > 0) units = g;
   }
   if (tail.heads == 0) std::memset(tail.item, 0xff, sizeof(tail.item));

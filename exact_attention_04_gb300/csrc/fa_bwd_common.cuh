@@ -72,7 +72,7 @@ struct DtSched {
     T = (N + BK - 1) / BK;
     P = (T + 1) / 2;
     per_bh = causal ? P : T;
-    units = (BH - (causal ? tail_heads : 0)) * per_bh * nsplit;
+    units = (BH - tail_heads) * per_bh * nsplit;
   }
   __device__ void decode(int u, int& bh, int& pp, int& h) const {
     bh = u / (per_bh * nsplit);
@@ -102,7 +102,7 @@ struct DtSched {
       it.u += gridDim.x;
       it.kt = 0;
     }
-    if (!causal || tail.heads == 0 || blockIdx.x >= kTailCtas || it.k >= kTailItems) return false;
+    if (tail.heads == 0 || blockIdx.x >= kTailCtas || it.k >= kTailItems) return false;
     const int e = tail.item[blockIdx.x][it.k];
     if (e < 0) return false;
     ++it.k;

@@ -758,13 +758,16 @@ cudaError_t launch(const BwdParams& p, int num_sms, int max_smem, cudaStream_t s
   long long units = static_cast<long long>(BH) * per_bh * NS;
   TailTable tail;
   tail.heads = 0;
-  if (p.causal) {
+  if (p.causal || (BS && p.block_mask_host)) {
     // single key blocks in the tail: up to one CTA per block
     const long long blocks = static_cast<long long>(BH) * T * NS;
     const int g = static_cast<int>(blocks < num_sms ? blocks : num_sms);
     // the tail's K/V heads share their group's Q and dO through L2
     const long long qdo_bytes = 2ll * (p.H / p.H_kv) * p.N * D * 2;
-    plan_causal_tail(BH, T, NS, g, false, qdo_bytes, &tail);
+    if (p.causal)
+      plan_causal_tail(BH, T, NS, g, false, qdo_bytes, &tail);
+    else                       // key blocks cost their computed query steps
+      plan_mask_tail(p.block_mask_host, BH, T, NS, g, false, p.N, p.wl, p.wr, qdo_bytes, &tail);
     if (tail.heads > 0) units = g;
   }
   if (tail.heads == 0) std::memset(tail.item, 0xff, sizeof(tail.item));

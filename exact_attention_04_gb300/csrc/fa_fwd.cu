@@ -150,7 +150,9 @@ __device__ __forceinline__ void record_failure(int* status, volatile int* abort,
 }
 
 // Static persistent schedule.  Non-causal: one unit per (bh, q-tile), bh-major
-// so CTAs running at the same time share K/V in L2.  Causal: a unit pairs
+// so CTAs running at the same time share K/V in L2 (with a block mask and its
+// host copy, the last heads' tiles go in a host-planned tail as below, costed
+// by their computed key blocks).  Causal: a unit pairs
 // q-tile T-1-p (longest: T-p key blocks) with q-tile p (p+1 key blocks), the
 // longest first, so every unit costs T+1 key blocks; the units go
 // round-robin, except those of the last tail_heads heads, whose single tiles
@@ -161,7 +163,7 @@ struct Sched {
   __device__ Sched(int BH, int N, int causal_, int tail_heads) : causal(causal_) {
     T = (N + BM - 1) / BM;
     P = (T + 1) / 2;
-    units = causal ? (BH - tail_heads) * P : BH * T;
+    units = (BH - tail_heads) * (causal ? P : T);
   }
   __device__ int ntiles(int u) const {
     if (!causal) return 1;
@@ -987,13 +989,16 @@ cudaError_t launch(const FwdParams& p, int num_sms, int max_smem, cudaStream_t s
     const int T = (p.N + BM - 1) / BM;
     const int BH = p.B * p.H;
     units = p.causal ? static_cast<long long>(BH) * ((T + 1) / 2) : static_cast<long long>(BH) * T;
-    if (p.causal) {
+    if (p.causal || (BS && p.block_mask_host)) {
       // single tiles in the tail: up to one CTA per tile
       const long long tiles = static_cast<long long>(BH) * T;
       const int g = static_cast<int>(tiles < num_sms ? tiles : num_sms);
       // the tail's heads share their K and V through L2
       const long long kv_bytes = 2ll * p.N * D * (FP8 ? 1 : 2);
-      plan_causal_tail(BH, T, 1, g, true, kv_bytes, &tail);
+      if (p.causal)
+        plan_causal_tail(BH, T, 1, g, true, kv_bytes, &tail);
+      else                     // tiles cost their computed key blocks
+        plan_mask_tail(p.block_mask_host, BH, T, 1, g, true, p.N, p.wl, p.wr, kv_bytes, &tail);
       if (tail.heads > 0) units = g;
     }
   }

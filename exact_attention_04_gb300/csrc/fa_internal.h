@@ -42,6 +42,9 @@ struct FwdParams {
   // is computed (blocks of 128), or nullptr
   const uint8_t* block_mask;
   int bm_t;
+  // a host copy of the block mask, or nullptr; read by the launch (never by a
+  // kernel) to balance the schedule
+  const uint8_t* block_mask_host;
 };
 
 struct BwdParams {
@@ -70,6 +73,9 @@ struct BwdParams {
   // is computed (blocks of 128), or nullptr
   const uint8_t* block_mask;
   int bm_t;
+  // a host copy of the block mask, or nullptr; read by the launch (never by a
+  // kernel) to balance the schedule
+  const uint8_t* block_mask_host;
 };
 
 // Causal schedules.  A causal work item (a query tile of the forward, a key
@@ -105,6 +111,16 @@ __host__ __device__ constexpr int tail_block(int code) { return code & 2047; }
 constexpr long long kTailL2Bytes = 64ll << 20;
 void plan_causal_tail(int BH, int T, int nsplit, int G, bool fwd, long long head_bytes,
                       TailTable* t);
+
+// The same tail for a block-sparse schedule, whose items are not paired: the
+// units are single items (bh-major) dealt round-robin, and an item costs its
+// computed blocks, which the host counts in its copy of the block mask
+// (bm_host, [T, T] row-major) within the window (wl, wr) over N positions.
+// fwd: query tile m costs its row's computed key blocks; backward: key block
+// n costs 2 query steps per computed query block of its column.  Every head
+// shares the mask, so the costs are the same for every head.
+void plan_mask_tail(const uint8_t* bm_host, int BH, int T, int nsplit, int G, bool fwd, int N,
+                    int wl, int wr, long long head_bytes, TailTable* t);
 
 // Wait site recorded when the dynamic shared memory cannot hold the kernel's
 // layout at a 1024-byte aligned base.

@@ -25,9 +25,22 @@ _lib = None
 
 class FaVariant(ctypes.Structure):
     """fa_variant_t: K/V heads, flash-attn's (left, right) window (-1 =
-    unbounded) and a block mask (device pointer or None)."""
+    unbounded), a block mask (device pointer or None) and its host copy (host
+    pointer or None)."""
     _fields_ = [("h_kv", ctypes.c_int), ("window_left", ctypes.c_int),
-                ("window_right", ctypes.c_int), ("block_mask", ctypes.c_void_p)]
+                ("window_right", ctypes.c_int), ("block_mask", ctypes.c_void_p),
+                ("block_mask_host", ctypes.c_void_p)]
+
+
+class BlockMask:
+    """A block mask on the device together with its host copy.  Any function
+    taking block_mask= accepts one in place of the CUDA tensor; the library
+    then reads the host copy to balance its schedule (the results are the
+    same either way)."""
+
+    def __init__(self, mask, device=None):
+        self.host = torch.as_tensor(mask).to(torch.uint8).cpu().contiguous()
+        self.device = self.host.to("cuda" if device is None else device)
 
 
 class FAError(RuntimeError):
@@ -237,14 +250,21 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, scale, causal=False, kv_len=
 
 
 def _check_block_mask(bm, N):
-    """A block mask: a contiguous uint8 CUDA tensor [T, T], T = ceil(N/128)."""
+    """(device pointer, host pointer) of a block mask: a contiguous uint8
+    CUDA tensor [T, T], T = ceil(N/128), or a BlockMask holding one and its
+    host copy.  The caller keeps bm alive across the call."""
     if bm is None:
-        return None
+        return None, None
     t = -(-N // 128)
+    host = None
+    if isinstance(bm, BlockMask):
+        host, bm = bm.host, bm.device
+        if host.dtype != torch.uint8 or tuple(host.shape) != (t, t) or not host.is_contiguous():
+            raise ValueError(f"block_mask: expected a host copy of shape [{t}, {t}]")
     if bm.dtype != torch.uint8 or not bm.is_cuda or tuple(bm.shape) != (t, t) \
             or not bm.is_contiguous():
         raise ValueError(f"block_mask: expected a contiguous uint8 CUDA tensor [{t}, {t}]")
-    return bm
+    return bm.data_ptr(), None if host is None else host.data_ptr()
 
 
 def _variant(q, k, window, block_mask=None):
@@ -255,15 +275,15 @@ def _variant(q, k, window, block_mask=None):
             or H % k.shape[1]:
         raise ValueError(f"k: shape {tuple(k.shape)} does not group the {H} query heads")
     wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
-    bm = _check_block_mask(block_mask, N)
-    return FaVariant(int(k.shape[1]), wl, wr, None if bm is None else bm.data_ptr())
+    return FaVariant(int(k.shape[1]), wl, wr, *_check_block_mask(block_mask, N))
 
 
 def fa_fwd_v(q, k, v, o, lse, scale, causal=False, kv_len=None, window=None, stream=None,
              block_mask=None):
     """Calls fa_fwd_v: k, v are [B,H_kv,N,d] (H_kv divides H); window is
     flash-attn's (left, right), -1 = unbounded; block_mask a uint8 CUDA
-    tensor [ceil(N/128)]^2, zero where a (query block, key block) is skipped."""
+    tensor [ceil(N/128)]^2, zero where a (query block, key block) is skipped,
+    or a BlockMask (the same with its host copy, for a balanced schedule)."""
     _check_qkv("q", q)
     B, H, N, d = q.shape
     var = _variant(q, k, window, block_mask)
@@ -397,8 +417,7 @@ def fa_fwd_fp8(buf, o, lse, scale, causal=False, kv_len=None, window=None, strea
         raise ValueError("lse: expected fp32 CUDA tensor [B,H,N]")
     kv_len = _check_kv_len(kv_len, B)
     wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
-    bm = _check_block_mask(block_mask, N)
-    var = FaVariant(int(Hkv), wl, wr, None if bm is None else bm.data_ptr())
+    var = FaVariant(int(Hkv), wl, wr, *_check_block_mask(block_mask, N))
     _raise(load().fa_fwd_fp8(_ptr(buf["q8"]), _ptr(buf["q_scale"]), _ptr(buf["k8"]),
                              _ptr(buf["k_scale"]), _ptr(buf["v8t"]), _ptr(buf["v_scale"]),
                              _ptr(o), _ptr(lse), B, H, N, d, float(scale), int(bool(causal)),

@@ -143,14 +143,24 @@ fa_status_t fa_bwd_dq(void* dq, int B, int H, int N, int d, float scale, void* w
  *   mask, tiles are scheduled one per unit instead of in causal pairs.  The
  *   caller keeps the mask unchanged until the call's work has run.  fa_decode
  *   rejects a block mask (FA_ERR_UNSUPPORTED).
- * A NULL variant pointer means {H, -1, -1, NULL}; an aggregate initialiser
- * that stops after window_right leaves block_mask NULL.
+ * block_mask_host: NULL, or host memory holding the same T * T bytes as
+ *   block_mask (ignored when block_mask is NULL).  The call reads it before
+ *   it returns, on the calling thread, to balance its persistent schedule:
+ *   a tile's work is its count of computed blocks, and the last heads' tiles
+ *   go, most work first, to the least-loaded SMs.  The results do not depend
+ *   on it; a copy that differs from block_mask only unbalances the schedule.
+ *   NULL: tiles go round-robin, which with an uneven mask can leave some SMs
+ *   with a third more work than the mean.
+ * A NULL variant pointer means {H, -1, -1, NULL, NULL}; an aggregate
+ * initialiser that stops after window_right (or block_mask) leaves the later
+ * members NULL.
  */
 typedef struct fa_variant {
   int h_kv;
   int window_left;
   int window_right;
   const unsigned char* block_mask;
+  const unsigned char* block_mask_host;
 } fa_variant_t;
 
 /*
@@ -287,7 +297,7 @@ const char* fa_status_string(fa_status_t status);
 
 /* Library version as major*10000 + minor*100 + patch.  1.1: fa_variant_t
  * gained block_mask (a trailing member, NULL in aggregate initialisers that
- * stop before it). */
+ * stop before it).  1.2: fa_variant_t gained block_mask_host (the same). */
 int fa_version(void);
 
 #ifdef __cplusplus

@@ -46,7 +46,32 @@ def test_status_strings_and_version(lib):
     assert fa.fa_status_string(fa.FA_OK) == "FA_OK"
     assert fa.fa_status_string(fa.FA_ERR_TIMEOUT) == "FA_ERR_TIMEOUT"
     assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"
-    assert fa.fa_version() >= 10100         # fa_variant_t with block_mask
+    assert fa.fa_version() >= 10200         # fa_variant_t with block_mask_host
+
+
+def test_variant_layout_matches_the_header(tmp_path):
+    """The binding's FaVariant has the size and member offsets that a C
+    compiler gives fa_variant_t from include/fa.h."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stddef.h>\n#include <stdio.h>\n#include "fa.h"\n'
+        "int main(void) { printf(\"%zu %zu %zu %zu %zu %zu\\n\", sizeof(fa_variant_t),"
+        " offsetof(fa_variant_t, h_kv), offsetof(fa_variant_t, window_left),"
+        " offsetof(fa_variant_t, window_right), offsetof(fa_variant_t, block_mask),"
+        " offsetof(fa_variant_t, block_mask_host)); return 0; }\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    V = fa.FaVariant
+    assert got == [ctypes.sizeof(V), V.h_kv.offset, V.window_left.offset,
+                   V.window_right.offset, V.block_mask.offset, V.block_mask_host.offset]
 
 
 def test_workspace_bytes(lib):
@@ -125,6 +150,33 @@ def test_variant_argument_errors(lib):
         assert call(8) == fa.FA_ERR_INVALID_ARG          # more K/V heads than query heads
         assert call(2, wl=-2) == fa.FA_ERR_INVALID_ARG
         assert call(2, wr=-5) == fa.FA_ERR_INVALID_ARG
+
+
+def test_block_mask_binding_passes_both_copies(lib):
+    """A BlockMask gives the variant its device pointer and its host copy's
+    pointer; a plain tensor gives no host copy; wrong shapes are refused."""
+    import torch
+
+    class FakeCuda:                      # a stand-in for a CUDA uint8 tensor (no GPU here)
+        dtype, is_cuda, shape = torch.uint8, True, (2, 2)
+
+        def is_contiguous(self):
+            return True
+
+        def data_ptr(self):
+            return 0x1000
+
+    bm = fa.BlockMask.__new__(fa.BlockMask)
+    bm.host = torch.tensor([[1, 0], [1, 1]], dtype=torch.uint8)
+    bm.device = FakeCuda()
+    assert fa._check_block_mask(bm, 256) == (0x1000, bm.host.data_ptr())
+    assert fa._check_block_mask(FakeCuda(), 200) == (0x1000, None)
+    assert fa._check_block_mask(None, 200) == (None, None)
+    with pytest.raises(ValueError):
+        fa._check_block_mask(bm, 512)     # T = 4, not 2
+    bm.host = torch.ones(2, 3, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        fa._check_block_mask(bm, 256)
 
 
 def test_variant_binding_checks_shapes(lib):

@@ -152,12 +152,13 @@ def test_backward_key_block_with_no_query_has_zero_gradient():
 def test_blocksparse_bench_workload_sampled_heads():
     """The bench's block-sparse workload (B=2, H=16, N=8192, d=128, the local +
     global + random pattern at about 25 % density), two heads against the
-    oracle, forward and backward, in the launch configuration the bench times."""
+    oracle, forward and backward, in the launch configuration the bench times
+    (the mask with its host copy, so the schedule is the balanced one)."""
     from exact_attention_04_gb300.workloads import block_sparse_mask
     w = random_case(2, 16, 8192, 128, seed=12, causal=False)
     inp = make_inputs(w)
     bm = block_sparse_mask(64, seed=12)
-    bm_gpu = torch.from_numpy(bm).cuda()
+    bm_gpu = fa.BlockMask(bm)
     g = P.to_gpu(inp)
     o, lse = fa.forward(g["q"], g["k"], g["v"], scale=w.scale, block_mask=bm_gpu)
     dq, dk, dv = fa.backward(g["q"], g["k"], g["v"], o, lse, g["do"], scale=w.scale,
@@ -202,3 +203,33 @@ def test_block_mask_with_window_forward_and_backward(d, causal, window):
     P.check_grad(P.f64(dq), dq_r, "dQ (window + block mask)")
     P.check_grad(P.f64(dk), dk_r, "dK (window + block mask)")
     P.check_grad(P.f64(dv), dv_r, "dV (window + block mask)")
+
+
+@pytest.mark.parametrize("d,Hkv,window", [(128, 16, None), (256, 16, None), (64, 16, None),
+                                          (128, 4, (-1, 0))])
+def test_balanced_schedule_matches_round_robin(d, Hkv, window):
+    """With the mask's host copy the launch plans a balanced tail of tiles and
+    key blocks; without it every item goes round-robin.  A tile's, or a key
+    block's, arithmetic does not depend on the SM that runs it, so O, LSE, dK
+    and dV agree bit for bit; dQ is summed across key blocks in L2 in an
+    order that varies, so it agrees within a bf16 unit.  A tile or key block
+    the plan missed or ran twice would show here (at N = 8192 the plan has
+    a tail of 14 heads on 152 SMs)."""
+    from exact_attention_04_gb300.workloads import block_sparse_mask
+    w = random_case(2, 16, 8192, d, seed=d + Hkv, causal=False, h_kv=Hkv)
+    g = P.to_gpu(make_inputs(w))
+    bm = block_sparse_mask(64, seed=12)
+    plain, balanced = torch.from_numpy(bm).cuda(), fa.BlockMask(bm)
+    out = []
+    for m in (plain, balanced):
+        o, lse = fa.forward(g["q"], g["k"], g["v"], scale=w.scale, window=window, block_mask=m)
+        grads = fa.backward(g["q"], g["k"], g["v"], o, lse, g["do"], scale=w.scale,
+                            window=window, block_mask=m)
+        out.append((o, lse) + tuple(grads))
+    fa.fa_check()
+    (o1, l1, dq1, dk1, dv1), (o2, l2, dq2, dk2, dv2) = out
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    diff = (dq1.float() - dq2.float()).abs().max().item()
+    assert diff <= 2 ** -7 * dq1.float().abs().max().item(), diff
+    assert (dq1 != dq2).float().mean().item() < 0.01

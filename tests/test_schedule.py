@@ -161,3 +161,148 @@ def test_plan_is_repeatable_across_interleaved_calls(plan):
             t = plan(*s)
             assert t.heads == t0.heads
             assert all(list(t.item[c]) == list(t0.item[c]) for c in range(TAIL_CTAS))
+
+
+# ---- block-sparse schedules: single items, costed by the mask ----
+
+MASK_PLAN = "_ZN2fa14plan_mask_tailEPKhiiiibiiixPNS_9TailTableE"   # fa::plan_mask_tail
+UNB = -1                                  # an unbounded window side, as the binding passes it
+
+
+@pytest.fixture(scope="module")
+def mask_plan():
+    fabuild.build()
+    lib = fa.load()
+    f = getattr(lib, MASK_PLAN)
+    f.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_bool, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_longlong,
+                  ctypes.POINTER(TailTable)]
+    f.restype = None
+
+    def run(bm, BH, nsplit, G, fwd, N, wl=1 << 30, wr=1 << 30, head_bytes=0):
+        t = TailTable()
+        f(None if bm is None else bytes(bm.astype("uint8").ravel()), BH, bm.shape[0] if bm is not None else 1,
+          nsplit, G, fwd, N, wl, wr, head_bytes, ctypes.byref(t))
+        return t
+    return run
+
+
+def mask_costs(bm, fwd, N, wl, wr):
+    """Item costs counted position by position: a block is computed for an
+    item when its mask entry is set and some (query, key) pair of the two
+    blocks is inside the window."""
+    T = bm.shape[0]
+    out = []
+    for b in range(T):
+        n = 0
+        for o in range(T):
+            a, c = (b, o) if fwd else (o, b)          # (query block, key block)
+            seen = any(i - wl <= j <= i + wr
+                       for i in range(128 * a, min(128 * a + 128, N))
+                       for j in range(128 * c, min(128 * c + 128, N)))
+            n += bool(bm[a, c]) and seen
+        out.append((n if fwd else 2 * n) + (3 if fwd else 4))
+    return out
+
+
+def walk_single(t, BH, T, nsplit, G):
+    """Each CTA's items as the kernels walk them without pairing: unit u is
+    (head u // (T nsplit), block (u // nsplit) % T, half u % nsplit) on CTA
+    u % G, then the CTA's tail row."""
+    per_cta = [[] for _ in range(G)]
+    for u in range((BH - t.heads) * T * nsplit):
+        bh, rem = divmod(u, T * nsplit)
+        n, h = divmod(rem, nsplit)
+        per_cta[u % G].append((bh, h, n))
+    for c in range(min(G, TAIL_CTAS)):
+        row = [e for e in t.item[c]]
+        ends = [k for k, e in enumerate(row) if e < 0]
+        assert all(e < 0 for e in row[ends[0]:]) if ends else True
+        per_cta[c] += [(e >> 12, (e >> 11) & 1, e & 2047) for e in row if e >= 0]
+    return per_cta
+
+
+def bench_mask(T=64, seed=12):
+    from exact_attention_04_gb300.workloads import block_sparse_mask
+    return block_sparse_mask(T, seed=seed)
+
+
+MASK_SHAPES = [
+    # BH, nsplit, G, fwd
+    (32, 1, 152, True),       # B=2, H=16, N=8192 forward
+    (32, 1, 152, False),      # its backward
+    (32, 2, 152, False),      # d = 256
+    (16, 1, 152, False),      # GQA K/V heads
+    (3, 1, 20, True),
+]
+
+
+@pytest.mark.parametrize("BH,nsplit,G,fwd", MASK_SHAPES)
+def test_mask_plan_covers_every_item_once(mask_plan, BH, nsplit, G, fwd):
+    bm = bench_mask()
+    T = bm.shape[0]
+    t = mask_plan(bm, BH, nsplit, G, fwd, 128 * T)
+    assert 0 < t.heads <= BH
+    got = sorted(x for c in walk_single(t, BH, T, nsplit, G) for x in c)
+    assert got == sorted((bh, h, n) for bh in range(BH) for h in range(nsplit) for n in range(T))
+
+
+@pytest.mark.parametrize("fwd", [True, False])
+@pytest.mark.parametrize("N,wl,wr", [(1000, 1 << 30, 1 << 30), (1000, 1 << 30, 0), (900, 200, 60)])
+def test_mask_plan_costs_count_the_computed_blocks(mask_plan, fwd, N, wl, wr):
+    """On one head and one CTA per item, the tail runs item b on its own CTA
+    when every item fits, longest first; so the table's order gives the
+    planner's costs back (strictly, where they differ)."""
+    T = -(-N // 128)
+    rng = __import__("numpy").random.default_rng(5)
+    bm = (rng.random((T, T)) < 0.5).astype("uint8")
+    want = mask_costs(bm, fwd, N, wl, wr)
+    # a single CTA takes every item of one head in cost order (T <= 8 items)
+    t = mask_plan(bm, 1, 1, 1, fwd, N, wl, wr)
+    assert t.heads == 1
+    order = [e & 2047 for e in t.item[0] if e >= 0]
+    assert sorted(order) == list(range(T))
+    costs = [want[b] for b in order]
+    assert costs == sorted(costs, reverse=True)
+    # ties keep block order
+    for a, b in zip(order, order[1:]):
+        if want[a] == want[b]:
+            assert a < b
+
+
+def test_mask_plan_costs_decide_the_order_on_many_ctas(mask_plan):
+    """A mask whose rows (forward) or columns (backward) hold k blocks for
+    item k: each item goes to its own CTA, the costliest to CTA 0."""
+    import numpy as np
+    T = 6
+    bm = np.tril(np.ones((T, T), np.uint8))          # row a: a + 1 blocks; column b: T - b
+    t = mask_plan(bm, 1, 1, T, True, 128 * T)
+    assert [t.item[c][0] & 2047 for c in range(T)] == [5, 4, 3, 2, 1, 0]
+    t = mask_plan(bm, 1, 1, T, False, 128 * T)
+    assert [t.item[c][0] & 2047 for c in range(T)] == [0, 1, 2, 3, 4, 5]
+
+
+@pytest.mark.parametrize("BH,nsplit,G,fwd,bound", [
+    (32, 1, 152, True, 0.03), (32, 1, 152, False, 0.03), (32, 2, 152, False, 0.03)])
+def test_mask_plan_balances_the_block_sparse_step(mask_plan, BH, nsplit, G, fwd, bound):
+    """On the local + global + random mask, round-robin leaves the busiest SM
+    10 to 35 % above the mean; the planned tail brings it within `bound`."""
+    bm = bench_mask()
+    T = bm.shape[0]
+    cost = mask_costs(bm, fwd, 128 * T, 1 << 30, 1 << 30)
+    t = mask_plan(bm, BH, nsplit, G, fwd, 128 * T)
+    loads = [sum(cost[n] for _, _, n in c) for c in walk_single(t, BH, T, nsplit, G)]
+    mean = sum(loads) / G
+    rr = [0] * G
+    for u in range(BH * T * nsplit):
+        rr[u % G] += cost[(u // nsplit) % T]
+    assert max(rr) > mean * 1.1
+    assert max(loads) <= mean * (1 + bound), (max(loads) / mean, max(rr) / mean)
+
+
+def test_mask_plan_without_a_mask_plans_nothing(mask_plan):
+    t = TailTable()
+    f = getattr(fa.load(), MASK_PLAN)
+    f(None, 32, 64, 1, 152, True, 8192, 1 << 30, 1 << 30, 0, ctypes.byref(t))
+    assert t.heads == 0
+    assert all(t.item[c][k] == -1 for c in range(TAIL_CTAS) for k in range(TAIL_ITEMS))
