@@ -233,3 +233,51 @@ def test_balanced_schedule_matches_round_robin(d, Hkv, window):
     diff = (dq1.float() - dq2.float()).abs().max().item()
     assert diff <= 2 ** -7 * dq1.float().abs().max().item(), diff
     assert (dq1 != dq2).float().mean().item() < 0.01
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_balanced_schedule_matches_round_robin_fp8(d):
+    """The E4M3 forward with and without the mask's host copy: the same tiles
+    with the same arithmetic, so O and LSE agree bit for bit."""
+    from exact_attention_04_gb300.workloads import block_sparse_mask
+    w = random_case(2, 16, 8192, d, seed=d + 7, causal=False)
+    g = P.to_gpu(make_inputs(w))
+    bm = block_sparse_mask(64, seed=3)
+    o1, l1, _ = fa.forward_fp8(g["q"], g["k"], g["v"], scale=w.scale,
+                               block_mask=torch.from_numpy(bm).cuda())
+    o2, l2, _ = fa.forward_fp8(g["q"], g["k"], g["v"], scale=w.scale, block_mask=fa.BlockMask(bm))
+    fa.fa_check()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_balanced_schedule_with_padding_against_oracle():
+    """Key padding with the balanced schedule (the plan counts blocks over the
+    full length; the kernels still stop at each entry's kv_len), two heads
+    against the oracle."""
+    from exact_attention_04_gb300.workloads import block_sparse_mask
+    N = 4000
+    w = random_case(2, 8, N, 128, seed=41, causal=False, kv_len_range=(1500, N))
+    inp = make_inputs(w)
+    T = -(-N // 128)
+    bm = block_sparse_mask(T, seed=4, band=2, n_random=3)
+    g = P.to_gpu(inp)
+    kv = g.get("kv_len")
+    m = fa.BlockMask(bm)
+    o, lse = fa.forward(g["q"], g["k"], g["v"], scale=w.scale, kv_len=kv, block_mask=m)
+    dq, dk, dv = fa.backward(g["q"], g["k"], g["v"], o, lse, g["do"], scale=w.scale, kv_len=kv,
+                             block_mask=m)
+    fa.fa_check()
+    kvl = None if inp.get("kv_len") is None else [int(x) for x in inp["kv_len"]]
+    for b, h in ((0, 3), (1, 6)):
+        one = {n: inp[n][b:b + 1, h:h + 1] for n in ("q", "k", "v", "do")}
+        kl = None if kvl is None else [kvl[b]]
+        o_r, l_r = oracle.attention_fwd(P.f64(one["q"]), P.f64(one["k"]), P.f64(one["v"]),
+                                        w.scale, kv_len=kl, block_mask=bm)
+        P.check_o(P.f64(o[b:b + 1, h:h + 1]), o_r, f"padded block-sparse O ({b},{h})")
+        P.check_lse(P.f64(lse[b:b + 1, h:h + 1]), l_r, f"padded block-sparse LSE ({b},{h})")
+        dq_r, dk_r, dv_r, _ = oracle.attention_bwd(P.f64(one["q"]), P.f64(one["k"]),
+                                                   P.f64(one["v"]), P.f64(one["do"]), w.scale,
+                                                   kv_len=kl, block_mask=bm)
+        P.check_grad(P.f64(dq[b:b + 1, h:h + 1]), dq_r, f"padded block-sparse dQ ({b},{h})")
+        P.check_grad(P.f64(dk[b:b + 1, h:h + 1]), dk_r, f"padded block-sparse dK ({b},{h})")
+        P.check_grad(P.f64(dv[b:b + 1, h:h + 1]), dv_r, f"padded block-sparse dV ({b},{h})")

@@ -15,6 +15,10 @@ returns:
 - rows are -1-terminated and within their capacity;
 - each CTA's items run longest first;
 - the plan beats plain round-robin of pairs.
+
+The block-sparse planner (plan_mask_tail) gets the same checks with single
+items dealt round-robin, plus its costs: the computed blocks of each item,
+counted position by position in the mask and the window.
 """
 import ctypes
 
