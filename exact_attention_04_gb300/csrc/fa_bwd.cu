@@ -745,7 +745,7 @@ cudaError_t launch_main(const BwdParams& p, int num_sms, int max_smem, cudaStrea
                              : static_cast<long long>(BH) * T;
   TailTable tail;
   tail.heads = 0;
-  if (p.causal || (BS && p.block_mask_host)) {
+  if (p.causal || (BS && p.block_mask_host && T == p.bm_t)) {
     // single key blocks in the tail: up to one CTA per block; the tail's
     // K/V heads share their group's Q and dO through L2
     const long long blocks = static_cast<long long>(BH) * T;

@@ -758,7 +758,7 @@ cudaError_t launch(const BwdParams& p, int num_sms, int max_smem, cudaStream_t s
   long long units = static_cast<long long>(BH) * per_bh * NS;
   TailTable tail;
   tail.heads = 0;
-  if (p.causal || (BS && p.block_mask_host)) {
+  if (p.causal || (BS && p.block_mask_host && T == p.bm_t)) {
     // single key blocks in the tail: up to one CTA per block
     const long long blocks = static_cast<long long>(BH) * T * NS;
     const int g = static_cast<int>(blocks < num_sms ? blocks : num_sms);

@@ -989,7 +989,9 @@ cudaError_t launch(const FwdParams& p, int num_sms, int max_smem, cudaStream_t s
     const int T = (p.N + BM - 1) / BM;
     const int BH = p.B * p.H;
     units = p.causal ? static_cast<long long>(BH) * ((T + 1) / 2) : static_cast<long long>(BH) * T;
-    if (p.causal || (BS && p.block_mask_host)) {
+    // (the mask planner reads the host copy as [T, T]: tiles and mask blocks
+    // are both 128 rows)
+    if (p.causal || (BS && p.block_mask_host && T == p.bm_t)) {
       // single tiles in the tail: up to one CTA per tile
       const long long tiles = static_cast<long long>(BH) * T;
       const int g = static_cast<int>(tiles < num_sms ? tiles : num_sms);
