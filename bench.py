@@ -38,10 +38,13 @@ from exact_attention_04_gb300.workloads import (WORKLOADS, block_sparse_mask,  #
 METRIC = "attention fwd/bwd TFLOP/s on 1 GB300 and % of dense-BF16 roofline vs N"
 HEADLINE = "large_head_b2_h16_n8192_d128_causal"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# Every source a kernel's DRAM traffic depends on: its own file, the headers
+# it includes, and fa_api.cu (the host planner that sets its schedule).
+_COMMON_SOURCES = ["fa_api.cu", "fa_internal.h", "fa_window.cuh", "sm103_ptx.cuh"]
 KERNEL_SOURCES = {
-    "fa_fwd_kernel": ["fa_fwd.cu", "sm103_ptx.cuh"],
-    "bwd_main_kernel": ["fa_bwd.cu", "fa_api.cu", "sm103_ptx.cuh"],
-    "bwd_dt_kernel": ["fa_bwd_dt.cu", "fa_bwd_common.cuh", "fa_api.cu", "sm103_ptx.cuh"],
+    "fa_fwd_kernel": ["fa_fwd.cu"] + _COMMON_SOURCES,
+    "bwd_main_kernel": ["fa_bwd.cu"] + _COMMON_SOURCES,
+    "bwd_dt_kernel": ["fa_bwd_dt.cu", "fa_bwd_common.cuh"] + _COMMON_SOURCES,
 }
 
 
