@@ -219,10 +219,10 @@ def walk_single(t, BH, T, nsplit, G):
         n, h = divmod(rem, nsplit)
         per_cta[u % G].append((bh, h, n))
     for c in range(min(G, TAIL_CTAS)):
-        row = [e for e in t.item[c]]
-        ends = [k for k, e in enumerate(row) if e < 0]
-        assert all(e < 0 for e in row[ends[0]:]) if ends else True
-        per_cta[c] += [(e >> 12, (e >> 11) & 1, e & 2047) for e in row if e >= 0]
+        row = list(t.item[c])
+        live = [e for e in row if e >= 0]
+        assert row[:len(live)] == live, f"CTA {c}: an entry after the end of its row"
+        per_cta[c] += [(e >> 12, (e >> 11) & 1, e & 2047) for e in live]
     return per_cta
 
 
