@@ -310,3 +310,19 @@ def test_mask_plan_without_a_mask_plans_nothing(mask_plan):
     f(None, 32, 64, 1, 152, True, 8192, 1 << 30, 1 << 30, 0, ctypes.byref(t))
     assert t.heads == 0
     assert all(t.item[c][k] == -1 for c in range(TAIL_CTAS) for k in range(TAIL_ITEMS))
+
+
+def test_mask_plans_are_memoised_per_mask(mask_plan):
+    """Two masks of one shape get their own plans, and asking again, after
+    other plans, returns each one's plan unchanged."""
+    import numpy as np
+    a = bench_mask(seed=12)
+    b = np.ascontiguousarray(a[::-1])                 # the same rows in reverse order
+    pa, pb = mask_plan(a, 32, 1, 152, True, 8192), mask_plan(b, 32, 1, 152, True, 8192)
+    rows = lambda t: [list(t.item[c]) for c in range(TAIL_CTAS)]
+    assert rows(pa) != rows(pb)
+    for _ in range(2):
+        for s in range(9):                            # more plans than the memo holds
+            mask_plan(bench_mask(seed=100 + s), 32, 1, 152, True, 8192)
+        assert rows(mask_plan(a, 32, 1, 152, True, 8192)) == rows(pa)
+        assert rows(mask_plan(b, 32, 1, 152, True, 8192)) == rows(pb)
