@@ -476,6 +476,39 @@ fa_status_t bwd_setup(fa::BwdParams* p, DeviceInfo** di, int B, int H, int N, in
   return FA_OK;
 }
 
+}  // namespace
+
+namespace fa {
+
+// The checks fa_bwd makes, in fa_bwd's order and with its status codes, for
+// a caller that supplies a workspace of exactly workspace_bytes at a valid
+// address: pointers, kv_len, sizes, the workspace size, then the device.
+fa_status_t bwd_check_args(const void* q, const void* k, const void* v, const void* o,
+                           const void* dO, const float* lse, const void* dq, const void* dk,
+                           const void* dv, int B, int H, int N, int d, float scale,
+                           int causal, const int* kv_len, size_t workspace_bytes) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dv))
+    return FA_ERR_INVALID_ARG;
+  if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) return FA_ERR_INVALID_ARG;
+  const fa_status_t sz = check_sizes(B, H, N, d, scale);
+  if (sz != FA_OK) return sz;
+  Variant var;
+  const fa_status_t vs = resolve_variant(nullptr, H, causal, &var);
+  if (vs != FA_OK) return vs;
+  if (workspace_bytes < fa_bwd_workspace_bytes(B, H, N, d)) return FA_ERR_INVALID_ARG;
+  DeviceInfo* di = device_info(nullptr);
+  if (!di || di->err != cudaSuccess) return FA_ERR_CUDA;
+  if (!di->supported) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+}  // namespace fa
+
+namespace {
+
 fa_status_t bwd_prep_impl(const fa::BwdParams& p, int d, void* stream) {
   return fa::launch_bwd_prep(p, d, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK
                                                                                      : FA_ERR_CUDA;

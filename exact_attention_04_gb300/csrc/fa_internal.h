@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa.h"
+
 namespace fa {
 
 // Device status word values written by kernels that gave up waiting:
@@ -132,6 +134,13 @@ inline size_t smem_request(size_t bytes, int max_optin) {
   const size_t room = static_cast<size_t>(max_optin) > bytes ? max_optin - bytes : 0;
   return bytes + (room < 1024 ? room : 1024);
 }
+
+// fa_bwd's argument and device checks, in its order and with its status
+// codes, for a workspace of workspace_bytes at a valid address.
+fa_status_t bwd_check_args(const void* q, const void* k, const void* v, const void* o,
+                           const void* dO, const float* lse, const void* dq, const void* dk,
+                           const void* dv, int B, int H, int N, int d, float scale,
+                           int causal, const int* kv_len, size_t workspace_bytes);
 
 cudaError_t launch_fwd(const FwdParams& p, int d, int num_sms, int max_smem, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const BwdParams& p, int d, cudaStream_t stream);

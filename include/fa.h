@@ -259,7 +259,8 @@ fa_status_t fa_selftest_wait_timeout(unsigned int timeout_us, void* stream);
 
 /*
  * fa_bwd_noalloc: the backward pass for callers that cannot allocate device
- * memory.  Same arguments, results and errors as fa_bwd, minus the workspace:
+ * memory.  Same arguments, results and errors as fa_bwd (checked in the same
+ * order), minus the workspace:
  * the scratch fa_bwd needs (fa_bwd_workspace_bytes(B,H,N,d) bytes) comes from
  * a fixed array of FA_BWD_NOALLOC_MAX_SCRATCH_BYTES that the library keeps in
  * device memory, so this call allocates nothing.  It is meant for code that is
@@ -272,8 +273,10 @@ fa_status_t fa_selftest_wait_timeout(unsigned int timeout_us, void* stream);
  *   elements).
  * - Every GPU that loads this part of the library holds the array until the
  *   process exits.  Its device address is looked up on the first call on each
- *   device (with that device current); make that first call before any
- *   stream capture.
+ *   device that passes the argument checks (with that device current); make
+ *   that first call before any stream capture.  A lookup that fails returns
+ *   FA_ERR_CUDA, leaves no error pending in cudaGetLastError(), and is tried
+ *   again by the next call.
  * - All calls share the array: calls whose kernels overlap on the GPU race
  *   and give wrong gradients.  Calls ordered on one stream are fine; each call
  *   re-initialises the scratch it reads, so no state carries over.

@@ -245,3 +245,30 @@ def test_decode_split_choice(lib):
         if B * hk < sms:
             assert B * hk * s <= sms
     assert fa.fa_decode_splits(0, 8, 100) == 0
+
+
+def test_noalloc_backward_reports_fa_bwd_status_codes(lib):
+    """fa_bwd_noalloc checks its arguments as fa_bwd does, in the same order,
+    so a bad call gets the same status from both (here every case fails
+    before the device is touched, or at the device lookup on a host without
+    a GPU).  Only a problem larger than the fixed scratch differs: it is
+    refused with FA_ERR_INVALID_ARG, as fa_bwd refuses a workspace too small."""
+    import torch
+    ok = 0x1000
+
+    def both(q=ok, lse=ok, kv=None, B=1, H=1, N=128, d=64, scale=0.125):
+        a = lib.fa_bwd(P(q), P(ok), P(ok), P(ok), P(ok), P(lse), P(ok), P(ok), P(ok), B, H, N,
+                       d, scale, 0, P(kv) if kv else None, P(0x100000), 1 << 40, None)
+        b = lib.fa_bwd_noalloc(P(q), P(ok), P(ok), P(ok), P(ok), P(lse), P(ok), P(ok), P(ok),
+                               B, H, N, d, scale, 0, P(kv) if kv else None, None)
+        return a, b
+    cases = [dict(q=0), dict(q=0x1008), dict(lse=0x1002), dict(kv=0x1001), dict(B=0),
+             dict(B=0, d=100), dict(N=0, d=32), dict(d=100), dict(d=100, scale=0.0),
+             dict(scale=float("nan")), dict(B=1 << 14, H=1 << 10, N=1 << 10)]
+    if not torch.cuda.is_available():
+        cases.append({})                 # valid arguments: both stop at the device lookup
+    for c in cases:
+        a, b = both(**c)
+        assert a == b, (c, a, b)
+        assert a != fa.FA_OK
+    assert both(B=1, H=1, N=131072, d=128)[1] == fa.FA_ERR_INVALID_ARG
