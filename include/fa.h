@@ -234,10 +234,16 @@ fa_status_t fa_decode(const void* q, const void* k, const void* v, void* o, floa
  *
  * fa_fwd_fp8 computes O (bf16 [B,H,N,d]) and LSE (fp32 [B,H,N]) from them:
  * S = (q8 k8^T) * q_scale * k_scale * scale on the tensor core in FP32; the
- * online softmax of fa_fwd over 128-key blocks, with the reference maximum
- * raised at every new block maximum; P enters the P V product as E4M3(256 P)
- * against v8t, the row sum adds the unrounded P; O = v_scale * (P V) /
- * (256 * l).  causal, kv_len and the variant as for fa_fwd_v.
+ * online softmax of fa_fwd over 128-key blocks.  A row's reference maximum m
+ * starts at its first block's maximum and is raised to a block's maximum
+ * only when that exceeds m by more than a factor 2^4, so P = exp(S - m) <=
+ * 16; P enters the P V product as E4M3(16 P) <= 256 against v8t (FP32
+ * accumulation), the row sum l adds the unrounded P, and O = v_scale *
+ * (sum of E4M3(16 P) v8) / (16 l), LSE = m + ln l.  The result differs from
+ * exact attention of the dequantised inputs (x8 * scale) only by E4M3's
+ * rounding of P (2^-4 of a weight in E4M3's normal range, 2^-10 of the row's
+ * largest weight below it) and FP32 rounding.  causal, kv_len and the
+ * variant as for fa_fwd_v.
  */
 fa_status_t fa_fp8_quantize(const void* q, const void* k, const void* v, int B, int H, int N,
                             int d, const fa_variant_t* variant, void* q8, float* q_scale,

@@ -6,7 +6,12 @@ smoke check and the benchmark's CPU legs use it.
 "4. FlashAttention 深度剖析" 4.5.4 gives the method in three points: E4M3
 for the forward, a scale per K block applied when the block is loaded, and
 FP32 accumulation of the FP8 products.  It does not fix the rest; the
-readings used here (and by the GPU path, which is checked against this file):
+readings below are also the GPU kernel's.  The GPU path is not
+checked against this file: its parity test compares it with exact attention
+(attn_oracle.c) of the dequantised inputs under a bound derived from E4M3's
+spacing, which any slack and multiplier in range satisfy.  This file serves
+the CPU pins of that bound (it shows the bound holds for several tunings and
+fails for planted mistakes) and is a step-by-step diagnostic:
 
 * E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits, subnormals, largest
   finite 448, no infinities.  Conversion from fp32 rounds to nearest, ties
@@ -123,7 +128,7 @@ def quantize_v_transposed(v):
 
 
 def attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=False, kv_len=None, H_kv=None,
-                  rows=None, window=None, block_mask=None):
+                  rows=None, window=None, block_mask=None, slack=SLACK, p_mult=P_MULT):
     """O [B,H,N,d] and LSE [B,H,N] of the FP8 forward, step by step.
 
     q8 [B,H,N,d] codes with sq [B,H,ceil(N/128)]; k8 [B,H_kv,N,d] with
@@ -133,7 +138,11 @@ def attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=False, kv_len=None, H_k
     the same visibility rule as the bf16 oracle; causal caps right at 0.
     block_mask: [nb, nb] (or None), zero where key block j is skipped for
     the rows of query block i // 128 (Block-Sparse FlashAttention, "炉案与百步
-    之外的仓库…" 第八部分): the recurrence passes over that block."""
+    之外的仓库…" 第八部分): the recurrence passes over that block.
+    slack, p_mult: the rescale slack (natural-log units) and the power-of-two
+    multiplier of the E4M3 P operand.  The pages fix neither; the defaults
+    are the readings above, and the tests also run other choices (0 and 256,
+    8 ln 2 and 1) to show that their parity bound does not depend on them."""
     wl, wr = (-1, -1) if window is None else (int(window[0]), int(window[1]))
     if causal:
         wr = 0
@@ -167,16 +176,16 @@ def attention_fp8(q8, sq, k8, sk, v8t, sv, scale, causal=False, kv_len=None, H_k
                     mb = s.max()
                     if m == -np.inf:
                         m = mb
-                    elif mb > m + SLACK:               # raise the reference to the new max
+                    elif mb > m + slack:               # raise the reference to the new max
                         alpha = np.exp(m - mb)
                         acc *= alpha
                         l *= alpha
                         m = mb
                     p = np.exp(s - m)
-                    p8 = e4m3_decode(e4m3_round((p * P_MULT).astype(np.float32)))
+                    p8 = e4m3_decode(e4m3_round((p * p_mult).astype(np.float32)))
                     l += p.sum()
                     acc += V[b, hk, :, lo:hi] @ p8
                 if l > 0:
-                    O[b, h, i] = float(sv[b, hk]) * acc / (P_MULT * l)
+                    O[b, h, i] = float(sv[b, hk]) * acc / (p_mult * l)
                     LSE[b, h, i] = m + np.log(l)
     return O, LSE

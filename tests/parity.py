@@ -150,3 +150,107 @@ def sample_rows(N, k=48, seed=0):
     rows = {0, 1, N - 1, N - 2, min(127, N - 1), min(128, N - 1), N // 2}
     rows |= set(int(r) for r in rng.integers(0, N, size=k))
     return np.array(sorted(r for r in rows if 0 <= r < N), dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) forward.  The reference is exact attention (the fp64 oracle) of
+# the DEQUANTISED inputs qd = q8*sq, kd = k8*sk, vd = v8*sv, which are the
+# values the E4M3 kernel multiplies.  What separates the kernel's O from it
+# is the rounding of P to E4M3 before the P.V product ("4. FlashAttention
+# 深度剖析" 4.5.4: E4M3 operands, fp32 accumulation), plus fp32 arithmetic.
+#
+# Bound.  Let w_j be the exact weights of a row and w_max their maximum.  A
+# kernel feeds x_j = c_b * w_j * l (its operand for key j: some multiplier
+# times the weight against its running normaliser l) to E4M3 and divides the
+# P.V sum by the same c*l it summed from the UNROUNDED p.  E4M3 rounds a
+# normal x (>= 2^-6) to within half a quantum, at most 2^-4 * x, and a
+# subnormal x to within min(x, 2^-10).  Provided (i) the row's largest
+# operand is at least 1 at the final reference (the kernel's reference never
+# exceeds the row maximum, and its multiplier is >= 1), (ii) the reference
+# never moves down, and (iii) no operand exceeds 448 (no saturation), the
+# error of weight j after normalisation is at most
+#     e_j = max(2^-4 w_j, min(w_j, 2^-10 w_max)),
+# so |O_gpu - O_exact| <= sum_j e_j |vd_j| elementwise, plus fp32 rounding of
+# the scores, the exponentials and the sums (FP8_FP32_REL of sum_j w_j |vd_j|)
+# and bf16's rounding of the stored O (2^-8 relative).  Nothing in it names
+# the kernel's slack or multiplier: any choice that satisfies (i)-(iii)
+# passes.  LSE = m + ln l adds unrounded p, so it must match the exact LSE
+# to LSE_ABS like the bf16 path.
+# ---------------------------------------------------------------------------
+FP8_P_REL = 2.0 ** -4          # half an E4M3 quantum, relative, normal values
+FP8_P_SUB = 2.0 ** -10         # half the E4M3 subnormal spacing 2^-9, absolute
+FP8_FP32_REL = 4e-3            # fp32 scores (|s| < ~200), exp2, sums over <= 32768 keys
+
+
+def dequantize(r, N):
+    """qd, kd, vd (float64 [B,H,N,d] / [B,H_kv,N,d]) from E4M3 codes and scales
+    as the oracle's quantisers write them (q8, q_scale, k8, k_scale, v8t,
+    v_scale)."""
+    from oracle import fp8_ref as F
+    qd = F.e4m3_decode(r["q8"]) * np.repeat(r["q_scale"], 128, axis=2)[:, :, :N, None]
+    kd = F.e4m3_decode(r["k8"]) * np.repeat(r["k_scale"], 128, axis=2)[:, :, :N, None]
+    vd = (F.e4m3_decode(r["v8t"][..., :N]).transpose(0, 1, 3, 2)
+          * r["v_scale"][:, :, None, None])
+    return qd, kd, vd
+
+
+def oracle_weights(q, k, scale, causal=False, kv_len=None, window=None, block_mask=None,
+                   rows=None):
+    """Exact attention weights P [len(rows) or N, N] of one head (q, k float64
+    [N, d]) as the oracle computes them: O = P V with V one-hot over a chunk
+    of d keys gives P's columns of that chunk, masks included."""
+    N, d = q.shape
+    rows_arr = np.arange(N) if rows is None else np.asarray(rows)
+    Pm = np.zeros((rows_arr.size, N))
+    for c0 in range(0, N, d):
+        n = min(d, N - c0)
+        onehot = np.zeros((N, d))
+        onehot[c0 + np.arange(n), np.arange(n)] = 1.0
+        if rows is None:
+            o, _ = oracle.attention_fwd(q[None, None], k[None, None], onehot[None, None], scale,
+                                        causal=causal, kv_len=kv_len, window=window,
+                                        block_mask=block_mask)
+            o = o[0, 0]
+        else:
+            assert block_mask is None
+            o, _ = oracle.attention_fwd_rows(q, k, onehot, rows_arr, scale, causal=causal,
+                                             kv_len=None if kv_len is None else kv_len[0],
+                                             window=window)
+        Pm[:, c0:c0 + n] = o[:, :n]
+    return Pm
+
+
+def fp8_o_bound(Pw, vd, o_ref):
+    """Elementwise bound on |O_fp8 - O_exact| for weights Pw [R, N], values vd
+    [N, d] and the exact O [R, d] (see the derivation above)."""
+    wmax = Pw.max(axis=1, keepdims=True)
+    e = np.maximum(FP8_P_REL * Pw, np.minimum(Pw, FP8_P_SUB * wmax))
+    av = np.abs(vd)
+    body = e @ av + FP8_FP32_REL * (Pw @ av)
+    return body * (1 + O_REL_ROUND) + O_REL_ROUND * np.abs(o_ref) + 1e-6
+
+
+def check_fp8_head(o_gpu, lse_gpu, qd, kd, vd, scale, causal=False, kv_len=None, window=None,
+                   block_mask=None, rows=None, what=""):
+    """One head: O and LSE of the E4M3 forward (rows of it, if given) against
+    exact attention of the dequantised inputs (qd, kd, vd [N, d])."""
+    if rows is None:
+        o_ref, lse_ref = oracle.attention_fwd(qd[None, None], kd[None, None], vd[None, None],
+                                              scale, causal=causal, kv_len=kv_len,
+                                              window=window, block_mask=block_mask)
+        o_ref, lse_ref = o_ref[0, 0], lse_ref[0, 0]
+    else:
+        o_ref, lse_ref = oracle.attention_fwd_rows(qd, kd, vd, rows, scale, causal=causal,
+                                                   kv_len=None if kv_len is None else kv_len[0],
+                                                   window=window)
+    Pw = oracle_weights(qd, kd, scale, causal=causal, kv_len=kv_len, window=window,
+                        block_mask=block_mask, rows=rows)
+    o_gpu = np.asarray(o_gpu, dtype=np.float64)
+    assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite output"
+    bound = fp8_o_bound(Pw, vd, o_ref)
+    err = np.abs(o_gpu - o_ref)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert np.all(err <= bound), \
+        f"{what}: |dO|={err[worst]:.3e} > E4M3 bound {bound[worst]:.3e} at {worst}"
+    check_lse(lse_gpu, lse_ref, what)
+    return float((err / bound).max())

@@ -89,12 +89,14 @@ def test_fp8_forward_block_mask_against_oracle(N, d, causal):
     q8, sq = F.quantize_rows(q.reshape(2, N, d))
     k8, sk = F.quantize_rows(k.reshape(2, N, d))
     v8t, sv = F.quantize_v_transposed(v.reshape(2, N, d))
-    o_ref, lse_ref = F.attention_fp8(q8.reshape(1, 2, N, d), sq.reshape(1, 2, -1),
-                                     k8.reshape(1, 2, N, d), sk.reshape(1, 2, -1),
-                                     v8t.reshape(1, 2, d, -1), sv.reshape(1, 2), w.scale,
-                                     causal=causal, block_mask=bm)
-    P.check_o(P.f64(o), o_ref, w.name + " O (fp8, block mask)")
-    P.check_lse(P.f64(lse), lse_ref, w.name + " LSE (fp8, block mask)")
+    r = {"q8": q8.reshape(1, 2, N, d), "q_scale": sq.reshape(1, 2, -1),
+         "k8": k8.reshape(1, 2, N, d), "k_scale": sk.reshape(1, 2, -1),
+         "v8t": v8t.reshape(1, 2, d, -1), "v_scale": sv.reshape(1, 2)}
+    qd, kd, vd = P.dequantize(r, N)
+    for h in range(2):
+        P.check_fp8_head(P.f64(o[0, h]), P.f64(lse[0, h]), qd[0, h], kd[0, h], vd[0, h],
+                         w.scale, causal=causal, block_mask=bm,
+                         what=f"{w.name} head {h} (fp8, block mask)")
 
 
 

@@ -2,17 +2,18 @@
 
 The quantiser (fa_fp8_quantize) must write the same bytes and scales as the
 oracle's quantisers (integer work: bit-exact).  The FP8 forward (fa_fwd_fp8)
-is compared with the oracle's step-by-step FP8 algorithm run on the oracle's
-own quantisation of the same bf16 inputs, with the O and LSE tolerances of
-parity.py (the two differ only where fp32 and fp64 round a product or an
-exponent differently, which can move a P onto the neighbouring E4M3 value).
-A last check bounds the FP8 result against exact attention, the method's own
-error, loosely."""
+is compared, element by element, with EXACT attention (the fp64 oracle) of
+the dequantised inputs q8*sq, k8*sk, v8*sv, under the bound of
+parity.fp8_o_bound: it follows from E4M3's spacing alone (2^-4 relative for
+a normal P operand, 2^-10 absolute below the normal range) and names none of
+the kernel's choices (rescale slack, P multiplier), so any kernel that keeps
+its P operands unsaturated and its reference rising must pass.  LSE adds
+unrounded P, so it must match the exact LSE to 1e-3 as in the bf16 path.
+"""
 import numpy as np
 import pytest
 import torch
 
-import oracle
 from oracle import fp8_ref as F
 from exact_attention_04_gb300 import build as fabuild
 from exact_attention_04_gb300 import fa
@@ -79,45 +80,52 @@ CASES = [
 ]
 
 
+def check_fp8(w, inp, o, lse, bh_list=None, rows=None, block_mask=None):
+    """Every listed head (all heads by default) of the E4M3 forward against
+    exact attention of the oracle-quantised, dequantised inputs."""
+    r = oracle_quantize(inp)
+    B, H, N, _ = inp["q"].shape
+    Hkv = inp["k"].shape[1]
+    qd, kd, vd = P.dequantize(r, N)
+    worst = 0.0
+    for b, h in (bh_list or [(b, h) for b in range(B) for h in range(H)]):
+        hk = h // (H // Hkv)
+        kv = None if inp["kv_len"] is None else [int(inp["kv_len"][b])]
+        og, lg = P.f64(o[b, h]), P.f64(lse[b, h])
+        if rows is not None:
+            og, lg = og[rows], lg[rows]
+        worst = max(worst, P.check_fp8_head(og, lg, qd[b, h], kd[b, hk], vd[b, hk], w.scale,
+                                            causal=w.causal, kv_len=kv, window=w.window,
+                                            block_mask=block_mask, rows=rows,
+                                            what=f"{w.name} head {b},{h} (fp8)"))
+    return worst
+
+
 @pytest.mark.parametrize("B,H,Hkv,N,d,causal,kv,window", CASES)
-def test_fp8_forward_against_oracle(B, H, Hkv, N, d, causal, kv, window):
+def test_fp8_forward_against_exact_attention(B, H, Hkv, N, d, causal, kv, window):
     w = random_case(B, H, N, d, seed=3 * N + d, causal=causal, kv_len_range=kv, h_kv=Hkv,
                     window=window)
     inp = make_inputs(w, with_grad_out=False)
     o, lse, _ = run(w, inp)
-    r = oracle_quantize(inp)
-    kvn = None if inp["kv_len"] is None else inp["kv_len"].numpy()
-    o_ref, lse_ref = F.attention_fp8(r["q8"], r["q_scale"], r["k8"], r["k_scale"], r["v8t"],
-                                     r["v_scale"], w.scale, causal=causal, kv_len=kvn,
-                                     window=window)
-    P.check_o(P.f64(o), o_ref, w.name + " O (fp8)")
-    P.check_lse(P.f64(lse), lse_ref, w.name + " LSE (fp8)")
+    check_fp8(w, inp, o, lse)
 
 
-def test_fp8_forward_near_exact_attention():
-    """FP8's own error against exact attention of the bf16 inputs: a loose
-    bound (E4M3 keeps 3 mantissa bits), checked on average and at worst."""
-    w = random_case(1, 4, 1024, 128, seed=21, causal=True)
+def test_fp8_forward_large_scores_against_exact_attention():
+    """Q and K scaled by 3, as in the large-head-dimension workload: scores of
+    standard deviation about 9 put most P operands below E4M3's normal range
+    and make the running maximum jump often (many O rescales)."""
+    w = random_case(1, 4, 1024, 128, seed=21, causal=True, qk_gain=3.0)
     inp = make_inputs(w, with_grad_out=False)
     o, lse, _ = run(w, inp)
-    o_ref, lse_ref = oracle.attention_fwd(P.f64(inp["q"]), P.f64(inp["k"]), P.f64(inp["v"]),
-                                          w.scale, causal=True)
-    err = np.abs(P.f64(o) - o_ref)
-    assert err.mean() <= 0.02 * np.abs(o_ref).max()
-    assert err.max() <= 0.15 * np.abs(o_ref).max()
-    assert np.abs(P.f64(lse) - lse_ref).max() <= 0.1
+    check_fp8(w, inp, o, lse)
 
 
 def test_fp8_long_sequence_sampled_rows():
     w = WORKLOADS["long_seq_b4_h32_n8192_d128_causal"]
     inp = make_inputs(w, with_grad_out=False)
     o, lse, _ = run(w, inp)
-    b, h = 3, 31
-    one = {k: (None if t is None else t[b:b + 1, h:h + 1].contiguous()) for k, t in inp.items()
-           if k in ("q", "k", "v")}
-    r = oracle_quantize(one)
-    rows = [0, 1, 127, 128, 4095, 4096, 6000, 8191]
-    o_ref, lse_ref = F.attention_fp8(r["q8"], r["q_scale"], r["k8"], r["k_scale"], r["v8t"],
-                                     r["v_scale"], w.scale, causal=True, rows=rows)
-    P.check_o(P.f64(o)[b:b + 1, h:h + 1, rows], o_ref[:, :, rows], w.name + " O (fp8)")
-    P.check_lse(P.f64(lse)[b:b + 1, h:h + 1, rows], lse_ref[:, :, rows], w.name + " LSE (fp8)")
+    rows = P.sample_rows(w.N, 40, seed=8)
+    for b, h in P.sample_heads(w.B, w.H, 4, seed=8):
+        sub = {n: inp[n][b:b + 1, h:h + 1].contiguous() for n in ("q", "k", "v")}
+        sub["kv_len"] = None
+        check_fp8(w, sub, o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], rows=rows)

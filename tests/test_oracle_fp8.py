@@ -169,3 +169,97 @@ def test_slack_keeps_16p_inside_e4m3(peak):
     w = np.exp(s - lse_ref[0, 0, rows][:, None])
     bound = 2.0 ** -4 * (w @ np.abs(vd[0, 0])) * (1 + 1e-9)
     assert np.all(np.abs(o[0, 0, rows] - o_ref[0, 0, rows]) <= bound)
+
+
+# ---------------------------------------------------------------------------
+# The parity bound of the E4M3 forward (tests/parity.py: fp8_o_bound).  The
+# GPU kernel is compared with exact attention of the dequantised inputs under
+# a bound that follows from E4M3's spacing alone.  Here, on the CPU, the
+# step-by-step FP8 algorithm of oracle/fp8_ref.py is run with several
+# choices of the rescale slack and the P multiplier that the pages leave
+# open: every choice must stay within the bound (so the bound does not
+# encode the kernel's tuning), the bound must not be vacuous, and planted
+# mistakes must break it.
+# ---------------------------------------------------------------------------
+import parity as PB
+
+TUNINGS = [(0.0, 256.0), (4 * np.log(2), 16.0), (8 * np.log(2), 1.0), (0.0, 1.0)]
+
+
+def _fp8_case(gain, seed=61, B=1, H=2, N=300, d=32):
+    rng = np.random.default_rng(seed)
+    q = (rng.standard_normal((B, H, N, d)) * gain).astype(np.float32)
+    k = (rng.standard_normal((B, H, N, d)) * gain).astype(np.float32)
+    v = rng.standard_normal((B, H, N, d)).astype(np.float32)
+    q8, sq = F.quantize_rows(q.reshape(B * H, N, d))
+    k8, sk = F.quantize_rows(k.reshape(B * H, N, d))
+    v8t, sv = F.quantize_v_transposed(v.reshape(B * H, N, d))
+    return {"q8": q8.reshape(B, H, N, d), "q_scale": sq.reshape(B, H, -1),
+            "k8": k8.reshape(B, H, N, d), "k_scale": sk.reshape(B, H, -1),
+            "v8t": v8t.reshape(B, H, d, -1), "v_scale": sv.reshape(B, H)}
+
+
+def _ratio_to_bound(r, causal, slack, mult, v_scale_factor=1.0, block_mask=None):
+    """max over elements of |O_fp8 - O_exact| / bound, for fp8_ref run with
+    the given tuning (and planted changes), against exact attention of the
+    dequantised inputs; also the share of visible keys whose weight sits
+    below 2^-10 of its row's maximum (the subnormal regime at multiplier 16)."""
+    N, d = r["q8"].shape[2], r["q8"].shape[3]
+    scale = 1 / np.sqrt(d)
+    qd, kd, vd = PB.dequantize(r, N)
+    o, lse = F.attention_fp8(r["q8"], r["q_scale"], r["k8"], r["k_scale"], r["v8t"],
+                             r["v_scale"] * v_scale_factor, scale, causal=causal, slack=slack,
+                             p_mult=mult, block_mask=block_mask)
+    worst, sub, vis = 0.0, 0, 0
+    for h in range(r["q8"].shape[1]):
+        Pw = PB.oracle_weights(qd[0, h], kd[0, h], scale, causal=causal)
+        o_ref, lse_ref = oracle.attention_fwd(qd[:, h:h + 1], kd[:, h:h + 1], vd[:, h:h + 1],
+                                              scale, causal=causal)
+        bound = PB.fp8_o_bound(Pw, vd[0, h], o_ref[0, 0])
+        worst = max(worst, float((np.abs(o[0, h] - o_ref[0, 0]) / bound).max()))
+        rel = Pw / Pw.max(axis=1, keepdims=True)
+        sub += int((rel[Pw > 0] < 2.0 ** -10).sum())
+        vis += int((Pw > 0).sum())
+        if block_mask is None:
+            np.testing.assert_allclose(lse[0, h], lse_ref[0, 0], rtol=0, atol=1e-10)
+    return worst, sub / vis
+
+
+@pytest.mark.parametrize("gain", [1.0, 3.0])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("slack,mult", TUNINGS)
+def test_fp8_bound_holds_for_any_tuning(gain, causal, slack, mult):
+    """Slack 0 / 2^4 / 2^8 (in e-units 0, 4 ln 2, 8 ln 2) and multipliers
+    256 / 16 / 1 all keep the largest P operand of a row in [1, 448] and the
+    reference rising, so each must satisfy the E4M3 bound.  gain 1 puts
+    nearly every weight in E4M3's normal range; gain 3 (scores of standard
+    deviation about 9) puts most of them in the subnormal range, so both
+    terms of the bound are exercised."""
+    worst, sub = _ratio_to_bound(_fp8_case(gain), causal, slack, mult)
+    assert worst <= 1.0, worst
+    if gain == 3.0:
+        assert sub > 0.5                 # mostly subnormal operands
+    else:
+        assert sub < 0.05                # mostly normal operands
+
+
+def test_fp8_bound_is_not_vacuous():
+    """The default tuning comes within a factor 2 of the bound somewhere in
+    each regime, so the bound is not so loose that it pins nothing."""
+    for gain in (1.0, 3.0):
+        worst, _ = _ratio_to_bound(_fp8_case(gain), True, F.SLACK, F.P_MULT)
+        assert worst >= 0.5, (gain, worst)
+
+
+@pytest.mark.parametrize("gain", [1.0, 3.0])
+def test_fp8_bound_catches_planted_mistakes(gain):
+    """Planted in the oracle, on the CPU: a V scale off by a quarter, a
+    dropped key block, and a multiplier (4096) that saturates E4M3.  Each
+    must exceed the bound somewhere."""
+    r = _fp8_case(gain)
+    T = 3
+    drop = np.ones((T, T), dtype=np.uint8)
+    drop[2, 1] = 0
+    assert _ratio_to_bound(r, True, F.SLACK, F.P_MULT, v_scale_factor=1.25)[0] > 1.0
+    assert _ratio_to_bound(r, False, F.SLACK, F.P_MULT, block_mask=drop)[0] > 1.0
+    assert _ratio_to_bound(r, True, 0.0, 4096.0)[0] > 1.0

@@ -326,3 +326,23 @@ def test_mask_plans_are_memoised_per_mask(mask_plan):
             mask_plan(bench_mask(seed=100 + s), 32, 1, 152, True, 8192)
         assert rows(mask_plan(a, 32, 1, 152, True, 8192)) == rows(pa)
         assert rows(mask_plan(b, 32, 1, 152, True, 8192)) == rows(pb)
+
+
+@pytest.mark.parametrize("B,H,N,d,fwd", [
+    (8, 32, 4096, 128, True), (4, 32, 8192, 128, True), (2, 32, 16384, 128, True),
+    (1, 32, 32768, 128, True), (2, 16, 8192, 128, True), (2, 16, 8192, 256, True),
+    (2, 16, 8192, 128, False), (2, 16, 8192, 256, False)])
+def test_last_head_of_the_large_workloads_runs_in_the_tail(plan, B, H, N, d, fwd):
+    """The GPU parity tests of the long-sequence and large-head workloads
+    compare every row of four heads, always including the last head
+    (B-1, H-1).  With 152 CTAs (one GB300) that head's items run in the
+    host-planned tail, with the arguments the launches pass, so the full-size
+    parity covers both the paired units and the tail."""
+    BH, T = B * H, N // 128
+    nsplit = 2 if (not fwd and d == 256) else 1
+    head_bytes = 2 * N * d * 2                     # K+V (forward) or Q+dO (backward)
+    G = min(BH * T * (1 if fwd else nsplit), 152)
+    t = plan(BH, T, nsplit, G, fwd, head_bytes)
+    assert t.heads >= 1
+    tail_heads = {e >> 12 for c in range(min(G, TAIL_CTAS)) for e in t.item[c] if e >= 0}
+    assert BH - 1 in tail_heads
