@@ -20,7 +20,8 @@ constexpr int KCH = 128 * 128;     // 128 rows x 128 bytes
 constexpr int QCH = 64 * 128;      // 64 rows x 128 bytes
 constexpr int kRowWarps = 8;       // two per sub-partition, one per 32-query half
 constexpr int kDrainWarp0 = 3 + kRowWarps;   // four dQ drain warps
-constexpr int kThreads = 32 * (kDrainWarp0 + 4);   // 15 warps
+constexpr int kReduceWarp = kDrainWarp0 + 4; // d = 256: issues the dQ bulk reduce-adds
+constexpr int kThreads = 32 * (kDrainWarp0 + 4);   // 15 warps (16 with the reduce warp)
 // With 15 warps one sub-partition holds four: 128 registers a thread at most
 // (the compiler is told 512 threads so that it plans for that).
 constexpr int kRegThreads = 512;
@@ -28,7 +29,7 @@ constexpr int kRegThreads = 512;
 enum Site {
   kSiteProdKV = 64, kSiteProdQ, kSiteMmaKV, kSiteMmaQ, kSiteMmaP, kSiteMmaDs, kSiteMmaDq,
   kSiteMmaAcc, kSiteRowS, kSiteRowDp, kSiteRowDsFree, kSiteRowAcc, kSiteDrainDq, kSiteDtDrain,
-  kSiteStageFree, kSiteStageFull, kSiteRowV, kSiteMmaV
+  kSiteStageFree, kSiteStageFull, kSiteRowV, kSiteMmaV, kSiteProdDo, kSiteMmaDo
 };
 
 __device__ __forceinline__ void record_failure(int* status, volatile int* abort, int site) {

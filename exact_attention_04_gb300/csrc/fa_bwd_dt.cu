@@ -12,11 +12,16 @@
 //   dQ^T_h = K[:, h]^T dS^T     (128 head-dim rows x 64 queries)
 // dQ^T sits in tensor memory with one lane per head-dimension column, and the
 // fp32 accumulator in global memory is kept transposed too ([BH, d, Npad]), so
-// each drain thread owns one contiguous run of 64 queries.  For d = 128 the
-// four drain warps write the tile with 16-byte stores into a swizzled shared
-// staging buffer and one thread adds it to the accumulator with two bulk
-// tensor reduce-adds (the L2 does the adds); for d = 256 (no room for the
-// tile) each thread adds its run with 16-byte atomics.
+// each drain thread owns one contiguous run of 64 queries.  The four drain
+// warps write the tile with 16-byte stores into a swizzled shared staging
+// buffer and one thread adds it to the accumulator with two bulk tensor
+// reduce-adds (the L2 does the adds).  For d = 128 the staging buffer is a
+// buffer of its own.  For d = 256 there is no room for one: the tile (32 KB)
+// goes into the step's dO buffer, which no product reads any more once the
+// step's dQ^T is complete, and a reduce warp issues the reduce-adds and then
+// hands the dO buffer back to the producer.  Q and dO then have barriers of
+// their own, so that Q buffers go back to the producer as soon as the
+// products have read them.
 // With d = 256 the two halves of a key block are separate work items; both
 // recompute S^T and dP^T (the price of fitting dK and dV in tensor memory).
 //
@@ -26,7 +31,8 @@
 //
 // Warps: 0 TMA producer; 1 issuer A (S^T, dP^T; owns tensor memory); 2
 // issuer B (dV, dK, dQ^T); 3..10 key-row warps, two per sub-partition, one
-// per 32-query half (P^T, dS^T, dK/dV epilogue); 11..14 dQ drain warps.  A
+// per 32-query half (P^T, dS^T, dK/dV epilogue); 11..14 dQ drain warps; 15
+// (d = 256) the reduce warp.  A
 // tcgen05.mma instruction holds its issuing warp for about 100 cycles here,
 // longer than the tensor core needs for these shapes, so the products of a
 // step are split over two issuer warps.  (A third issuer for dP^T measured
@@ -66,9 +72,12 @@ struct DtCfg {
   static constexpr bool V_TMEM = (D == 256);
   static constexpr int STAGES = D == 128 ? 3 : 2;
   static constexpr int NSB = D == 128 ? 2 : 1;       // S and dP buffers
-  // d = 128 has room for a 64 x 128 fp32 staging tile: dQ^T goes to global
-  // memory as bulk reduce-adds.  d = 256 uses atomics.
-  static constexpr bool DQ_TMA = (D == 128);
+  // dQ^T goes to global memory as bulk reduce-adds of a 64 x 128 fp32 tile
+  // staged in shared memory: a buffer of its own at d = 128, the step's dO
+  // buffer at d = 256 (STAGE_IN_DO; Q and dO then have separate barriers and
+  // a reduce warp returns the dO buffer once the reduce-adds have read it).
+  static constexpr bool STAGE_IN_DO = (D == 256);
+  static constexpr int THREADS = kThreads + (STAGE_IN_DO ? 32 : 0);
   // NSB S buffers of 64 columns from TM_S: S^T of a step, then P^T (bf16
   // pairs in columns [0,16) and [32,48), see pcol).  NSB dP buffers from
   // TM_DP: dP^T, then dS^T (bf16, same columns), then dQ^T.  d = 256: V
@@ -88,11 +97,14 @@ struct DtSmem {
   alignas(1024) uint8_t dO[DtCfg<D>::STAGES][DtCfg<D>::Q_BYTES];
   alignas(1024) uint8_t ds[2][KCH];              // dS^T bf16, 128 keys x 64 queries, double buffer
   alignas(DtCfg<D>::V_TMEM ? 16 : 1024) uint8_t v[DtCfg<D>::V_SMEM_BYTES];
-  alignas(DtCfg<D>::DQ_TMA ? 1024 : 16) float dq_stage[DtCfg<D>::DQ_TMA ? BQ * DH : 4];   // dQ^T tile, 2 x [d][32 queries]
+  alignas(DtCfg<D>::STAGE_IN_DO ? 16 : 1024) float dq_stage[DtCfg<D>::STAGE_IN_DO ? 4 : BQ * DH];   // dQ^T tile, 2 x [d][32 queries]
   alignas(16) float lse2[DtCfg<D>::STAGES][BQ];
   alignas(16) float delta[DtCfg<D>::STAGES][BQ];
   uint64_t kv_full, kv_empty;
   uint64_t q_full[DtCfg<D>::STAGES], q_empty[DtCfg<D>::STAGES];
+  // STAGE_IN_DO: dO loaded (do_full), dO buffer free again (do_empty, after the
+  // reduce-adds of the dQ^T tile staged in it have read it), tile staged (stg_full)
+  uint64_t do_full[DtCfg<D>::STAGES], do_empty[DtCfg<D>::STAGES], stg_full[DtCfg<D>::STAGES];
   // per tensor-memory buffer (g % NSB) or per shared dS buffer (g & 1)
   uint64_t s_full[2], p_full[2], dp_full[2], ds_full[2], ds_free[2];
   uint64_t dq_full[2], dq_free[2], acc_full, acc_free;
@@ -134,6 +146,9 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 2);         // both MMA issuers read the stage
+      mbar_init(&sm.do_full[s], 1);
+      mbar_init(&sm.do_empty[s], 1);        // the reduce warp
+      mbar_init(&sm.stg_full[s], 4);        // the drain warps
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.s_full[b], 1);
@@ -168,10 +183,15 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&p.tq);
-      prefetch_tmap(&p.tk);
-      prefetch_tmap(&p.tv);
+    // lane 0: K, V and the Q stages; with STAGE_IN_DO, lane 1 loads the dO
+    // stages on their own barriers (lane 0 loads both otherwise)
+    const bool dlane = C::STAGE_IN_DO && lane == 1;
+    if (lane == 0 || dlane) {
+      if (!dlane) {
+        prefetch_tmap(&p.tq);
+        prefetch_tmap(&p.tk);
+        prefetch_tmap(&p.tv);
+      }
       prefetch_tmap(&p.tdo);
       uint32_t w_it = 0, g = 0;
       bool ok = true;
@@ -184,38 +204,58 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
           const int nst = count_steps(sk, i0, i1);
           if (nst == 0) i1 = i0;
           if (i0 >= i1) continue;
-          if (!mbar_wait(&sm.kv_empty, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
-            record_failure(p.status, abort, kSiteProdKV);
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&sm.kv_full, (C::V_TMEM ? 1 : 2) * C::KV_BYTES);
+          if (!dlane) {
+            if (!mbar_wait(&sm.kv_empty, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteProdKV);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.kv_full, (C::V_TMEM ? 1 : 2) * C::KV_BYTES);
 #pragma unroll
-          for (int c = 0; c < C::NCH; ++c) {
-            tma_load_3d(sm.k + c * KCH, &p.tk, &sm.kv_full, 64 * c, n * BK, kvbh);
-            if constexpr (!C::V_TMEM)
-              tma_load_3d(sm.v + c * KCH, &p.tv, &sm.kv_full, 64 * c, n * BK, kvbh);
+            for (int c = 0; c < C::NCH; ++c) {
+              tma_load_3d(sm.k + c * KCH, &p.tk, &sm.kv_full, 64 * c, n * BK, kvbh);
+              if constexpr (!C::V_TMEM)
+                tma_load_3d(sm.v + c * KCH, &p.tv, &sm.kv_full, 64 * c, n * BK, kvbh);
+            }
+            ++w_it;
           }
-          ++w_it;
           StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv), sk);
           for (int s = 0; s < nst * G; ++s, wk.next()) {
             const int i = wk.i;
             const int bh = wk.bh;
             const int st = g % C::STAGES;
+            const size_t roff = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(i) * BQ;
+            if (dlane) {
+              // dO and D of the step, once the reduce-adds of the dQ^T tile
+              // staged in this buffer STAGES steps ago have read it
+              if (!mbar_wait(&sm.do_empty[st], ((g / C::STAGES) & 1) ^ 1, abort, kWaitTimeoutNs)) {
+                record_failure(p.status, abort, kSiteProdDo);
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&sm.do_full[st], C::Q_BYTES + BQ * 4);
+#pragma unroll
+              for (int c = 0; c < C::NCH; ++c)
+                tma_load_3d(sm.dO[st] + c * QCH, &p.tdo, &sm.do_full[st], 64 * c, i * BQ, bh);
+              bulk_load(sm.delta[st], p.delta + roff, BQ * 4, &sm.do_full[st]);
+              ++g;
+              continue;
+            }
             if (!mbar_wait(&sm.q_empty[st], ((g / C::STAGES) & 1) ^ 1, abort, kWaitTimeoutNs)) {
               record_failure(p.status, abort, kSiteProdQ);
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&sm.q_full[st], 2 * C::Q_BYTES + 2 * BQ * 4);
+            mbar_arrive_expect_tx(&sm.q_full[st], (C::STAGE_IN_DO ? 1 : 2) * (C::Q_BYTES + BQ * 4));
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c) {
               tma_load_3d(sm.q[st] + c * QCH, &p.tq, &sm.q_full[st], 64 * c, i * BQ, bh);
-              tma_load_3d(sm.dO[st] + c * QCH, &p.tdo, &sm.q_full[st], 64 * c, i * BQ, bh);
+              if constexpr (!C::STAGE_IN_DO)
+                tma_load_3d(sm.dO[st] + c * QCH, &p.tdo, &sm.q_full[st], 64 * c, i * BQ, bh);
             }
-            const size_t roff = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(i) * BQ;
             bulk_load(sm.lse2[st], p.lse2 + roff, BQ * 4, &sm.q_full[st]);
-            bulk_load(sm.delta[st], p.delta + roff, BQ * 4, &sm.q_full[st]);
+            if constexpr (!C::STAGE_IN_DO)
+              bulk_load(sm.delta[st], p.delta + roff, BQ * 4, &sm.q_full[st]);
             ++g;
           }
         }
@@ -226,7 +266,7 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
       for (int s = 0; s < C::STAGES; ++s) {
         if (g > static_cast<uint32_t>(s)) {
           const uint32_t nph = (g - 1 - s) / C::STAGES;
-          if (!mbar_wait(&sm.q_full[s], nph & 1, nullptr, kWaitTimeoutNs))
+          if (!mbar_wait(dlane ? &sm.do_full[s] : &sm.q_full[s], nph & 1, nullptr, kWaitTimeoutNs))
             record_failure(p.status, abort, kSiteDtDrain);
         }
       }
@@ -279,6 +319,7 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
               mma_bf16_ss_w(tmem + C::TM_S + 64 * b, dK0 + (((kk / 4) * KCH + (kk % 4) * 32) >> 4),
                             dq + (((kk / 4) * QCH + (kk % 4) * 32) >> 4), kIdS, kk > 0 ? 1u : 0u);
             mma_commit_w(&sm.s_full[b]);
+            if constexpr (C::STAGE_IN_DO) mma_commit_w(&sm.q_empty[st]);   // A's reads of Q(gg)
             return true;
           };
           // dP^T(gg) = V dO^T into dP buffer gg%NSB once the drain has read
@@ -290,6 +331,11 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
             const int st = gg % C::STAGES;
             if (gg >= C::NSB && !mbar_wait_warp(&sm.dq_free[b], ph ^ 1, abort, kWaitTimeoutNs)) {
               issuer_fail(p.status, abort, lane, kSiteMmaDq);
+              return false;
+            }
+            if (C::STAGE_IN_DO &&
+                !mbar_wait_warp(&sm.do_full[st], (gg / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+              issuer_fail(p.status, abort, lane, kSiteMmaDo);
               return false;
             }
             tc_fence_after_sync();
@@ -305,7 +351,8 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
                               bk, kIdS, kk > 0 ? 1u : 0u);
             }
             mma_commit_w(&sm.dp_full[b]);
-            mma_commit_w(&sm.q_empty[st]);          // A's reads of this stage are done
+            if constexpr (!C::STAGE_IN_DO)
+              mma_commit_w(&sm.q_empty[st]);        // A's reads of this stage are done
             return true;
           };
           // dP^T(g) goes ahead of S^T(g+1): the row warps need it first
@@ -366,6 +413,11 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
             }
             if (first && !mbar_wait_warp(&sm.acc_free, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
               fail(kSiteMmaAcc);
+              break;
+            }
+            if (C::STAGE_IN_DO &&
+                !mbar_wait_warp(&sm.do_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+              fail(kSiteMmaDo);
               break;
             }
             tc_fence_after_sync();
@@ -641,13 +693,14 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
         ++w_it;
       }
     }
-  } else {
+  } else if (warp < kDrainWarp0 + 4) {
     // ------------------------------------------------------------ dQ drain warps
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;            // head-dimension column within the half
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const bool issuer = (warp == kDrainWarp0 && lane == 0);  // issues the bulk reduce-adds
-    if (C::DQ_TMA && issuer) prefetch_tmap(&p.tdq);
+    // issues the bulk reduce-adds (d = 128; at d = 256 the reduce warp does)
+    const bool issuer = !C::STAGE_IN_DO && warp == kDrainWarp0 && lane == 0;
+    if (issuer) prefetch_tmap(&p.tdq);
     uint32_t g = 0;
     bool ok = true;
     DtIter it{static_cast<int>(blockIdx.x), 0, 0};
@@ -680,7 +733,22 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.dq_free[tb]);
-          if constexpr (C::DQ_TMA) {
+          if constexpr (C::STAGE_IN_DO) {
+            // staging in the step's dO buffer (no product reads it once dQ^T
+            // is complete): the same two swizzled boxes, 16 KB apart
+            const int st = g % C::STAGES;
+            uint4* row0 = reinterpret_cast<uint4*>(sm.dO[st]) + r * 8;
+            uint4* row1 = row0 + DH * 8;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              row0[j ^ (r & 7)] = make_uint4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              row1[j ^ (r & 7)] = make_uint4(v1[4 * j], v1[4 * j + 1], v1[4 * j + 2], v1[4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.stg_full[st]);
+          } else {
             // staging: two boxes of [128 columns][32 queries] fp32 in the
             // 128-byte swizzle of the tensor map; this thread owns row r of
             // each and writes it as eight 16-byte chunks, chunk j at j ^ (r & 7)
@@ -716,25 +784,48 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-          } else {
-            // row h*DH + r of the transposed accumulator, queries q0 .. q0+63
-            // (q0 + 64 <= Npad: the tail lands in the padding)
-            float4* acc = reinterpret_cast<float4*>(
-                p.dq_acc + (static_cast<size_t>(bh) * D + h * DH + r) * p.Npad + q0);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              atomicAdd(acc + j, make_float4(__uint_as_float(v0[4 * j]), __uint_as_float(v0[4 * j + 1]),
-                                             __uint_as_float(v0[4 * j + 2]), __uint_as_float(v0[4 * j + 3])));
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              atomicAdd(acc + 8 + j, make_float4(__uint_as_float(v1[4 * j]), __uint_as_float(v1[4 * j + 1]),
-                                                 __uint_as_float(v1[4 * j + 2]), __uint_as_float(v1[4 * j + 3])));
           }
         }
       }
     }
     // every reduce-add must have landed before the CTA exits
-    if (C::DQ_TMA && issuer) bulk_wait_group<0>();
+    if (issuer) bulk_wait_group<0>();
+  } else {
+    // ------------------------------------------------------------ reduce warp (d = 256)
+    // Adds each step's staged dQ^T tile to the accumulator with two bulk
+    // tensor reduce-adds, then returns the dO buffer it was staged in.
+    if (C::STAGE_IN_DO && lane == 0) {
+      prefetch_tmap(&p.tdq);
+      uint32_t g = 0;
+      bool ok = true;
+      DtIter it{static_cast<int>(blockIdx.x), 0, 0};
+      for (int kvbh, h, n; ok && sched.next(tail, it, kvbh, h, n);) {
+        int i0, i1;
+        dt_range(p, n, dt_len(p, kvbh), i0, i1);
+        const StepMask sk{BS ? p.block_mask + n : nullptr, p.bm_t, BK / BQ};
+        const int nst = count_steps(sk, i0, i1);
+        if (nst == 0) i1 = i0;
+        StepWalk wk(i0, i1, q_head_of(kvbh, 0, p.H, p.H_kv), sk);
+        for (int s = 0; s < nst * G; ++s, ++g, wk.next()) {
+          const int st = g % C::STAGES;
+          if (!mbar_wait(&sm.stg_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
+            record_failure(p.status, abort, kSiteStageFull);
+            ok = false;
+            break;
+          }
+          // queries past N land in the padding up to Npad, never read
+          const float* box = reinterpret_cast<const float*>(sm.dO[st]);
+          tma_reduce_add_3d(&p.tdq, box, wk.i * BQ, h * DH, wk.bh);
+          tma_reduce_add_3d(&p.tdq, box + 32 * DH, wk.i * BQ + 32, h * DH, wk.bh);
+          bulk_commit_group();
+          bulk_wait_group_read<0>();
+          mbar_arrive(&sm.do_empty[st]);
+        }
+      }
+      // every reduce-add must have landed before the CTA exits
+      bulk_wait_group<0>();
+    }
+    __syncwarp();
   }
 
   tc_fence_before_sync();
@@ -772,7 +863,7 @@ cudaError_t launch(const BwdParams& p, int num_sms, int max_smem, cudaStream_t s
   }
   if (tail.heads == 0) std::memset(tail.item, 0xff, sizeof(tail.item));
   const int grid = static_cast<int>(units < num_sms ? units : num_sms);
-  bwd_dt_kernel<D, BS><<<grid, kThreads, smem, stream>>>(p, tail);
+  bwd_dt_kernel<D, BS><<<grid, DtCfg<D>::THREADS, smem, stream>>>(p, tail);
   return cudaGetLastError();
 }
 
