@@ -5,7 +5,12 @@ tolerances.
 Tolerances (GPU bf16/fp32 outputs vs the fp64 oracle):
 * O:   |dO_ij| <= 1e-2 + 2^-8 |O_ref,ij| for every element (the 2^-8 term is
        the largest relative error of rounding a value to bf16), and
-       max|dO| <= 2e-2 max|O_ref|.
+       max|dO| <= 2e-2 max|O_ref|.  The kernels round P to bf16 before the
+       P V product ("4. FlashAttention 深度剖析" 4.7.3 casts p to V's type),
+       which moves each weight by up to 2^-8 of itself while the row sum
+       adds the unrounded p; so an element may also move by
+       2^-8 sum_k P_ik |V_kj|.  Where the first bound fails, that term is
+       computed from the oracle (attention of |V|) and added.
 * LSE: max|dLSE| <= 1e-3.
 * dQ, dK, dV: max|d| <= 2e-2 max|ref| + 1e-5 per tensor (the 1e-5 floor only
   matters when the exact gradient is identically zero, e.g. a single visible
@@ -36,11 +41,19 @@ def to_gpu(inputs):
     return out
 
 
-def check_o(o_gpu, o_ref, what=""):
+P_REL_ROUND = 2.0 ** -8
+
+
+def check_o(o_gpu, o_ref, what="", abs_v_attention=None):
+    """abs_v_attention: None, or a callable returning sum_k P_ik |V_kj| (exact
+    attention of |V|, the oracle's) shaped like o_ref; it is called only when
+    the bound without the P-rounding term fails somewhere."""
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
     err = np.abs(o_gpu - o_ref)
     assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite output"
     bound = O_ABS + O_REL_ROUND * np.abs(o_ref)
+    if abs_v_attention is not None and not np.all(err <= bound):
+        bound = bound + P_REL_ROUND * np.asarray(abs_v_attention(), dtype=np.float64)
     worst = np.unravel_index(np.argmax(err - bound), err.shape)
     assert np.all(err <= bound), f"{what}: |dO|={err[worst]:.3e} > {bound[worst]:.3e} at {worst}"
     assert err.max() <= O_REL_MAX * np.abs(o_ref).max(), f"{what}: max|dO|={err.max():.3e}"
@@ -93,15 +106,20 @@ def kv_of(inp, b):
 def compare_forward_full(w, inp, o, lse, bh_list=None):
     """Whole-tensor (or per listed head) forward comparison."""
     if bh_list is None:
-        o_ref, lse_ref = oracle.attention_fwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), w.scale,
-                                              causal=w.causal, kv_len=inp["kv_len"])
-        return check_o(f64(o), o_ref, w.name), check_lse(f64(lse), lse_ref, w.name)
+        q, k, v = f64(inp["q"]), f64(inp["k"]), f64(inp["v"])
+        o_ref, lse_ref = oracle.attention_fwd(q, k, v, w.scale, causal=w.causal,
+                                              kv_len=inp["kv_len"])
+        av = lambda: oracle.attention_fwd(q, k, np.abs(v), w.scale, causal=w.causal,  # noqa: E731
+                                          kv_len=inp["kv_len"])[0]
+        return check_o(f64(o), o_ref, w.name, av), check_lse(f64(lse), lse_ref, w.name)
     eo = el = 0.0
     for b, h in bh_list:
         x = heads(inp, b, h)
         o_ref, lse_ref = oracle.attention_fwd(x["q"], x["k"], x["v"], w.scale, causal=w.causal,
                                               kv_len=kv_of(inp, b))
-        eo = max(eo, check_o(f64(o[b:b + 1, h:h + 1]), o_ref, f"{w.name} head {b},{h}"))
+        av = lambda x=x, b=b: oracle.attention_fwd(x["q"], x["k"], np.abs(x["v"]), w.scale,  # noqa: E731
+                                                   causal=w.causal, kv_len=kv_of(inp, b))[0]
+        eo = max(eo, check_o(f64(o[b:b + 1, h:h + 1]), o_ref, f"{w.name} head {b},{h}", av))
         el = max(el, check_lse(f64(lse[b:b + 1, h:h + 1]), lse_ref, f"{w.name} head {b},{h}"))
     return eo, el
 
@@ -113,7 +131,9 @@ def compare_forward_rows(w, inp, o, lse, bh_list, rows):
         q, k, v = (f64(inp[n][b, h]) for n in ("q", "k", "v"))
         kv = None if inp["kv_len"] is None else int(inp["kv_len"][b])
         o_ref, lse_ref = oracle.attention_fwd_rows(q, k, v, rows, w.scale, causal=w.causal, kv_len=kv)
-        eo = max(eo, check_o(f64(o[b, h, rows]), o_ref, f"{w.name} head {b},{h}"))
+        av = lambda q=q, k=k, v=v, kv=kv: oracle.attention_fwd_rows(  # noqa: E731
+            q, k, np.abs(v), rows, w.scale, causal=w.causal, kv_len=kv)[0]
+        eo = max(eo, check_o(f64(o[b, h, rows]), o_ref, f"{w.name} head {b},{h}", av))
         el = max(el, check_lse(f64(lse[b, h, rows]), lse_ref, f"{w.name} head {b},{h}"))
     return eo, el
 
