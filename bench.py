@@ -43,7 +43,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 _COMMON_SOURCES = ["fa_api.cu", "fa_internal.h", "fa_window.cuh", "sm103_ptx.cuh"]
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["fa_fwd.cu"] + _COMMON_SOURCES,
-    "bwd_main_kernel": ["fa_bwd.cu"] + _COMMON_SOURCES,
+    "bwd_d64_kernel": ["fa_bwd_d64.cu", "fa_bwd_common.cuh"] + _COMMON_SOURCES,
     "bwd_dt_kernel": ["fa_bwd_dt.cu", "fa_bwd_common.cuh"] + _COMMON_SOURCES,
 }
 
@@ -51,7 +51,7 @@ KERNEL_SOURCES = {
 def bwd_kernel_names(d):
     """Device names of the backward's main and dQ-conversion kernels: d = 64
     runs the query-row kernel, d = 128 and 256 the transposed-dQ one."""
-    return ("bwd_main_kernel", "bwd_post_kernel") if d == 64 else ("bwd_dt_kernel",
+    return ("bwd_d64_kernel", "bwd_post_kernel") if d == 64 else ("bwd_dt_kernel",
                                                                     "bwd_post_t_kernel")
 
 
@@ -563,6 +563,14 @@ def visible_pairs(L, N, causal):
     return L * (L + 1) // 2 + (N - L) * L if causal else N * L
 
 
+def roofline_frac(flops, nbytes, ms, peaks):
+    """Achieved FLOP/s over the roofline min(pi, AI * beta): pi the measured
+    dense bf16 peak, beta the measured HBM bandwidth, AI = algorithmic FLOPs
+    per algorithmic byte."""
+    roof = min(peaks["bf16_tflops"] * 1e12, flops / nbytes * peaks["hbm_gbs"] * 1e9)
+    return round(flops / (ms * 1e-3) / roof, 4)
+
+
 def run_sweep(fa, peaks, only=None):
     """Every other workload, timed briefly: TFLOP/s, fraction of peak, GB/s of
     algorithmic traffic (inputs read + outputs written once).  only: keep the
@@ -606,6 +614,7 @@ def run_sweep(fa, peaks, only=None):
                  "fwd_frac_of_peak": round(w.fwd_flops() / (fwd_ms * 1e-3) / 1e12
                                            / peaks["bf16_tflops"], 4),
                  "fwd_gbs": round(fwd_bytes / (fwd_ms * 1e-3) / 1e9, 1),
+                 "fwd_frac_of_roofline": roofline_frac(w.fwd_flops(), fwd_bytes, fwd_ms, peaks),
                  "timing": "median of 20 steps, L2 flushed before each"}
         if r.backward:
             bwd_ms = sum(v for k, v in per_phase.items() if k != "fa_fwd_kernel")
@@ -614,7 +623,9 @@ def run_sweep(fa, peaks, only=None):
                           "bwd_tflops": round(w.bwd_flops() / (bwd_ms * 1e-3) / 1e12, 2),
                           "bwd_frac_of_peak": round(w.bwd_flops() / (bwd_ms * 1e-3) / 1e12
                                                     / peaks["bf16_tflops"], 4),
-                          "bwd_gbs": round(bwd_bytes / (bwd_ms * 1e-3) / 1e9, 1)})
+                          "bwd_gbs": round(bwd_bytes / (bwd_ms * 1e-3) / 1e9, 1),
+                          "bwd_frac_of_roofline": roofline_frac(w.bwd_flops(), bwd_bytes, bwd_ms,
+                                                                peaks)})
         if w.backward and not r.backward:
             entry["bwd"] = "not built for this head dimension"
         if inp["kv_len"] is not None and w.window is None:

@@ -142,6 +142,23 @@ bool make_acc_map(CUtensorMap* m, void* base, int d, int npad, int BH) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 accumulator [BH, Npad, d] (d = 64) as a 3-D tensor (d, Npad, BH): box
+// of 32 columns (128 bytes) x 128 rows, 128-byte swizzle (the target of bulk
+// reduce-adds).
+bool make_acc_rows_map(CUtensorMap* m, void* base, int d, int npad, int BH) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(npad),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(npad) * d * 4};
+  const cuuint32_t box[3] = {32, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t round_up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // The variant as the kernels see it: K/V heads, and the window folded with
@@ -517,8 +534,8 @@ fa_status_t bwd_prep_impl(const fa::BwdParams& p, int d, void* stream) {
 fa_status_t bwd_main_impl(fa::BwdParams& p, const DeviceInfo* di, const void* q, const void* k,
                           const void* v, const void* dO, int d, void* stream) {
   const int BH = p.B * p.H;
-  // d = 64: 128-query steps with dQ in query rows; d = 128, 256: 64-query
-  // steps with dQ^T in head-dimension rows (fa_bwd_dt.cu).
+  // d = 64: 128-query steps with dQ in query rows (fa_bwd_d64.cu); d = 128,
+  // 256: 64-query steps with dQ^T in head-dimension rows (fa_bwd_dt.cu).
   const bool dt = d != 64;
   const int qrows = dt ? 64 : 128;
   const int BHkv = p.B * p.H_kv;
@@ -526,10 +543,11 @@ fa_status_t bwd_main_impl(fa::BwdParams& p, const DeviceInfo* di, const void* q,
       !make_map(&p.tv, v, d, p.N, BHkv) || !make_map(&p.tdo, dO, d, p.N, BH, qrows))
     return FA_ERR_CUDA;
   if (dt && !make_acc_map(&p.tdq, p.dq_acc, d, p.Npad, BH)) return FA_ERR_CUDA;
+  if (!dt && !make_acc_rows_map(&p.tdq, p.dq_acc, d, p.Npad, BH)) return FA_ERR_CUDA;
   p.v = v;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = dt ? fa::launch_bwd_main_dt(p, d, di->num_sms, di->max_smem, s)
-                           : fa::launch_bwd_main(p, d, di->num_sms, di->max_smem, s);
+                           : fa::launch_bwd_main_d64(p, di->num_sms, di->max_smem, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

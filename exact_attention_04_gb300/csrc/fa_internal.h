@@ -51,7 +51,8 @@ struct FwdParams {
 
 struct BwdParams {
   CUtensorMap tq, tk, tv, tdo; // bf16 [BH, N, d] as above
-  CUtensorMap tdq;             // fp32 dQ^T accumulator [BH, d, Npad], box (32, 128, 1), SW128
+  CUtensorMap tdq;             // fp32 dQ accumulator: d = 128, 256 transposed [BH, d, Npad],
+                               // d = 64 [BH, Npad, d]; box (32, 128, 1), SW128
   const void* o;               // bf16 [B, H, N, d]
   const void* dO;              // bf16 [B, H, N, d]
   const void* v;               // bf16 [B, H, N, d] (d = 256 reads V rows directly)
@@ -144,8 +145,6 @@ fa_status_t bwd_check_args(const void* q, const void* k, const void* v, const vo
 
 cudaError_t launch_fwd(const FwdParams& p, int d, int num_sms, int max_smem, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const BwdParams& p, int d, cudaStream_t stream);
-cudaError_t launch_bwd_main(const BwdParams& p, int d, int num_sms, int max_smem,
-                            cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdParams& p, int d, cudaStream_t stream);
 // 64-query-step backward main kernel with dQ^T (head dimensions 128, 256);
 // its Q and dO tensor maps have a box of 64 rows.
@@ -172,5 +171,10 @@ cudaError_t launch_decode_combine(const FwdParams& p, int d, void* o, float* lse
                                   cudaStream_t stream);
 cudaError_t launch_bwd_main_dt(const BwdParams& p, int d, int num_sms, int max_smem,
                                cudaStream_t stream);
+// Backward main kernel for head dimension 64 (fa_bwd_d64.cu): 128-query
+// steps, dQ staged and added by bulk tensor reduce-adds through tdq, a map of
+// the [BH, Npad, 64] accumulator with a box of 32 columns x 128 rows.
+cudaError_t launch_bwd_main_d64(const BwdParams& p, int num_sms, int max_smem,
+                                cudaStream_t stream);
 
 }  // namespace fa
