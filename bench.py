@@ -487,7 +487,8 @@ class BlockSparseRunner:
     """Forward (fa_fwd_v) and backward (fa_bwd_v) of block-sparse attention:
     the local + global + random block pattern of block_sparse_mask.  balanced:
     pass the mask with its host copy (fa.BlockMask), so the launches plan a
-    balanced schedule; else the device mask alone (round-robin)."""
+    balanced tail on the host; else the device mask alone, whose tiles and key
+    blocks the kernels sort by cost on the device (the cost-sorted deal)."""
 
     def __init__(self, fa, balanced=True):
         c = BLOCK_SPARSE
@@ -534,7 +535,7 @@ def sweep_blocksparse(fa, peaks, flush_buf):
         torch.cuda.synchronize()
         timed.append(time_steps(r, 20, flush=lambda: flush_l2(flush_buf), median=True)[0])
         fa.fa_check()
-    per_phase, rr = timed
+    per_phase, dev = timed
     c = BLOCK_SPARSE
     fwd_flops = 4.0 * c["B"] * c["H"] * c["d"] * r.computed_pairs()
     dense = 4.0 * c["B"] * c["H"] * c["d"] * c["N"] * c["N"]
@@ -550,8 +551,9 @@ def sweep_blocksparse(fa, peaks, flush_buf):
             "bwd_frac_of_peak": round(2.5 * fwd_flops / (bwd_ms * 1e-3) / 1e12
                                       / peaks["bf16_tflops"], 4),
             "dense_equivalent_tflops": round(dense / (fwd_ms * 1e-3) / 1e12, 2),
-            "round_robin": {"fwd_ms": round(rr["fwd"], 4), "bwd_ms": round(rr["bwd"], 4),
-                            "note": "the device mask alone: no host copy, no balanced tail"},
+            "device_planned": {"fwd_ms": round(dev["fwd"], 4), "bwd_ms": round(dev["bwd"], 4),
+                               "note": "the device mask alone (no host copy): the cost-sorted "
+                                       "deal planned on the device"},
             "flops": "computed (query, key) pairs only: 4 d per pair forward, 2.5x backward",
             "timing": "median of 20 steps, L2 flushed before each"}
 

@@ -430,6 +430,8 @@ fa_status_t fa_fwd_v(const void* q, const void* k, const void* v, void* o, float
   p.block_mask = var.bm;
   p.bm_t = (N + 127) / 128;
   p.block_mask_host = var.bmh;
+  // a block mask without a host copy: each CTA sorts the tiles by cost
+  p.cost_sorted = (var.bm && !var.bmh && !p.causal && p.bm_t <= fa::kFwdOrderMaxT) ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.status = di->status;
   if (fa::launch_fwd(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -438,14 +440,17 @@ fa_status_t fa_fwd_v(const void* q, const void* k, const void* v, void* o, float
 }
 
 // Workspace layout: D [B*H, Npad] fp32, L2 [B*H, Npad] fp32, dQ_acc of
-// B*H*Npad*d fp32 ([B*H, Npad, d] for d = 64, [B*H, d, Npad] otherwise), each
-// region starting on a 256-byte boundary (Npad = N rounded up to 128).
+// B*H*Npad*d fp32 ([B*H, Npad, d] for d = 64, [B*H, d, Npad] otherwise), and
+// the cost-sorted order of the key blocks (Npad / 128 uint32, used with a
+// block mask that has no host copy), each region starting on a 256-byte
+// boundary (Npad = N rounded up to 128).
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (check_sizes(B, H, N, d, 1.f) != FA_OK) return 0;
   const size_t npad = (static_cast<size_t>(N) + 127) / 128 * 128;
   const size_t padded_rows = static_cast<size_t>(B) * H * npad;
   return 2 * round_up256(padded_rows * sizeof(float)) +
-         round_up256(padded_rows * d * sizeof(float));
+         round_up256(padded_rows * d * sizeof(float)) +
+         round_up256(npad / 128 * sizeof(uint32_t));
 }
 
 }  // extern "C"
@@ -475,6 +480,7 @@ fa_status_t bwd_setup(fa::BwdParams* p, DeviceInfo** di, int B, int H, int N, in
   p->delta = static_cast<float*>(workspace);
   p->lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + stat_bytes);
   p->dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * stat_bytes);
+  const size_t acc_bytes = round_up256(static_cast<size_t>(BH) * npad * d * sizeof(float));
   p->Npad = npad;
   p->kv_len = kv_len;
   p->B = B;
@@ -487,6 +493,11 @@ fa_status_t bwd_setup(fa::BwdParams* p, DeviceInfo** di, int B, int H, int N, in
   p->block_mask = var.bm;
   p->bm_t = (N + 127) / 128;
   p->block_mask_host = var.bmh;
+  // a block mask without a host copy: the key blocks' cost-sorted order,
+  // planned on the device into the workspace's last region
+  if (var.bm && !var.bmh && !p->causal && p->bm_t <= fa::kOrderMaxT)
+    p->cost_order = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + 2 * stat_bytes +
+                                                acc_bytes);
   p->scale = scale;
   p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p->status = (*di)->status;
@@ -546,6 +557,7 @@ fa_status_t bwd_main_impl(fa::BwdParams& p, const DeviceInfo* di, const void* q,
   if (!dt && !make_acc_rows_map(&p.tdq, p.dq_acc, d, p.Npad, BH)) return FA_ERR_CUDA;
   p.v = v;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.cost_order && fa::launch_bwd_order(p, s) != cudaSuccess) return FA_ERR_CUDA;
   const cudaError_t e = dt ? fa::launch_bwd_main_dt(p, d, di->num_sms, di->max_smem, s)
                            : fa::launch_bwd_main_d64(p, di->num_sms, di->max_smem, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -816,6 +828,7 @@ fa_status_t fa_fwd_fp8(const void* q8, const float* q_scale, const void* k8,
   p.block_mask = var.bm;
   p.bm_t = nb;
   p.block_mask_host = var.bmh;
+  p.cost_sorted = (var.bm && !var.bmh && !p.causal && nb <= fa::kFwdOrderMaxT) ? 1 : 0;
   return fa::launch_fwd_fp8(p, d, di->num_sms, di->max_smem, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? FA_OK

@@ -1,12 +1,15 @@
-// Attention backward for sm_103a: three launches on one stream.  This file
-// holds the first and the last; the main kernel lives in fa_bwd_d64.cu
-// (head dimension 64) and fa_bwd_dt.cu (128 and 256).
+// Attention backward for sm_103a: three launches on one stream (four with a
+// block mask that has no host copy).  This file holds all but the main
+// kernel, which lives in fa_bwd_d64.cu (head dimension 64) and fa_bwd_dt.cu
+// (128 and 256).
 //
 //  1. bwd_pre   D_i = sum_t dO_it * O_it and L2_i = LSE_i * log2(e) per query
 //               row (padded to a multiple of 128 rows: D = 0, L2 = +inf past
 //               N), and zero the fp32 dQ accumulator.  Memory bound.
 //  2. bwd_main  recomputes P from Q, K and L2 per 128-key block, writes dK and
 //               dV, and adds dS K into the fp32 dQ accumulator.
+//     bwd_order (a block mask without a host copy, before bwd_main) sorts
+//               the key blocks by cost for bwd_main's schedule.
 //  3. bwd_post  dQ = bf16(scale * dQ_acc) (d = 64: [BH, Npad, d] accumulator;
 //               d = 128, 256: transposed [BH, d, Npad]).
 //
@@ -21,6 +24,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_internal.h"
+#include "fa_order.cuh"
 #include "fa_window.cuh"
 #include "sm103_ptx.cuh"
 
@@ -133,6 +137,32 @@ cudaError_t launch_prep(const BwdParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// The key blocks' cost-sorted order (fa_order.cuh) for a block mask without
+// a host copy: key block n costs the computed query blocks of its mask
+// column among the queries its keys are visible to (the window; kv_len,
+// which differs by batch entry, is left out).  One CTA, a key block a
+// thread; the mask's column reads are coalesced across the threads.
+__global__ void __launch_bounds__(kOrderMaxT) bwd_order_kernel(const __grid_constant__ BwdParams p) {
+  __shared__ uint32_t cost[kOrderMaxT];
+  const int T = p.bm_t;
+  const int n = threadIdx.x;
+  if (n < T) {
+    int q_lo, q_hi;
+    visible_queries(n * 128, 128, p.N, p.N, p.wl, p.wr, q_lo, q_hi);
+    uint32_t c = 0;
+    if (q_hi > q_lo)
+      for (int a = q_lo / 128; a < (q_hi + 127) / 128; ++a)
+        c += __ldg(p.block_mask + static_cast<size_t>(a) * p.bm_t + n) != 0;
+    cost[n] = c;
+  }
+  __syncthreads();
+  if (n < T) {
+    uint32_t e;
+    const int pos = order_rank(cost, T, n, e);
+    p.cost_order[pos] = e;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_prep(const BwdParams& p, int d, cudaStream_t stream) {
@@ -142,6 +172,14 @@ cudaError_t launch_bwd_prep(const BwdParams& p, int d, cudaStream_t stream) {
     case 256: return launch_prep<256>(p, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_bwd_order(const BwdParams& p, cudaStream_t stream) {
+  if (!p.cost_order || !p.block_mask || p.bm_t < 1 || p.bm_t > kOrderMaxT)
+    return cudaErrorInvalidValue;
+  const int threads = (p.bm_t + 31) / 32 * 32;
+  bwd_order_kernel<<<1, threads, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_post(const BwdParams& p, int d, cudaStream_t stream) {

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_internal.h"
+#include "fa_order.cuh"
 #include "fa_window.cuh"
 #include "sm103_ptx.cuh"
 
@@ -66,10 +67,16 @@ struct DtIter {
   int u, kt, k;
 };
 
+// A block mask without a host copy (order != nullptr): the items (K/V head,
+// key block; the halves of d adjacent) go in the cost-sorted turning deal of
+// fa_order.cuh instead, from the order planned into the workspace.
 struct DtSched {
   int T, P, per_bh, units, causal, nsplit;   // units: the round-robin units
-  __device__ DtSched(int BH, int N, int causal_, int nsplit_, int tail_heads)
-      : causal(causal_), nsplit(nsplit_) {
+  int BH;
+  const uint32_t* order;                     // the cost-sorted order, or nullptr
+  __device__ DtSched(int BH_, int N, int causal_, int nsplit_, int tail_heads,
+                     const uint32_t* order_)
+      : causal(causal_), nsplit(nsplit_), BH(BH_), order(order_) {
     T = (N + BK - 1) / BK;
     P = (T + 1) / 2;
     per_bh = causal ? P : T;
@@ -92,6 +99,14 @@ struct DtSched {
   // The next work item of this CTA (K/V head, half of d, key block); false
   // when it has none left.  Every role walks the same sequence.
   __device__ bool next(const TailTable& tail, DtIter& it, int& kvbh, int& h, int& n) const {
+    if (order) {   // round it.k of the cost-sorted deal
+      const long long k = order_deal(it.k, gridDim.x, blockIdx.x);
+      if (k >= static_cast<long long>(BH) * T * nsplit) return false;
+      ++it.k;
+      h = static_cast<int>(k % nsplit);
+      order_item(order, BH, k / nsplit, kvbh, n);
+      return true;
+    }
     while (it.u < units) {
       int pp;
       decode(it.u, kvbh, pp, h);

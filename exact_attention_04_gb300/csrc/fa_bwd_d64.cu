@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kSThreads, 1) bwd_d64_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-  const DtSched sched(p.B * p.H_kv, p.N, p.causal, 1, tail.heads);
+  const DtSched sched(p.B * p.H_kv, p.N, p.causal, 1, tail.heads, BS ? p.cost_order : nullptr);
   const int G = p.H / p.H_kv;                     // query heads per K/V head
 
   if (warp == 0) {

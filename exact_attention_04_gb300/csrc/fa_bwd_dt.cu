@@ -178,7 +178,8 @@ __global__ void __launch_bounds__(kRegThreads, 1) bwd_dt_kernel(const __grid_con
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-  const DtSched sched(p.B * p.H_kv, p.N, p.causal, C::NSPLIT, tail.heads);
+  const DtSched sched(p.B * p.H_kv, p.N, p.causal, C::NSPLIT, tail.heads,
+                      BS ? p.cost_order : nullptr);
   const int G = p.H / p.H_kv;                     // query heads per K/V head
 
   if (warp == 0) {

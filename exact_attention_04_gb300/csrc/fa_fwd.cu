@@ -56,6 +56,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_internal.h"
+#include "fa_order.cuh"
 #include "fa_window.cuh"
 #include "sm103_ptx.cuh"
 
@@ -134,6 +135,9 @@ struct FwdSmem {
   // row and reads the other, so it only overwrites the value it has just read
   uint64_t pair_bar[4];
   float xch[C::NHALF == 2 ? 2 : 1][C::NHALF == 2 ? BM : 1];
+  // a block mask without a host copy: the tiles' costs, then their
+  // cost-sorted order (fa_order.cuh)
+  uint32_t order[kFwdOrderMaxT];
   uint32_t tmem_base;
   int abort;
 };
@@ -158,9 +162,15 @@ __device__ __forceinline__ void record_failure(int* status, volatile int* abort,
 // round-robin, except those of the last tail_heads heads, whose single tiles
 // come from the host-planned tail table (longest first on the least-loaded
 // CTA), so that the last round of equal units does not leave CTAs idle.
+//
+// A block mask without a host copy (order != nullptr): the items go in the
+// cost-sorted turning deal of fa_order.cuh instead, from this CTA's table.
 struct Sched {
   int T, P, units, causal;   // units: the round-robin units (tile pairs when causal)
-  __device__ Sched(int BH, int N, int causal_, int tail_heads) : causal(causal_) {
+  int BH;
+  const uint32_t* order;     // the cost-sorted order, or nullptr
+  __device__ Sched(int BH_, int N, int causal_, int tail_heads, const uint32_t* order_)
+      : causal(causal_), BH(BH_), order(order_) {
     T = (N + BM - 1) / BM;
     P = (T + 1) / 2;
     units = (BH - tail_heads) * (causal ? P : T);
@@ -297,6 +307,15 @@ __device__ __forceinline__ bool next_tile(const FwdParams& p, const TailTable& t
     it.u += gridDim.x;
     return true;
   } else {
+    if (BS && sched.order) {   // round it.k of the cost-sorted deal
+      const long long k = order_deal(it.k, gridDim.x, blockIdx.x);
+      if (k >= static_cast<long long>(sched.BH) * sched.T) return false;
+      ++it.k;
+      int bh, m;
+      order_item(sched.order, sched.BH, k, bh, m);
+      make_tile<false, BS>(p, 0, bh, m, t);
+      return true;
+    }
     while (it.u < sched.units) {
       if (it.kt < sched.ntiles(it.u)) {
         int bh, m;
@@ -373,12 +392,36 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
     tmem_alloc(&sm.tmem_base, C::TM_COLS);
     tmem_relinquish();
   }
+  // A block mask without a host copy: every tile's cost (its computed key
+  // blocks), then the cost-sorted order, a tile a thread (the launch keeps
+  // T <= kFwdOrderMaxT).
+  if constexpr (BS && !DEC) {
+    static_assert(C::THREADS >= kFwdOrderMaxT, "one tile a thread");
+    if (p.cost_sorted) {
+      const int T = (p.N + BM - 1) / BM;
+      const int t = threadIdx.x;
+      if (t < T) {
+        int jlo;
+        const int n = tile_blocks(p, t, p.N, jlo);
+        const uint8_t* row = p.block_mask + static_cast<size_t>(t) * p.bm_t;
+        uint32_t c = 0;
+        for (int j = jlo; j < jlo + n; ++j) c += __ldg(row + j) != 0;
+        sm.order[t] = c;
+      }
+      __syncthreads();
+      uint32_t e = 0;
+      const int pos = t < T ? order_rank(sm.order, T, t, e) : 0;
+      __syncthreads();
+      if (t < T) sm.order[pos] = e;
+    }
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
   const int BH = p.B * p.H;
-  const Sched sched(BH, p.N, p.causal, DEC ? 0 : tail.heads);
+  const Sched sched(BH, p.N, p.causal, DEC ? 0 : tail.heads,
+                    (BS && !DEC && p.cost_sorted) ? sm.order : nullptr);
   const int nunits = DEC ? p.B * p.H_kv * p.splits : sched.units;
 
   if (warp == 0) {

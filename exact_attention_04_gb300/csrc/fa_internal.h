@@ -47,6 +47,9 @@ struct FwdParams {
   // a host copy of the block mask, or nullptr; read by the launch (never by a
   // kernel) to balance the schedule
   const uint8_t* block_mask_host;
+  // nonzero: a block mask without a host copy, whose tiles each CTA sorts
+  // by cost at its start (the cost-sorted deal of fa_order.cuh)
+  int cost_sorted;
 };
 
 struct BwdParams {
@@ -79,7 +82,19 @@ struct BwdParams {
   // a host copy of the block mask, or nullptr; read by the launch (never by a
   // kernel) to balance the schedule
   const uint8_t* block_mask_host;
+  // a block mask without a host copy: [bm_t] packed entries of the key
+  // blocks sorted by cost (fa_order.cuh), written into the workspace by
+  // bwd_order_kernel before the main kernel; nullptr otherwise
+  uint32_t* cost_order;
 };
+
+// Cost-sorted deal of a block-sparse schedule planned on the device (a block
+// mask without a host copy): the tiles (forward) or key blocks (backward) are
+// sorted by their computed blocks, longest first, and the items dealt over
+// the CTAs in that order.  Entries pack 10-bit fields, so T <= kOrderMaxT;
+// the forward keeps its table in shared memory, of kFwdOrderMaxT entries.
+constexpr int kOrderMaxT = 1024;
+constexpr int kFwdOrderMaxT = 256;
 
 // Causal schedules.  A causal work item (a query tile of the forward, a key
 // block of the backward) costs in proportion to its distance from one end of
@@ -145,6 +160,8 @@ fa_status_t bwd_check_args(const void* q, const void* k, const void* v, const vo
 
 cudaError_t launch_fwd(const FwdParams& p, int d, int num_sms, int max_smem, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const BwdParams& p, int d, cudaStream_t stream);
+// Writes p.cost_order (a block mask without a host copy; T <= kOrderMaxT).
+cudaError_t launch_bwd_order(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_post(const BwdParams& p, int d, cudaStream_t stream);
 // 64-query-step backward main kernel with dQ^T (head dimensions 128, 256);
 // its Q and dO tensor maps have a box of 64 rows.

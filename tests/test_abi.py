@@ -79,7 +79,8 @@ def test_workspace_bytes(lib):
     npad = 256
     stat = -(-B * H * npad * 4 // 256) * 256
     acc = -(-B * H * npad * d * 4 // 256) * 256
-    assert fa.fa_bwd_workspace_bytes(B, H, N, d) == 2 * stat + acc
+    order = -(-(npad // 128) * 4 // 256) * 256     # the key blocks' cost-sorted order
+    assert fa.fa_bwd_workspace_bytes(B, H, N, d) == 2 * stat + acc + order
     assert fa.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
     assert fa.fa_bwd_workspace_bytes(1, 1, 1, 96) == 0
 

@@ -209,14 +209,16 @@ def test_block_mask_with_window_forward_and_backward(d, causal, window):
 
 @pytest.mark.parametrize("d,Hkv,window", [(128, 16, None), (256, 16, None), (64, 16, None),
                                           (128, 4, (-1, 0))])
-def test_balanced_schedule_matches_round_robin(d, Hkv, window):
+def test_host_and_device_planned_schedules_agree(d, Hkv, window):
     """With the mask's host copy the launch plans a balanced tail of tiles and
-    key blocks; without it every item goes round-robin.  A tile's, or a key
-    block's, arithmetic does not depend on the SM that runs it, so O, LSE, dK
-    and dV agree bit for bit; dQ is summed across key blocks in L2 in an
-    order that varies, so it agrees within a bf16 unit.  A tile or key block
-    the plan missed or ran twice would show here (at N = 8192 the plan has
-    a tail of 14 heads on 152 SMs)."""
+    key blocks; without it each CTA sorts the tiles (and the backward's
+    planning kernel the key blocks) by cost on the device and takes its
+    items in the turning deal.  A tile's, or a key block's, arithmetic does
+    not depend on the SM that runs it, so O, LSE, dK and dV agree bit for
+    bit; dQ is summed across key blocks in L2 in an order that varies, so it
+    agrees within a bf16 unit.  A tile or key block either plan missed or ran
+    twice would show here (at N = 8192 the host plan has a tail of 14 heads
+    on 152 SMs, the device deal 14 rounds)."""
     from exact_attention_04_gb300.workloads import block_sparse_mask
     w = random_case(2, 16, 8192, d, seed=d + Hkv, causal=False, h_kv=Hkv)
     g = P.to_gpu(make_inputs(w))
@@ -238,9 +240,10 @@ def test_balanced_schedule_matches_round_robin(d, Hkv, window):
 
 
 @pytest.mark.parametrize("d", [128, 256])
-def test_balanced_schedule_matches_round_robin_fp8(d):
-    """The E4M3 forward with and without the mask's host copy: the same tiles
-    with the same arithmetic, so O and LSE agree bit for bit."""
+def test_host_and_device_planned_schedules_agree_fp8(d):
+    """The E4M3 forward with and without the mask's host copy (the host-planned
+    tail, the device's cost-sorted deal): the same tiles with the same
+    arithmetic, so O and LSE agree bit for bit."""
     from exact_attention_04_gb300.workloads import block_sparse_mask
     w = random_case(2, 16, 8192, d, seed=d + 7, causal=False)
     g = P.to_gpu(make_inputs(w))
@@ -283,3 +286,71 @@ def test_balanced_schedule_with_padding_against_oracle():
         P.check_grad(P.f64(dq[b:b + 1, h:h + 1]), dq_r, f"padded block-sparse dQ ({b},{h})")
         P.check_grad(P.f64(dk[b:b + 1, h:h + 1]), dk_r, f"padded block-sparse dK ({b},{h})")
         P.check_grad(P.f64(dv[b:b + 1, h:h + 1]), dv_r, f"padded block-sparse dV ({b},{h})")
+
+
+def _both_schedules(w, bm, window=None):
+    """Forward and backward with the device mask alone and with its host
+    copy; returns the two (o, lse, dq, dk, dv)."""
+    g = P.to_gpu(make_inputs(w))
+    out = []
+    for m in (torch.from_numpy(bm).cuda(), fa.BlockMask(bm)):
+        o, lse = fa.forward(g["q"], g["k"], g["v"], scale=w.scale, window=window, block_mask=m)
+        grads = fa.backward(g["q"], g["k"], g["v"], o, lse, g["do"], scale=w.scale,
+                            window=window, block_mask=m)
+        out.append((o, lse) + tuple(grads))
+    fa.fa_check()
+    return out
+
+
+def _agree(out):
+    (o1, l1, dq1, dk1, dv1), (o2, l2, dq2, dk2, dv2) = out
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    diff = (dq1.float() - dq2.float()).abs().max().item()
+    assert diff <= 2 ** -7 * dq1.float().abs().max().item(), diff
+
+
+@pytest.mark.parametrize("d,Hkv", [(64, 8), (128, 2), (256, 8)])
+def test_device_deal_with_skewed_costs(d, Hkv):
+    """A mask with empty rows and columns (items of cost zero), a full row
+    and a full column (the costliest items) and many ties: the device deal
+    against the host plan (bit for bit, as above) and two heads against the
+    oracle.  2 x 8 heads of 32 tiles are 512 items, four rounds of the deal
+    on 152 SMs."""
+    N = 4096
+    T = N // 128
+    bm = random_mask(T, 0.3, seed=d + Hkv)
+    bm[[3, 17, 30]] = 0
+    bm[:, [5, 21]] = 0
+    bm[9] = 1
+    bm[:, 12] = 1
+    w = random_case(2, 8, N, d, seed=5 * d + Hkv, causal=False, h_kv=Hkv)
+    out = _both_schedules(w, bm)
+    _agree(out)
+    o, lse, dq, dk, dv = out[0]
+    inp = make_inputs(w)
+    g = 8 // Hkv                            # query heads per K/V head
+    for b, h in ((0, 1), (1, 8 - g)):
+        kvh = h // g
+        one = {"q": inp["q"][b:b + 1, h:h + 1], "do": inp["do"][b:b + 1, h:h + 1],
+               "k": inp["k"][b:b + 1, kvh:kvh + 1], "v": inp["v"][b:b + 1, kvh:kvh + 1]}
+        o_r, l_r = oracle.attention_fwd(P.f64(one["q"]), P.f64(one["k"]), P.f64(one["v"]),
+                                        w.scale, block_mask=bm)
+        P.check_o(P.f64(o[b:b + 1, h:h + 1]), o_r, f"device deal O ({b},{h})")
+        P.check_lse(P.f64(lse[b:b + 1, h:h + 1]), l_r, f"device deal LSE ({b},{h})")
+        dq_r, _, _, _ = oracle.attention_bwd(P.f64(one["q"]), P.f64(one["k"]), P.f64(one["v"]),
+                                             P.f64(one["do"]), w.scale, block_mask=bm)
+        P.check_grad(P.f64(dq[b:b + 1, h:h + 1]), dq_r, f"device deal dQ ({b},{h})")
+
+
+@pytest.mark.parametrize("N", [257 * 128, 1025 * 128])
+def test_device_deal_size_limits(N):
+    """Past 256 tiles the forward's table does not fit its shared memory and
+    the forward goes round-robin; past 1024 key blocks the backward's
+    entries cannot hold them and the backward goes round-robin too.  Either
+    way against the host plan, bit for bit (as above)."""
+    from exact_attention_04_gb300.workloads import block_sparse_mask
+    T = N // 128
+    w = random_case(1, 2, N, 64, seed=T, causal=False)
+    bm = block_sparse_mask(T, seed=T, band=1, n_random=2)
+    _agree(_both_schedules(w, bm))
