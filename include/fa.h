@@ -72,8 +72,10 @@ fa_status_t fa_fwd(const void* q, const void* k, const void* v, void* o, float* 
  * Bytes of device workspace fa_bwd needs for these sizes: the fp32 row
  * statistics D = rowsum(dO o O) and LSE*log2(e), each [B*H, Npad] with Npad =
  * N rounded up to 128, and the fp32 dQ accumulator of B*H*Npad*d elements
- * ([B*H, Npad, d] for d = 64, [B*H, d, Npad] for d = 128 and 256); each region
- * starts on a 256-byte boundary.  Returns 0 for invalid sizes.
+ * ([B*H, Npad, d] for d = 64, [B*H, d, Npad] for d = 128 and 256), and
+ * Npad/128 uint32 for the key blocks' schedule order (written when a block
+ * mask comes without its host copy); each region starts on a 256-byte
+ * boundary.  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -149,8 +151,14 @@ fa_status_t fa_bwd_dq(void* dq, int B, int H, int N, int d, float scale, void* w
  *   a tile's work is its count of computed blocks, and the last heads' tiles
  *   go, most work first, to the least-loaded SMs.  The results do not depend
  *   on it; a copy that differs from block_mask only unbalances the schedule.
- *   NULL: tiles go round-robin, which with an uneven mask can leave some SMs
- *   with a third more work than the mean.
+ *   NULL (and no causal flag): the kernels plan the schedule on the device
+ *   from block_mask: the tiles (the backward's key blocks) are sorted by
+ *   their computed blocks, most first, and dealt over the SMs in rounds that
+ *   turn direction, which leaves the busiest SM some 8 % above the mean on
+ *   an uneven mask (about 2 % with the host copy).  Past 256 tiles
+ *   (forward) or 1024 key blocks (backward) they go round-robin instead,
+ *   which with an uneven mask can leave some SMs with a third more work
+ *   than the mean.
  * A NULL variant pointer means {H, -1, -1, NULL, NULL}; an aggregate
  * initialiser that stops after window_right (or block_mask) leaves the later
  * members NULL.
