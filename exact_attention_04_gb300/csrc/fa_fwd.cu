@@ -112,7 +112,16 @@ struct Cfg {
   // a quarter of the time the softmax of one warp does, so two warps share
   // each row (agreeing on its maximum once a block); elsewhere one.
   static constexpr int NHALF = (D == 64 && !FP8) ? 2 : 1;
-  static constexpr int THREADS = NHALF == 2 ? 352 : 256;
+  // EPI: four epilogue warps take each tile's O / l, bf16 store and LSE off
+  // the softmax warps, with O in two tensor-memory buffers (tile parity) so
+  // the next tile's P V need not wait for the previous tile's O to be read.
+  // At d = 64 the tiles of short sequences have few key blocks and the
+  // epilogue was a large share of the softmax warps' time per tile.
+  static constexpr bool EPI = (D == 64 && !FP8);
+  static constexpr int NOB = EPI ? 2 : 1;            // O buffers
+  static constexpr int EPI_WARP0 = 3 + 4 * NHALF;    // first epilogue warp
+  static constexpr int THREADS = NHALF == 2 ? (EPI ? 480 : 352) : 256;
+  static_assert(TM_O + D * NOB <= TM_COLS, "tensor memory budget (O buffers)");
 };
 
 template <int D, bool FP8 = false>
@@ -128,7 +137,12 @@ struct FwdSmem {
   uint64_t s_free[C::NSB];   // SEP: the softmax has loaded S buffer b
   uint64_t p_full[C::NPB];   // the softmax wrote P of block g into P buffer g % NPB
   uint64_t pv_done[C::NPB];  // O += P V of block g (P buffer g % NPB) has completed
-  uint64_t o_free;
+  // O buffer b (EPI: tile parity) has been read out of tensor memory
+  uint64_t o_free[C::NOB];
+  // EPI: the tile's last P V into O buffer b has completed; its rows' 1 / l
+  // and LSE are in ostat[b]
+  uint64_t o_done[C::NOB], stats_full[C::NOB];
+  float ostat[C::NOB][2][C::EPI ? BM : 1];
   uint64_t mma_done, pv_mma_done;
   // NHALF = 2: the warp pairs' barriers and exchanged partial maxima / sums;
   // in its n-th exchange the warp of half h writes slot h ^ (n & 1) of its
@@ -384,7 +398,11 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
     }
     for (int q = 0; q < 4; ++q) mbar_init(&sm.pair_bar[q], 64);
     mbar_init(&sm.pv_mma_done, 1);
-    mbar_init(&sm.o_free, 4 * C::NHALF);
+    for (int b = 0; b < C::NOB; ++b) {
+      mbar_init(&sm.o_free[b], C::EPI ? 4 : 4 * C::NHALF);
+      mbar_init(&sm.o_done[b], 1);
+      mbar_init(&sm.stats_full[b], 128);
+    }
     mbar_init(&sm.mma_done, 1);
     fence_mbar_init();
   }
@@ -631,9 +649,11 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
               ok = false;
               break;
             }
-            // a tile's first P V starts a fresh O: the previous tile's epilogue
-            // must have read O out of tensor memory
-            if (j == 0 && !mbar_wait_warp(&sm.o_free, (t_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+            // a tile's first P V starts a fresh O: the epilogue of the tile
+            // that last used this O buffer must have read it out of tensor memory
+            const uint32_t ob = t_it % C::NOB;
+            if (j == 0 && !mbar_wait_warp(&sm.o_free[ob], ((t_it / C::NOB) & 1) ^ 1, abort,
+                                          kWaitTimeoutNs)) {
               issuer_fail(p.status, abort, lane, kSiteMmaO);
               ok = false;
               break;
@@ -654,13 +674,14 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
               const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), BN * 128, 1024);
 #pragma unroll
               for (int kk = 0; kk < BN / 16; ++kk) {
-                mma_bf16_ts_w(tmem + C::TM_O, tmem + C::TM_P + C::P_STRIDE * b + kk * 8,
+                mma_bf16_ts_w(tmem + C::TM_O + D * ob, tmem + C::TM_P + C::P_STRIDE * b + kk * 8,
                             dv0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescPV,
                             (j == 0 && kk == 0) ? 0u : 1u);
               }
             }
             mma_commit_w(&sm.v_empty[st]);
             mma_commit_w(&sm.pv_done[b]);
+            if (C::EPI && j == nkv - 1) mma_commit_w(&sm.o_done[ob]);
           }
           ++t_it;
         }
@@ -670,6 +691,90 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
         issuer_fail(p.status, abort, lane, kSiteDrain);
     }
     __syncwarp();
+  } else if (C::EPI && warp >= C::EPI_WARP0) {
+    // ------------------------------------------------------------ epilogue warps
+    // One warp per sub-partition (its 32 tensor-memory lanes are 32 query
+    // rows); each row's O / l into bf16 O (decode: fp32 partials) and its LSE.
+    const int quarter = warp & 3;
+    const int row_local = quarter * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o);
+    const bool st32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+    uint32_t e_it = 0;
+    bool ok = true;
+    TileIter it{static_cast<int>(blockIdx.x), 0, 0};
+    for (Tile t; ok && next_tile<DEC, BS>(p, tail, sched, nunits, it, t);) {
+      const bool row_valid = row_local < t.rows;
+      const size_t row_off = static_cast<size_t>(t.out0 + row_local);
+      if (t.nkv == 0) {   // no key is visible to the tile's rows: O = 0, LSE = -inf
+        if (row_valid) {
+          if constexpr (DEC) {
+            float4* dst = reinterpret_cast<float4*>(p.o_part + row_off * D);
+#pragma unroll
+            for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            p.lse_part[row_off] = -INFINITY;
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(out + row_off * D);
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+            p.lse[row_off] = -INFINITY;
+          }
+        }
+        continue;
+      }
+      const uint32_t ob = e_it % C::NOB;
+      const uint32_t ph = (e_it / C::NOB) & 1;
+      ++e_it;
+      if (!warp_wait(&sm.stats_full[ob], ph, abort) || !warp_wait(&sm.o_done[ob], ph, abort)) {
+        if (lane == 0) record_failure(p.status, abort, kSiteSmEpi);
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const float inv_l = sm.ostat[ob][0][row_local];
+      const float lse_row = sm.ostat[ob][1][row_local];
+      uint32_t orr[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld_x32(t_lane + C::TM_O + D * ob + 32 * c, orr + 32 * c);
+      tmem_wait_ld();
+      reg_fence<D>(orr);
+      // O buffer ob (and ostat[ob]) may now take the tile two ahead
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.o_free[ob]);
+      if (row_valid) {
+        if constexpr (DEC) {
+          // the workspace is 256-byte aligned and a row is D floats
+          float* dst = p.o_part + row_off * D;
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) {
+            uint32_t r8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) r8[e] = __float_as_uint(__uint_as_float(orr[8 * i + e]) * inv_l);
+            st_global_v8(dst + 8 * i, r8);
+          }
+          p.lse_part[row_off] = lse_row;
+        } else {
+          __nv_bfloat16* dst = out + row_off * D;
+#pragma unroll
+          for (int i = 0; i < D / 16; ++i) {                // 16 columns a step
+            uint32_t pk8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              pk8[e] = pack_bf16x2(__uint_as_float(orr[16 * i + 2 * e]) * inv_l,
+                                   __uint_as_float(orr[16 * i + 2 * e + 1]) * inv_l);
+            if (st32) {
+              st_global_v8(dst + 16 * i, pk8);
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * i);
+              d4[0] = make_uint4(pk8[0], pk8[1], pk8[2], pk8[3]);
+              d4[1] = make_uint4(pk8[4], pk8[5], pk8[6], pk8[7]);
+            }
+          }
+          p.lse[row_off] = lse_row;
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ softmax warps
     const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
@@ -678,10 +783,11 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
     constexpr int DO = D / C::NHALF;               // O columns of this warp
     const int row_local = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t t_o = t_lane + C::TM_O + DO * hf;
+    const uint32_t t_o0 = t_lane + C::TM_O + DO * hf;   // this warp's columns of O buffer 0
+    uint32_t t_o = t_o0;                                 // ... of the current tile's O buffer
     const float c2 = p.scale_log2;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o);
-    uint32_t kv_it = 0, hs = 0;
+    uint32_t kv_it = 0, hs = 0, e_it = 0;               // e_it: tiles with key blocks
     bool ok = true;
     // NHALF = 2: one exchange with the partner warp (same rows, other keys)
     auto exchange = [&](float v, float& other) -> bool {
@@ -727,7 +833,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
         if (c0 + OB == DO / 32) {
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.o_free);
+          if (lane == 0) mbar_arrive(&sm.o_free[0]);
         }
         if constexpr (DEC) {
           if (row_valid) {
@@ -793,6 +899,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
         const float q_sc = FP8 ? __ldg(p.q_scale + t.qs) : 1.f;
         const bool row_valid = row_local < t.rows;
         const size_t row_off = static_cast<size_t>(t.out0 + row_local);
+        if (C::EPI && nkv == 0) continue;   // the epilogue warps write its rows
         if (nkv == 0) {
           if (!finish()) {
             ok = false;
@@ -813,6 +920,8 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           }
           continue;
         }
+        const uint32_t ob = e_it % C::NOB;   // this tile's O buffer
+        t_o = t_o0 + D * ob;
         float m_ref = -INFINITY;    // reference maximum, base-2 units of S*scale
         float l = 0.f;
         for (int j = 0, jbs = next_block<BS>(t, t.jlo); j < nkv;
@@ -978,7 +1087,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           // the previous tile's epilogue, now that this tile's first P is out
           // (bf16; with E4M3 the call in this loop measured 6 % slower on
           // long tiles, so its epilogue runs at the end of the tile)
-          if constexpr (!FP8) {
+          if constexpr (!FP8 && !C::EPI) {
             if (j == 0 && !finish()) {
               ok = false;
               break;
@@ -995,6 +1104,24 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
             break;
           }
           l += l_other;
+        }
+        if constexpr (C::EPI) {
+          // hand the tile to the epilogue warps: 1 / l and LSE per row into
+          // ostat[ob], once the epilogue two tiles back has read that slot
+          // (it reads the slot before it frees O buffer ob)
+          ++e_it;
+          if (hf == 0) {
+            if (!warp_wait(&sm.o_free[ob], (((e_it - 1) / C::NOB) & 1) ^ 1, abort)) {
+              if (lane == 0) record_failure(p.status, abort, kSiteSmEpi);
+              ok = false;
+              break;
+            }
+            sm.ostat[ob][0][row_local] = l > 0.f ? 1.f / l : 0.f;
+            sm.ostat[ob][1][row_local] =
+                l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            mbar_arrive(&sm.stats_full[ob]);
+          }
+          continue;
         }
         pend = {true, kv_it - 1, l, m_ref, row_off, row_valid, t.kvbh};
         if constexpr (FP8) {
