@@ -68,6 +68,7 @@ using namespace ptx;
 constexpr int BM = 128;          // query rows per tile = TMEM lanes = MMA M
 constexpr int BN = 128;          // keys per block = MMA N of S
 constexpr int CHUNK = 128 * 128; // bytes of one 128-row x 64-column bf16 chunk (SW128 atom rows)
+constexpr int kKvlCache = 256;   // batch entries whose kv_len the d = 64 kernels stage
 // bf16: the reference maximum moves only when a block exceeds it by more than
 // 24 (log2 units), so P <= 2^24, l <= N * 2^24 and O~ stay far inside fp32's
 // (and P inside bf16's) range, and most blocks of even large-score rows skip
@@ -139,10 +140,13 @@ struct FwdSmem {
   uint64_t pv_done[C::NPB];  // O += P V of block g (P buffer g % NPB) has completed
   // O buffer b (EPI: tile parity) has been read out of tensor memory
   uint64_t o_free[C::NOB];
-  // EPI: the tile's last P V into O buffer b has completed; its rows' 1 / l
-  // and LSE are in ostat[b]
+  // EPI: the tile's last P V into O buffer b has completed; its rows' row
+  // sums and reference maximum are in ostat[b]
   uint64_t o_done[C::NOB], stats_full[C::NOB];
-  float ostat[C::NOB][2][C::EPI ? BM : 1];
+  // EPI: per row, the two key halves' row sums and the reference maximum
+  float ostat[C::NOB][3][C::EPI ? BM : 1];
+  // EPI: kv_len staged at the start (batches up to kKvlCache)
+  int kvl[C::EPI ? kKvlCache : 1];
   uint64_t mma_done, pv_mma_done;
   // NHALF = 2: the warp pairs' barriers and exchanged partial maxima / sums;
   // in its n-th exchange the warp of half h writes slot h ^ (n & 1) of its
@@ -183,8 +187,10 @@ struct Sched {
   int T, P, units, causal;   // units: the round-robin units (tile pairs when causal)
   int BH;
   const uint32_t* order;     // the cost-sorted order, or nullptr
-  __device__ Sched(int BH_, int N, int causal_, int tail_heads, const uint32_t* order_)
-      : causal(causal_), BH(BH_), order(order_) {
+  const int* kvl;            // kv_len staged in shared memory, or nullptr
+  __device__ Sched(int BH_, int N, int causal_, int tail_heads, const uint32_t* order_,
+                   const int* kvl_)
+      : causal(causal_), BH(BH_), order(order_), kvl(kvl_) {
     T = (N + BM - 1) / BM;
     P = (T + 1) / 2;
     units = (BH - tail_heads) * (causal ? P : T);
@@ -206,10 +212,11 @@ struct Sched {
   }
 };
 
-__device__ __forceinline__ int seq_len(const FwdParams& p, int bh) {
+// kvl: kv_len staged in shared memory, or nullptr (read from global).
+__device__ __forceinline__ int seq_len(const FwdParams& p, int bh, const int* kvl) {
   int len = p.N;
   if (p.kv_len) {
-    len = __ldg(p.kv_len + bh / p.H);
+    len = kvl ? kvl[bh / p.H] : __ldg(p.kv_len + bh / p.H);
     len = len < 0 ? 0 : (len > p.N ? p.N : len);
   }
   return len;
@@ -250,12 +257,13 @@ struct Tile {
 // BS: the launch carries a block mask (a separate instantiation, so that the
 // kernels without one keep the plain block walk).
 template <bool DEC, bool BS = false>
-__device__ __forceinline__ void make_tile(const FwdParams& p, int u, int bh, int m, Tile& t) {
+__device__ __forceinline__ void make_tile(const FwdParams& p, int u, int bh, int m, Tile& t,
+                                          const int* kvl) {
   if constexpr (!DEC) {
     t.qy = m * BM;
     t.qz = bh;
     t.kvbh = kv_head_of(bh, p.H, p.H_kv);
-    t.len = seq_len(p, bh);
+    t.len = seq_len(p, bh, kvl);
     t.qlo = m * BM;
     t.qhi = m * BM + BM - 1;
     t.nkv = tile_blocks(p, m, t.len, t.jlo);
@@ -276,7 +284,7 @@ __device__ __forceinline__ void make_tile(const FwdParams& p, int u, int bh, int
     t.qy = row0;
     t.qz = 0;
     t.kvbh = kvbh;
-    t.len = seq_len(p, (kvbh / p.H_kv) * p.H);
+    t.len = seq_len(p, (kvbh / p.H_kv) * p.H, kvl);
     t.qlo = t.len - p.Nq;
     t.qhi = t.len - 1;
     int k_lo, k_hi;
@@ -317,7 +325,7 @@ __device__ __forceinline__ bool next_tile(const FwdParams& p, const TailTable& t
                                           const Sched& sched, int nunits, TileIter& it, Tile& t) {
   if constexpr (DEC) {
     if (it.u >= nunits) return false;
-    make_tile<true>(p, it.u, 0, 0, t);
+    make_tile<true>(p, it.u, 0, 0, t, sched.kvl);
     it.u += gridDim.x;
     return true;
   } else {
@@ -327,7 +335,7 @@ __device__ __forceinline__ bool next_tile(const FwdParams& p, const TailTable& t
       ++it.k;
       int bh, m;
       order_item(sched.order, sched.BH, k, bh, m);
-      make_tile<false, BS>(p, 0, bh, m, t);
+      make_tile<false, BS>(p, 0, bh, m, t, sched.kvl);
       return true;
     }
     while (it.u < sched.units) {
@@ -335,7 +343,7 @@ __device__ __forceinline__ bool next_tile(const FwdParams& p, const TailTable& t
         int bh, m;
         sched.tile(it.u, it.kt, bh, m);
         ++it.kt;
-        make_tile<false, BS>(p, 0, bh, m, t);
+        make_tile<false, BS>(p, 0, bh, m, t, sched.kvl);
         return true;
       }
       it.u += gridDim.x;
@@ -345,7 +353,7 @@ __device__ __forceinline__ bool next_tile(const FwdParams& p, const TailTable& t
     const int e = tail.item[blockIdx.x][it.k];
     if (e < 0) return false;
     ++it.k;
-    make_tile<false, BS>(p, 0, tail_head(e), tail_block(e), t);
+    make_tile<false, BS>(p, 0, tail_head(e), tail_block(e), t, sched.kvl);
     return true;
   }
 }
@@ -401,7 +409,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
     for (int b = 0; b < C::NOB; ++b) {
       mbar_init(&sm.o_free[b], C::EPI ? 4 : 4 * C::NHALF);
       mbar_init(&sm.o_done[b], 1);
-      mbar_init(&sm.stats_full[b], 128);
+      mbar_init(&sm.stats_full[b], 32 * 4 * C::NHALF);
     }
     mbar_init(&sm.mma_done, 1);
     fence_mbar_init();
@@ -409,6 +417,11 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
   if (warp == 1) {
     tmem_alloc(&sm.tmem_base, C::TM_COLS);
     tmem_relinquish();
+  }
+  // (EPI) every tile's setup reads its batch entry's kv_len: stage them once
+  if constexpr (C::EPI) {
+    if (p.kv_len && p.B <= kKvlCache)
+      for (int b = threadIdx.x; b < p.B; b += C::THREADS) sm.kvl[b] = __ldg(p.kv_len + b);
   }
   // A block mask without a host copy: every tile's cost (its computed key
   // blocks), then the cost-sorted order, a tile a thread (the launch keeps
@@ -439,7 +452,8 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
   const uint32_t tmem = sm.tmem_base;
   const int BH = p.B * p.H;
   const Sched sched(BH, p.N, p.causal, DEC ? 0 : tail.heads,
-                    (BS && !DEC && p.cost_sorted) ? sm.order : nullptr);
+                    (BS && !DEC && p.cost_sorted) ? sm.order : nullptr,
+                    (C::EPI && p.kv_len && p.B <= kKvlCache) ? sm.kvl : nullptr);
   const int nunits = DEC ? p.B * p.H_kv * p.splits : sched.units;
 
   if (warp == 0) {
@@ -731,8 +745,10 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
         break;
       }
       tc_fence_after_sync();
-      const float inv_l = sm.ostat[ob][0][row_local];
-      const float lse_row = sm.ostat[ob][1][row_local];
+      const float l = sm.ostat[ob][0][row_local] + sm.ostat[ob][1][row_local];
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float lse_row =
+          l > 0.f ? (sm.ostat[ob][2][row_local] + log2f(l)) * 0.69314718055994531f : -INFINITY;
       uint32_t orr[D];
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) tmem_ld_x32(t_lane + C::TM_O + D * ob + 32 * c, orr + 32 * c);
@@ -1095,7 +1111,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           }
         }
         if (!ok) break;
-        if constexpr (C::NHALF == 2) {
+        if constexpr (C::NHALF == 2 && !C::EPI) {
           // the row sum over both halves of the keys
           float l_other;
           if (!exchange(l, l_other)) {
@@ -1106,21 +1122,19 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           l += l_other;
         }
         if constexpr (C::EPI) {
-          // hand the tile to the epilogue warps: 1 / l and LSE per row into
-          // ostat[ob], once the epilogue two tiles back has read that slot
-          // (it reads the slot before it frees O buffer ob)
+          // hand the tile to the epilogue warps: this half's row sum (the
+          // epilogue adds the halves) and the reference maximum, which both
+          // halves share, into ostat[ob] once the epilogue two tiles back has
+          // read that slot (it reads the slot before it frees O buffer ob)
           ++e_it;
-          if (hf == 0) {
-            if (!warp_wait(&sm.o_free[ob], (((e_it - 1) / C::NOB) & 1) ^ 1, abort)) {
-              if (lane == 0) record_failure(p.status, abort, kSiteSmEpi);
-              ok = false;
-              break;
-            }
-            sm.ostat[ob][0][row_local] = l > 0.f ? 1.f / l : 0.f;
-            sm.ostat[ob][1][row_local] =
-                l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
-            mbar_arrive(&sm.stats_full[ob]);
+          if (!warp_wait(&sm.o_free[ob], (((e_it - 1) / C::NOB) & 1) ^ 1, abort)) {
+            if (lane == 0) record_failure(p.status, abort, kSiteSmEpi);
+            ok = false;
+            break;
           }
+          sm.ostat[ob][hf][row_local] = l;
+          if (hf == 0) sm.ostat[ob][2][row_local] = m_ref;
+          mbar_arrive(&sm.stats_full[ob]);
           continue;
         }
         pend = {true, kv_it - 1, l, m_ref, row_off, row_valid, t.kvbh};
