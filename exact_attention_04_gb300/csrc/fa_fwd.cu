@@ -109,20 +109,22 @@ struct Cfg {
   static constexpr uint32_t TM_COLS = 512;
   static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
   // NHALF softmax warps per sub-partition, each taking BN / NHALF keys of a
-  // block and D / NHALF columns of O.  At d = 64 the products of a block take
-  // a quarter of the time the softmax of one warp does, so two warps share
-  // each row (agreeing on its maximum once a block); elsewhere one.
+  // block.  At d = 64 the products of a block take a quarter of the time the
+  // softmax of one warp does, so two warps share each row, each with a
+  // running maximum, row sum and O accumulator of its own over its half of
+  // the keys (O in NHALF parts of D columns, merged by the epilogue).  The
+  // two warps of a sub-partition never wait for each other, so one computes
+  // while the other waits for tensor memory; elsewhere one warp a row.
   static constexpr int NHALF = (D == 64 && !FP8) ? 2 : 1;
-  // EPI: four epilogue warps take each tile's O / l, bf16 store and LSE off
-  // the softmax warps, with O in two tensor-memory buffers (tile parity) so
-  // the next tile's P V need not wait for the previous tile's O to be read.
-  // At d = 64 the tiles of short sequences have few key blocks and the
-  // epilogue was a large share of the softmax warps' time per tile.
-  static constexpr bool EPI = (D == 64 && !FP8);
-  static constexpr int NOB = EPI ? 2 : 1;            // O buffers
+  static constexpr int OCOLS = D * NHALF;            // columns of O (its key halves)
+  // EPI (d = 64): four epilogue warps merge each tile's O halves, divide by
+  // l, store bf16 O and LSE, off the softmax warps, whose time per tile the
+  // epilogue was a large share of at the few key blocks of short sequences.
+  static constexpr bool EPI = NHALF == 2;
+  static constexpr int NOB = 1;                      // O buffers
   static constexpr int EPI_WARP0 = 3 + 4 * NHALF;    // first epilogue warp
-  static constexpr int THREADS = NHALF == 2 ? (EPI ? 480 : 352) : 256;
-  static_assert(TM_O + D * NOB <= TM_COLS, "tensor memory budget (O buffers)");
+  static constexpr int THREADS = EPI ? 480 : 256;
+  static_assert(TM_O + OCOLS * NOB <= TM_COLS, "tensor memory budget (O)");
 };
 
 template <int D, bool FP8 = false>
@@ -136,23 +138,21 @@ struct FwdSmem {
   uint64_t v_full[C::STAGES], v_empty[C::STAGES];
   uint64_t s_full[C::NSB];   // S of block g is in S buffer g % NSB
   uint64_t s_free[C::NSB];   // SEP: the softmax has loaded S buffer b
-  uint64_t p_full[C::NPB];   // the softmax wrote P of block g into P buffer g % NPB
+  // the softmax wrote (key half h of) P of block g into P buffer g % NPB:
+  // p_full[(g % NPB) * NHALF + h]
+  uint64_t p_full[C::NPB * C::NHALF];
   uint64_t pv_done[C::NPB];  // O += P V of block g (P buffer g % NPB) has completed
-  // O buffer b (EPI: tile parity) has been read out of tensor memory
+  // O buffer b has been read out of tensor memory
   uint64_t o_free[C::NOB];
   // EPI: the tile's last P V into O buffer b has completed; its rows' row
-  // sums and reference maximum are in ostat[b]
+  // sums and reference maxima are in ostat[b]
   uint64_t o_done[C::NOB], stats_full[C::NOB];
-  // EPI: per row, the two key halves' row sums and the reference maximum
-  float ostat[C::NOB][3][C::EPI ? BM : 1];
+  // EPI: per row, the key halves' row sums [0, NHALF) and reference maxima
+  // [NHALF, 2 NHALF)
+  float ostat[C::NOB][2 * C::NHALF][C::EPI ? BM : 1];
   // EPI: kv_len staged at the start (batches up to kKvlCache)
   int kvl[C::EPI ? kKvlCache : 1];
   uint64_t mma_done, pv_mma_done;
-  // NHALF = 2: the warp pairs' barriers and exchanged partial maxima / sums;
-  // in its n-th exchange the warp of half h writes slot h ^ (n & 1) of its
-  // row and reads the other, so it only overwrites the value it has just read
-  uint64_t pair_bar[4];
-  float xch[C::NHALF == 2 ? 2 : 1][C::NHALF == 2 ? BM : 1];
   // a block mask without a host copy: the tiles' costs, then their
   // cost-sorted order (fa_order.cuh)
   uint32_t order[kFwdOrderMaxT];
@@ -401,13 +401,12 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
       mbar_init(&sm.s_free[b], 4);
     }
     for (int b = 0; b < C::NPB; ++b) {
-      mbar_init(&sm.p_full[b], 4 * C::NHALF);
+      for (int h = 0; h < C::NHALF; ++h) mbar_init(&sm.p_full[b * C::NHALF + h], 4);
       mbar_init(&sm.pv_done[b], 1);
     }
-    for (int q = 0; q < 4; ++q) mbar_init(&sm.pair_bar[q], 64);
     mbar_init(&sm.pv_mma_done, 1);
     for (int b = 0; b < C::NOB; ++b) {
-      mbar_init(&sm.o_free[b], C::EPI ? 4 : 4 * C::NHALF);
+      mbar_init(&sm.o_free[b], 4);
       mbar_init(&sm.o_done[b], 1);
       mbar_init(&sm.stats_full[b], 32 * 4 * C::NHALF);
     }
@@ -652,11 +651,6 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           if (nkv == 0) continue;
           for (int j = 0; j < nkv; ++j, ++g) {
             const uint32_t b = g % C::NPB;
-            if (!mbar_wait_warp(&sm.p_full[b], (g / C::NPB) & 1, abort, kWaitTimeoutNs)) {
-              issuer_fail(p.status, abort, lane, kSiteMmaP);
-              ok = false;
-              break;
-            }
             const int st = g % C::STAGES;
             if (!mbar_wait_warp(&sm.v_full[st], (g / C::STAGES) & 1, abort, kWaitTimeoutNs)) {
               issuer_fail(p.status, abort, lane, kSiteMmaV);
@@ -672,27 +666,44 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
               ok = false;
               break;
             }
-            tc_fence_after_sync();
-            if constexpr (FP8) {
-              // transposed V block: D rows x 128 keys, the K-major B operand;
-              // P as E4M3, four keys a tensor-memory column, 32 keys a step
-              const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), 16, 1024);
+            // each key half's product as soon as its P is written, into the
+            // half's own part of O (NHALF = 2)
 #pragma unroll
-              for (int kk = 0; kk < BN / 32; ++kk)
-                mma_e4m3_ts_w(tmem + C::TM_O, tmem + C::TM_P + C::P_STRIDE * b + kk * 8,
-                              dv0 + static_cast<uint64_t>((kk * 32) >> 4), kIdescPV,
-                              (j == 0 && kk == 0) ? 0u : 1u);
-            } else {
-              // V block: BN rows (keys) x D columns, MN-major B operand: 64-column
-              // chunks BN*128 bytes apart (LBO), 8-key groups 1024 bytes apart (SBO).
-              const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), BN * 128, 1024);
+            for (int h = 0; h < C::NHALF; ++h) {
+              if (!mbar_wait_warp(&sm.p_full[b * C::NHALF + h], (g / C::NPB) & 1, abort,
+                                  kWaitTimeoutNs)) {
+                issuer_fail(p.status, abort, lane, kSiteMmaP);
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
+              const uint32_t d_o = tmem + C::TM_O + C::OCOLS * ob + D * h;
+              if constexpr (FP8) {
+                // transposed V block: D rows x 128 keys, the K-major B operand;
+                // P as E4M3, four keys a tensor-memory column, 32 keys a step
+                const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), 16, 1024);
 #pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk) {
-                mma_bf16_ts_w(tmem + C::TM_O + D * ob, tmem + C::TM_P + C::P_STRIDE * b + kk * 8,
-                            dv0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescPV,
-                            (j == 0 && kk == 0) ? 0u : 1u);
+                for (int kk = 0; kk < BN / 32; ++kk)
+                  mma_e4m3_ts_w(d_o, tmem + C::TM_P + C::P_STRIDE * b + kk * 8,
+                                dv0 + static_cast<uint64_t>((kk * 32) >> 4), kIdescPV,
+                                (j == 0 && kk == 0) ? 0u : 1u);
+              } else {
+                // V block: BN rows (keys) x D columns, MN-major B operand: 64-column
+                // chunks BN*128 bytes apart (LBO), 8-key groups 1024 bytes apart
+                // (SBO); half h takes the 16-key steps [h KH, (h + 1) KH), its P
+                // at the start of its S columns (BN / NHALF) h
+                constexpr int KH = BN / 16 / C::NHALF;
+                const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), BN * 128, 1024);
+#pragma unroll
+                for (int k = 0; k < KH; ++k) {
+                  const int kk = h * KH + k;
+                  mma_bf16_ts_w(d_o, tmem + C::TM_P + C::P_STRIDE * b + (BN / C::NHALF) * h + k * 8,
+                                dv0 + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescPV,
+                                (j == 0 && k == 0) ? 0u : 1u);
+                }
               }
             }
+            if (!ok) break;
             mma_commit_w(&sm.v_empty[st]);
             mma_commit_w(&sm.pv_done[b]);
             if (C::EPI && j == nkv - 1) mma_commit_w(&sm.o_done[ob]);
@@ -745,40 +756,64 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
         break;
       }
       tc_fence_after_sync();
-      const float l = sm.ostat[ob][0][row_local] + sm.ostat[ob][1][row_local];
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const float lse_row =
-          l > 0.f ? (sm.ostat[ob][2][row_local] + log2f(l)) * 0.69314718055994531f : -INFINITY;
-      uint32_t orr[D];
+      // merge the key halves: each half h holds O_h and l_h relative to its
+      // own reference maximum m_h; relative to m = max_h m_h they weigh
+      // a_h = 2^(m_h - m), so O = sum_h a_h O_h / l with l = sum_h a_h l_h
+      float a[C::NHALF], m = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld_x32(t_lane + C::TM_O + D * ob + 32 * c, orr + 32 * c);
-      tmem_wait_ld();
-      reg_fence<D>(orr);
-      // O buffer ob (and ostat[ob]) may now take the tile two ahead
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.o_free[ob]);
-      if (row_valid) {
+      for (int h = 0; h < C::NHALF; ++h) m = fmaxf(m, sm.ostat[ob][C::NHALF + h][row_local]);
+      float l = 0.f;
+#pragma unroll
+      for (int h = 0; h < C::NHALF; ++h) {
+        const float mh = sm.ostat[ob][C::NHALF + h][row_local];
+        a[h] = mh == -INFINITY ? 0.f : ex2_approx(mh - m);
+        l += a[h] * sm.ostat[ob][h][row_local];
+      }
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const float lse_row = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+#pragma unroll
+      for (int h = 0; h < C::NHALF; ++h) a[h] *= inv_l;
+      // 32 columns a round: the halves' columns from tensor memory, merged
+      // and stored (O buffer ob, and ostat[ob], are free after the last load)
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t orr[C::NHALF][32];
+#pragma unroll
+        for (int h = 0; h < C::NHALF; ++h)
+          tmem_ld_x32(t_lane + C::TM_O + C::OCOLS * ob + D * h + 32 * c, orr[h]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < C::NHALF; ++h) reg_fence<32>(orr[h]);
+        if (c == D / 32 - 1) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.o_free[ob]);
+        }
+        float o[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          o[e] = __uint_as_float(orr[0][e]) * a[0];
+#pragma unroll
+          for (int h = 1; h < C::NHALF; ++h) o[e] = fmaf(__uint_as_float(orr[h][e]), a[h], o[e]);
+        }
+        if (!row_valid) continue;
         if constexpr (DEC) {
           // the workspace is 256-byte aligned and a row is D floats
-          float* dst = p.o_part + row_off * D;
+          float* dst = p.o_part + row_off * D + 32 * c;
 #pragma unroll
-          for (int i = 0; i < D / 8; ++i) {
+          for (int i = 0; i < 4; ++i) {
             uint32_t r8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) r8[e] = __float_as_uint(__uint_as_float(orr[8 * i + e]) * inv_l);
+            for (int e = 0; e < 8; ++e) r8[e] = __float_as_uint(o[8 * i + e]);
             st_global_v8(dst + 8 * i, r8);
           }
-          p.lse_part[row_off] = lse_row;
         } else {
-          __nv_bfloat16* dst = out + row_off * D;
+          __nv_bfloat16* dst = out + row_off * D + 32 * c;
 #pragma unroll
-          for (int i = 0; i < D / 16; ++i) {                // 16 columns a step
+          for (int i = 0; i < 2; ++i) {                // 16 columns a step
             uint32_t pk8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              pk8[e] = pack_bf16x2(__uint_as_float(orr[16 * i + 2 * e]) * inv_l,
-                                   __uint_as_float(orr[16 * i + 2 * e + 1]) * inv_l);
+            for (int e = 0; e < 8; ++e) pk8[e] = pack_bf16x2(o[16 * i + 2 * e], o[16 * i + 2 * e + 1]);
             if (st32) {
               st_global_v8(dst + 16 * i, pk8);
             } else {
@@ -787,8 +822,13 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
               d4[1] = make_uint4(pk8[4], pk8[5], pk8[6], pk8[7]);
             }
           }
-          p.lse[row_off] = lse_row;
         }
+      }
+      if (row_valid) {
+        if constexpr (DEC)
+          p.lse_part[row_off] = lse_row;
+        else
+          p.lse[row_off] = lse_row;
       }
     }
   } else {
@@ -796,27 +836,15 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
     const int quarter = warp & 3;                  // TMEM lanes 32*quarter .. +31
     const int hf = (warp - 3) >> 2;                // key half (NHALF = 2)
     constexpr int NC = BN / C::NHALF;              // S columns (keys) of this warp
-    constexpr int DO = D / C::NHALF;               // O columns of this warp
+    constexpr int DO = D;                          // O columns of this warp's O part
     const int row_local = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t t_o0 = t_lane + C::TM_O + DO * hf;   // this warp's columns of O buffer 0
+    const uint32_t t_o0 = t_lane + C::TM_O + D * hf;    // this warp's O part in O buffer 0
     uint32_t t_o = t_o0;                                 // ... of the current tile's O buffer
     const float c2 = p.scale_log2;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.o);
-    uint32_t kv_it = 0, hs = 0, e_it = 0;               // e_it: tiles with key blocks
+    uint32_t kv_it = 0, e_it = 0;                       // e_it: tiles with key blocks
     bool ok = true;
-    // NHALF = 2: one exchange with the partner warp (same rows, other keys)
-    auto exchange = [&](float v, float& other) -> bool {
-      const int flip = static_cast<int>(hs & 1);
-      sm.xch[hf ^ flip][row_local] = v;
-      tc_fence_before_sync();
-      mbar_arrive(&sm.pair_bar[quarter]);
-      if (!warp_wait(&sm.pair_bar[quarter], hs & 1, abort)) return false;
-      tc_fence_after_sync();
-      other = sm.xch[hf ^ 1 ^ flip][row_local];
-      ++hs;
-      return true;
-    };
     // The epilogue of a tile (O / l into bf16 O, and LSE): run once the next
     // tile's first block of P is written, so that the softmax warps spend the
     // wait for this tile's last P V on that block instead of idling; the next
@@ -992,18 +1020,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           mx1 = fmax3(mx1, s[NC - 2], s[NC - 1]);
           // this block's multiplier from MMA output to base-2 units of S*scale
           const float cb = FP8 ? c2 * q_sc * __ldg(p.k_scale + t.kvbh * p.nb + jb) : c2;
-          float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cb;
-          if constexpr (C::NHALF == 2) {
-            // the partner's half of the block (it loaded its S before arriving,
-            // so its columns may now take this warp's P)
-            float m_other;
-            if (!exchange(m_blk, m_other)) {
-              if (lane == 0) record_failure(p.status, abort, kSiteSmPair);
-              ok = false;
-              break;
-            }
-            m_blk = fmaxf(m_blk, m_other);
-          }
+          const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cb;
           float alpha = 1.f;
           bool rescale = false;
           if (m_ref == -INFINITY) {
@@ -1057,9 +1074,11 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
             break;
           }
           if constexpr (C::SEP) tc_fence_after_sync();
-          // (NHALF = 2: this warp's keys from column NC / 2 * hf)
+          // (NHALF = 2: this warp's keys at the start of its own S columns,
+          // NC * hf, which only this warp reads: the other half may still be
+          // loading its S)
           constexpr int PCOLS = FP8 ? NC / 4 : NC / 2;
-          const uint32_t t_p = t_lane + C::TM_P + C::P_STRIDE * pb + PCOLS * hf;
+          const uint32_t t_p = t_lane + C::TM_P + C::P_STRIDE * pb + NC * hf;
           tmem_st_x32(t_p, pk);
           if constexpr (PCOLS == 64) tmem_st_x32(t_p + 32, pk + 32);
           if (__any_sync(0xffffffffu, rescale && j > 0)) {
@@ -1098,7 +1117,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           tmem_wait_st();
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.p_full[pb]);
+          if (lane == 0) mbar_arrive(&sm.p_full[pb * C::NHALF + hf]);
           ++kv_it;
           // the previous tile's epilogue, now that this tile's first P is out
           // (bf16; with E4M3 the call in this loop measured 6 % slower on
@@ -1111,21 +1130,11 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
           }
         }
         if (!ok) break;
-        if constexpr (C::NHALF == 2 && !C::EPI) {
-          // the row sum over both halves of the keys
-          float l_other;
-          if (!exchange(l, l_other)) {
-            if (lane == 0) record_failure(p.status, abort, kSiteSmPair);
-            ok = false;
-            break;
-          }
-          l += l_other;
-        }
         if constexpr (C::EPI) {
-          // hand the tile to the epilogue warps: this half's row sum (the
-          // epilogue adds the halves) and the reference maximum, which both
-          // halves share, into ostat[ob] once the epilogue two tiles back has
-          // read that slot (it reads the slot before it frees O buffer ob)
+          // hand the tile to the epilogue warps: this half's row sum and
+          // reference maximum into ostat[ob], once the epilogue of the tile
+          // that last used O buffer ob has read that slot (it reads the slot
+          // before it frees the buffer)
           ++e_it;
           if (!warp_wait(&sm.o_free[ob], (((e_it - 1) / C::NOB) & 1) ^ 1, abort)) {
             if (lane == 0) record_failure(p.status, abort, kSiteSmEpi);
@@ -1133,7 +1142,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
             break;
           }
           sm.ostat[ob][hf][row_local] = l;
-          if (hf == 0) sm.ostat[ob][2][row_local] = m_ref;
+          sm.ostat[ob][C::NHALF + hf][row_local] = m_ref;
           mbar_arrive(&sm.stats_full[ob]);
           continue;
         }
