@@ -32,8 +32,9 @@
 // i.e. key rows for S^T, dP^T, dV, dK and query rows for dQ; its share of a
 // step is queries 32j .. 32j+31 (P^T, dS^T), dQ columns 16j .. 16j+15, and dK,
 // dV columns 16j .. 16j+15.  Per step g a row warp computes P^T(g), then
-// takes its share of dQ(g-1) (complete while P^T(g) was computed) out of
-// tensor memory into the staging, then dS^T(g).
+// dS^T(g) into tensor memory (dK(g) may start), then takes its share of
+// dQ(g-1) out of tensor memory into the staging, and only then copies dS(g)
+// to shared memory, whose single buffer dQ(g-1) was reading.
 // Issuers run converged and one elect.sync lane issues; within one issuer the
 // tensor core keeps issue order.  Every wait is bounded: a wait that gives up
 // records the site in the status word, raises the CTA's abort flag, and the
@@ -69,7 +70,9 @@ struct SSmem {
   alignas(16) float delta[2][SQ];
   uint64_t kv_full, kv_empty;
   uint64_t q_full[2], q_empty[2], do_full[2], do_empty[2];
-  uint64_t s_full, p_full, dv_done, dp_full, ds_full, dk_done, dq_full, dq_free;
+  // ds_tm: dS^T(g) is in tensor memory (dK(g) may start); ds_full: its copy
+  // is in shared memory (dQ(g) may start)
+  uint64_t s_full, p_full, dv_done, dp_full, ds_tm, ds_full, dk_done, dq_full, dq_free;
   uint64_t stg_full[2], stg_free[2];
   uint64_t acc_full, acc_free;
   uint64_t mma_done, mma_done_b;
@@ -147,6 +150,7 @@ __global__ void __launch_bounds__(kSThreads, 1) bwd_d64_kernel(const __grid_cons
     mbar_init(&sm.p_full, kSRowWarps);
     mbar_init(&sm.dv_done, 1);
     mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.ds_tm, kSRowWarps);
     mbar_init(&sm.ds_full, kSRowWarps);
     mbar_init(&sm.dk_done, 1);
     mbar_init(&sm.dq_full, 1);
@@ -339,7 +343,7 @@ __global__ void __launch_bounds__(kSThreads, 1) bwd_d64_kernel(const __grid_cons
                         (first && kk == 0) ? 0u : 1u);
         mma_commit_w(&sm.dv_done);
         // dK += dS^T Q_i
-        if (!mbar_wait_warp(&sm.ds_full, ph, abort, kWaitTimeoutNs)) {
+        if (!mbar_wait_warp(&sm.ds_tm, ph, abort, kWaitTimeoutNs)) {
           fail(kSiteMmaDs);
           break;
         }
@@ -353,8 +357,9 @@ __global__ void __launch_bounds__(kSThreads, 1) bwd_d64_kernel(const __grid_cons
         mma_commit_w(&sm.do_empty[st]);           // B's reads of dO(g) (and the row warps' of D)
         if (last) mma_commit_w(&sm.acc_full);
         // dQ_i = dS K into its own columns once the row warps have taken
-        // dQ(g-1) out of them
-        if (g > 0 && !mbar_wait_warp(&sm.dq_free, (g - 1) & 1, abort, kWaitTimeoutNs)) {
+        // dQ(g-1) out of them and written dS(g) to shared memory
+        if ((g > 0 && !mbar_wait_warp(&sm.dq_free, (g - 1) & 1, abort, kWaitTimeoutNs)) ||
+            !mbar_wait_warp(&sm.ds_full, ph, abort, kWaitTimeoutNs)) {
           fail(kSiteMmaDq);
           break;
         }
@@ -529,13 +534,7 @@ __global__ void __launch_bounds__(kSThreads, 1) bwd_d64_kernel(const __grid_cons
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.p_full);
-        // ---- the previous step's dQ, complete while this P^T was computed;
-        // once it is complete the dS^T buffer is free for this step's copy
-        if (g > 0 && !drain(g - 1)) {
-          ok = false;
-          break;
-        }
-        // ---- dS^T = P^T o (dP^T - D)
+        // ---- dS^T = P^T o (dP^T - D) into tensor memory (for dK)
         if (!warp_wait(&sm.dp_full, ph, abort)) {
           if (lane == 0) record_failure(p.status, abort, kSiteRowDp);
           ok = false;
@@ -543,13 +542,13 @@ __global__ void __launch_bounds__(kSThreads, 1) bwd_d64_kernel(const __grid_cons
         }
         tc_fence_after_sync();
         const uint32_t t_dp = t_lane + TM_DP + 32 * j4;
+        uint32_t dk[16];
         {
           uint32_t sr[32];
           tmem_ld_x32(t_dp, sr);
           tmem_wait_ld();
           reg_fence<32>(sr);
           const float4* d4p = reinterpret_cast<const float4*>(sm.delta[st]) + 8 * j4;
-          uint32_t dk[16];
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
             const float4 d4 = d4p[t];
@@ -566,8 +565,20 @@ __global__ void __launch_bounds__(kSThreads, 1) bwd_d64_kernel(const __grid_cons
             dk[2 * t + 1] = pack_bf16x2(d2, d3);
           }
           tmem_st_x16(t_dp, dk);
-          // row = key r, this quarter's 32 queries = 4 units of 16 bytes in
-          // the 64-query chunk j4 / 2, XOR-swizzled by (r & 7)
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.ds_tm);
+        // ---- the previous step's dQ (once it is complete the shared dS
+        // buffer it read is free for this step's copy)
+        if (g > 0 && !drain(g - 1)) {
+          ok = false;
+          break;
+        }
+        // ---- dS for dQ(g): row = key r, this quarter's 32 queries = 4 units
+        // of 16 bytes in the 64-query chunk j4 / 2, XOR-swizzled by (r & 7)
+        {
           uint8_t* rowp = sm.ds + (j4 >> 1) * SCH + r * 128;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -577,8 +588,6 @@ __global__ void __launch_bounds__(kSThreads, 1) bwd_d64_kernel(const __grid_cons
           }
         }
         fence_proxy_async_smem();
-        tmem_wait_st();
-        tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.ds_full);
       }
