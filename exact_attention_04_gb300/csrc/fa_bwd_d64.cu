@@ -172,247 +172,257 @@ __global__ void __launch_bounds__(kSThreads, 1) bwd_d64_kernel(const __grid_cons
   const DtSched sched(p.B * p.H_kv, p.N, p.causal, 1, tail.heads, BS ? p.cost_order : nullptr);
   const int G = p.H / p.H_kv;                     // query heads per K/V head
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // lane 0: K, V and the Q stages (with L2); lane 1: the dO stages (with D)
-    const bool dlane = lane == 1;
-    if (lane < 2) {
-      if (!dlane) {
-        prefetch_tmap(&p.tq);
-        prefetch_tmap(&p.tk);
-        prefetch_tmap(&p.tv);
-      } else {
-        prefetch_tmap(&p.tdo);
+  // Registers: the launch gives every thread 96.  The first warpgroup
+  // (producer, issuers, reduce warp) needs far fewer, and the row warps
+  // spill at 96, so the row warpgroups take what the first one gives back:
+  // 128 x 64 + 512 x 104 = the launch's 640 x 96 = 61,440.
+  static_assert(kSRowWarp0 == 4 && kSRowWarps % 4 == 0, "roles aligned to warpgroups");
+  static_assert(128 * 64 + 32 * kSRowWarps * 104 <= kSThreads * 96, "register split");
+  if (warp < kSRowWarp0) {
+    setmaxnreg_dec<64>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      // lane 0: K, V and the Q stages (with L2); lane 1: the dO stages (with D)
+      const bool dlane = lane == 1;
+      if (lane < 2) {
+        if (!dlane) {
+          prefetch_tmap(&p.tq);
+          prefetch_tmap(&p.tk);
+          prefetch_tmap(&p.tv);
+        } else {
+          prefetch_tmap(&p.tdo);
+        }
+        uint32_t w_it = 0, g = 0;
+        bool ok = true;
+        DtIter it{static_cast<int>(blockIdx.x), 0, 0};
+        for (int kvbh, h, n; ok && sched.next(tail, it, kvbh, h, n);) {
+          const SItem wi = s_item<BS>(p, kvbh, n, G);
+          if (wi.nsteps == 0) continue;
+          if (!dlane) {
+            if (!mbar_wait(&sm.kv_empty, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteProdKV);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sm.kv_full, 2 * SCH);
+            tma_load_3d(sm.k, &p.tk, &sm.kv_full, 0, n * BK, kvbh);
+            tma_load_3d(sm.v, &p.tv, &sm.kv_full, 0, n * BK, kvbh);
+            ++w_it;
+          }
+          StepWalk wk(wi.i0, wi.i1, q_head_of(kvbh, 0, p.H, p.H_kv), wi.sk);
+          for (int s = 0; s < wi.nsteps; ++s, ++g, wk.next()) {
+            const int st = g & 1;
+            const uint32_t ph = ((g >> 1) & 1) ^ 1;
+            const size_t roff = static_cast<size_t>(wk.bh) * p.Npad + static_cast<size_t>(wk.i) * SQ;
+            uint64_t* empty = dlane ? &sm.do_empty[st] : &sm.q_empty[st];
+            uint64_t* full = dlane ? &sm.do_full[st] : &sm.q_full[st];
+            if (!mbar_wait(empty, ph, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, dlane ? kSiteProdDo : kSiteProdQ);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full, SCH + SQ * 4);
+            tma_load_3d(dlane ? sm.dO[st] : sm.q[st], dlane ? &p.tdo : &p.tq, full, 0, wk.i * SQ,
+                        wk.bh);
+            bulk_load(dlane ? sm.delta[st] : sm.lse2[st], (dlane ? p.delta : p.lse2) + roff, SQ * 4,
+                      full);
+          }
+        }
+        // no copy may still be landing in shared memory when the CTA exits
+        if (!dlane && w_it > 0 && !mbar_wait(&sm.kv_full, (w_it - 1) & 1, nullptr, kWaitTimeoutNs))
+          record_failure(p.status, abort, kSiteDtDrain);
+        for (int s = 0; s < 2; ++s) {
+          if (g > static_cast<uint32_t>(s)) {
+            const uint32_t nph = (g - 1 - s) / 2;
+            if (!mbar_wait(dlane ? &sm.do_full[s] : &sm.q_full[s], nph & 1, nullptr, kWaitTimeoutNs))
+              record_failure(p.status, abort, kSiteDtDrain);
+          }
+        }
       }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ issuer A
+      constexpr uint32_t kId = idesc_bf16_f32(BK, SQ, 0, 0);        // S^T, dP^T
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sm.k), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sm.v), 16, 1024);
       uint32_t w_it = 0, g = 0;
       bool ok = true;
       DtIter it{static_cast<int>(blockIdx.x), 0, 0};
       for (int kvbh, h, n; ok && sched.next(tail, it, kvbh, h, n);) {
         const SItem wi = s_item<BS>(p, kvbh, n, G);
         if (wi.nsteps == 0) continue;
-        if (!dlane) {
-          if (!mbar_wait(&sm.kv_empty, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
-            record_failure(p.status, abort, kSiteProdKV);
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&sm.kv_full, 2 * SCH);
-          tma_load_3d(sm.k, &p.tk, &sm.kv_full, 0, n * BK, kvbh);
-          tma_load_3d(sm.v, &p.tv, &sm.kv_full, 0, n * BK, kvbh);
-          ++w_it;
+        if (!mbar_wait_warp(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
+          issuer_fail(p.status, abort, lane, kSiteMmaKV);
+          ok = false;
+          break;
         }
-        StepWalk wk(wi.i0, wi.i1, q_head_of(kvbh, 0, p.H, p.H_kv), wi.sk);
-        for (int s = 0; s < wi.nsteps; ++s, ++g, wk.next()) {
+        for (int s = 0; s < wi.nsteps; ++s, ++g) {
           const int st = g & 1;
-          const uint32_t ph = ((g >> 1) & 1) ^ 1;
-          const size_t roff = static_cast<size_t>(wk.bh) * p.Npad + static_cast<size_t>(wk.i) * SQ;
-          uint64_t* empty = dlane ? &sm.do_empty[st] : &sm.q_empty[st];
-          uint64_t* full = dlane ? &sm.do_full[st] : &sm.q_full[st];
-          if (!mbar_wait(empty, ph, abort, kWaitTimeoutNs)) {
-            record_failure(p.status, abort, dlane ? kSiteProdDo : kSiteProdQ);
+          // S^T(g) into the S buffer once dV(g-1) has read P^T(g-1) out of it
+          if (g > 0 && !mbar_wait_warp(&sm.dv_done, (g - 1) & 1, abort, kWaitTimeoutNs)) {
+            issuer_fail(p.status, abort, lane, kSiteMmaP);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full, SCH + SQ * 4);
-          tma_load_3d(dlane ? sm.dO[st] : sm.q[st], dlane ? &p.tdo : &p.tq, full, 0, wk.i * SQ,
-                      wk.bh);
-          bulk_load(dlane ? sm.delta[st] : sm.lse2[st], (dlane ? p.delta : p.lse2) + roff, SQ * 4,
-                    full);
+          if (!mbar_wait_warp(&sm.q_full[st], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
+            issuer_fail(p.status, abort, lane, kSiteMmaQ);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t dq = sdesc_sw128(smem_u32(sm.q[st]), 16, 1024);
+  #pragma unroll
+          for (int kk = 0; kk < SD / 16; ++kk)
+            mma_bf16_ss_w(tmem + TM_S, dK0 + ((kk * 32) >> 4), dq + ((kk * 32) >> 4), kId,
+                          kk > 0 ? 1u : 0u);
+          mma_commit_w(&sm.s_full);
+          mma_commit_w(&sm.q_empty[st]);
+          // dP^T(g) into the dP buffer once dK(g-1) has read dS^T(g-1) out of it
+          if (g > 0 && !mbar_wait_warp(&sm.dk_done, (g - 1) & 1, abort, kWaitTimeoutNs)) {
+            issuer_fail(p.status, abort, lane, kSiteMmaDs);
+            ok = false;
+            break;
+          }
+          if (!mbar_wait_warp(&sm.do_full[st], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
+            issuer_fail(p.status, abort, lane, kSiteMmaDo);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t ddo = sdesc_sw128(smem_u32(sm.dO[st]), 16, 1024);
+  #pragma unroll
+          for (int kk = 0; kk < SD / 16; ++kk)
+            mma_bf16_ss_w(tmem + TM_DP, dV0 + ((kk * 32) >> 4), ddo + ((kk * 32) >> 4), kId,
+                          kk > 0 ? 1u : 0u);
+          mma_commit_w(&sm.dp_full);
+          mma_commit_w(&sm.do_empty[st]);
         }
+        if (!ok) break;
+        mma_commit_w(&sm.kv_empty);                 // A's reads of K and V are done
+        ++w_it;
       }
-      // no copy may still be landing in shared memory when the CTA exits
-      if (!dlane && w_it > 0 && !mbar_wait(&sm.kv_full, (w_it - 1) & 1, nullptr, kWaitTimeoutNs))
-        record_failure(p.status, abort, kSiteDtDrain);
-      for (int s = 0; s < 2; ++s) {
-        if (g > static_cast<uint32_t>(s)) {
-          const uint32_t nph = (g - 1 - s) / 2;
-          if (!mbar_wait(dlane ? &sm.do_full[s] : &sm.q_full[s], nph & 1, nullptr, kWaitTimeoutNs))
-            record_failure(p.status, abort, kSiteDtDrain);
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ issuer A
-    constexpr uint32_t kId = idesc_bf16_f32(BK, SQ, 0, 0);        // S^T, dP^T
-    const uint64_t dK0 = sdesc_sw128(smem_u32(sm.k), 16, 1024);
-    const uint64_t dV0 = sdesc_sw128(smem_u32(sm.v), 16, 1024);
-    uint32_t w_it = 0, g = 0;
-    bool ok = true;
-    DtIter it{static_cast<int>(blockIdx.x), 0, 0};
-    for (int kvbh, h, n; ok && sched.next(tail, it, kvbh, h, n);) {
-      const SItem wi = s_item<BS>(p, kvbh, n, G);
-      if (wi.nsteps == 0) continue;
-      if (!mbar_wait_warp(&sm.kv_full, w_it & 1, abort, kWaitTimeoutNs)) {
-        issuer_fail(p.status, abort, lane, kSiteMmaKV);
-        ok = false;
-        break;
-      }
-      for (int s = 0; s < wi.nsteps; ++s, ++g) {
-        const int st = g & 1;
-        // S^T(g) into the S buffer once dV(g-1) has read P^T(g-1) out of it
-        if (g > 0 && !mbar_wait_warp(&sm.dv_done, (g - 1) & 1, abort, kWaitTimeoutNs)) {
-          issuer_fail(p.status, abort, lane, kSiteMmaP);
-          ok = false;
-          break;
-        }
-        if (!mbar_wait_warp(&sm.q_full[st], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
-          issuer_fail(p.status, abort, lane, kSiteMmaQ);
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint64_t dq = sdesc_sw128(smem_u32(sm.q[st]), 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < SD / 16; ++kk)
-          mma_bf16_ss_w(tmem + TM_S, dK0 + ((kk * 32) >> 4), dq + ((kk * 32) >> 4), kId,
-                        kk > 0 ? 1u : 0u);
-        mma_commit_w(&sm.s_full);
-        mma_commit_w(&sm.q_empty[st]);
-        // dP^T(g) into the dP buffer once dK(g-1) has read dS^T(g-1) out of it
-        if (g > 0 && !mbar_wait_warp(&sm.dk_done, (g - 1) & 1, abort, kWaitTimeoutNs)) {
-          issuer_fail(p.status, abort, lane, kSiteMmaDs);
-          ok = false;
-          break;
-        }
-        if (!mbar_wait_warp(&sm.do_full[st], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
-          issuer_fail(p.status, abort, lane, kSiteMmaDo);
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint64_t ddo = sdesc_sw128(smem_u32(sm.dO[st]), 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < SD / 16; ++kk)
-          mma_bf16_ss_w(tmem + TM_DP, dV0 + ((kk * 32) >> 4), ddo + ((kk * 32) >> 4), kId,
-                        kk > 0 ? 1u : 0u);
-        mma_commit_w(&sm.dp_full);
-        mma_commit_w(&sm.do_empty[st]);
-      }
-      if (!ok) break;
-      mma_commit_w(&sm.kv_empty);                 // A's reads of K and V are done
-      ++w_it;
-    }
-    // every tcgen05 op issued by this thread must finish before exit
-    mma_commit_w(&sm.mma_done);
-    if (!mbar_wait_warp(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
-      issuer_fail(p.status, abort, lane, kSiteDtDrain);
-    __syncwarp();
-  } else if (warp == 2) {
-    // ------------------------------------------------------------ issuer B
-    constexpr uint32_t kIdAcc = idesc_bf16_f32(BK, SD, 0, 1);     // dV, dK (B MN-major)
-    constexpr uint32_t kIdDq = idesc_bf16_f32(SQ, SD, 1, 1);      // dQ (A, B MN-major)
-    // dS^T as the MN-major A operand of dQ (64-query chunks SCH apart), K as
-    // its MN-major B operand
-    const uint64_t dDS = sdesc_sw128(smem_u32(sm.ds), SCH, 1024);
-    const uint64_t dKmn = sdesc_sw128(smem_u32(sm.k), SCH, 1024);
-    uint32_t w_it = 0, g = 0;
-    bool ok = true;
-    auto fail = [&](int site) {
-      issuer_fail(p.status, abort, lane, site);
-      ok = false;
-    };
-    DtIter it{static_cast<int>(blockIdx.x), 0, 0};
-    for (int kvbh, h, n; ok && sched.next(tail, it, kvbh, h, n);) {
-      const SItem wi = s_item<BS>(p, kvbh, n, G);
-      if (wi.nsteps == 0) continue;
-      for (int s = 0; s < wi.nsteps; ++s, ++g) {
-        const int st = g & 1;
-        const uint32_t ph = g & 1;
-        const bool first = (s == 0);
-        const bool last = (s + 1 == wi.nsteps);
-        // dV += P^T dO_i
-        if (!mbar_wait_warp(&sm.p_full, ph, abort, kWaitTimeoutNs)) {
-          fail(kSiteMmaP);
-          break;
-        }
-        if (first && !mbar_wait_warp(&sm.acc_free, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
-          fail(kSiteMmaAcc);
-          break;
-        }
-        if (!mbar_wait_warp(&sm.do_full[st], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
-          fail(kSiteMmaDo);
-          break;
-        }
-        tc_fence_after_sync();
-        const uint64_t dOmn = sdesc_sw128(smem_u32(sm.dO[st]), SCH, 1024);
-        const uint64_t dQmn = sdesc_sw128(smem_u32(sm.q[st]), SCH, 1024);
-#pragma unroll
-        for (int kk = 0; kk < SQ / 16; ++kk)
-          mma_bf16_ts_w(tmem + TM_DV, tmem + TM_S + scol(kk), dOmn + ((kk * 2048) >> 4), kIdAcc,
-                        (first && kk == 0) ? 0u : 1u);
-        mma_commit_w(&sm.dv_done);
-        // dK += dS^T Q_i
-        if (!mbar_wait_warp(&sm.ds_tm, ph, abort, kWaitTimeoutNs)) {
-          fail(kSiteMmaDs);
-          break;
-        }
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < SQ / 16; ++kk)
-          mma_bf16_ts_w(tmem + TM_DK, tmem + TM_DP + scol(kk), dQmn + ((kk * 2048) >> 4), kIdAcc,
-                        (first && kk == 0) ? 0u : 1u);
-        mma_commit_w(&sm.dk_done);
-        mma_commit_w(&sm.q_empty[st]);            // B's reads of Q(g) (and the row warps' of L2)
-        mma_commit_w(&sm.do_empty[st]);           // B's reads of dO(g) (and the row warps' of D)
-        if (last) mma_commit_w(&sm.acc_full);
-        // dQ_i = dS K into its own columns once the row warps have taken
-        // dQ(g-1) out of them and written dS(g) to shared memory
-        if ((g > 0 && !mbar_wait_warp(&sm.dq_free, (g - 1) & 1, abort, kWaitTimeoutNs)) ||
-            !mbar_wait_warp(&sm.ds_full, ph, abort, kWaitTimeoutNs)) {
-          fail(kSiteMmaDq);
-          break;
-        }
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_bf16_ss_w(tmem + TM_DQ, dDS + ((kk * 2048) >> 4), dKmn + ((kk * 2048) >> 4), kIdDq,
-                        kk > 0 ? 1u : 0u);
-        mma_commit_w(&sm.dq_full);
-        if (last) mma_commit_w(&sm.kv_empty);     // B's reads of K are done
-      }
-      if (!ok) break;
-      ++w_it;
-    }
-    mma_commit_w(&sm.mma_done_b);
-    if (!mbar_wait_warp(&sm.mma_done_b, 0, nullptr, kWaitTimeoutNs))
-      issuer_fail(p.status, abort, lane, kSiteDtDrain);
-    __syncwarp();
-  } else if (warp == 3) {
-    // ------------------------------------------------------------ reduce warp
-    // Adds each step's staged dQ to the accumulator with two bulk tensor
-    // reduce-adds, and frees the previous step's buffer once its reduce-adds
-    // have read it (so two steps' reduce-adds can be in flight).
-    if (lane == 0) {
-      prefetch_tmap(&p.tdq);
-      uint32_t g = 0;
+      // every tcgen05 op issued by this thread must finish before exit
+      mma_commit_w(&sm.mma_done);
+      if (!mbar_wait_warp(&sm.mma_done, 0, nullptr, kWaitTimeoutNs))
+        issuer_fail(p.status, abort, lane, kSiteDtDrain);
+      __syncwarp();
+    } else if (warp == 2) {
+      // ------------------------------------------------------------ issuer B
+      constexpr uint32_t kIdAcc = idesc_bf16_f32(BK, SD, 0, 1);     // dV, dK (B MN-major)
+      constexpr uint32_t kIdDq = idesc_bf16_f32(SQ, SD, 1, 1);      // dQ (A, B MN-major)
+      // dS^T as the MN-major A operand of dQ (64-query chunks SCH apart), K as
+      // its MN-major B operand
+      const uint64_t dDS = sdesc_sw128(smem_u32(sm.ds), SCH, 1024);
+      const uint64_t dKmn = sdesc_sw128(smem_u32(sm.k), SCH, 1024);
+      uint32_t w_it = 0, g = 0;
       bool ok = true;
+      auto fail = [&](int site) {
+        issuer_fail(p.status, abort, lane, site);
+        ok = false;
+      };
       DtIter it{static_cast<int>(blockIdx.x), 0, 0};
       for (int kvbh, h, n; ok && sched.next(tail, it, kvbh, h, n);) {
         const SItem wi = s_item<BS>(p, kvbh, n, G);
-        StepWalk wk(wi.i0, wi.i1, q_head_of(kvbh, 0, p.H, p.H_kv), wi.sk);
-        for (int s = 0; s < wi.nsteps; ++s, ++g, wk.next()) {
-          const int b = g & 1;
-          if (!mbar_wait(&sm.stg_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
-            record_failure(p.status, abort, kSiteStageFull);
-            ok = false;
+        if (wi.nsteps == 0) continue;
+        for (int s = 0; s < wi.nsteps; ++s, ++g) {
+          const int st = g & 1;
+          const uint32_t ph = g & 1;
+          const bool first = (s == 0);
+          const bool last = (s + 1 == wi.nsteps);
+          // dV += P^T dO_i
+          if (!mbar_wait_warp(&sm.p_full, ph, abort, kWaitTimeoutNs)) {
+            fail(kSiteMmaP);
             break;
           }
-          // rows (queries) past N land in the padding up to Npad, never read
-          tma_reduce_add_3d(&p.tdq, sm.stage[b], 0, wk.i * SQ, wk.bh);
-          tma_reduce_add_3d(&p.tdq, sm.stage[b] + SCH, 32, wk.i * SQ, wk.bh);
-          bulk_commit_group();
-          if (g > 0) {
-            bulk_wait_group_read<1>();
-            mbar_arrive(&sm.stg_free[b ^ 1]);
+          if (first && !mbar_wait_warp(&sm.acc_free, (w_it & 1) ^ 1, abort, kWaitTimeoutNs)) {
+            fail(kSiteMmaAcc);
+            break;
+          }
+          if (!mbar_wait_warp(&sm.do_full[st], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
+            fail(kSiteMmaDo);
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t dOmn = sdesc_sw128(smem_u32(sm.dO[st]), SCH, 1024);
+          const uint64_t dQmn = sdesc_sw128(smem_u32(sm.q[st]), SCH, 1024);
+  #pragma unroll
+          for (int kk = 0; kk < SQ / 16; ++kk)
+            mma_bf16_ts_w(tmem + TM_DV, tmem + TM_S + scol(kk), dOmn + ((kk * 2048) >> 4), kIdAcc,
+                          (first && kk == 0) ? 0u : 1u);
+          mma_commit_w(&sm.dv_done);
+          // dK += dS^T Q_i
+          if (!mbar_wait_warp(&sm.ds_tm, ph, abort, kWaitTimeoutNs)) {
+            fail(kSiteMmaDs);
+            break;
+          }
+          tc_fence_after_sync();
+  #pragma unroll
+          for (int kk = 0; kk < SQ / 16; ++kk)
+            mma_bf16_ts_w(tmem + TM_DK, tmem + TM_DP + scol(kk), dQmn + ((kk * 2048) >> 4), kIdAcc,
+                          (first && kk == 0) ? 0u : 1u);
+          mma_commit_w(&sm.dk_done);
+          mma_commit_w(&sm.q_empty[st]);            // B's reads of Q(g) (and the row warps' of L2)
+          mma_commit_w(&sm.do_empty[st]);           // B's reads of dO(g) (and the row warps' of D)
+          if (last) mma_commit_w(&sm.acc_full);
+          // dQ_i = dS K into its own columns once the row warps have taken
+          // dQ(g-1) out of them and written dS(g) to shared memory
+          if ((g > 0 && !mbar_wait_warp(&sm.dq_free, (g - 1) & 1, abort, kWaitTimeoutNs)) ||
+              !mbar_wait_warp(&sm.ds_full, ph, abort, kWaitTimeoutNs)) {
+            fail(kSiteMmaDq);
+            break;
+          }
+          tc_fence_after_sync();
+  #pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            mma_bf16_ss_w(tmem + TM_DQ, dDS + ((kk * 2048) >> 4), dKmn + ((kk * 2048) >> 4), kIdDq,
+                          kk > 0 ? 1u : 0u);
+          mma_commit_w(&sm.dq_full);
+          if (last) mma_commit_w(&sm.kv_empty);     // B's reads of K are done
+        }
+        if (!ok) break;
+        ++w_it;
+      }
+      mma_commit_w(&sm.mma_done_b);
+      if (!mbar_wait_warp(&sm.mma_done_b, 0, nullptr, kWaitTimeoutNs))
+        issuer_fail(p.status, abort, lane, kSiteDtDrain);
+      __syncwarp();
+    } else {
+      // ------------------------------------------------------------ reduce warp
+      // Adds each step's staged dQ to the accumulator with two bulk tensor
+      // reduce-adds, and frees the previous step's buffer once its reduce-adds
+      // have read it (so two steps' reduce-adds can be in flight).
+      if (lane == 0) {
+        prefetch_tmap(&p.tdq);
+        uint32_t g = 0;
+        bool ok = true;
+        DtIter it{static_cast<int>(blockIdx.x), 0, 0};
+        for (int kvbh, h, n; ok && sched.next(tail, it, kvbh, h, n);) {
+          const SItem wi = s_item<BS>(p, kvbh, n, G);
+          StepWalk wk(wi.i0, wi.i1, q_head_of(kvbh, 0, p.H, p.H_kv), wi.sk);
+          for (int s = 0; s < wi.nsteps; ++s, ++g, wk.next()) {
+            const int b = g & 1;
+            if (!mbar_wait(&sm.stg_full[b], (g >> 1) & 1, abort, kWaitTimeoutNs)) {
+              record_failure(p.status, abort, kSiteStageFull);
+              ok = false;
+              break;
+            }
+            // rows (queries) past N land in the padding up to Npad, never read
+            tma_reduce_add_3d(&p.tdq, sm.stage[b], 0, wk.i * SQ, wk.bh);
+            tma_reduce_add_3d(&p.tdq, sm.stage[b] + SCH, 32, wk.i * SQ, wk.bh);
+            bulk_commit_group();
+            if (g > 0) {
+              bulk_wait_group_read<1>();
+              mbar_arrive(&sm.stg_free[b ^ 1]);
+            }
           }
         }
+        // every reduce-add must have landed before the CTA exits
+        bulk_wait_group<0>();
       }
-      // every reduce-add must have landed before the CTA exits
-      bulk_wait_group<0>();
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    setmaxnreg_inc<104>();
     // ------------------------------------------------------------ row warps
     const int quarter = warp & 3;
     const int j4 = (warp - kSRowWarp0) >> 2;

@@ -101,6 +101,18 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Warpgroup register reallocation: every warp of a warpgroup executes the
+// same instruction, and the code it dominates is compiled to N registers a
+// thread.  An increase draws on the registers the block was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ dependent launch
 
 // Programmatic dependent launch: once every CTA of this grid has executed
