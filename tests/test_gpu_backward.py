@@ -120,5 +120,31 @@ def test_padding_lengths_one_to_n_every_head(d):
     P.compare_backward(w, inp, P.gpu_backward(w, g, o, lse))
 
 
+@pytest.mark.parametrize("d,B,H,N,causal,kv,mask", [
+    (64, 2, 4, 384, True, None, False), (64, 16, 16, 512, False, (256, 512), False),
+    (64, 2, 8, 4096, False, None, True), (128, 2, 4, 2048, True, None, False),
+    (256, 1, 4, 1024, True, None, False)])
+def test_backward_is_deterministic(d, B, H, N, causal, kv, mask):
+    """Reruns on the same inputs: dK and dV are each accumulated in tensor
+    memory by one CTA, so they must agree bit for bit; dQ is summed across
+    key blocks in L2 in an order that varies, so within a bf16 unit.  A race
+    between the kernels' warps (the d = 64 kernel runs its warpgroups at
+    different register counts) would show as bits that change between
+    runs."""
+    from exact_attention_04_gb300.workloads import block_sparse_mask
+    w = random_case(B, H, N, d, seed=N + d, causal=causal, kv_len_range=kv)
+    g = P.to_gpu(make_inputs(w))
+    bm = torch.from_numpy(block_sparse_mask(-(-N // 128), seed=3)).cuda() if mask else None
+    o, lse = fa.forward(g["q"], g["k"], g["v"], scale=w.scale, causal=causal, kv_len=g["kv_len"],
+                        block_mask=bm)
+    runs = [fa.backward(g["q"], g["k"], g["v"], o, lse, g["do"], scale=w.scale, causal=causal,
+                        kv_len=g["kv_len"], block_mask=bm) for _ in range(6)]
+    fa.fa_check()
+    dq0, dk0, dv0 = runs[0]
+    for dq, dk, dv in runs[1:]:
+        assert torch.equal(dk, dk0) and torch.equal(dv, dv0)
+        assert (dq.float() - dq0.float()).abs().max().item() <= 2 ** -7 * dq0.float().abs().max().item()
+
+
 def test_status_clean_after_runs():
     fa.fa_check()
