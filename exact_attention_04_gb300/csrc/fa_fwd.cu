@@ -99,7 +99,10 @@ struct Cfg {
   static constexpr bool SEP = (D == 256 && !FP8);
   // NSB S buffers: block g uses columns [128*(g%NSB), +128).  NPB P buffers
   // (without SEP, P buffer b is the start of S buffer b).
-  static constexpr int NSB = SEP ? 1 : (D <= 128 ? 3 : 2);
+  // (E4M3 at d = 128 takes the key-half split below with two S buffers, so
+  // that its two 128-column O parts fit.)
+  static constexpr bool F8SPLIT = FP8 && D == 128;
+  static constexpr int NSB = SEP ? 1 : (F8SPLIT ? 2 : (D <= 128 ? 3 : 2));
   static constexpr int NPB = SEP ? 2 : NSB;
   static constexpr int PW = FP8 ? BN / 4 : BN / 2;   // columns of one block's P
   static constexpr uint32_t TM_S = 0;
@@ -109,17 +112,19 @@ struct Cfg {
   static constexpr uint32_t TM_COLS = 512;
   static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
   // NHALF softmax warps per sub-partition, each taking BN / NHALF keys of a
-  // block.  At d = 64 the products of a block take a quarter of the time the
-  // softmax of one warp does, so two warps share each row, each with a
-  // running maximum, row sum and O accumulator of its own over its half of
-  // the keys (O in NHALF parts of D columns, merged by the epilogue).  The
-  // two warps of a sub-partition never wait for each other, so one computes
-  // while the other waits for tensor memory; elsewhere one warp a row.
-  static constexpr int NHALF = (D == 64 && !FP8) ? 2 : 1;
+  // block.  At bf16 d = 64 and E4M3 d = 128 the products of a block take a
+  // fraction of the time the softmax of one warp does, so two warps share
+  // each row, each with a running maximum, row sum and O accumulator of its
+  // own over its half of the keys (O in NHALF parts of D columns, merged by
+  // the epilogue).  The two warps of a sub-partition never wait for each
+  // other, so one computes while the other waits (for tensor memory, on a
+  // barrier); elsewhere one warp a row.
+  static constexpr int NHALF = ((D == 64 && !FP8) || F8SPLIT) ? 2 : 1;
   static constexpr int OCOLS = D * NHALF;            // columns of O (its key halves)
-  // EPI (d = 64): four epilogue warps merge each tile's O halves, divide by
-  // l, store bf16 O and LSE, off the softmax warps, whose time per tile the
-  // epilogue was a large share of at the few key blocks of short sequences.
+  // EPI (with the split): four epilogue warps merge each tile's O halves,
+  // divide by l, store bf16 O and LSE, off the softmax warps (whose time per
+  // tile the epilogue was a large share of at the few key blocks of short
+  // sequences).
   static constexpr bool EPI = NHALF == 2;
   static constexpr int NOB = 1;                      // O buffers
   static constexpr int EPI_WARP0 = 3 + 4 * NHALF;    // first epilogue warp
@@ -151,7 +156,7 @@ struct FwdSmem {
   // [NHALF, 2 NHALF)
   float ostat[C::NOB][2 * C::NHALF][C::EPI ? BM : 1];
   // EPI: kv_len staged at the start (batches up to kKvlCache)
-  int kvl[C::EPI ? kKvlCache : 1];
+  int kvl[C::EPI && D == 64 ? kKvlCache : 1];
   uint64_t mma_done, pv_mma_done;
   // a block mask without a host copy: the tiles' costs, then their
   // cost-sorted order (fa_order.cuh)
@@ -418,7 +423,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
     tmem_relinquish();
   }
   // (EPI) every tile's setup reads its batch entry's kv_len: stage them once
-  if constexpr (C::EPI) {
+  if constexpr (C::EPI && D == 64) {
     if (p.kv_len && p.B <= kKvlCache)
       for (int b = threadIdx.x; b < p.B; b += C::THREADS) sm.kvl[b] = __ldg(p.kv_len + b);
   }
@@ -452,7 +457,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
   const int BH = p.B * p.H;
   const Sched sched(BH, p.N, p.causal, DEC ? 0 : tail.heads,
                     (BS && !DEC && p.cost_sorted) ? sm.order : nullptr,
-                    (C::EPI && p.kv_len && p.B <= kKvlCache) ? sm.kvl : nullptr);
+                    (C::EPI && D == 64 && p.kv_len && p.B <= kKvlCache) ? sm.kvl : nullptr);
   const int nunits = DEC ? p.B * p.H_kv * p.splits : sched.units;
 
   if (warp == 0) {
@@ -680,13 +685,18 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
               const uint32_t d_o = tmem + C::TM_O + C::OCOLS * ob + D * h;
               if constexpr (FP8) {
                 // transposed V block: D rows x 128 keys, the K-major B operand;
-                // P as E4M3, four keys a tensor-memory column, 32 keys a step
+                // P as E4M3, four keys a tensor-memory column, 32 keys a step;
+                // half h takes the steps [h KH8, (h + 1) KH8), its P at the
+                // start of its S columns (BN / NHALF) h
+                constexpr int KH8 = BN / 32 / C::NHALF;
                 const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[st]), 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < BN / 32; ++kk)
-                  mma_e4m3_ts_w(d_o, tmem + C::TM_P + C::P_STRIDE * b + kk * 8,
+                for (int k = 0; k < KH8; ++k) {
+                  const int kk = h * KH8 + k;
+                  mma_e4m3_ts_w(d_o, tmem + C::TM_P + C::P_STRIDE * b + (BN / C::NHALF) * h + k * 8,
                                 dv0 + static_cast<uint64_t>((kk * 32) >> 4), kIdescPV,
-                                (j == 0 && kk == 0) ? 0u : 1u);
+                                (j == 0 && k == 0) ? 0u : 1u);
+                }
               } else {
                 // V block: BN rows (keys) x D columns, MN-major B operand: 64-column
                 // chunks BN*128 bytes apart (LBO), 8-key groups 1024 bytes apart
@@ -769,8 +779,11 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
         a[h] = mh == -INFINITY ? 0.f : ex2_approx(mh - m);
         l += a[h] * sm.ostat[ob][h][row_local];
       }
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const float lse_row = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      // FP8: P entered the product as 16 P (and l sums 16 P), V in units of
+      // its head scale
+      const float inv_l = l > 0.f ? (FP8 ? __ldg(p.v_scale + t.kvbh) / l : 1.f / l) : 0.f;
+      const float lse_row =
+          l > 0.f ? (m + (log2f(l) - (FP8 ? kFp8Shift : 0.f))) * 0.69314718055994531f : -INFINITY;
 #pragma unroll
       for (int h = 0; h < C::NHALF; ++h) a[h] *= inv_l;
       // 32 columns a round: the halves' columns from tensor memory, merged
@@ -1093,7 +1106,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
             tc_fence_after_sync();
             // this warp's columns of O, up to 128 per round trip (S is no
             // longer live), scaled two at a time
-            constexpr int RC = DO < 128 ? DO / 32 : 4;
+            constexpr int RC = DO < 128 ? DO / 32 : (C::NHALF == 2 ? 1 : 4);
             const uint64_t a2 = f2_make(alpha, alpha);
 #pragma unroll 1
             for (int c0 = 0; c0 < DO / 32; c0 += RC) {
