@@ -103,6 +103,9 @@ WORKLOADS = {w.name: w for w in [
     Workload("gpt2_small_b8_h12_n1024_d64_causal", 8, 12, 1024, 64, causal=True, seed=2,
              backward=True),
     *[_long_seq(N, c) for N in (4096, 8192, 16384, 32768) for c in (False, True)],
+    # head dimension 64 at a long sequence, forward and backward
+    Workload("long_d64_b4_h16_n4096_full", 4, 16, 4096, 64, causal=False, seed=8,
+             backward=True),
     Workload("large_head_b2_h16_n8192_d128_causal", 2, 16, 8192, 128, causal=True, seed=4,
              backward=True, qk_gain=3.0),
     Workload("large_head_b2_h16_n8192_d256_causal", 2, 16, 8192, 256, causal=True, seed=4,

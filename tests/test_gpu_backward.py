@@ -146,5 +146,16 @@ def test_backward_is_deterministic(d, B, H, N, causal, kv, mask):
         assert (dq.float() - dq0.float()).abs().max().item() <= 2 ** -7 * dq0.float().abs().max().item()
 
 
+def test_long_d64_config_backward_four_heads():
+    """Head dimension 64 at N = 4096: four seeded heads, always (0,0) and
+    (B-1,H-1), every row."""
+    w = WORKLOADS["long_d64_b4_h16_n4096_full"]
+    inp = make_inputs(w)
+    g, o, lse = P.gpu_forward(w, inp)
+    bh = P.sample_heads(w.B, w.H, 4, seed=w.N)
+    P.compare_forward_full(w, inp, o, lse, bh)
+    P.compare_backward(w, inp, P.gpu_backward(w, g, o, lse), bh)
+
+
 def test_status_clean_after_runs():
     fa.fa_check()
