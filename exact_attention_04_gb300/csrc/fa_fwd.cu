@@ -28,6 +28,10 @@
 //               O / l, LSE = (m + log2 l) * ln 2 (bf16: after the next
 //               tile's first block, so that the wait for the tile's last
 //               P V is spent on that block).
+// With the key-half split (bf16 d = 64, E4M3 d = 128; 480 threads) warps
+// 3..10 are the softmax warps, two a row, each over half of every block's
+// keys with a maximum, sum and O part of its own, and warps 11..14 are
+// epilogue warps that merge a tile's O parts, divide and store (see Cfg).
 //
 // The recurrence is the online softmax of "注意力为什么受限于显存带宽：用算术
 // 强度与分块把 FlashAttention 推导清楚" (section 六) and "4. FlashAttention 深度
@@ -43,8 +47,9 @@
 // Loop order: outer over Q tiles, inner over key blocks (section 4.4.3);
 // key blocks entirely above the causal diagonal are never loaded (section
 // 4.3.2, last note).  Tensor memory columns: NSB S buffers of 128 (3 for
-// d <= 128, 2 for E4M3 d = 256), a block's P (packed bf16 pairs, or E4M3
-// quads) written over the first columns of its own S buffer, then O;
+// bf16 d <= 128, 2 for E4M3), a block's P (packed bf16 pairs, or E4M3
+// quads) written over the first columns of its own S buffer (with the
+// split: of its half's S columns), then O (with the split: two parts);
 // S_{j+NSB} may overwrite S buffer j % NSB only after P_j V_j has completed
 // (pv_done).  bf16 d = 256 (O takes 256 columns): one S buffer and two P
 // buffers of their own (SEP), so that the S buffer is free as soon as the
@@ -155,7 +160,7 @@ struct FwdSmem {
   // EPI: per row, the key halves' row sums [0, NHALF) and reference maxima
   // [NHALF, 2 NHALF)
   float ostat[C::NOB][2 * C::NHALF][C::EPI ? BM : 1];
-  // EPI: kv_len staged at the start (batches up to kKvlCache)
+  // EPI at d = 64: kv_len staged at the start (batches up to kKvlCache)
   int kvl[C::EPI && D == 64 ? kKvlCache : 1];
   uint64_t mma_done, pv_mma_done;
   // a block mask without a host copy: the tiles' costs, then their
@@ -422,7 +427,8 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
     tmem_alloc(&sm.tmem_base, C::TM_COLS);
     tmem_relinquish();
   }
-  // (EPI) every tile's setup reads its batch entry's kv_len: stage them once
+  // (EPI at d = 64, where tiles of short sequences switch often) every tile's setup
+  // reads its batch entry's kv_len: stage them once
   if constexpr (C::EPI && D == 64) {
     if (p.kv_len && p.B <= kKvlCache)
       for (int b = threadIdx.x; b < p.B; b += C::THREADS) sm.kvl[b] = __ldg(p.kv_len + b);
