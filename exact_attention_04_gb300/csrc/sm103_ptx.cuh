@@ -66,6 +66,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Whether the phase of `bar` with parity `parity` has completed, without
+// blocking (acquire on success, as a completed wait).
+__device__ __forceinline__ bool mbar_test(const uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `bar` with parity `parity` to complete.  Never
 // spins forever: gives up after `timeout_ns` of global time, or as soon as
 // another warp of the CTA has raised `*abort` (checked every 64 polls; pass
