@@ -89,8 +89,10 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  * by fa_fwd with the same scale, causal and kv_len).  Outputs dq, dk, dv
  * (bf16 [B,H,N,d]).  workspace: caller-owned device memory of at least
  * fa_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte aligned; its contents on
- * entry do not matter and on return are unspecified.  dQ is accumulated in
- * fp32 with atomic adds, so its last bits can differ from run to run.
+ * entry do not matter and on return are unspecified.  dQ is summed over the
+ * key blocks in fp32 by bulk reduce-adds that the L2 performs in an order
+ * that varies, so its last bits can differ from run to run; dK and dV are
+ * each accumulated by one SM and repeat bit for bit.
  */
 fa_status_t fa_bwd(const void* q, const void* k, const void* v, const void* o,
                    const void* dO, const float* lse, void* dq, void* dk, void* dv,
