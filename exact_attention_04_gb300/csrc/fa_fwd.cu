@@ -865,8 +865,9 @@ __global__ void __launch_bounds__(Cfg<D, FP8>::THREADS, 1)
     uint32_t kv_it = 0, e_it = 0;                       // e_it: tiles with key blocks
     // kEarlyS: one warp a row (d = 128, 256) tests for the next block's S
     // while its P store lands, and skips the wait when it is there (1 % on
-    // the causal d = 128 forward; with the key-half split, whose tiles are
-    // short, the extra code measured 5 % slower)
+    // the causal d = 128 forward).  With the key-half split (bf16 d = 64,
+    // E4M3 d = 128), where the two warps of a row cover each other's waits,
+    // it measured 1-5 % slower.
     constexpr bool kEarlyS = !C::EPI;
     bool ok = true;
     // The epilogue of a tile (O / l into bf16 O, and LSE): run once the next
