@@ -765,12 +765,18 @@ def oracle_whole(name):
 
 
 def cpu_baseline(w, inp):
+    """The oracle on one sampled head of the workload (its TFLOP/s is the
+    line's value), the whole workload's time extrapolated from it (heads are
+    independent and equal in work, so the time is linear in B*H), and the
+    small configurations run whole."""
     run, flops, threads, desc = oracle_sample(w, inp)
     t0 = time.perf_counter()
     run()
     sec = time.perf_counter() - t0
     return {"value": round(flops / sec / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle", "sample": desc, "seconds": round(sec, 3),
+            "extrapolated": {"seconds": round(sec * w.B * w.H, 3), "heads": w.B * w.H,
+                             "note": "the sampled head's time x B*H heads"},
             "whole_small_configs": [oracle_whole(n) for n in ORACLE_WHOLE]}
 
 

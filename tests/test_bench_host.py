@@ -130,3 +130,16 @@ def test_reference_arm_prints_one_contract_line():
     assert r["e2e"] == {"value": r["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert r["vs_baseline"] is None
+
+
+def test_cpu_baseline_extrapolates_from_its_head_sample():
+    """The oracle baseline times one head and states the whole workload's
+    extrapolated time, B*H times the sample's, next to the small configs run
+    whole."""
+    from exact_attention_04_gb300.workloads import random_case, make_inputs
+    w = random_case(3, 2, 256, 64, seed=5, causal=True)
+    cb = bench.cpu_baseline(w, make_inputs(w))
+    assert cb["kind"] == "oracle" and cb["unit"] == "TFLOP/s" and cb["value"] > 0
+    assert cb["extrapolated"]["heads"] == 6
+    assert abs(cb["extrapolated"]["seconds"] - 6 * cb["seconds"]) <= 6e-3
+    assert [c["workload"] for c in cb["whole_small_configs"]] == list(bench.ORACLE_WHOLE)
