@@ -28,7 +28,9 @@ def _rank(rank, world, port, out):
 
 def test_two_gloo_ranks_max_and_barrier():
     world, port = 2, _free_port()
-    with mp.Manager() as m:
+    # spawn, not fork: earlier tests may have started threads (the oracle's
+    # OpenMP pool) in this process
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank, args=(world, port, out), nprocs=world, join=True)
         got = dict(out)
